@@ -1,0 +1,69 @@
+"""The oracle's pins must reject a plausibly broken oracle.
+
+Each case plants one mistake in a copy of oracle.c (on the CPU, in a temporary
+directory), builds it, and runs every pin of the oracle suites against that
+copy: at least one pin has to fail. The shipped oracle.c is never modified."""
+import inspect
+import os
+
+import pytest
+
+pytestmark = pytest.mark.filterwarnings("ignore:overflow encountered in cast")
+
+import oracle
+from tests import test_oracle_codec, test_oracle_gemm
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, text in oracle.c, replacement) -- one planted mistake each
+MUTANTS = [
+    ("transposed_B", "a * lut[brow[j]]", "a * lut[B[j * K + k]]"),
+    ("dropped_last_k", "for (int64_t k = 0; k < K; ++k) {\n                double a",
+     "for (int64_t k = 0; k + 1 < K; ++k) {\n                double a"),
+    ("bias_per_row", "(bias ? oracle_half_to_double(bias[j]) : 0.0)",
+     "(bias ? oracle_half_to_double(bias[j % 2]) : 0.0)"),
+    ("gelu_wrong_scale", "erf(x / sqrt(2.0))", "erf(x / 2.0)"),
+    ("gelu_tanh_form", "0.5 * x * (1.0 + erf(x / sqrt(2.0)))",
+     "0.5 * x * (1.0 + tanh(0.7978845608028654 * (x + 0.044715 * x * x * x)))"),
+    ("gelu_before_bias", "double x = s + (bias ? oracle_half_to_double(bias[j]) : 0.0);\n    return gelu ? oracle_gelu(x) : x;",
+     "double x = (gelu ? oracle_gelu(s) : s);\n    return x + (bias ? oracle_half_to_double(bias[j]) : 0.0);"),
+    ("rounding_through_fp32", "if (C) C[r * N + j] = oracle_double_to_half(y);",
+     "if (C) C[r * N + j] = oracle_double_to_half((double)(float)y);"),
+    ("round_ties_away", "double q = nearbyint(ldexp(a, 10 - e));", "double q = round(ldexp(a, 10 - e));"),
+    ("subnormal_exponent", "v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    ("normal_exponent_bias", "v = ldexp((double)(1024 + f), e - 25);", "v = ldexp((double)(1024 + f), e - 24);"),
+    ("overflow_threshold", "if (a >= 65520.0)", "if (a >= 65504.0)"),
+    ("fp32_accumulation", "double* acc = (double*)malloc((size_t)N * sizeof(double));",
+     "float* acc = (float*)malloc((size_t)N * sizeof(float));"),
+    ("sampled_wrong_index", "oracle_half_to_double(B[k * N + j])", "oracle_half_to_double(B[j * K + k])"),
+]
+
+
+def _pins():
+    fns = []
+    for mod in (test_oracle_codec, test_oracle_gemm):
+        for name, fn in inspect.getmembers(mod, inspect.isfunction):
+            if name.startswith("test_") and "oracle_lib" in inspect.signature(fn).parameters:
+                fns.append(fn)
+    return fns
+
+
+def test_every_pin_passes_on_the_shipped_oracle(oracle_lib):
+    for fn in _pins():
+        fn(oracle_lib)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_reject_mutant(tmp_path, name, old, new):
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation site for {name} not found exactly once"
+    src = tmp_path / f"oracle_{name}.c"
+    src.write_text(text.replace(old, new))
+    lib = oracle.load_library(oracle.compile_source(str(src), str(tmp_path / f"lib_{name}.so")))
+    failures = []
+    for fn in _pins():
+        try:
+            fn(lib)
+        except (AssertionError, RuntimeError, ValueError) as e:
+            failures.append(fn.__name__)
+    assert failures, f"no pin caught the planted mistake {name}"

@@ -1,0 +1,65 @@
+"""Workload definitions and the algorithmic flop/byte counts the benchmark
+reports, pinned to the worked traffic example of "TileLang: writing LLM GPU
+kernels by thinking in tiles", section 2, "A back-of-the-envelope calculation"."""
+import os
+
+import numpy as np
+import torch
+
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _kv(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as fh:
+        for line in fh:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                k, v = line.split()
+                out[k] = int(v)
+    return out
+
+
+def test_traffic_worked_example():
+    g = _kv("traffic_4096.txt")
+    w = workloads.custom(g["M"], g["N"], g["K"], seed=0)
+    assert w.flops() == g["flops"]
+    assert round(w.flops() / 1e9) == g["flops_page_billions"]
+    assert w.bytes() == g["ideal_bytes"] == 3 * g["matrix_bytes"]
+    assert g["matrix_bytes"] // 2 ** 20 == g["matrix_page_mb"]
+    assert g["ideal_bytes"] // 2 ** 20 == g["ideal_page_mb"]
+    # naive: every output reads a K-row of A and a K-column of B, 2 bytes each
+    assert g["M"] * g["N"] * (2 * g["K"]) * 2 == g["naive_input_bytes"]
+    assert round(g["naive_input_bytes"] / 1e9) == g["naive_page_gb"]
+
+
+def test_five_workloads_shapes():
+    names = [w.name for w in workloads.ALL]
+    assert len(set(names)) == 5
+    assert (workloads.SQUARE_8192.M, workloads.SQUARE_8192.N, workloads.SQUARE_8192.K) == (8192,) * 3
+    d = workloads.DECODE
+    assert (d.M, d.N, d.K) == (16, 28672, 8192)
+    assert d.bytes() == 2 * (16 * 8192 + 8192 * 28672 + 16 * 28672) == 470_941_696
+    r = workloads.RAGGED_GELU
+    assert all(x % 64 for x in (r.M, r.N, r.K)) and r.gelu and r.has_bias
+
+
+def test_inputs_are_seeded_and_fp16():
+    w = workloads.custom(33, 17, 9, seed=5, bias=workloads.Dist("uniform", -0.1, 0.1))
+    A1, B1, b1 = w.inputs()
+    A2, B2, b2 = w.inputs()
+    assert A1.dtype == B1.dtype == b1.dtype == torch.float16
+    assert torch.equal(A1, A2) and torch.equal(B1, B2) and torch.equal(b1, b2)
+    assert A1.shape == (33, 9) and B1.shape == (9, 17) and b1.shape == (17,)
+    assert float(A1.abs().max()) <= 1.0 and float(b1.abs().max()) <= 0.1
+    other = workloads.custom(33, 17, 9, seed=6).inputs()[0]
+    assert not torch.equal(A1, other)
+
+
+def test_integer_distribution_is_integer():
+    w = workloads.custom(20, 20, 20, seed=1, dist=workloads.Dist("int", -2, 2))
+    A, B, _ = w.inputs()
+    a = A.float().numpy()
+    assert np.array_equal(a, np.round(a)) and a.min() >= -2 and a.max() <= 2

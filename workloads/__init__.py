@@ -1,0 +1,117 @@
+"""Seeded synthetic inputs for the fp16 GEMM workloads.
+
+This module holds no GEMM, bias or GELU arithmetic: it only names the workloads
+(shapes, value distributions, seeds) and draws their inputs. Both the CUDA path's
+tests/benchmark and the CPU oracle consume the identical bits it produces.
+
+Recipe (one reading, since the pages give none): a CPU ``torch.Generator``
+seeded with the workload's seed draws A, then B, then the bias (when present),
+in that order, as float32; uniform[lo, hi] is ``lo + (hi - lo) * torch.rand``,
+normal(0, s) is ``s * torch.randn``; each is then rounded to float16 (to
+nearest, ties to even).
+
+The shapes stand in for the pages' own GEMM examples (4096^3 and 2048^3 fp16
+tiles, 128x128x32 blocking) and for the transformer shapes they motivate (an
+FFN up-projection and a decode-time skinny product).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class Dist:
+    kind: str          # "uniform" or "normal"
+    a: float           # uniform: low;  normal: mean (always 0 here)
+    b: float           # uniform: high; normal: standard deviation
+
+    def draw(self, shape, gen: torch.Generator) -> torch.Tensor:
+        if self.kind == "uniform":
+            x = torch.rand(shape, generator=gen, dtype=torch.float32)
+            x = self.a + (self.b - self.a) * x
+        elif self.kind == "normal":
+            x = self.a + self.b * torch.randn(shape, generator=gen, dtype=torch.float32)
+        elif self.kind == "int":
+            # integer-valued entries in [a, b] (exact in fp16 and in any fp32 sum
+            # of the sizes the exact tests use)
+            x = torch.randint(int(self.a), int(self.b) + 1, shape, generator=gen).to(torch.float32)
+        else:
+            raise ValueError(self.kind)
+        return x.to(torch.float16)
+
+
+U1 = Dist("uniform", -1.0, 1.0)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    seed: int
+    a_dist: Dist = U1
+    b_dist: Dist = U1
+    bias_dist: Dist | None = None
+    gelu: bool = False
+    note: str = field(default="", compare=False)
+
+    @property
+    def has_bias(self) -> bool:
+        return self.bias_dist is not None
+
+    def describe(self) -> str:
+        epi = ("bias+" if self.has_bias else "") + ("gelu" if self.gelu else ("none" if not self.has_bias else ""))
+        return f"{self.name}: M={self.M} N={self.N} K={self.K} epilogue={epi.rstrip('+')} seed={self.seed}"
+
+    def inputs(self, device: str = "cpu"):
+        """(A, B, bias_or_None) as contiguous float16 tensors on ``device``."""
+        g = torch.Generator(device="cpu")
+        g.manual_seed(self.seed)
+        A = self.a_dist.draw((self.M, self.K), g)
+        B = self.b_dist.draw((self.K, self.N), g)
+        bias = self.bias_dist.draw((self.N,), g) if self.bias_dist is not None else None
+        if device != "cpu":
+            A = A.to(device)
+            B = B.to(device)
+            bias = bias.to(device) if bias is not None else None
+        return A, B, bias
+
+    # algorithmic work: what the method must do, each operand touched once
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    def bytes(self) -> int:
+        n = 2 * (self.M * self.K + self.K * self.N + self.M * self.N)
+        if self.has_bias:
+            n += 2 * self.N
+        return n
+
+
+# The five workloads. Names say what they are.
+SQUARE_256 = Workload("square_256", 256, 256, 256, seed=0,
+                      note="fp16 GEMM 256^3, uniform[-1,1], no epilogue")
+RAGGED_GELU = Workload("ragged_1000x1030x520_bias_gelu", 1000, 1030, 520, seed=1,
+                       bias_dist=Dist("uniform", -0.1, 0.1), gelu=True,
+                       note="ragged shape, no dimension a multiple of 64, bias + exact-erf GELU")
+SQUARE_8192 = Workload("square_8192", 8192, 8192, 8192, seed=2,
+                       note="fp16 GEMM 8192^3, uniform[-1,1], no epilogue; tensor-bound")
+FFN_UP = Workload("ffn_up_4096x14336x4096_bias_gelu", 4096, 14336, 4096, seed=3,
+                  a_dist=Dist("normal", 0.0, 1.0), b_dist=Dist("normal", 0.0, 0.02),
+                  bias_dist=Dist("normal", 0.0, 0.02), gelu=True,
+                  note="FFN up-projection, tokens x hidden -> 14336, fused bias + GELU")
+DECODE = Workload("decode_16x28672x8192", 16, 28672, 8192, seed=4,
+                  a_dist=Dist("normal", 0.0, 1.0), b_dist=Dist("normal", 0.0, 0.02),
+                  note="decode-shaped skinny GEMM; HBM-bound on reading B")
+
+ALL = (SQUARE_256, RAGGED_GELU, SQUARE_8192, FFN_UP, DECODE)
+BY_NAME = {w.name: w for w in ALL}
+
+
+def custom(M: int, N: int, K: int, seed: int, dist: Dist = U1, bias: Dist | None = None,
+           gelu: bool = False) -> Workload:
+    """An ad-hoc workload (edge-shape tests) with the same generator recipe."""
+    return Workload(f"custom_{M}x{N}x{K}_s{seed}", M, N, K, seed=seed, a_dist=dist, b_dist=dist,
+                    bias_dist=bias, gelu=gelu)
