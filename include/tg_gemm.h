@@ -1,0 +1,162 @@
+/*
+ * tg_gemm — fp16 tiled tensor-core GEMM with an optional fused bias + GELU
+ * epilogue, for one GB300 (sm_103a) GPU. C ABI.
+ *
+ * The operation (the problem statement of "TileLang: writing LLM GPU kernels by
+ * thinking in tiles", sections 2 and 3, with the epilogue of "Designing
+ * high-performance GPU kernels with TileLang ...", section 3 "Epilogue Fusion
+ * and Memory Efficiency"):
+ *
+ *     C[i,j] = epi( sum_k A[i,k] * B[k,j] + bias[j] )
+ *
+ *   A      M x K, IEEE binary16, row-major (leading dimension K)
+ *   B      K x N, IEEE binary16, row-major (leading dimension N)
+ *   bias   N binary16 values, added to column j of every row; NULL means no bias
+ *   C      M x N, IEEE binary16, row-major (leading dimension N)
+ *   epi    identity (TG_EPI_NONE) or GELU(x) = 0.5 x (1 + erf(x / sqrt 2))
+ *          (TG_EPI_GELU, the exact-erf form)
+ *
+ * Products are accumulated in fp32 by the tensor core; bias and GELU are
+ * applied in fp32 to the unrounded sum while the tile is still on chip; the
+ * result is rounded once to binary16 (to nearest, ties to even; overflow gives
+ * +-inf). The order of the fp32 accumulation is not specified: results agree
+ * with an exact computation to within fp32 accumulation error plus one final
+ * binary16 rounding, and are bit-identical from run to run on the same GPU.
+ *
+ * Pointers and ownership. Unless a function says otherwise, A, B, bias and C
+ * are DEVICE pointers on the current CUDA device, owned by the caller; the
+ * library never frees or keeps them past the call. C must not overlap A, B or
+ * bias (checked). Any alignment is accepted; 16-byte-aligned base pointers with
+ * K and N multiples of 8 take the fast (TMA) path, anything else a slower path
+ * with ordinary loads.
+ *
+ * Streams. `stream` is a cudaStream_t (NULL = the legacy default stream). Each
+ * call only enqueues work and returns without synchronising. Calls are
+ * stream-ordered; the library keeps a separate scratch buffer per stream, so
+ * concurrent calls on different streams are safe.
+ *
+ * Errors. Every function returns a tg_status; TG_OK is 0. Argument errors are
+ * detected on the host before anything is enqueued. tg_last_error() gives a
+ * human-readable message for the last failure on the calling thread.
+ */
+#ifndef TG_GEMM_H
+#define TG_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Binary-compatible with cudaStream_t / CUstream. */
+typedef struct CUstream_st* tg_stream_t;
+
+typedef enum {
+    TG_EPI_NONE = 0, /* C = A@B (+ bias) */
+    TG_EPI_GELU = 1  /* C = GELU(A@B (+ bias)), exact erf */
+} tg_epilogue;
+
+typedef enum {
+    TG_OK = 0,
+    TG_ERR_INVALID_ARG = 1,        /* bad pointer, size, epilogue, kernel choice or overlap */
+    TG_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not compute capability 10.3 */
+    TG_ERR_CUDA = 3,               /* a CUDA runtime/driver call or a launch failed */
+    TG_ERR_TIMEOUT = 4,            /* a kernel's bounded wait expired (see tg_device_status) */
+    TG_ERR_NO_MEMORY = 5           /* the library could not allocate its scratch buffer */
+} tg_status;
+
+/* Kernel selection for tg_gemm_ex (tg_gemm always uses TG_KERNEL_AUTO). */
+typedef enum {
+    TG_KERNEL_AUTO = 0,      /* choose by shape and alignment (below) */
+    TG_KERNEL_TILED_TMA = 1, /* persistent 128x256 tiles, TMA loads, tcgen05 MMA into TMEM.
+                                Needs K % 8 == 0, N % 8 == 0, A and B 16-byte aligned. */
+    TG_KERNEL_TILED_LSU = 2, /* the same tiles with operands staged by ordinary loads;
+                                any shape and alignment */
+    TG_KERNEL_SPLITK = 3     /* skinny M <= 128: computes C^T = B^T A^T so N fills the
+                                128-row MMA, with K split across CTAs; same TMA needs
+                                as TG_KERNEL_TILED_TMA */
+} tg_kernel;
+
+/*
+ * C = epi(A @ B + bias) on `stream`.
+ *
+ * M, N, K >= 0 and each < 2^31. M == 0 or N == 0: nothing is done. K == 0: the
+ * empty sum is 0, so C = epi(bias) (or epi(0) without bias). `epilogue` is a
+ * tg_epilogue value. A, B may be NULL only when the product is empty.
+ *
+ * Kernel choice: M <= 128 with TMA-compatible operands -> TG_KERNEL_SPLITK;
+ * otherwise TMA-compatible -> TG_KERNEL_TILED_TMA; otherwise TG_KERNEL_TILED_LSU.
+ */
+tg_status tg_gemm(const void* A, const void* B, const void* bias, void* C,
+                  int64_t M, int64_t N, int64_t K, int epilogue, tg_stream_t stream);
+
+/*
+ * tg_gemm with an explicit kernel (a tg_kernel value) and, for
+ * TG_KERNEL_SPLITK, an explicit number of K slices `split_k` (0 = automatic,
+ * otherwise 1..64 and at most ceil(K / 64)). A kernel whose requirements the
+ * arguments do not meet is TG_ERR_INVALID_ARG. Results of all kernels agree
+ * within the accumulation-order tolerance stated above; on inputs whose
+ * products and partial sums are exact in fp32 they are bit-identical.
+ */
+tg_status tg_gemm_ex(const void* A, const void* B, const void* bias, void* C,
+                     int64_t M, int64_t N, int64_t K, int epilogue, int kernel, int split_k,
+                     tg_stream_t stream);
+
+/*
+ * End-to-end form with HOST operands: copies hA, hB, hbias (host, preferably
+ * pinned) into the caller's device buffers dA, dB, dbias, runs tg_gemm on
+ * them, and copies the result dC back into host hC, all enqueued on `stream`
+ * (returns without synchronising; hC is valid after the stream completes).
+ * hbias and dbias are both NULL or both non-NULL. Device buffers must hold
+ * M*K, K*N, N and M*N binary16 values; they are owned by the caller.
+ */
+tg_status tg_gemm_staged(const void* hA, const void* hB, const void* hbias, void* hC,
+                         void* dA, void* dB, void* dbias, void* dC,
+                         int64_t M, int64_t N, int64_t K, int epilogue, tg_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reports (and clears) the device-side status word
+ * that kernels set when one of their bounded waits expires: TG_OK or
+ * TG_ERR_TIMEOUT. `*where` (if not NULL) receives the code of the wait that
+ * expired first (0 if none). Every wait inside the kernels gives up after the
+ * watchdog limit (tg_set_watchdog_ns) instead of spinning forever; the kernel
+ * then drains its in-flight copies, frees its tensor memory and exits, leaving
+ * C unspecified.
+ */
+tg_status tg_device_status(tg_stream_t stream, int* where);
+
+/* Watchdog limit for every bounded wait, in ns (default 2e9; 0 restores it). */
+tg_status tg_set_watchdog_ns(uint64_t ns);
+
+/*
+ * Test hook for the watchdog: while `on` is non-zero, the TMA producer of the
+ * tiled kernel skips its arrival on the first pipeline stage of every CTA, so
+ * the consumers' bounded waits expire and the call ends with TG_ERR_TIMEOUT
+ * from tg_device_status. Off by default; has no effect on other kernels.
+ */
+tg_status tg_debug_skip_first_arrive(int on);
+
+/* Static description of a status code. */
+const char* tg_status_string(int status);
+
+/* Message for the last failure on the calling thread ("" if none). */
+const char* tg_last_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int tg_version(void);
+
+/*
+ * Shared memory (bytes per CTA) that a kernel configuration uses for its
+ * operand ring: stages * (BM*BK + BK*BN) * 2. Returns -1 for an unknown kernel.
+ * For TG_KERNEL_SPLITK the M-side tile is the padded M of a 16-row problem.
+ */
+int64_t tg_ring_bytes(int kernel);
+
+/* Frees the library's per-device scratch buffers. Call with no work in flight. */
+void tg_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TG_GEMM_H */

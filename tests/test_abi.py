@@ -1,0 +1,120 @@
+"""CPU checks of the C-ABI library: it loads without a GPU, exports every
+function include/tg_gemm.h declares, and rejects bad arguments on the host
+before touching a device (no compute call is made here)."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def tg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import tiled_tensor_core_tcgen05_gb300 as m
+    return m
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "tg_gemm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(tg_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_documented_entry_points():
+    names = _declared_functions()
+    assert "tg_gemm" in names and "tg_gemm_ex" in names and "tg_gemm_staged" in names
+    assert len(names) >= 11
+
+
+def test_library_exports_every_declared_function(tg):
+    lib = tg.library()
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert set(_declared_functions()) == set(tg.EXPORTS)
+
+
+def test_status_strings_and_version(tg):
+    assert tg.tg_status_string(0) == "TG_OK"
+    for s in range(1, 6):
+        assert tg.tg_status_string(s).startswith("TG_ERR_")
+    assert "unknown" in tg.tg_status_string(99)
+    assert tg.tg_version() >= 10000
+
+
+def test_ring_bytes_follow_the_tile_footprint_formula(tg):
+    # tiled kernels: 4 stages of a 128x64 A tile and a 64x256 B tile, fp16
+    assert tg.tg_ring_bytes(tg.KERNEL_TILED_TMA) == tg.ring_bytes(128, 256, 64, 4) == 196608
+    assert tg.tg_ring_bytes(tg.KERNEL_TILED_LSU) == tg.ring_bytes(128, 256, 64, 4)
+    assert tg.tg_ring_bytes(tg.KERNEL_SPLITK) % tg.ring_bytes(16, 128, 64, 1) == 0
+    assert tg.tg_ring_bytes(tg.KERNEL_SPLITK) <= 227 * 1024
+    assert tg.tg_ring_bytes(42) == -1
+
+
+def test_footprint_worked_example(tg):
+    # "TileLang: you write the dataflow, the compiler owns the schedule", section
+    # "What a tile costs, exactly": 128/128/32, 3 stages, fp16 -> 16 KB per stage, 48 KB
+    g = {}
+    for line in open(os.path.join(ROOT, "tests", "golden", "smem_footprint.txt")):
+        line = line.split("#", 1)[0].strip()
+        if line:
+            k, v = line.split()
+            g[k] = int(v)
+    bm, bn, bk, st, b = g["block_M"], g["block_N"], g["block_K"], g["num_stages"], g["bytes_per_elem"]
+    assert tg.ring_bytes(bm, bn, bk, 1, b) == g["stage_kb"] * 1024
+    assert tg.ring_bytes(bm, bn, bk, st, b) == g["total_kb"] * 1024
+    assert bm * bn * 4 == g["accum_kb"] * 1024
+    assert bm * bn * 4 // 4 // g["threads"] == g["regs_per_thread"]
+
+
+@pytest.mark.parametrize("args,msg", [
+    (dict(epilogue=2), "epilogue"),
+    (dict(M=-1), "sizes"),
+    (dict(K=2 ** 31), "sizes"),
+    (dict(kernel=9), "kernel"),
+    (dict(split_k=65), "split_k"),
+    (dict(split_k=-1), "split_k"),
+    (dict(C=0), "C is NULL"),
+    (dict(A=0), "A or B"),
+    (dict(C=0x10000 + 10), "overlaps"),
+    (dict(kernel=1, K=12), "TG_KERNEL_TILED_TMA"),
+    (dict(kernel=1, A=0x10002), "TG_KERNEL_TILED_TMA"),
+    (dict(kernel=3, M=129), "TG_KERNEL_SPLITK"),
+    (dict(kernel=3, N=20), "TG_KERNEL_SPLITK"),
+    (dict(kernel=1, split_k=2), "split_k applies"),
+])
+def test_invalid_arguments_rejected_on_host(tg, args, msg):
+    base = dict(A=0x10000, B=0x20000000, bias=None, C=0x40000000, M=64, N=64, K=64, epilogue=0,
+                kernel=0, split_k=0)
+    base.update(args)
+    with pytest.raises(tg.TgError) as ei:
+        tg.tg_gemm_ex(base["A"] or None, base["B"] or None, base["bias"], base["C"] or None, base["M"],
+                      base["N"], base["K"], base["epilogue"], base["kernel"], base["split_k"], None)
+    assert ei.value.status == tg.ERR_INVALID_ARG
+    assert msg in str(ei.value)
+
+
+def test_empty_products_need_no_device(tg):
+    # M == 0 or N == 0: nothing to do, so success without any CUDA call
+    tg.tg_gemm(None, None, None, None, 0, 5, 7, 0, None)
+    tg.tg_gemm(None, None, None, None, 5, 0, 7, 1, None)
+
+
+def test_staged_argument_checks(tg):
+    with pytest.raises(tg.TgError):
+        tg.tg_gemm_staged(1, 2, 3, 4, 5, 6, None, 8, 4, 4, 4, 0, None)   # hbias without dbias
+    with pytest.raises(tg.TgError):
+        tg.tg_gemm_staged(1, 2, None, 4, 5, 6, None, 8, -1, 4, 4, 0, None)
+
+
+def test_product_package_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "tiled_tensor_core_tcgen05_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "oracle." not in text.replace("oracle.c", ""), f
+                assert "liboracle" not in text, f

@@ -1,0 +1,186 @@
+"""Python binding for libtg_gemm.so, the GB300 fp16 tiled tensor-core GEMM.
+
+C[i,j] = epi(sum_k A[i,k] B[k,j] + bias[j]), epi = identity or exact-erf GELU:
+the GEMM of "TileLang: writing LLM GPU kernels by thinking in tiles"
+(sections 2-3) with the GELU(MatMul + Bias) epilogue of "Designing
+high-performance GPU kernels with TileLang ..." (section 3).
+
+This module only marshals arguments into the C ABI declared in
+include/tg_gemm.h: every step of the computation runs in the library's CUDA
+kernels. Functions named tg_* mirror the C entry points one to one (raw
+pointers as ints, sizes, a stream handle); ``gemm`` and ``gemm_staged`` accept
+torch tensors and pass their pointers and torch's current stream. There is no
+CPU path: if the library has not been built, importing this package raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtg_gemm.so")
+
+EPI_NONE, EPI_GELU = 0, 1
+KERNEL_AUTO, KERNEL_TILED_TMA, KERNEL_TILED_LSU, KERNEL_SPLITK = 0, 1, 2, 3
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NO_MEMORY = range(6)
+
+# every symbol include/tg_gemm.h declares
+EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_device_status", "tg_set_watchdog_ns",
+           "tg_debug_skip_first_arrive", "tg_status_string", "tg_last_error", "tg_version",
+           "tg_ring_bytes", "tg_shutdown")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+                      "(or python tiled_tensor_core_tcgen05_gb300/build.py); there is no fallback path")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_vp, _i64, _int, _u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64
+_lib.tg_gemm.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
+_lib.tg_gemm_ex.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp]
+_lib.tg_gemm_staged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
+_lib.tg_device_status.argtypes = [_vp, ctypes.POINTER(_int)]
+_lib.tg_set_watchdog_ns.argtypes = [_u64]
+_lib.tg_debug_skip_first_arrive.argtypes = [_int]
+_lib.tg_status_string.argtypes = [_int]
+_lib.tg_status_string.restype = ctypes.c_char_p
+_lib.tg_last_error.argtypes = []
+_lib.tg_last_error.restype = ctypes.c_char_p
+_lib.tg_version.argtypes = []
+_lib.tg_ring_bytes.argtypes = [_int]
+_lib.tg_ring_bytes.restype = _i64
+_lib.tg_shutdown.argtypes = []
+_lib.tg_shutdown.restype = None
+for _name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_device_status", "tg_set_watchdog_ns",
+              "tg_debug_skip_first_arrive", "tg_version"):
+    getattr(_lib, _name).restype = _int
+
+
+class TgError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{tg_status_string(status)}: {message}")
+        self.status = status
+
+
+def _check(status: int) -> None:
+    if status != OK:
+        raise TgError(status, tg_last_error())
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+# ---------------------------------------------------------------- raw C ABI
+
+def tg_gemm(A: int, B: int, bias: int | None, C: int, M: int, N: int, K: int, epilogue: int,
+            stream: int | None) -> None:
+    _check(_lib.tg_gemm(A, B, bias, C, M, N, K, epilogue, stream))
+
+
+def tg_gemm_ex(A: int, B: int, bias: int | None, C: int, M: int, N: int, K: int, epilogue: int,
+               kernel: int, split_k: int, stream: int | None) -> None:
+    _check(_lib.tg_gemm_ex(A, B, bias, C, M, N, K, epilogue, kernel, split_k, stream))
+
+
+def tg_gemm_staged(hA, hB, hbias, hC, dA, dB, dbias, dC, M, N, K, epilogue, stream) -> None:
+    _check(_lib.tg_gemm_staged(hA, hB, hbias, hC, dA, dB, dbias, dC, M, N, K, epilogue, stream))
+
+
+def tg_device_status(stream: int | None) -> tuple[int, int]:
+    where = _int(0)
+    st = _lib.tg_device_status(stream, ctypes.byref(where))
+    return st, where.value
+
+
+def tg_set_watchdog_ns(ns: int) -> None:
+    _check(_lib.tg_set_watchdog_ns(ns))
+
+
+def tg_debug_skip_first_arrive(on: bool) -> None:
+    _check(_lib.tg_debug_skip_first_arrive(1 if on else 0))
+
+
+def tg_status_string(status: int) -> str:
+    return _lib.tg_status_string(status).decode()
+
+
+def tg_last_error() -> str:
+    return _lib.tg_last_error().decode()
+
+
+def tg_version() -> int:
+    return _lib.tg_version()
+
+
+def tg_ring_bytes(kernel: int) -> int:
+    return _lib.tg_ring_bytes(kernel)
+
+
+def tg_shutdown() -> None:
+    _lib.tg_shutdown()
+
+
+# ---------------------------------------------------------------- torch form
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _dev_fp16(t, name):
+    if t.dtype.__repr__() != "torch.float16":
+        raise TypeError(f"{name} must be float16, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (row-major)")
+    return t.data_ptr()
+
+
+def gemm(A, B, bias=None, gelu: bool = False, out=None, kernel: int = KERNEL_AUTO, split_k: int = 0,
+         stream=None):
+    """C = epi(A @ B + bias) for CUDA float16 tensors A (M, K), B (K, N), bias (N,).
+
+    Runs on ``stream`` (default: torch's current stream) and returns ``out``
+    (allocated with torch when not given). Asynchronous like any CUDA op.
+    """
+    import torch
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError(f"shape mismatch {tuple(A.shape)} @ {tuple(B.shape)}")
+    M, K = A.shape
+    N = B.shape[1]
+    if bias is not None and tuple(bias.shape) != (N,):
+        raise ValueError(f"bias must have shape ({N},)")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    elif tuple(out.shape) != (M, N):
+        raise ValueError("out has the wrong shape")
+    pa = _dev_fp16(A, "A") if A.numel() else None
+    pb = _dev_fp16(B, "B") if B.numel() else None
+    pbias = _dev_fp16(bias, "bias") if bias is not None else None
+    pc = _dev_fp16(out, "out") if out.numel() else None
+    tg_gemm_ex(pa, pb, pbias, pc, M, N, K, EPI_GELU if gelu else EPI_NONE, kernel, split_k,
+               _stream_handle(stream))
+    return out
+
+
+def gemm_staged(hA, hB, hbias, hC, dA, dB, dbias, dC, gelu: bool = False, stream=None) -> None:
+    """End-to-end form: host (pinned) tensors hA, hB, hbias are copied into the
+    device tensors dA, dB, dbias, the GEMM runs, and the result is copied from dC
+    into host hC, all on ``stream``."""
+    M, K = hA.shape
+    N = hB.shape[1]
+    tg_gemm_staged(hA.data_ptr(), hB.data_ptr(), hbias.data_ptr() if hbias is not None else None,
+                   hC.data_ptr(), dA.data_ptr(), dB.data_ptr(),
+                   dbias.data_ptr() if dbias is not None else None, dC.data_ptr(), M, N, K,
+                   EPI_GELU if gelu else EPI_NONE, _stream_handle(stream))
+
+
+def ring_bytes(block_M: int, block_N: int, block_K: int, num_stages: int, elem_bytes: int = 2) -> int:
+    """Shared memory a pipelined tile ring needs: every stage holds one
+    block_M x block_K tile of A and one block_K x block_N tile of B
+    ("TileLang: you write the dataflow, the compiler owns the schedule",
+    section "What a tile costs, exactly")."""
+    return num_stages * (block_M * block_K + block_K * block_N) * elem_bytes

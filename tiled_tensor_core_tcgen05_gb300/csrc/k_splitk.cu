@@ -1,0 +1,271 @@
+// Skinny-M GEMM (M <= 128, e.g. decode with a handful of tokens): swap the
+// operands and split K.
+//
+// With M small, C = A @ B is bound by reading B once from HBM. The kernel
+// computes the transposed product C^T = B^T @ A^T so that N fills the
+// 128-row side of the tensor-core MMA and M (padded to 16) is the MMA's N:
+//   MMA operand "A" = a 128 (n) x 64 (k) slice of B, which is N-major in memory;
+//   MMA operand "B" = a 64 (k) x M slice of A^T, i.e. A's rows, K-major.
+// One work unit is (128-column slice of N, range of K blocks); units are
+// spread over a persistent grid. With more than one K slice, each unit
+// writes an fp32 partial tile to a scratch buffer; the last unit of a column
+// slice to finish (an arrival counter) adds the partials in slice order
+// 0, 1, ..., applies bias and GELU and writes C, so results do not depend on
+// which CTA finishes last. The counter is reset by that last unit, so it is
+// zero again for the next launch.
+//
+// The product and epilogue are those of "TileLang: writing LLM GPU kernels by
+// thinking in tiles" (sections 2-3) and "Designing high-performance GPU
+// kernels with TileLang ..." (section 3, GELU(MatMul + Bias)); the pages give
+// no skinny-shape schedule, this one is designed for GB300's HBM.
+#include "tg_device.cuh"
+#include "tg_internal.h"
+
+namespace tg {
+namespace {
+
+constexpr int kBoxB = kSkBK * 64 * 2;       // 64 (k) x 64 (n) N-major box, 8 KB
+constexpr int kStageBBytes = 2 * kBoxB;     // 128 columns of N
+constexpr int kThreads = 6 * 32;            // producer, MMA, 4 epilogue warps
+constexpr int kEpiThreads = 128;
+
+struct Layout {
+    int stage_bytes, ring, bar_full, bar_empty, bar_acc_full, bar_acc_empty, bar_drain, tmem_slot,
+        abort_slot, flag_slot, used, alloc;
+};
+
+__host__ __device__ inline Layout layout_for(int m_pad, int stages) {
+    Layout L;
+    L.stage_bytes = kStageBBytes + m_pad * 128;  // multiple of 2048: keeps 1024-B alignment
+    L.ring = stages * L.stage_bytes;
+    L.bar_full = L.ring;
+    L.bar_empty = L.bar_full + 8 * stages;
+    L.bar_acc_full = L.bar_empty + 8 * stages;
+    L.bar_acc_empty = L.bar_acc_full + 16;
+    L.bar_drain = L.bar_acc_empty + 16;
+    L.tmem_slot = L.bar_drain + 8;
+    L.abort_slot = L.tmem_slot + 4;
+    L.flag_slot = L.abort_slot + 4;
+    L.used = L.flag_slot + 4;
+    L.alloc = L.used + 1024;
+    return L;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
+                       const SplitArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const Layout L = layout_for(args.m_pad, args.stages);
+    const int S = args.stages;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    auto full_bar = [&](int s) { return sbase + L.bar_full + 8 * s; };
+    auto empty_bar = [&](int s) { return sbase + L.bar_empty + 8 * s; };
+    auto acc_full_bar = [&](int b) { return sbase + L.bar_acc_full + 8 * b; };
+    auto acc_empty_bar = [&](int b) { return sbase + L.bar_acc_empty + 8 * b; };
+    const uint32_t drain_bar = sbase + L.bar_drain;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_slot);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L.flag_slot);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.tmem_slot);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full_bar(b), 1);
+            mbar_init(acc_empty_bar(b), kEpiThreads);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmA);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), args.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const WaitCtx wc{abort_flag, args.wd.status, args.wd.limit_ns};
+    const int stage_tx = L.stage_bytes;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_stream = l2_policy_evict_first();  // B: read exactly once
+            const uint64_t pol_keep = l2_policy_evict_last();     // A: re-read by every unit
+            int stage = 0;
+            uint32_t phase = 0;
+            uint64_t issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x) {
+                const int nt = u / args.splits;
+                const int sp = u - nt * args.splits;
+                const int kb0 = sp * args.kb_per_split;
+                const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_phase(empty_bar(stage), phase ^ 1, wc, kSiteProducerEmpty)) { ok = false; break; }
+                    const uint32_t sB = sbase + stage * L.stage_bytes;
+                    const uint32_t sA = sB + kStageBBytes;
+                    mbar_arrive_expect_tx(full_bar(stage), stage_tx);
+                    tma_load_2d_hint(sB, &tmB, full_bar(stage), nt * kSkBN, kb * kSkBK, pol_stream);
+                    tma_load_2d_hint(sB + kBoxB, &tmB, full_bar(stage), nt * kSkBN + 64, kb * kSkBK, pol_stream);
+                    tma_load_2d_hint(sA, &tmA, full_bar(stage), kb * kSkBK, 0, pol_keep);
+                    issued_mask |= 1ull << stage;
+                    issued_parity = (issued_parity & ~(1ull << stage)) | (uint64_t(phase) << stage);
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+            }
+            for (int s = 0; s < S; ++s)
+                if (issued_mask & (1ull << s)) wait_phase_drain(full_bar(s), (issued_parity >> s) & 1, wc);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32(128, args.m_pad, /*a_mn_major=*/true, /*b_mn_major=*/false);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x, ++it) {
+                const int nt = u / args.splits;
+                const int sp = u - nt * args.splits;
+                const int kb0 = sp * args.kb_per_split;
+                const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
+                const int b = it & 1;
+                if (!wait_phase(acc_empty_bar(b), ((it >> 1) & 1) ^ 1, wc, kSiteMmaAccEmpty)) break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * args.tmem_stride;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_phase(full_bar(stage), phase, wc, kSiteMmaFull)) { ok = false; break; }
+                    tc_fence_after_sync();
+                    const uint32_t sB = sbase + stage * L.stage_bytes;
+                    const uint32_t sA = sB + kStageBBytes;
+                    const uint64_t a_desc = smem_desc_sw128(sB, kBoxB, 1024);  // N-major slice of B
+                    const uint64_t b_desc = smem_desc_sw128(sA, 16, 1024);     // K-major rows of A
+#pragma unroll
+                    for (int k = 0; k < kSkBK / 16; ++k)
+                        mma_f16(d_tmem, a_desc + (uint64_t)((k * 2048) >> 4), b_desc + (uint64_t)((k * 32) >> 4),
+                                idesc, (kb != kb0) || (k != 0));
+                    mma_commit(empty_bar(stage));
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(acc_full_bar(b));
+            }
+            mma_commit(drain_bar);
+            wait_phase_drain(drain_bar, 0, wc);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;
+        const int ept = threadIdx.x - 64;  // 0..127
+        const int chunks = args.m_pad / 16;
+        int it = 0;
+        for (int u = blockIdx.x; u < args.num_units; u += gridDim.x, ++it) {
+            const int nt = u / args.splits;
+            const int sp = u - nt * args.splits;
+            const int b = it & 1;
+            const bool ok = wait_phase(acc_full_bar(b), (it >> 1) & 1, wc, kSiteEpilogueAccFull);
+            // all 128 epilogue threads stop together, so the named barriers below
+            // never wait for a thread that has left
+            if (named_barrier_or(1, kEpiThreads, !ok)) break;
+            tc_fence_after_sync();
+            const int n = nt * kSkBN + quarter * 32 + lane;  // this thread's output column
+            const bool n_ok = n < args.N;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * args.tmem_stride;
+            const float bias_n = (args.bias != nullptr && n_ok) ? __half2float(args.bias[n]) : 0.0f;
+            for (int c = 0; c < chunks; ++c) {
+                uint32_t r[16];
+                __syncwarp();  // tcgen05.ld is warp-collective; lanes diverged on the column mask
+                tmem_ld_32x32b_x16(taddr + c * 16, r);
+                tmem_ld_wait();
+                if (c == chunks - 1) {
+                    tc_fence_before_sync();
+                    mbar_arrive(acc_empty_bar(b));
+                }
+                if (!n_ok) continue;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int m = c * 16 + i;
+                    if (m >= args.M) break;
+                    const float v = __uint_as_float(r[i]);
+                    if (args.splits == 1)
+                        args.C[static_cast<int64_t>(m) * args.N + n] = __float2half_rn(epi_value(v, bias_n, args.gelu));
+                    else
+                        args.ws[(static_cast<int64_t>(sp) * args.M + m) * args.N + n] = v;
+                }
+            }
+            if (args.splits > 1) {
+                // publish this slice's partials, then count arrivals for column slice nt
+                __threadfence();
+                named_barrier_sync(1, kEpiThreads);
+                if (ept == 0) {
+                    const unsigned int prev = atomicAdd(args.counters + nt, 1u);
+                    *last_flag = (prev == static_cast<unsigned int>(args.splits - 1)) ? 1 : 0;
+                }
+                named_barrier_sync(1, kEpiThreads);
+                if (*last_flag) {
+                    __threadfence();
+                    if (n_ok) {
+                        for (int m = 0; m < args.M; ++m) {
+                            float s = 0.0f;
+                            for (int q = 0; q < args.splits; ++q)  // fixed order: deterministic
+                                s += __ldcg(args.ws + (static_cast<int64_t>(q) * args.M + m) * args.N + n);
+                            args.C[static_cast<int64_t>(m) * args.N + n] = __float2half_rn(epi_value(s, bias_n, args.gelu));
+                        }
+                    }
+                    if (ept == 0) atomicExch(args.counters + nt, 0u);
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, args.tmem_cols);
+    }
+}
+
+}  // namespace
+
+int split_stage_bytes(int m_pad) { return layout_for(m_pad, 1).stage_bytes; }
+
+int split_stages_for(int m_pad) {
+    int s = kSkSmemBudget / split_stage_bytes(m_pad);
+    if (s > 16) s = 16;
+    if (s < 2) s = 2;
+    return s;
+}
+
+int split_smem_bytes(int m_pad, int stages) { return layout_for(m_pad, stages).alloc; }
+
+cudaError_t launch_splitk(const SplitArgs& a, const CUtensorMap& tmB, const CUtensorMap& tmA, int grid,
+                          cudaStream_t stream) {
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_done[dev]) {
+        e = cudaFuncSetAttribute(splitk_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    const int smem = split_smem_bytes(a.m_pad, a.stages);
+    splitk_gemm_kernel<<<grid, kThreads, smem, stream>>>(tmB, tmA, a);
+    return cudaGetLastError();
+}
+
+}  // namespace tg

@@ -1,0 +1,358 @@
+// Persistent tiled GEMM C = epi(A @ B + bias) on the Blackwell tensor core.
+//
+// The tile program of "TileLang: writing LLM GPU kernels by thinking in tiles"
+// (section 3: a C tile per thread block, A/B tiles staged in shared memory,
+// T.gemm on the tiles, a pipelined K loop, the fragment written back) and of
+// "TileLang: you write the dataflow, the compiler owns the schedule" (section
+// "The tile program"), with the epilogue GELU(MatMul + Bias) applied on chip as
+// in "Designing high-performance GPU kernels with TileLang ...", section 3.
+//
+// GB300 design (not the pages' Ampere/Hopper schedule):
+//   * one CTA per SM, persistent over 128 x 256 output tiles in grouped order;
+//   * warp roles: a producer (one TMA-issuing lane, or four warps of ordinary
+//     loads when TMA cannot describe the operands), one MMA-issuing lane, and
+//     four epilogue warps;
+//   * a 4-stage ring of 48 KB stages (A 128x64 K-major, B 64x256 N-major, both
+//     in the 128-byte swizzled layout) guarded by full/empty mbarriers;
+//   * tcgen05.mma (M=128, N=256, K=16) accumulating in tensor memory; two
+//     256-column accumulators so the epilogue of one tile overlaps the
+//     mainloop of the next;
+//   * the epilogue reads TMEM with tcgen05.ld, adds bias, applies GELU in fp32,
+//     rounds once to binary16 and stores with masking for ragged M/N.
+#include "tg_device.cuh"
+#include "tg_internal.h"
+
+namespace tg {
+namespace {
+
+constexpr int kStageA = kBM * kBK * 2;  // 16 KB: 128 rows x 128 B
+constexpr int kStageB = kBK * kBN * 2;  // 32 KB: four 64x64 N-major boxes of 8 KB
+constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kRingBytes = kStages * kStageBytes;
+constexpr int kBoxB = kBK * 64 * 2;  // one 64 (k) x 64 (n) box, 8 KB
+constexpr int kTmemCols = 2 * kBN;   // two accumulators of 256 fp32 columns
+
+// Barrier block after the ring: full[S], empty[S], acc_full[2], acc_empty[2], drain.
+constexpr int kBarFull = kRingBytes;
+constexpr int kBarEmpty = kBarFull + 8 * kStages;
+constexpr int kBarAccFull = kBarEmpty + 8 * kStages;
+constexpr int kBarAccEmpty = kBarAccFull + 16;
+constexpr int kBarDrain = kBarAccEmpty + 16;
+constexpr int kTmemSlot = kBarDrain + 8;
+constexpr int kAbortSlot = kTmemSlot + 4;
+constexpr int kSmemUsed = kAbortSlot + 4;
+constexpr int kSmemAlloc = kSmemUsed + 1024;  // slack to align the ring to 1024 B
+
+// Operand descriptors: A is K-major (8-row groups 1024 B apart); B is N-major
+// with 64-column atoms 8 KB apart (one TMA box each) and 8-row K groups 1024 B
+// apart. One K=16 step advances A by 32 B within the swizzled row and B by 16
+// rows (2048 B).
+constexpr uint32_t kIdesc = idesc_f16_f32(kBM, kBN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+
+template <bool kTma>
+struct Roles {
+    static constexpr int kProducerWarps = kTma ? 1 : 4;
+    static constexpr int kMmaWarp = kProducerWarps;
+    static constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks, int group_m,
+                                            int& mb, int& nb) {
+    const int per_group = group_m * n_blocks;
+    const int g = tile / per_group;
+    const int first_m = g * group_m;
+    const int gsize = min(m_blocks - first_m, group_m);
+    const int local = tile - g * per_group;
+    mb = first_m + local % gsize;
+    nb = local / gsize;
+}
+
+// ---- ordinary-load staging into the same swizzled layout TMA produces ----
+
+template <int VEC>
+struct VecT;
+template <> struct VecT<8> { using T = uint4; };
+template <> struct VecT<2> { using T = uint32_t; };
+template <> struct VecT<1> { using T = uint16_t; };
+
+// A tile: rows m0..m0+127, k0..k0+63; byte (r, k) = r*128 + ((k/8) ^ (r%8))*16 + (k%8)*2.
+template <int VEC>
+__device__ __forceinline__ void stage_A(uint8_t* sA, const __half* __restrict__ A, int M, int K,
+                                        int m0, int k0, int ptid) {
+    using T = typename VecT<VEC>::T;
+    constexpr int kUnitsPerRow = kBK / VEC;
+    constexpr int kPerThread = kBM * kUnitsPerRow / 128;
+    constexpr int kBatch = kPerThread < 8 ? kPerThread : 8;
+#pragma unroll 1
+    for (int i0 = 0; i0 < kPerThread; i0 += kBatch) {
+        T val[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int u = ptid + 128 * (i0 + j);
+            const int r = u / kUnitsPerRow;
+            const int k = (u % kUnitsPerRow) * VEC;
+            const int gm = m0 + r, gk = k0 + k;
+            if (gm < M && gk < K)
+                val[j] = *reinterpret_cast<const T*>(A + static_cast<int64_t>(gm) * K + gk);
+            else
+                val[j] = T{};
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int u = ptid + 128 * (i0 + j);
+            const int r = u / kUnitsPerRow;
+            const int k = (u % kUnitsPerRow) * VEC;
+            const int off = r * 128 + ((((k * 2) >> 4) ^ (r & 7)) << 4) + ((k * 2) & 15);
+            *reinterpret_cast<T*>(sA + off) = val[j];
+        }
+    }
+}
+
+// B tile: k0..k0+63, n0..n0+255; byte (k, n) = (n/64)*8192 + k*128 + (((n%64)/8) ^ (k%8))*16 + (n%8)*2.
+template <int VEC>
+__device__ __forceinline__ void stage_B(uint8_t* sB, const __half* __restrict__ B, int N, int K,
+                                        int n0, int k0, int ptid) {
+    using T = typename VecT<VEC>::T;
+    constexpr int kUnitsPerRow = kBN / VEC;
+    constexpr int kPerThread = kBK * kUnitsPerRow / 128;
+    constexpr int kBatch = 8;
+#pragma unroll 1
+    for (int i0 = 0; i0 < kPerThread; i0 += kBatch) {
+        T val[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int u = ptid + 128 * (i0 + j);
+            const int k = u / kUnitsPerRow;
+            const int n = (u % kUnitsPerRow) * VEC;
+            const int gk = k0 + k, gn = n0 + n;
+            if (gk < K && gn < N)
+                val[j] = *reinterpret_cast<const T*>(B + static_cast<int64_t>(gk) * N + gn);
+            else
+                val[j] = T{};
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int u = ptid + 128 * (i0 + j);
+            const int k = u / kUnitsPerRow;
+            const int n = (u % kUnitsPerRow) * VEC;
+            const int nn = n & 63;
+            const int off = (n >> 6) * kBoxB + k * 128 + ((((nn * 2) >> 4) ^ (k & 7)) << 4) + ((nn * 2) & 15);
+            *reinterpret_cast<T*>(sB + off) = val[j];
+        }
+    }
+}
+
+template <bool kTma>
+__global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
+    tiled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const TiledArgs args) {
+    using R = Roles<kTma>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    auto full_bar = [&](int s) { return sbase + kBarFull + 8 * s; };
+    auto empty_bar = [&](int s) { return sbase + kBarEmpty + 8 * s; };
+    auto acc_full_bar = [&](int b) { return sbase + kBarAccFull + 8 * b; };
+    auto acc_empty_bar = [&](int b) { return sbase + kBarAccEmpty + 8 * b; };
+    const uint32_t drain_bar = sbase + kBarDrain;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortSlot);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), kTma ? 1 : R::kProducerWarps * 32);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full_bar(b), 1);
+            mbar_init(acc_empty_bar(b), 128);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (kTma && threadIdx.x == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == R::kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const WaitCtx wc{abort_flag, args.wd.status, args.wd.limit_ns};
+
+    if (warp < R::kProducerWarps) {
+        // ------------------------------------------------------------ producer
+        if constexpr (kTma) {
+            if (lane == 0) {
+                int stage = 0;
+                uint32_t phase = 0;
+                uint32_t issued_mask = 0, issued_parity = 0;
+                for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x) {
+                    int mb, nb;
+                    tile_coords(tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
+                    bool ok = true;
+                    for (int kb = 0; kb < args.num_kb; ++kb) {
+                        if (!wait_phase(empty_bar(stage), phase ^ 1, wc, kSiteProducerEmpty)) { ok = false; break; }
+                        const bool skip = args.wd.skip_first_arrive && tile == (int)blockIdx.x && kb == 0;
+                        if (!skip) {
+                            const uint32_t sA = sbase + stage * kStageBytes;
+                            const uint32_t sB = sA + kStageA;
+                            mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+                            tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, mb * kBM);
+#pragma unroll
+                            for (int j = 0; j < kBN / 64; ++j)
+                                tma_load_2d(sB + j * kBoxB, &tmB, full_bar(stage), nb * kBN + j * 64, kb * kBK);
+                            issued_mask |= 1u << stage;
+                            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                        }
+                        if (++stage == kStages) { stage = 0; phase ^= 1; }
+                    }
+                    if (!ok) break;
+                }
+                // let every copy this thread started land before the CTA can exit
+                for (int s = 0; s < kStages; ++s)
+                    if (issued_mask & (1u << s)) wait_phase_drain(full_bar(s), (issued_parity >> s) & 1, wc);
+            }
+        } else {
+            const int ptid = threadIdx.x;  // 0..127
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
+                bool ok = true;
+                for (int kb = 0; kb < args.num_kb; ++kb) {
+                    if (!wait_phase(empty_bar(stage), phase ^ 1, wc, kSiteProducerEmpty)) { ok = false; break; }
+                    uint8_t* sA = smem + stage * kStageBytes;
+                    uint8_t* sB = sA + kStageA;
+                    const int m0 = mb * kBM, n0 = nb * kBN, k0 = kb * kBK;
+                    if (args.a_vec == 8) stage_A<8>(sA, args.A, args.M, args.K, m0, k0, ptid);
+                    else if (args.a_vec == 2) stage_A<2>(sA, args.A, args.M, args.K, m0, k0, ptid);
+                    else stage_A<1>(sA, args.A, args.M, args.K, m0, k0, ptid);
+                    if (args.b_vec == 8) stage_B<8>(sB, args.B, args.N, args.K, n0, k0, ptid);
+                    else if (args.b_vec == 2) stage_B<2>(sB, args.B, args.N, args.K, n0, k0, ptid);
+                    else stage_B<1>(sB, args.B, args.N, args.K, n0, k0, ptid);
+                    fence_proxy_async_smem();
+                    mbar_arrive(full_bar(stage));
+                    if (++stage == kStages) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp == R::kMmaWarp) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x, ++it) {
+                const int b = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!wait_phase(acc_empty_bar(b), acc_phase ^ 1, wc, kSiteMmaAccEmpty)) break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * kBN;
+                for (int kb = 0; kb < args.num_kb; ++kb) {
+                    if (!wait_phase(full_bar(stage), phase, wc, kSiteMmaFull)) { ok = false; break; }
+                    tc_fence_after_sync();
+                    const uint32_t sA = sbase + stage * kStageBytes;
+                    const uint32_t sB = sA + kStageA;
+                    const uint64_t a_desc = smem_desc_sw128(sA, 16, 1024);
+                    const uint64_t b_desc = smem_desc_sw128(sB, kBoxB, 1024);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k)
+                        mma_f16(d_tmem, a_desc + (uint64_t)((k * 32) >> 4), b_desc + (uint64_t)((k * 2048) >> 4),
+                                kIdesc, (kb | k) != 0);
+                    mma_commit(empty_bar(stage));  // frees the stage once these MMAs finish
+                    if (++stage == kStages) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(acc_full_bar(b));  // accumulator b is complete
+            }
+            // all MMAs issued by this thread complete before TMEM is released
+            mma_commit(drain_bar);
+            wait_phase_drain(drain_bar, 0, wc);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
+        const int row_in_tile = quarter * 32 + lane;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++it) {
+            int mb, nb;
+            tile_coords(tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
+            const int b = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            if (!wait_phase(acc_full_bar(b), acc_phase, wc, kSiteEpilogueAccFull)) break;
+            tc_fence_after_sync();
+            const int row = mb * kBM + row_in_tile;
+            const int n0 = nb * kBN;
+            const int chunks = min(kBN / 32, (args.N - n0 + 31) / 32);
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kBN;
+            __half* crow = args.C + static_cast<int64_t>(row) * args.N;
+            for (int c = 0; c < chunks; ++c) {
+                uint32_t r[32];
+                __syncwarp();  // tcgen05.ld is warp-collective; lanes diverged on the row mask
+                tmem_ld_32x32b_x32(taddr + c * 32, r);
+                tmem_ld_wait();
+                if (c == chunks - 1) {
+                    tc_fence_before_sync();
+                    mbar_arrive(acc_empty_bar(b));  // TMEM buffer b may be overwritten
+                }
+                if (row < args.M)
+                    epilogue_row32(r, crow, args.bias, n0 + c * 32, args.N, args.gelu, args.c_vec, args.bias_vec);
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == R::kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <bool kTma>
+cudaError_t launch(const TiledArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB, int grid,
+                   cudaStream_t stream) {
+    using R = Roles<kTma>;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_done[dev]) {
+        e = cudaFuncSetAttribute(tiled_gemm_kernel<kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    CUtensorMap dummy{};
+    tiled_gemm_kernel<kTma><<<grid, R::kThreads, kSmemAlloc, stream>>>(tmA ? *tmA : dummy, tmB ? *tmB : dummy, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int tiled_smem_bytes(bool) { return kSmemAlloc; }
+int tiled_threads(bool tma) { return tma ? Roles<true>::kThreads : Roles<false>::kThreads; }
+
+cudaError_t launch_tiled_tma(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
+                             cudaStream_t stream) {
+    return launch<true>(a, &tmA, &tmB, grid, stream);
+}
+
+cudaError_t launch_tiled_lsu(const TiledArgs& a, int grid, cudaStream_t stream) {
+    return launch<false>(a, nullptr, nullptr, grid, stream);
+}
+
+}  // namespace tg

@@ -1,0 +1,410 @@
+// C-ABI front end: argument checks, kernel choice, TMA descriptors, per-stream
+// scratch, the device watchdog word, and launches. The operation and its
+// conventions are documented in include/tg_gemm.h.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+
+#include "tg_gemm.h"
+#include "tg_internal.h"
+
+namespace {
+
+using namespace tg;
+
+thread_local std::string t_last_error;
+std::atomic<uint64_t> g_watchdog_ns{2000000000ull};
+std::atomic<int> g_skip_first_arrive{0};
+
+// First expired wait of any kernel since the last tg_device_status (0 = none).
+__device__ int g_status_word;
+
+tg_status fail(tg_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return s;
+}
+
+tg_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(TG_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+struct Scratch {
+    float* ws = nullptr;
+    size_t ws_bytes = 0;
+    unsigned int* counters = nullptr;
+    size_t n_counters = 0;
+};
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    int* status_ptr = nullptr;
+    std::unordered_map<cudaStream_t, Scratch> scratch;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Current device, checked to be compute capability 10.3; fills the per-device
+// state on first use. Caller holds g_mu.
+tg_status current_device(int* dev_out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(TG_ERR_UNSUPPORTED_DEVICE, "device ordinal %d out of range", dev);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (major != 10 || minor != 3)
+            return fail(TG_ERR_UNSUPPORTED_DEVICE, "device %d is compute capability %d.%d; this library is built for 10.3 (sm_103a)",
+                        dev, major, minor);
+        if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status_ptr), g_status_word)) != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q{};
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        d.ready = true;
+    }
+    *dev_out = dev;
+    return TG_OK;
+}
+
+// Row-major [outer][inner] fp16 matrix, 128-byte-swizzled box of box_inner x box_outer,
+// out-of-bounds elements read as zero.
+tg_status make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                   uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %llu x %llu matrix", (int)r,
+                    (unsigned long long)outer, (unsigned long long)inner);
+    return TG_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
+    if (!a || !b || a_bytes <= 0 || b_bytes <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(b_bytes) && b0 < a0 + static_cast<uintptr_t>(a_bytes);
+}
+
+int vec_width(const void* p, int64_t ld) {
+    if (ld % 8 == 0 && aligned(p, 16)) return 8;
+    if (ld % 2 == 0 && aligned(p, 4)) return 2;
+    return 1;
+}
+
+Watchdog watchdog(const DeviceState& d) {
+    return Watchdog{d.status_ptr, g_watchdog_ns.load(), g_skip_first_arrive.load()};
+}
+
+// Split count for the skinny kernel: minimise (waves of units) x (K blocks per
+// unit), with a small charge for the extra reduction; ties keep fewer splits.
+int choose_splits(int n_tiles, int kb_total, int sm_count) {
+    int best_s = 1;
+    double best = 1e300;
+    const int smax = kb_total < kSkMaxSplits ? kb_total : kSkMaxSplits;
+    for (int s = 1; s <= smax; ++s) {
+        const int kbps = (kb_total + s - 1) / s;
+        const int s_eff = (kb_total + kbps - 1) / kbps;
+        if (s_eff != s) continue;
+        const long units = static_cast<long>(n_tiles) * s;
+        const long waves = (units + sm_count - 1) / sm_count;
+        const double cost = static_cast<double>(waves) * kbps * (s > 1 ? 1.02 : 1.0);
+        if (cost < best) {
+            best = cost;
+            best_s = s;
+        }
+    }
+    return best_s;
+}
+
+tg_status ensure_scratch(DeviceState& d, cudaStream_t stream, size_t ws_bytes, size_t n_counters, Scratch** out) {
+    Scratch& s = d.scratch[stream];
+    cudaError_t e;
+    if (s.ws_bytes < ws_bytes) {
+        if (s.ws) cudaFree(s.ws);
+        s.ws = nullptr;
+        s.ws_bytes = 0;
+        if ((e = cudaMalloc(reinterpret_cast<void**>(&s.ws), ws_bytes)) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(TG_ERR_NO_MEMORY, "split-K scratch of %zu bytes: %s", ws_bytes, cudaGetErrorString(e));
+        }
+        s.ws_bytes = ws_bytes;
+    }
+    if (s.n_counters < n_counters) {
+        if (s.counters) cudaFree(s.counters);
+        s.counters = nullptr;
+        s.n_counters = 0;
+        if ((e = cudaMalloc(reinterpret_cast<void**>(&s.counters), n_counters * sizeof(unsigned int))) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(TG_ERR_NO_MEMORY, "split-K counters: %s", cudaGetErrorString(e));
+        }
+        if ((e = cudaMemsetAsync(s.counters, 0, n_counters * sizeof(unsigned int), stream)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemsetAsync(counters)");
+        s.n_counters = n_counters;
+    }
+    *out = &s;
+    return TG_OK;
+}
+
+tg_status run_splitk(DeviceState& d, const __half* A, const __half* B, const __half* bias, __half* C, int M, int N,
+                     int K, int gelu, int split_k, cudaStream_t stream) {
+    SplitArgs a{};
+    a.A = A; a.B = B; a.bias = bias; a.C = C;
+    a.M = M; a.N = N; a.K = K; a.gelu = gelu;
+    a.m_pad = (M + 15) / 16 * 16;
+    a.tmem_stride = 16;
+    while (a.tmem_stride < a.m_pad) a.tmem_stride *= 2;
+    a.tmem_cols = 2 * a.tmem_stride < 32 ? 32 : 2 * a.tmem_stride;
+    a.stages = split_stages_for(a.m_pad);
+    a.n_tiles = (N + kSkBN - 1) / kSkBN;
+    a.kb_total = (K + kSkBK - 1) / kSkBK;
+    int s = split_k > 0 ? split_k : choose_splits(a.n_tiles, a.kb_total, d.sm_count);
+    if (s > a.kb_total) s = a.kb_total;
+    a.kb_per_split = (a.kb_total + s - 1) / s;
+    a.splits = (a.kb_total + a.kb_per_split - 1) / a.kb_per_split;
+    a.num_units = a.n_tiles * a.splits;
+    a.wd = watchdog(d);
+    if (a.splits > 1) {
+        Scratch* sc = nullptr;
+        tg_status st = ensure_scratch(d, stream, static_cast<size_t>(a.splits) * M * N * sizeof(float),
+                                      static_cast<size_t>(a.n_tiles), &sc);
+        if (st != TG_OK) return st;
+        a.ws = sc->ws;
+        a.counters = sc->counters;
+    }
+    CUtensorMap tmB, tmA;
+    tg_status st = make_map(&tmB, B, N, K, 64, kSkBK);
+    if (st != TG_OK) return st;
+    if ((st = make_map(&tmA, A, K, M, kSkBK, a.m_pad)) != TG_OK) return st;
+    const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
+    cudaError_t e = launch_splitk(a, tmB, tmA, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "split-K kernel launch");
+    return TG_OK;
+}
+
+tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, const __half* bias, __half* C, int M,
+                    int N, int K, int gelu, cudaStream_t stream) {
+    TiledArgs a{};
+    a.A = A; a.B = B; a.bias = bias; a.C = C;
+    a.M = M; a.N = N; a.K = K; a.gelu = gelu;
+    a.m_blocks = (M + kBM - 1) / kBM;
+    a.n_blocks = (N + kBN - 1) / kBN;
+    a.num_tiles = a.m_blocks * a.n_blocks;
+    a.num_kb = (K + kBK - 1) / kBK;
+    a.group_m = kGroupM;
+    a.c_vec = (N % 8 == 0 && aligned(C, 16)) ? 1 : 0;
+    a.bias_vec = (bias != nullptr && aligned(bias, 16)) ? 1 : 0;
+    a.a_vec = vec_width(A, K);
+    a.b_vec = vec_width(B, N);
+    a.wd = watchdog(d);
+    const int grid = a.num_tiles < d.sm_count ? a.num_tiles : d.sm_count;
+    cudaError_t e;
+    if (tma) {
+        CUtensorMap tmA, tmB;
+        tg_status st = make_map(&tmA, A, K, M, kBK, kBM);
+        if (st != TG_OK) return st;
+        if ((st = make_map(&tmB, B, N, K, 64, kBK)) != TG_OK) return st;
+        e = launch_tiled_tma(a, tmA, tmB, grid, stream);
+    } else {
+        e = launch_tiled_lsu(a, grid, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "tiled kernel launch");
+    return TG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tg_status tg_gemm_ex(const void* A, const void* B, const void* bias, void* C, int64_t M, int64_t N, int64_t K,
+                     int epilogue, int kernel, int split_k, tg_stream_t stream_) {
+    t_last_error.clear();
+    const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    // ---- arguments (host only, nothing enqueued on failure)
+    if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_GELU)
+        return fail(TG_ERR_INVALID_ARG, "epilogue must be TG_EPI_NONE (0) or TG_EPI_GELU (1), got %d", epilogue);
+    if (kernel < TG_KERNEL_AUTO || kernel > TG_KERNEL_SPLITK)
+        return fail(TG_ERR_INVALID_ARG, "unknown kernel %d", kernel);
+    const int64_t kMax = 0x7FFFFFFFll;
+    if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax)
+        return fail(TG_ERR_INVALID_ARG, "sizes must be in [0, 2^31): M=%lld N=%lld K=%lld", (long long)M,
+                    (long long)N, (long long)K);
+    if (split_k < 0 || split_k > kSkMaxSplits)
+        return fail(TG_ERR_INVALID_ARG, "split_k must be 0 (automatic) or 1..%d, got %d", kSkMaxSplits, split_k);
+    if (M == 0 || N == 0) return TG_OK;
+    if (C == nullptr) return fail(TG_ERR_INVALID_ARG, "C is NULL");
+    if (K > 0 && (A == nullptr || B == nullptr)) return fail(TG_ERR_INVALID_ARG, "A or B is NULL");
+    const int64_t c_bytes = M * N * 2;
+    if (overlaps(C, c_bytes, A, K > 0 ? M * K * 2 : 0) || overlaps(C, c_bytes, B, K > 0 ? K * N * 2 : 0) ||
+        overlaps(C, c_bytes, bias, bias ? N * 2 : 0))
+        return fail(TG_ERR_INVALID_ARG, "C overlaps an input");
+    const bool tma_ok = K % 8 == 0 && N % 8 == 0 && aligned(A, 16) && aligned(B, 16);
+    if (kernel == TG_KERNEL_TILED_TMA && !tma_ok)
+        return fail(TG_ERR_INVALID_ARG, "TG_KERNEL_TILED_TMA needs K %% 8 == 0, N %% 8 == 0 and 16-byte aligned A, B");
+    if (kernel == TG_KERNEL_SPLITK && (!tma_ok || M > kSkMaxM))
+        return fail(TG_ERR_INVALID_ARG, "TG_KERNEL_SPLITK needs M <= %d, K %% 8 == 0, N %% 8 == 0 and 16-byte aligned A, B",
+                    kSkMaxM);
+    if (split_k > 0 && kernel != TG_KERNEL_SPLITK && kernel != TG_KERNEL_AUTO)
+        return fail(TG_ERR_INVALID_ARG, "split_k applies to TG_KERNEL_SPLITK only");
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    tg_status st = current_device(&dev);
+    if (st != TG_OK) return st;
+    DeviceState& d = g_dev[dev];
+    const __half* a = static_cast<const __half*>(A);
+    const __half* b = static_cast<const __half*>(B);
+    const __half* bi = static_cast<const __half*>(bias);
+    __half* c = static_cast<__half*>(C);
+    const int gelu = epilogue == TG_EPI_GELU ? 1 : 0;
+
+    if (K == 0) {
+        cudaError_t e = launch_fill(bi, c, M, N, gelu, d.sm_count, stream);
+        return e == cudaSuccess ? TG_OK : cuda_fail(e, "fill kernel launch");
+    }
+    int k = kernel;
+    if (k == TG_KERNEL_AUTO) k = (tma_ok && M <= kSkMaxM) ? TG_KERNEL_SPLITK : (tma_ok ? TG_KERNEL_TILED_TMA : TG_KERNEL_TILED_LSU);
+    if (k == TG_KERNEL_SPLITK)
+        return run_splitk(d, a, b, bi, c, (int)M, (int)N, (int)K, gelu, split_k, stream);
+    return run_tiled(d, k == TG_KERNEL_TILED_TMA, a, b, bi, c, (int)M, (int)N, (int)K, gelu, stream);
+}
+
+tg_status tg_gemm(const void* A, const void* B, const void* bias, void* C, int64_t M, int64_t N, int64_t K,
+                  int epilogue, tg_stream_t stream) {
+    return tg_gemm_ex(A, B, bias, C, M, N, K, epilogue, TG_KERNEL_AUTO, 0, stream);
+}
+
+tg_status tg_gemm_staged(const void* hA, const void* hB, const void* hbias, void* hC, void* dA, void* dB, void* dbias,
+                         void* dC, int64_t M, int64_t N, int64_t K, int epilogue, tg_stream_t stream_) {
+    t_last_error.clear();
+    const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if ((hbias == nullptr) != (dbias == nullptr))
+        return fail(TG_ERR_INVALID_ARG, "hbias and dbias must both be NULL or both be set");
+    if (M < 0 || N < 0 || K < 0) return fail(TG_ERR_INVALID_ARG, "negative size");
+    if (M > 0 && N > 0 && (hC == nullptr || dC == nullptr)) return fail(TG_ERR_INVALID_ARG, "C buffer is NULL");
+    if (M > 0 && N > 0 && K > 0 && (!hA || !hB || !dA || !dB)) return fail(TG_ERR_INVALID_ARG, "A or B buffer is NULL");
+    cudaError_t e;
+    if (M > 0 && N > 0 && K > 0) {
+        if ((e = cudaMemcpyAsync(dA, hA, M * K * 2, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+            return cuda_fail(e, "copy A to device");
+        if ((e = cudaMemcpyAsync(dB, hB, K * N * 2, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+            return cuda_fail(e, "copy B to device");
+    }
+    if (hbias && N > 0 && (e = cudaMemcpyAsync(dbias, hbias, N * 2, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+        return cuda_fail(e, "copy bias to device");
+    tg_status st = tg_gemm(dA, dB, dbias, dC, M, N, K, epilogue, stream_);
+    if (st != TG_OK) return st;
+    if (M > 0 && N > 0 && (e = cudaMemcpyAsync(hC, dC, M * N * 2, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+        return cuda_fail(e, "copy C to host");
+    return TG_OK;
+}
+
+tg_status tg_device_status(tg_stream_t stream_, int* where) {
+    t_last_error.clear();
+    if (where) *where = 0;
+    const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    tg_status st = current_device(&dev);
+    if (st != TG_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int v = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof v)) != cudaSuccess)
+        return cuda_fail(e, "read status word");
+    if (v == 0) return TG_OK;
+    const int zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero)) != cudaSuccess)
+        return cuda_fail(e, "clear status word");
+    // a CTA that gave up may have left split-K arrival counters non-zero
+    for (auto& kv : g_dev[dev].scratch)
+        if (kv.second.counters) cudaMemset(kv.second.counters, 0, kv.second.n_counters * sizeof(unsigned int));
+    cudaDeviceSynchronize();
+    if (where) *where = v;
+    return fail(TG_ERR_TIMEOUT, "a kernel wait expired (site %d)", v);
+}
+
+tg_status tg_set_watchdog_ns(uint64_t ns) {
+    g_watchdog_ns.store(ns == 0 ? 2000000000ull : ns);
+    return TG_OK;
+}
+
+tg_status tg_debug_skip_first_arrive(int on) {
+    g_skip_first_arrive.store(on ? 1 : 0);
+    return TG_OK;
+}
+
+const char* tg_status_string(int s) {
+    switch (s) {
+        case TG_OK: return "TG_OK";
+        case TG_ERR_INVALID_ARG: return "TG_ERR_INVALID_ARG: invalid argument";
+        case TG_ERR_UNSUPPORTED_DEVICE: return "TG_ERR_UNSUPPORTED_DEVICE: not a compute capability 10.3 device";
+        case TG_ERR_CUDA: return "TG_ERR_CUDA: a CUDA call failed";
+        case TG_ERR_TIMEOUT: return "TG_ERR_TIMEOUT: a kernel wait expired";
+        case TG_ERR_NO_MEMORY: return "TG_ERR_NO_MEMORY: scratch allocation failed";
+        default: return "unknown tg_status";
+    }
+}
+
+const char* tg_last_error(void) { return t_last_error.c_str(); }
+
+int tg_version(void) { return 10000; }
+
+int64_t tg_ring_bytes(int kernel) {
+    switch (kernel) {
+        case TG_KERNEL_TILED_TMA:
+        case TG_KERNEL_TILED_LSU:
+            return static_cast<int64_t>(kStages) * (kBM * kBK + kBK * kBN) * 2;
+        case TG_KERNEL_SPLITK:
+            return static_cast<int64_t>(split_stages_for(16)) * (16 * kSkBK + kSkBK * kSkBN) * 2;
+        default:
+            return -1;
+    }
+}
+
+void tg_shutdown(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (auto& d : g_dev) {
+        for (auto& kv : d.scratch) {
+            if (kv.second.ws) cudaFree(kv.second.ws);
+            if (kv.second.counters) cudaFree(kv.second.counters);
+        }
+        d.scratch.clear();
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,91 @@
+// Internal interface between the C-ABI front end (tg_api.cu) and the kernel
+// translation units. Not installed; not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace tg {
+
+// ---- tiled kernel geometry: one CTA computes a 128 x 256 tile of C, walking K
+// in 64-wide blocks through a 4-deep ring of shared-memory stages.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kGroupM = 16;  // tile rows per rasterisation group (L2 reuse)
+
+// ---- split-K (swap-AB) kernel geometry: one work unit is a 128-column slice of
+// N times a range of 64-wide K blocks; M (<= 128) is the MMA's N, padded to 16.
+constexpr int kSkBN = 128;
+constexpr int kSkBK = 64;
+constexpr int kSkMaxM = 128;
+constexpr int kSkMaxSplits = 64;
+constexpr int kSkSmemBudget = 200 * 1024;  // operand ring budget per CTA
+
+// Watchdog plumbing handed to every kernel: where to record the first wait that
+// expired, the limit, and the test hook that withholds one producer arrival.
+struct Watchdog {
+    int* status;          // device word; 0 = ok, else the code of the expired wait
+    uint64_t limit_ns;
+    int skip_first_arrive;
+};
+
+// Codes recorded in the status word (which wait expired first).
+enum WaitSite : int {
+    kSiteProducerEmpty = 1,
+    kSiteMmaFull = 2,
+    kSiteMmaAccEmpty = 3,
+    kSiteEpilogueAccFull = 4,
+    kSiteDrain = 5,
+};
+
+struct TiledArgs {
+    const __half* A;
+    const __half* B;
+    const __half* bias;  // may be null
+    __half* C;
+    int M, N, K;
+    int gelu;
+    int m_blocks, n_blocks, num_tiles, num_kb, group_m;
+    int c_vec;     // C rows start 16-byte aligned and N % 8 == 0: 16-byte stores
+    int bias_vec;  // bias 16-byte aligned: 16-byte loads
+    int a_vec;     // ordinary-load staging width for A in elements: 8, 2 or 1
+    int b_vec;     // same for B
+    Watchdog wd;
+};
+
+struct SplitArgs {
+    const __half* A;
+    const __half* B;
+    const __half* bias;
+    __half* C;
+    int M, N, K;
+    int gelu;
+    int m_pad;         // MMA N: M rounded up to a multiple of 16 (16..128)
+    int tmem_stride;   // TMEM columns between the two accumulator buffers (pow2 >= m_pad)
+    int tmem_cols;     // TMEM columns allocated (2 * tmem_stride, >= 32)
+    int stages;        // ring depth
+    int n_tiles, kb_total, kb_per_split, splits, num_units;
+    float* ws;               // splits * M * N fp32 partial sums (splits > 1)
+    unsigned int* counters;  // n_tiles arrival counters, zero between launches
+    Watchdog wd;
+};
+
+int split_stage_bytes(int m_pad);
+int split_smem_bytes(int m_pad, int stages);
+int split_stages_for(int m_pad);
+int tiled_smem_bytes(bool tma);
+int tiled_threads(bool tma);
+
+cudaError_t launch_tiled_tma(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                             int grid, cudaStream_t stream);
+cudaError_t launch_tiled_lsu(const TiledArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_splitk(const SplitArgs& a, const CUtensorMap& tmB, const CUtensorMap& tmA,
+                          int grid, cudaStream_t stream);
+cudaError_t launch_fill(const __half* bias, __half* C, int64_t M, int64_t N, int gelu,
+                        int sm_count, cudaStream_t stream);
+
+}  // namespace tg
