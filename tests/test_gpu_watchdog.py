@@ -1,0 +1,59 @@
+"""The kernels' bounded waits: a withheld producer arrival must end the call
+with TG_ERR_TIMEOUT (reported by tg_device_status) instead of hanging, and the
+device must stay usable for the next call.
+
+The test hook makes the tiled kernel's TMA producer skip its arrival on the
+first pipeline stage of every CTA, so the MMA thread's wait on that stage can
+never complete; its bounded wait expires, the CTA's other roles see the abort
+flag, in-flight copies are drained, tensor memory is freed and the kernel
+returns. Nothing faults or traps."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import tiled_tensor_core_tcgen05_gb300 as m
+    torch.cuda.set_device(0)
+    return m
+
+
+def test_withheld_arrival_times_out_and_recovers(tg):
+    w = workloads.custom(256, 512, 256, seed=31, dist=workloads.Dist("int", -2, 2))
+    A, B, _ = w.inputs()
+    dA, dB = A.cuda(), B.cuda()
+    assert tg.tg_device_status(None) == (tg.OK, 0)
+    tg.tg_set_watchdog_ns(20_000_000)  # 20 ms
+    tg.tg_debug_skip_first_arrive(True)
+    try:
+        tg.gemm(dA, dB, kernel=tg.KERNEL_TILED_TMA)
+        st, where = tg.tg_device_status(None)
+    finally:
+        tg.tg_debug_skip_first_arrive(False)
+        tg.tg_set_watchdog_ns(0)
+    assert st == tg.ERR_TIMEOUT
+    assert where == 2  # the MMA thread's wait on a full stage expired first
+    # the status word was cleared and the device still computes correctly
+    assert tg.tg_device_status(None) == (tg.OK, 0)
+    C = tg.gemm(dA, dB, kernel=tg.KERNEL_TILED_TMA)
+    ref = oracle.gemm(A, B).view(np.uint16)
+    assert np.array_equal(C.cpu().numpy().view(np.uint16), ref)
+    assert tg.tg_device_status(None) == (tg.OK, 0)
+
+
+def test_hook_off_by_default(tg):
+    w = workloads.custom(128, 256, 128, seed=32, dist=workloads.Dist("int", -2, 2))
+    A, B, _ = w.inputs()
+    C = tg.gemm(A.cuda(), B.cuda(), kernel=tg.KERNEL_TILED_TMA)
+    assert np.array_equal(C.cpu().numpy().view(np.uint16), oracle.gemm(A, B).view(np.uint16))
+    assert tg.tg_device_status(None) == (tg.OK, 0)

@@ -130,9 +130,14 @@ Watchdog watchdog(const DeviceState& d) {
     return Watchdog{d.status_ptr, g_watchdog_ns.load(), g_skip_first_arrive.load()};
 }
 
-// Split count for the skinny kernel: minimise (waves of units) x (K blocks per
-// unit), with a small charge for the extra reduction; ties keep fewer splits.
+// Split count for the skinny kernel. Time per CTA is modelled in units of one
+// K block's transfer: each work unit costs its K blocks plus a fixed charge
+// for refilling the pipeline and running its epilogue, and every split beyond
+// the first adds the partial-sum traffic of the final reduction. Minimise
+// (waves of units) x (cost per unit) + reduction; ties keep fewer splits.
 int choose_splits(int n_tiles, int kb_total, int sm_count) {
+    constexpr double kUnitOverhead = 6.0;   // pipeline refill + epilogue, in K blocks
+    constexpr double kReducePerSplit = 1.0; // partial tile written and read back
     int best_s = 1;
     double best = 1e300;
     const int smax = kb_total < kSkMaxSplits ? kb_total : kSkMaxSplits;
@@ -142,7 +147,7 @@ int choose_splits(int n_tiles, int kb_total, int sm_count) {
         if (s_eff != s) continue;
         const long units = static_cast<long>(n_tiles) * s;
         const long waves = (units + sm_count - 1) / sm_count;
-        const double cost = static_cast<double>(waves) * kbps * (s > 1 ? 1.02 : 1.0);
+        const double cost = static_cast<double>(waves) * (kbps + kUnitOverhead) + kReducePerSplit * (s - 1);
         if (cost < best) {
             best = cost;
             best_s = s;
