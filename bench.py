@@ -155,7 +155,10 @@ def barrier(pg):
 
 # ------------------------------------------------------------------ GPU arm
 
-def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sampler=None):
+KERNELS = {"auto": 0, "tiled": 1, "lsu": 2, "splitk": 3, "pair": 4}
+
+
+def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sampler=None, kernel: int = 0):
     """Time `steps` calls of tg_gemm on device-resident inputs. Returns the timed
     region (ms, max over ranks) and per-launch kernel durations."""
     import torch
@@ -168,8 +171,14 @@ def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sam
     args = (dA.data_ptr(), dB.data_ptr(), db.data_ptr() if db is not None else None, dC.data_ptr(),
             w.M, w.N, w.K, int(w.gelu))
     flush = torch.empty(flush_bytes, dtype=torch.uint8, device="cuda") if flush_bytes else None
+    def call():
+        if kernel:
+            tg.tg_gemm_ex(*args, kernel, 0, sh)
+        else:
+            tg.tg_gemm(*args, sh)
+
     for _ in range(warmup):
-        tg.tg_gemm(*args, sh)
+        call()
     torch.cuda.synchronize()
     st, where = tg.tg_device_status(None)
     if st != tg.OK:
@@ -187,7 +196,7 @@ def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sam
         if flush is not None:
             flush.zero_()  # evict the (L2-sized) inputs between steps
         starts[i].record(stream)
-        tg.tg_gemm(*args, sh)
+        call()
         ends[i].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -285,7 +294,7 @@ def run_gpu(args):
     main = workloads.BY_NAME[args.workload]
     sampler = ClockSampler(local) if rank == 0 else None
     res = time_workload(tg, main, args.steps, args.warmup, 0 if main.bytes() > 2 * l2 else 2 * l2 + (1 << 20),
-                        pg=pg, sampler=sampler)
+                        pg=pg, sampler=sampler, kernel=KERNELS[args.kernel])
     ms_per_step = res["region_ms"] / args.steps
     avg_launch = res["kernel_ms"] / args.steps
     value = world * main.flops() / (ms_per_step / 1e3) / 1e12
@@ -298,7 +307,8 @@ def run_gpu(args):
                    "epilogue": ("bias+" if main.has_bias else "") + ("gelu" if main.gelu else "none"),
                    "l2": (f"inputs larger than L2 ({main.bytes() / 1e6:.0f} MB vs {l2 / 1e6:.0f} MB)"
                           if main.bytes() > 2 * l2 else "L2 flushed between steps"),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "kernel": args.kernel},
         "gpu_launches": args.steps,
     }
     out["roofline"] = roofline_entry(main, avg_launch, pk, pk_kind, "tensor", recorded_traffic(main.name))
@@ -382,6 +392,8 @@ def main():
     ap.add_argument("--impl", choices=["tg", "reference"], default="tg")
     ap.add_argument("--workload", default="square_8192")
     ap.add_argument("--only-main", action="store_true", help="time the headline workload only")
+    ap.add_argument("--kernel", choices=sorted(KERNELS), default="auto",
+                    help="pin the kernel of the headline workload (profiling); default: the library's choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--ref-budget-s", type=float, default=60.0)

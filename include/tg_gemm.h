@@ -72,9 +72,12 @@ typedef enum {
                                 Needs K % 8 == 0, N % 8 == 0, A and B 16-byte aligned. */
     TG_KERNEL_TILED_LSU = 2, /* the same tiles with operands staged by ordinary loads;
                                 any shape and alignment */
-    TG_KERNEL_SPLITK = 3     /* skinny M <= 128: computes C^T = B^T A^T so N fills the
+    TG_KERNEL_SPLITK = 3,    /* skinny M <= 128: computes C^T = B^T A^T so N fills the
                                 128-row MMA, with K split across CTAs; same TMA needs
                                 as TG_KERNEL_TILED_TMA */
+    TG_KERNEL_TILED_PAIR = 4 /* 256x256 tiles on pairs of SMs (two-CTA clusters sharing
+                                one tensor-core MMA); same TMA needs as
+                                TG_KERNEL_TILED_TMA */
 } tg_kernel;
 
 /*
@@ -84,8 +87,10 @@ typedef enum {
  * empty sum is 0, so C = epi(bias) (or epi(0) without bias). `epilogue` is a
  * tg_epilogue value. A, B may be NULL only when the product is empty.
  *
- * Kernel choice: M <= 128 with TMA-compatible operands -> TG_KERNEL_SPLITK;
- * otherwise TMA-compatible -> TG_KERNEL_TILED_TMA; otherwise TG_KERNEL_TILED_LSU.
+ * Kernel choice (TMA-compatible means K % 8 == 0, N % 8 == 0 and 16-byte
+ * aligned A and B): not TMA-compatible -> TG_KERNEL_TILED_LSU; M <= 128 ->
+ * TG_KERNEL_SPLITK; at least one 256x256 tile per pair of SMs ->
+ * TG_KERNEL_TILED_PAIR; otherwise TG_KERNEL_TILED_TMA.
  */
 tg_status tg_gemm(const void* A, const void* B, const void* bias, void* C,
                   int64_t M, int64_t N, int64_t K, int epilogue, tg_stream_t stream);

@@ -49,8 +49,9 @@ def test_ring_bytes_follow_the_tile_footprint_formula(tg):
     # tiled kernels: 4 stages of a 128x64 A tile and a 64x256 B tile, fp16
     assert tg.tg_ring_bytes(tg.KERNEL_TILED_TMA) == tg.ring_bytes(128, 256, 64, 4) == 196608
     assert tg.tg_ring_bytes(tg.KERNEL_TILED_LSU) == tg.ring_bytes(128, 256, 64, 4)
-    assert tg.tg_ring_bytes(tg.KERNEL_SPLITK) % tg.ring_bytes(16, 128, 64, 1) == 0
+    assert tg.tg_ring_bytes(tg.KERNEL_SPLITK) % tg.ring_bytes(16, 256, 64, 1) == 0
     assert tg.tg_ring_bytes(tg.KERNEL_SPLITK) <= 227 * 1024
+    assert tg.tg_ring_bytes(tg.KERNEL_TILED_PAIR) == tg.ring_bytes(128, 128, 64, 6)
     assert tg.tg_ring_bytes(42) == -1
 
 
@@ -75,6 +76,7 @@ def test_footprint_worked_example(tg):
     (dict(M=-1), "sizes"),
     (dict(K=2 ** 31), "sizes"),
     (dict(kernel=9), "kernel"),
+    (dict(kernel=4, N=20), "TG_KERNEL_TILED_PAIR"),
     (dict(split_k=65), "split_k"),
     (dict(split_k=-1), "split_k"),
     (dict(C=0), "C is NULL"),

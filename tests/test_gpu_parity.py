@@ -61,6 +61,7 @@ def _kernels_for(tg, M, N, K):
     ks = [tg.KERNEL_AUTO, tg.KERNEL_TILED_LSU]
     if K % 8 == 0 and N % 8 == 0:
         ks.append(tg.KERNEL_TILED_TMA)
+        ks.append(tg.KERNEL_TILED_PAIR)
         if M <= 128:
             ks.append(tg.KERNEL_SPLITK)
     return ks

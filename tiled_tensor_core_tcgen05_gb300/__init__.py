@@ -21,7 +21,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libtg_gemm.so")
 
 EPI_NONE, EPI_GELU = 0, 1
-KERNEL_AUTO, KERNEL_TILED_TMA, KERNEL_TILED_LSU, KERNEL_SPLITK = 0, 1, 2, 3
+KERNEL_AUTO, KERNEL_TILED_TMA, KERNEL_TILED_LSU, KERNEL_SPLITK, KERNEL_TILED_PAIR = 0, 1, 2, 3, 4
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NO_MEMORY = range(6)
 
 # every symbol include/tg_gemm.h declares

@@ -6,8 +6,11 @@
 // 128-row side of the tensor-core MMA and M (padded to 16) is the MMA's N:
 //   MMA operand "A" = a 128 (n) x 64 (k) slice of B, which is N-major in memory;
 //   MMA operand "B" = a 64 (k) x M slice of A^T, i.e. A's rows, K-major.
-// One work unit is (128-column slice of N, range of K blocks); units are
-// spread over a persistent grid. With more than one K slice, each unit
+// One work unit is (256-column slice of N, range of K blocks): two such MMAs
+// per K step, into two TMEM accumulators, so each stage streams 512 contiguous
+// bytes of every B row it touches. Units are spread over a persistent grid,
+// slice-major, so CTAs running side by side read neighbouring columns of the
+// same rows of B. With more than one K slice, each unit
 // writes an fp32 partial tile to a scratch buffer; the last unit of a column
 // slice to finish (an arrival counter) adds the partials in slice order
 // 0, 1, ..., applies bias and GELU and writes C, so results do not depend on
@@ -24,8 +27,9 @@
 namespace tg {
 namespace {
 
-constexpr int kBoxB = kSkBK * 64 * 2;       // 64 (k) x 64 (n) N-major box, 8 KB
-constexpr int kStageBBytes = 2 * kBoxB;     // 128 columns of N
+constexpr int kBoxB = kSkBK * 64 * 2;          // 64 (k) x 64 (n) N-major box, 8 KB
+constexpr int kHalfBytes = 2 * kBoxB;          // one 128-column MMA half
+constexpr int kStageBBytes = kSkHalves * kHalfBytes;
 constexpr int kThreads = 6 * 32;            // producer, MMA, 4 epilogue warps
 constexpr int kEpiThreads = 128;
 
@@ -108,8 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x) {
-                const int nt = u / args.splits;
-                const int sp = u - nt * args.splits;
+                const int sp = u / args.n_tiles;
+                const int nt = u - sp * args.n_tiles;
                 const int kb0 = sp * args.kb_per_split;
                 const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -117,8 +121,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sB = sbase + stage * L.stage_bytes;
                     const uint32_t sA = sB + kStageBBytes;
                     mbar_arrive_expect_tx(full_bar(stage), stage_tx);
-                    tma_load_2d_hint(sB, &tmB, full_bar(stage), nt * kSkBN, kb * kSkBK, pol_stream);
-                    tma_load_2d_hint(sB + kBoxB, &tmB, full_bar(stage), nt * kSkBN + 64, kb * kSkBK, pol_stream);
+#pragma unroll
+                    for (int j = 0; j < kStageBBytes / kBoxB; ++j)
+                        tma_load_2d_hint(sB + j * kBoxB, &tmB, full_bar(stage), nt * kSkBN + j * 64, kb * kSkBK,
+                                         pol_stream);
                     tma_load_2d_hint(sA, &tmA, full_bar(stage), kb * kSkBK, 0, pol_keep);
                     issued_mask |= 1ull << stage;
                     issued_parity = (issued_parity & ~(1ull << stage)) | (uint64_t(phase) << stage);
@@ -137,25 +143,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x, ++it) {
-                const int nt = u / args.splits;
-                const int sp = u - nt * args.splits;
+                const int sp = u / args.n_tiles;
                 const int kb0 = sp * args.kb_per_split;
                 const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
                 const int b = it & 1;
                 if (!wait_phase(acc_empty_bar(b), ((it >> 1) & 1) ^ 1, wc, kSiteMmaAccEmpty)) break;
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + b * args.tmem_stride;
+                const uint32_t d_tmem = tmem_base + b * kSkHalves * args.tmem_stride;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase(full_bar(stage), phase, wc, kSiteMmaFull)) { ok = false; break; }
                     tc_fence_after_sync();
                     const uint32_t sB = sbase + stage * L.stage_bytes;
                     const uint32_t sA = sB + kStageBBytes;
-                    const uint64_t a_desc = smem_desc_sw128(sB, kBoxB, 1024);  // N-major slice of B
-                    const uint64_t b_desc = smem_desc_sw128(sA, 16, 1024);     // K-major rows of A
+                    const uint64_t b_desc = smem_desc_sw128(sA, 16, 1024);  // K-major rows of A
 #pragma unroll
-                    for (int k = 0; k < kSkBK / 16; ++k)
-                        mma_f16(d_tmem, a_desc + (uint64_t)((k * 2048) >> 4), b_desc + (uint64_t)((k * 32) >> 4),
-                                idesc, (kb != kb0) || (k != 0));
+                    for (int h = 0; h < kSkHalves; ++h) {
+                        const uint64_t a_desc = smem_desc_sw128(sB + h * kHalfBytes, kBoxB, 1024);  // N-major B
+#pragma unroll
+                        for (int k = 0; k < kSkBK / 16; ++k)
+                            mma_f16(d_tmem + h * args.tmem_stride, a_desc + (uint64_t)((k * 2048) >> 4),
+                                    b_desc + (uint64_t)((k * 32) >> 4), idesc, (kb != kb0) || (k != 0));
+                    }
                     mma_commit(empty_bar(stage));
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
@@ -173,37 +181,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int chunks = args.m_pad / 16;
         int it = 0;
         for (int u = blockIdx.x; u < args.num_units; u += gridDim.x, ++it) {
-            const int nt = u / args.splits;
-            const int sp = u - nt * args.splits;
+            const int sp = u / args.n_tiles;
+            const int nt = u - sp * args.n_tiles;
             const int b = it & 1;
             const bool ok = wait_phase(acc_full_bar(b), (it >> 1) & 1, wc, kSiteEpilogueAccFull);
             // all 128 epilogue threads stop together, so the named barriers below
             // never wait for a thread that has left
             if (named_barrier_or(1, kEpiThreads, !ok)) break;
             tc_fence_after_sync();
-            const int n = nt * kSkBN + quarter * 32 + lane;  // this thread's output column
-            const bool n_ok = n < args.N;
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * args.tmem_stride;
-            const float bias_n = (args.bias != nullptr && n_ok) ? __half2float(args.bias[n]) : 0.0f;
-            for (int c = 0; c < chunks; ++c) {
-                uint32_t r[16];
-                __syncwarp();  // tcgen05.ld is warp-collective; lanes diverged on the column mask
-                tmem_ld_32x32b_x16(taddr + c * 16, r);
-                tmem_ld_wait();
-                if (c == chunks - 1) {
-                    tc_fence_before_sync();
-                    mbar_arrive(acc_empty_bar(b));
-                }
-                if (!n_ok) continue;
+#pragma unroll 1
+            for (int h = 0; h < kSkHalves; ++h) {
+                const int n = nt * kSkBN + h * 128 + quarter * 32 + lane;  // this thread's output column
+                const bool n_ok = n < args.N;
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       (b * kSkHalves + h) * args.tmem_stride;
+                const float bias_n = (args.bias != nullptr && n_ok) ? __half2float(args.bias[n]) : 0.0f;
+                for (int c = 0; c < chunks; ++c) {
+                    uint32_t r[16];
+                    __syncwarp();  // tcgen05.ld is warp-collective; lanes diverged on the column mask
+                    tmem_ld_32x32b_x16(taddr + c * 16, r);
+                    tmem_ld_wait();
+                    if (h == kSkHalves - 1 && c == chunks - 1) {
+                        tc_fence_before_sync();
+                        mbar_arrive(acc_empty_bar(b));  // both accumulators of buffer b are read
+                    }
+                    if (!n_ok) continue;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int m = c * 16 + i;
-                    if (m >= args.M) break;
-                    const float v = __uint_as_float(r[i]);
-                    if (args.splits == 1)
-                        args.C[static_cast<int64_t>(m) * args.N + n] = __float2half_rn(epi_value(v, bias_n, args.gelu));
-                    else
-                        args.ws[(static_cast<int64_t>(sp) * args.M + m) * args.N + n] = v;
+                    for (int i = 0; i < 16; ++i) {
+                        const int m = c * 16 + i;
+                        if (m >= args.M) break;
+                        const float v = __uint_as_float(r[i]);
+                        if (args.splits == 1)
+                            args.C[static_cast<int64_t>(m) * args.N + n] = __float2half_rn(epi_value(v, bias_n, args.gelu));
+                        else
+                            args.ws[(static_cast<int64_t>(sp) * args.M + m) * args.N + n] = v;
+                    }
                 }
             }
             if (args.splits > 1) {
@@ -217,7 +229,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_barrier_sync(1, kEpiThreads);
                 if (*last_flag) {
                     __threadfence();
-                    if (n_ok) {
+#pragma unroll 1
+                    for (int h = 0; h < kSkHalves; ++h) {
+                        const int n = nt * kSkBN + h * 128 + quarter * 32 + lane;
+                        if (n >= args.N) continue;
+                        const float bias_n = args.bias != nullptr ? __half2float(args.bias[n]) : 0.0f;
                         for (int m = 0; m < args.M; ++m) {
                             float s = 0.0f;
                             for (int q = 0; q < args.splits; ++q)  // fixed order: deterministic

@@ -1,0 +1,269 @@
+// Persistent tiled GEMM C = epi(A @ B + bias) on CTA pairs: each cluster of two
+// CTAs (two SMs) computes a 256 x 256 tile of C with the pair form of the
+// Blackwell tensor-core MMA.
+//
+// Same computation as the single-CTA kernel (the tile program of "TileLang:
+// writing LLM GPU kernels by thinking in tiles", section 3, with the
+// GELU(MatMul + Bias) epilogue of "Designing high-performance GPU kernels with
+// TileLang ...", section 3). What the pair buys on GB300: one MMA of
+// M=256 x N=256 x K=16 reads A's 256 rows from the two SMs (128 each) and B's
+// 256 columns from the two SMs (128 each), so per SM and per MMA the shared
+// memory delivers 8 KB instead of the 12 KB a single-CTA 128 x 256 MMA needs,
+// and each SM streams half as much of B from L2.
+//
+// Roles, in both CTAs: warp 0 lane 0 loads this CTA's 128 rows of A and 128
+// columns of B for each K block by TMA into its own 6-stage ring; the copies
+// of BOTH CTAs complete on the even CTA's "full" barrier (the pair form of the
+// TMA copy), which the even CTA arms with the bytes of both halves. Warp 1
+// lane 0 of the even CTA issues the pair MMAs; warps 2..5 are the epilogue,
+// each CTA reading its own 128 accumulator rows from its own tensor memory.
+// MMA completion is committed to both CTAs at once (multicast), freeing the
+// stage in both rings and publishing the accumulator to both epilogues; both
+// epilogues release the accumulator to the issuer with one arrive per warp.
+#include "tg_device.cuh"
+#include "tg_internal.h"
+
+#ifndef TG_PAIR_ACC_BUFS
+#define TG_PAIR_ACC_BUFS 2
+#endif
+
+namespace tg {
+namespace {
+
+constexpr int kHalfM = kBM;                 // 128 rows of A per CTA
+constexpr int kHalfN = kBN / 2;             // 128 columns of B per CTA
+constexpr int kPairBM = 2 * kHalfM;         // 256 rows of C per cluster tile
+constexpr int kPairBN = kBN;                // 256 columns of C per cluster tile
+constexpr int kStageA = kHalfM * kBK * 2;   // 16 KB
+constexpr int kStageB = kBK * kHalfN * 2;   // 16 KB: two 64x64 N-major boxes
+constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kPairStages = 6;
+constexpr int kRingBytes = kPairStages * kStageBytes;
+constexpr int kBoxB = kBK * 64 * 2;
+constexpr int kAccBufs = TG_PAIR_ACC_BUFS;  // accumulators per CTA (256 fp32 columns each)
+constexpr int kTmemCols = kAccBufs * kPairBN;
+constexpr int kThreads = 6 * 32;
+
+constexpr int kBarFull = kRingBytes;
+constexpr int kBarEmpty = kBarFull + 8 * kPairStages;
+constexpr int kBarAccFull = kBarEmpty + 8 * kPairStages;
+constexpr int kBarAccEmpty = kBarAccFull + 16;
+constexpr int kBarDrain = kBarAccEmpty + 16;
+constexpr int kTmemSlot = kBarDrain + 8;
+constexpr int kAbortSlot = kTmemSlot + 4;
+constexpr int kSmemUsed = kAbortSlot + 4;
+constexpr int kSmemAlloc = kSmemUsed + 1024;
+
+// M=256 (pair), N=256, A K-major, B N-major.
+constexpr uint32_t kIdesc = idesc_f16_f32(kPairBM, kPairBN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+
+__device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks, int group_m, int& mb, int& nb) {
+    const int per_group = group_m * n_blocks;
+    const int g = tile / per_group;
+    const int first_m = g * group_m;
+    const int gsize = min(m_blocks - first_m, group_m);
+    const int local = tile - g * per_group;
+    mb = first_m + local % gsize;
+    nb = local / gsize;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tiled_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const TiledArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
+    const int cluster = blockIdx.x >> 1;
+    const int num_clusters = gridDim.x >> 1;
+
+    auto full_bar = [&](int s) { return sbase + kBarFull + 8 * s; };
+    auto empty_bar = [&](int s) { return sbase + kBarEmpty + 8 * s; };
+    auto acc_full_bar = [&](int b) { return sbase + kBarAccFull + 8 * b; };
+    auto acc_empty_bar = [&](int b) { return sbase + kBarAccEmpty + 8 * b; };
+    const uint32_t drain_bar = sbase + kBarDrain;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortSlot);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(full_bar(s), 1);  // even CTA: armed with both halves' bytes
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full_bar(b), 1);
+            mbar_init(acc_empty_bar(b), 8);  // one arrive per epilogue warp, both CTAs
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    cluster_sync();  // barriers of both CTAs initialised before any remote arrive
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const WaitCtx wc{abort_flag, args.wd.status, args.wd.limit_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (both CTAs)
+        if (lane == 0) {
+            const uint32_t leader_full0 = mapa_shared(full_bar(0), 0);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            for (int tile = cluster; tile < args.num_tiles && ok; tile += num_clusters) {
+                int mb, nb;
+                tile_coords(tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
+                const int m0 = mb * kPairBM + rank * kHalfM;
+                const int n0 = nb * kPairBN + rank * kHalfN;
+                for (int kb = 0; kb < args.num_kb; ++kb) {
+                    if (!wait_phase(empty_bar(stage), phase ^ 1, wc, kSiteProducerEmpty)) { ok = false; break; }
+                    const uint32_t sA = sbase + stage * kStageBytes;
+                    const uint32_t sB = sA + kStageA;
+                    const uint32_t fb = leader_full0 + 8 * stage;
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytes);
+                    tma_load_2d_pair(sA, &tmA, fb, kb * kBK, m0);
+                    tma_load_2d_pair(sB, &tmB, fb, n0, kb * kBK);
+                    tma_load_2d_pair(sB + kBoxB, &tmB, fb, n0 + 64, kb * kBK);
+                    issued_mask |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kPairStages) { stage = 0; phase ^= 1; }
+                }
+            }
+            // Before the CTA can leave: in the even CTA, every armed stage has
+            // landed (its barrier counts both halves); in both CTAs, the MMA's last
+            // commit to each stage of this ring (which follows the MMA's wait for
+            // that stage's copies) has arrived.
+            for (int s = 0; s < kPairStages; ++s)
+                if (issued_mask & (1u << s)) {
+                    if (rank == 0) wait_phase_drain(full_bar(s), (issued_parity >> s) & 1, wc);
+                    if (!*abort_flag) wait_phase_drain(empty_bar(s), (issued_parity >> s) & 1, wc);
+                }
+        }
+    } else if (warp == 1) {
+        if (rank == 0 && lane == 0) {
+            // -------------------------------------------------------- MMA issue (even CTA)
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int tile = cluster; tile < args.num_tiles && ok; tile += num_clusters, ++it) {
+                const int b = kAccBufs == 2 ? (it & 1) : 0;
+                const uint32_t acc_phase = kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
+                if (!wait_phase<true>(acc_empty_bar(b), acc_phase ^ 1, wc, kSiteMmaAccEmpty)) break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * kPairBN;
+                for (int kb = 0; kb < args.num_kb; ++kb) {
+                    if (!wait_phase(full_bar(stage), phase, wc, kSiteMmaFull)) { ok = false; break; }
+                    tc_fence_after_sync();
+                    const uint32_t sA = sbase + stage * kStageBytes;
+                    const uint32_t sB = sA + kStageA;
+                    const uint64_t a_desc = smem_desc_sw128(sA, 16, 1024);
+                    const uint64_t b_desc = smem_desc_sw128(sB, kBoxB, 1024);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k)
+                        mma_f16_pair(d_tmem, a_desc + (uint64_t)((k * 32) >> 4), b_desc + (uint64_t)((k * 2048) >> 4),
+                                     kIdesc, (kb | k) != 0);
+                    mma_commit_pair(empty_bar(stage), 0x3);  // stage free in both CTAs
+                    if (++stage == kPairStages) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit_pair(acc_full_bar(b), 0x3);  // accumulator ready in both CTAs
+            }
+            // every pair MMA issued here completes before tensor memory is freed
+            mma_commit_pair(drain_bar, 0x1);
+            wait_phase_drain(drain_bar, 0, wc);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int quarter = warp & 3;
+        const int row_in_tile = rank * kHalfM + quarter * 32 + lane;
+        const uint32_t leader_acc_empty0 = mapa_shared(acc_empty_bar(0), 0);
+        int it = 0;
+        for (int tile = cluster; tile < args.num_tiles; tile += num_clusters, ++it) {
+            int mb, nb;
+            tile_coords(tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
+            const int b = kAccBufs == 2 ? (it & 1) : 0;
+            const uint32_t acc_phase = kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
+            if (!wait_phase(acc_full_bar(b), acc_phase, wc, kSiteEpilogueAccFull)) break;
+            tc_fence_after_sync();
+            const int row = mb * kPairBM + row_in_tile;
+            const int n0 = nb * kPairBN;
+            const int chunks = min(kPairBN / 32, (args.N - n0 + 31) / 32);
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kPairBN;
+            __half* crow = args.C + static_cast<int64_t>(row) * args.N;
+            for (int c = 0; c < chunks; ++c) {
+                uint32_t r[32];
+                __syncwarp();
+                tmem_ld_32x32b_x32(taddr + c * 32, r);
+                tmem_ld_wait();
+                if (c == chunks - 1) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(leader_acc_empty0 + 8 * b);
+                }
+                if (row < args.M)
+                    epilogue_row32(r, crow, args.bias, n0 + c * 32, args.N, args.gelu, args.c_vec, args.bias_vec);
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while its peer may still signal it
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+
+int tiled_pair_smem_bytes() { return kSmemAlloc; }
+
+cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, int max_clusters,
+                              cudaStream_t stream) {
+    static bool attr_done[64] = {};
+    static int active_clusters[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_done[dev]) {
+        e = cudaFuncSetAttribute(tiled_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * max_clusters);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemAlloc;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, tiled_pair_kernel, &cfg);
+        if (e != cudaSuccess) return e;
+        active_clusters[dev] = n > 0 ? n : 1;
+        attr_done[dev] = true;
+    }
+    int clusters = dev < 64 ? active_clusters[dev] : 1;
+    if (clusters > max_clusters) clusters = max_clusters;
+    if (clusters > a.num_tiles) clusters = a.num_tiles;
+    if (clusters < 1) clusters = 1;
+    tiled_pair_kernel<<<2 * clusters, kThreads, kSmemAlloc, stream>>>(tmA, tmB, a);
+    return cudaGetLastError();
+}
+
+}  // namespace tg

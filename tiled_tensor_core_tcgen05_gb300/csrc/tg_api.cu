@@ -130,14 +130,18 @@ Watchdog watchdog(const DeviceState& d) {
     return Watchdog{d.status_ptr, g_watchdog_ns.load(), g_skip_first_arrive.load()};
 }
 
-// Split count for the skinny kernel. Time per CTA is modelled in units of one
-// K block's transfer: each work unit costs its K blocks plus a fixed charge
-// for refilling the pipeline and running its epilogue, and every split beyond
-// the first adds the partial-sum traffic of the final reduction. Minimise
-// (waves of units) x (cost per unit) + reduction; ties keep fewer splits.
+// Split count for the skinny kernel. Time is modelled in units of one K
+// block's transfer at one SM's streaming rate: a CTA's share is its waves of
+// work units, each costing its K blocks plus a fixed charge for refilling the
+// pipeline and running the epilogue. HBM saturates before every SM streams, so
+// the job can never beat total / (kHbmFraction * SMs). Every split beyond the
+// first adds the partial-sum traffic of the final reduction. Ties keep fewer
+// splits.
 int choose_splits(int n_tiles, int kb_total, int sm_count) {
-    constexpr double kUnitOverhead = 6.0;   // pipeline refill + epilogue, in K blocks
-    constexpr double kReducePerSplit = 1.0; // partial tile written and read back
+    constexpr double kUnitOverhead = 6.0;    // pipeline refill + epilogue, in K blocks
+    constexpr double kReducePerSplit = 2.0;  // partial tile written and read back
+    constexpr double kHbmFraction = 0.7;     // share of SMs whose streams saturate HBM
+    const double hbm_floor = static_cast<double>(n_tiles) * kb_total / (kHbmFraction * sm_count);
     int best_s = 1;
     double best = 1e300;
     const int smax = kb_total < kSkMaxSplits ? kb_total : kSkMaxSplits;
@@ -147,7 +151,9 @@ int choose_splits(int n_tiles, int kb_total, int sm_count) {
         if (s_eff != s) continue;
         const long units = static_cast<long>(n_tiles) * s;
         const long waves = (units + sm_count - 1) / sm_count;
-        const double cost = static_cast<double>(waves) * (kbps + kUnitOverhead) + kReducePerSplit * (s - 1);
+        double t = static_cast<double>(waves) * (kbps + kUnitOverhead);
+        if (t < hbm_floor) t = hbm_floor;
+        const double cost = t + kReducePerSplit * (s - 1);
         if (cost < best) {
             best = cost;
             best_s = s;
@@ -193,7 +199,7 @@ tg_status run_splitk(DeviceState& d, const __half* A, const __half* B, const __h
     a.m_pad = (M + 15) / 16 * 16;
     a.tmem_stride = 16;
     while (a.tmem_stride < a.m_pad) a.tmem_stride *= 2;
-    a.tmem_cols = 2 * a.tmem_stride < 32 ? 32 : 2 * a.tmem_stride;
+    a.tmem_cols = 2 * kSkHalves * a.tmem_stride < 32 ? 32 : 2 * kSkHalves * a.tmem_stride;
     a.stages = split_stages_for(a.m_pad);
     a.n_tiles = (N + kSkBN - 1) / kSkBN;
     a.kb_total = (K + kSkBK - 1) / kSkBK;
@@ -251,6 +257,29 @@ tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, 
     return TG_OK;
 }
 
+tg_status run_tiled_pair(DeviceState& d, const __half* A, const __half* B, const __half* bias, __half* C, int M,
+                         int N, int K, int gelu, cudaStream_t stream) {
+    TiledArgs a{};
+    a.A = A; a.B = B; a.bias = bias; a.C = C;
+    a.M = M; a.N = N; a.K = K; a.gelu = gelu;
+    a.m_blocks = (M + 2 * kBM - 1) / (2 * kBM);
+    a.n_blocks = (N + kBN - 1) / kBN;
+    a.num_tiles = a.m_blocks * a.n_blocks;
+    a.num_kb = (K + kBK - 1) / kBK;
+    a.group_m = kGroupM / 2;
+    a.c_vec = (N % 8 == 0 && aligned(C, 16)) ? 1 : 0;
+    a.bias_vec = (bias != nullptr && aligned(bias, 16)) ? 1 : 0;
+    a.a_vec = a.b_vec = 8;
+    a.wd = watchdog(d);
+    CUtensorMap tmA, tmB;
+    tg_status st = make_map(&tmA, A, K, M, kBK, kBM);
+    if (st != TG_OK) return st;
+    if ((st = make_map(&tmB, B, N, K, 64, kBK)) != TG_OK) return st;
+    cudaError_t e = launch_tiled_pair(a, tmA, tmB, d.sm_count / 2, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "pair tiled kernel launch");
+    return TG_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -262,7 +291,7 @@ tg_status tg_gemm_ex(const void* A, const void* B, const void* bias, void* C, in
     // ---- arguments (host only, nothing enqueued on failure)
     if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_GELU)
         return fail(TG_ERR_INVALID_ARG, "epilogue must be TG_EPI_NONE (0) or TG_EPI_GELU (1), got %d", epilogue);
-    if (kernel < TG_KERNEL_AUTO || kernel > TG_KERNEL_SPLITK)
+    if (kernel < TG_KERNEL_AUTO || kernel > TG_KERNEL_TILED_PAIR)
         return fail(TG_ERR_INVALID_ARG, "unknown kernel %d", kernel);
     const int64_t kMax = 0x7FFFFFFFll;
     if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax)
@@ -278,8 +307,9 @@ tg_status tg_gemm_ex(const void* A, const void* B, const void* bias, void* C, in
         overlaps(C, c_bytes, bias, bias ? N * 2 : 0))
         return fail(TG_ERR_INVALID_ARG, "C overlaps an input");
     const bool tma_ok = K % 8 == 0 && N % 8 == 0 && aligned(A, 16) && aligned(B, 16);
-    if (kernel == TG_KERNEL_TILED_TMA && !tma_ok)
-        return fail(TG_ERR_INVALID_ARG, "TG_KERNEL_TILED_TMA needs K %% 8 == 0, N %% 8 == 0 and 16-byte aligned A, B");
+    if ((kernel == TG_KERNEL_TILED_TMA || kernel == TG_KERNEL_TILED_PAIR) && !tma_ok)
+        return fail(TG_ERR_INVALID_ARG, "%s needs K %% 8 == 0, N %% 8 == 0 and 16-byte aligned A, B",
+                    kernel == TG_KERNEL_TILED_TMA ? "TG_KERNEL_TILED_TMA" : "TG_KERNEL_TILED_PAIR");
     if (kernel == TG_KERNEL_SPLITK && (!tma_ok || M > kSkMaxM))
         return fail(TG_ERR_INVALID_ARG, "TG_KERNEL_SPLITK needs M <= %d, K %% 8 == 0, N %% 8 == 0 and 16-byte aligned A, B",
                     kSkMaxM);
@@ -302,9 +332,21 @@ tg_status tg_gemm_ex(const void* A, const void* B, const void* bias, void* C, in
         return e == cudaSuccess ? TG_OK : cuda_fail(e, "fill kernel launch");
     }
     int k = kernel;
-    if (k == TG_KERNEL_AUTO) k = (tma_ok && M <= kSkMaxM) ? TG_KERNEL_SPLITK : (tma_ok ? TG_KERNEL_TILED_TMA : TG_KERNEL_TILED_LSU);
+    if (k == TG_KERNEL_AUTO) {
+        if (!tma_ok) {
+            k = TG_KERNEL_TILED_LSU;
+        } else if (M <= kSkMaxM) {
+            k = TG_KERNEL_SPLITK;
+        } else {
+            // CTA pairs once there is at least one wave of 256x256 tiles for them;
+            // smaller problems keep more, smaller 128x256 tiles on single CTAs
+            const int64_t pair_tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kBN - 1) / kBN);
+            k = pair_tiles >= d.sm_count / 2 ? TG_KERNEL_TILED_PAIR : TG_KERNEL_TILED_TMA;
+        }
+    }
     if (k == TG_KERNEL_SPLITK)
         return run_splitk(d, a, b, bi, c, (int)M, (int)N, (int)K, gelu, split_k, stream);
+    if (k == TG_KERNEL_TILED_PAIR) return run_tiled_pair(d, a, b, bi, c, (int)M, (int)N, (int)K, gelu, stream);
     return run_tiled(d, k == TG_KERNEL_TILED_TMA, a, b, bi, c, (int)M, (int)N, (int)K, gelu, stream);
 }
 
@@ -394,6 +436,8 @@ int64_t tg_ring_bytes(int kernel) {
         case TG_KERNEL_TILED_TMA:
         case TG_KERNEL_TILED_LSU:
             return static_cast<int64_t>(kStages) * (kBM * kBK + kBK * kBN) * 2;
+        case TG_KERNEL_TILED_PAIR:  // per CTA: its 128 rows of A and 128 columns of B, 6 stages
+            return static_cast<int64_t>(6) * (kBM * kBK + kBK * (kBN / 2)) * 2;
         case TG_KERNEL_SPLITK:
             return static_cast<int64_t>(split_stages_for(16)) * (16 * kSkBK + kSkBK * kSkBN) * 2;
         default:

@@ -16,13 +16,15 @@ struct WaitCtx {
 
 // Wait for the phase of `bar` with parity `parity` to complete. Gives up (and
 // returns false) when another wait of this CTA has already expired, or after
-// limit_ns, recording `site` as the first expired wait.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const WaitCtx& w,
-                                           int site) {
-    if (mbar_try_wait(bar, parity)) return true;
+// limit_ns, recording `site` as the first expired wait. kCluster: the barrier
+// receives arrives from another CTA of the cluster (acquire at cluster scope).
+template <bool kCluster = false>
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
+    auto try_once = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (try_once()) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_once()) return true;
         if (*w.abort) return false;
         if (globaltimer_ns() - t0 > w.limit_ns) {
             *w.abort = 1;

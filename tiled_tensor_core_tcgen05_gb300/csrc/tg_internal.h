@@ -17,9 +17,11 @@ constexpr int kBK = 64;
 constexpr int kStages = 4;
 constexpr int kGroupM = 16;  // tile rows per rasterisation group (L2 reuse)
 
-// ---- split-K (swap-AB) kernel geometry: one work unit is a 128-column slice of
-// N times a range of 64-wide K blocks; M (<= 128) is the MMA's N, padded to 16.
-constexpr int kSkBN = 128;
+// ---- split-K (swap-AB) kernel geometry: one work unit is a 256-column slice of
+// N (two 128-row MMA halves) times a range of 64-wide K blocks; M (<= 128) is
+// the MMA's N, padded to 16.
+constexpr int kSkHalves = 2;
+constexpr int kSkBN = 128 * kSkHalves;
 constexpr int kSkBK = 64;
 constexpr int kSkMaxM = 128;
 constexpr int kSkMaxSplits = 64;
@@ -65,8 +67,9 @@ struct SplitArgs {
     int M, N, K;
     int gelu;
     int m_pad;         // MMA N: M rounded up to a multiple of 16 (16..128)
-    int tmem_stride;   // TMEM columns between the two accumulator buffers (pow2 >= m_pad)
-    int tmem_cols;     // TMEM columns allocated (2 * tmem_stride, >= 32)
+    int tmem_stride;   // TMEM columns per accumulator (pow2 >= m_pad); a buffer holds
+                       // kSkHalves accumulators, two buffers alternate between units
+    int tmem_cols;     // TMEM columns allocated (2 * kSkHalves * tmem_stride, >= 32)
     int stages;        // ring depth
     int n_tiles, kb_total, kb_per_split, splits, num_units;
     float* ws;               // splits * M * N fp32 partial sums (splits > 1)
@@ -83,6 +86,9 @@ int tiled_threads(bool tma);
 cudaError_t launch_tiled_tma(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
                              int grid, cudaStream_t stream);
 cudaError_t launch_tiled_lsu(const TiledArgs& a, int grid, cudaStream_t stream);
+int tiled_pair_smem_bytes();
+cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, int max_clusters,
+                              cudaStream_t stream);
 cudaError_t launch_splitk(const SplitArgs& a, const CUtensorMap& tmB, const CUtensorMap& tmA,
                           int grid, cudaStream_t stream);
 cudaError_t launch_fill(const __half* bias, __half* C, int64_t M, int64_t N, int gelu,
