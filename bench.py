@@ -256,8 +256,11 @@ def roofline_entry(w, avg_launch_ms, pk, pk_kind, bound, traffic=None):
         peak = pk["hbm_gbs"]
         unit = "GB/s"
         peak_note = f"hbm_gbs of {pk_kind}"
-    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-            "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_note}
+    e = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+         "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_note}
+    if bound == "tensor" and "bf16_tflops_sustained" in pk:
+        e["frac_of_sustained"] = round(achieved / (pk["bf16_tflops_sustained"] * FP16_PER_BF16), 4)
+    return e
 
 
 def cpu_baseline(w, budget_s: float, metric_unit: str):
@@ -319,7 +322,7 @@ def run_gpu(args):
         for w in workloads.ALL:
             if w.name == main.name:
                 continue
-            steps = max(5, min(args.steps, 50))
+            steps = max(5, min(args.steps, 50))  # secondary workloads: at most 50 timed launches
             r = time_workload(tg, w, steps, max(3, args.warmup), 0 if w.bytes() > 2 * l2 else 2 * l2 + (1 << 20),
                               pg=pg)
             avg = r["kernel_ms"] / steps
@@ -387,7 +390,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["tg", "reference"], default="tg")
     ap.add_argument("--workload", default="square_8192")
