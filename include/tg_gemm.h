@@ -119,6 +119,42 @@ tg_status tg_gemm_staged(const void* hA, const void* hB, const void* hbias, void
                          void* dA, void* dB, void* dbias, void* dC,
                          int64_t M, int64_t N, int64_t K, int epilogue, tg_stream_t stream);
 
+/* Size of the fixed scratch array behind tg_gemm_splitk_noalloc (8 MiB). */
+#define TG_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/*
+ * The skinny split-K GEMM (TG_KERNEL_SPLITK) for callers that must not have the
+ * library allocate device memory during a call. Examples: a process that hands
+ * nearly all device memory to its own pool allocator at start-up, where a
+ * cudaMalloc from inside a library fails or fragments that pool; and a
+ * latency-bound serving loop, where cudaMalloc/cudaFree would synchronise the
+ * device and stall unrelated streams. The paper (the TileLang pages) has no
+ * counterpart to this entry point: it changes only where the scratch memory
+ * comes from, not what is computed.
+ *
+ * Same arguments and result as tg_gemm_ex(..., TG_KERNEL_SPLITK, split_k, ...):
+ * M <= 128, K % 8 == 0, N % 8 == 0, A and B 16-byte aligned; split_k 0 picks
+ * the number of K slices automatically, 1..64 fixes it. The caller still
+ * passes A, B, bias and C (device pointers it owns). With more than one K
+ * slice, the partial sums and arrival counters live in one fixed array of
+ * TG_NOALLOC_SCRATCH_BYTES compiled into the library's device image: every
+ * device that loads the library holds it until the process exits. A call whose
+ * slices need more (4 * slices * M * N bytes of partials plus 4 bytes per
+ * 256-column slice of N, rounded up to 256) returns TG_ERR_INVALID_ARG and
+ * enqueues nothing. Nothing is allocated or freed by any call.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture begins. Every call zeroes the counters on `stream` before
+ * its kernel and otherwise reuses the array as the previous call left it. All
+ * calls share the one array, so calls whose work can overlap on the GPU (for
+ * example on two streams without ordering between them) race and give wrong
+ * results; order them on one stream or with events.
+ */
+tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const void* bias, void* C,
+                                 int64_t M, int64_t N, int64_t K, int epilogue, int split_k,
+                                 tg_stream_t stream);
+
 /*
  * Synchronises `stream`, then reports (and clears) the device-side status word
  * that kernels set when one of their bounded waits expires: TG_OK or

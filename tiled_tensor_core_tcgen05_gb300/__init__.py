@@ -21,11 +21,13 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libtg_gemm.so")
 
 EPI_NONE, EPI_GELU = 0, 1
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024  # TG_NOALLOC_SCRATCH_BYTES
 KERNEL_AUTO, KERNEL_TILED_TMA, KERNEL_TILED_LSU, KERNEL_SPLITK, KERNEL_TILED_PAIR = 0, 1, 2, 3, 4
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NO_MEMORY = range(6)
 
 # every symbol include/tg_gemm.h declares
-EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_device_status", "tg_set_watchdog_ns",
+EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_device_status",
+           "tg_set_watchdog_ns",
            "tg_debug_skip_first_arrive", "tg_status_string", "tg_last_error", "tg_version",
            "tg_ring_bytes", "tg_shutdown")
 
@@ -38,6 +40,7 @@ _vp, _i64, _int, _u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_
 _lib.tg_gemm.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
 _lib.tg_gemm_ex.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp]
 _lib.tg_gemm_staged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
+_lib.tg_gemm_splitk_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.tg_device_status.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.tg_set_watchdog_ns.argtypes = [_u64]
 _lib.tg_debug_skip_first_arrive.argtypes = [_int]
@@ -50,7 +53,8 @@ _lib.tg_ring_bytes.argtypes = [_int]
 _lib.tg_ring_bytes.restype = _i64
 _lib.tg_shutdown.argtypes = []
 _lib.tg_shutdown.restype = None
-for _name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_device_status", "tg_set_watchdog_ns",
+for _name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_device_status",
+              "tg_set_watchdog_ns",
               "tg_debug_skip_first_arrive", "tg_version"):
     getattr(_lib, _name).restype = _int
 
@@ -84,6 +88,14 @@ def tg_gemm_ex(A: int, B: int, bias: int | None, C: int, M: int, N: int, K: int,
 
 def tg_gemm_staged(hA, hB, hbias, hC, dA, dB, dbias, dC, M, N, K, epilogue, stream) -> None:
     _check(_lib.tg_gemm_staged(hA, hB, hbias, hC, dA, dB, dbias, dC, M, N, K, epilogue, stream))
+
+
+def tg_gemm_splitk_noalloc(A: int, B: int, bias: int | None, C: int, M: int, N: int, K: int, epilogue: int,
+                           split_k: int, stream: int | None) -> None:
+    """The skinny split-K GEMM with its scratch in the library's fixed device
+    array, for callers that must not have the library allocate device memory
+    (see include/tg_gemm.h for the size limit and the sharing rules)."""
+    _check(_lib.tg_gemm_splitk_noalloc(A, B, bias, C, M, N, K, epilogue, split_k, stream))
 
 
 def tg_device_status(stream: int | None) -> tuple[int, int]:

@@ -457,3 +457,104 @@ void tg_shutdown(void) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// tg_gemm_splitk_noalloc: the skinny split-K path with its scratch in a fixed
+// array of the library's own device image instead of library-allocated memory.
+
+namespace {
+
+// Layout: one arrival counter per 256-column slice of N (padded to 256 bytes),
+// then the fp32 partial sums [split][M][N]. Loaded with the library's device
+// code, so every device that loads the library holds these bytes until exit.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TG_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch for each device, looked up on the first
+// call on that device (with that device current).
+unsigned char* g_noalloc_ptr[kMaxDevices] = {};
+
+}  // namespace
+
+extern "C" tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const void* bias, void* C, int64_t M,
+                                            int64_t N, int64_t K, int epilogue, int split_k, tg_stream_t stream_) {
+    t_last_error.clear();
+    const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_GELU)
+        return fail(TG_ERR_INVALID_ARG, "epilogue must be TG_EPI_NONE (0) or TG_EPI_GELU (1), got %d", epilogue);
+    const int64_t kMax = 0x7FFFFFFFll;
+    if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax)
+        return fail(TG_ERR_INVALID_ARG, "sizes must be in [0, 2^31): M=%lld N=%lld K=%lld", (long long)M,
+                    (long long)N, (long long)K);
+    if (split_k < 0 || split_k > kSkMaxSplits)
+        return fail(TG_ERR_INVALID_ARG, "split_k must be 0 (automatic) or 1..%d, got %d", kSkMaxSplits, split_k);
+    if (M == 0 || N == 0) return TG_OK;
+    if (C == nullptr) return fail(TG_ERR_INVALID_ARG, "C is NULL");
+    if (K > 0 && (A == nullptr || B == nullptr)) return fail(TG_ERR_INVALID_ARG, "A or B is NULL");
+    const int64_t c_bytes = M * N * 2;
+    if (overlaps(C, c_bytes, A, K > 0 ? M * K * 2 : 0) || overlaps(C, c_bytes, B, K > 0 ? K * N * 2 : 0) ||
+        overlaps(C, c_bytes, bias, bias ? N * 2 : 0))
+        return fail(TG_ERR_INVALID_ARG, "C overlaps an input");
+    if (M > kSkMaxM || (K > 0 && !(K % 8 == 0 && N % 8 == 0 && aligned(A, 16) && aligned(B, 16))))
+        return fail(TG_ERR_INVALID_ARG,
+                    "tg_gemm_splitk_noalloc needs M <= %d, K %% 8 == 0, N %% 8 == 0 and 16-byte aligned A, B", kSkMaxM);
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    tg_status st = current_device(&dev);
+    if (st != TG_OK) return st;
+    DeviceState& d = g_dev[dev];
+    const int gelu = epilogue == TG_EPI_GELU ? 1 : 0;
+    if (K == 0) {
+        cudaError_t e = launch_fill(static_cast<const __half*>(bias), static_cast<__half*>(C), M, N, gelu,
+                                    d.sm_count, stream);
+        return e == cudaSuccess ? TG_OK : cuda_fail(e, "fill kernel launch");
+    }
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static split-K scratch)");
+        g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
+    }
+
+    SplitArgs a{};
+    a.A = static_cast<const __half*>(A);
+    a.B = static_cast<const __half*>(B);
+    a.bias = static_cast<const __half*>(bias);
+    a.C = static_cast<__half*>(C);
+    a.M = (int)M; a.N = (int)N; a.K = (int)K; a.gelu = gelu;
+    a.m_pad = (a.M + 15) / 16 * 16;
+    a.tmem_stride = 16;
+    while (a.tmem_stride < a.m_pad) a.tmem_stride *= 2;
+    a.tmem_cols = 2 * kSkHalves * a.tmem_stride < 32 ? 32 : 2 * kSkHalves * a.tmem_stride;
+    a.stages = split_stages_for(a.m_pad);
+    a.n_tiles = (a.N + kSkBN - 1) / kSkBN;
+    a.kb_total = (a.K + kSkBK - 1) / kSkBK;
+    int s = split_k > 0 ? split_k : choose_splits(a.n_tiles, a.kb_total, d.sm_count);
+    if (s > a.kb_total) s = a.kb_total;
+    a.kb_per_split = (a.kb_total + s - 1) / s;
+    a.splits = (a.kb_total + a.kb_per_split - 1) / a.kb_per_split;
+    a.num_units = a.n_tiles * a.splits;
+    a.wd = watchdog(d);
+    if (a.splits > 1) {
+        const size_t counter_bytes = (static_cast<size_t>(a.n_tiles) * sizeof(unsigned int) + 255) / 256 * 256;
+        const size_t partial_bytes = static_cast<size_t>(a.splits) * a.M * a.N * sizeof(float);
+        if (counter_bytes + partial_bytes > static_cast<size_t>(TG_NOALLOC_SCRATCH_BYTES))
+            return fail(TG_ERR_INVALID_ARG,
+                        "tg_gemm_splitk_noalloc: %d K slices of a %lld x %lld product need %zu bytes of scratch, "
+                        "more than the %zu-byte static scratch (use fewer slices or tg_gemm)",
+                        a.splits, (long long)M, (long long)N, counter_bytes + partial_bytes,
+                        static_cast<size_t>(TG_NOALLOC_SCRATCH_BYTES));
+        // the arrival counters must start at zero; the partials are written before they are read
+        cudaError_t e = cudaMemsetAsync(g_noalloc_ptr[dev], 0, counter_bytes, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "clear static split-K counters");
+        a.counters = reinterpret_cast<unsigned int*>(g_noalloc_ptr[dev]);
+        a.ws = reinterpret_cast<float*>(g_noalloc_ptr[dev] + counter_bytes);
+    }
+    CUtensorMap tmB, tmA;
+    if ((st = make_map(&tmB, B, N, K, 64, kSkBK)) != TG_OK) return st;
+    if ((st = make_map(&tmA, A, K, M, kSkBK, a.m_pad)) != TG_OK) return st;
+    const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
+    cudaError_t e = launch_splitk(a, tmB, tmA, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "split-K kernel launch");
+    return TG_OK;
+}
