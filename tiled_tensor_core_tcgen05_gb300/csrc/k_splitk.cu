@@ -234,11 +234,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int n = nt * kSkBN + h * 128 + quarter * 32 + lane;
                         if (n >= args.N) continue;
                         const float bias_n = args.bias != nullptr ? __half2float(args.bias[n]) : 0.0f;
-                        for (int m = 0; m < args.M; ++m) {
-                            float s = 0.0f;
-                            for (int q = 0; q < args.splits; ++q)  // fixed order: deterministic
-                                s += __ldcg(args.ws + (static_cast<int64_t>(q) * args.M + m) * args.N + n);
-                            args.C[static_cast<int64_t>(m) * args.N + n] = __float2half_rn(epi_value(s, bias_n, args.gelu));
+                        for (int m0 = 0; m0 < args.M; m0 += 16) {
+                            // 16 rows at a time: 16 independent loads per slice in flight;
+                            // each row still sums its slices in order 0, 1, ... (deterministic)
+                            float s[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) s[i] = 0.0f;
+                            for (int q = 0; q < args.splits; ++q) {
+                                const float* wq = args.ws + (static_cast<int64_t>(q) * args.M + m0) * args.N + n;
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    if (m0 + i < args.M) s[i] += __ldcg(wq + static_cast<int64_t>(i) * args.N);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (m0 + i < args.M)
+                                    args.C[static_cast<int64_t>(m0 + i) * args.N + n] =
+                                        __float2half_rn(epi_value(s[i], bias_n, args.gelu));
                         }
                     }
                     if (ept == 0) atomicExch(args.counters + nt, 0u);

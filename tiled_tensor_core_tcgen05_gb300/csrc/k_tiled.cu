@@ -11,7 +11,7 @@
 //   * one CTA per SM, persistent over 128 x 256 output tiles in grouped order;
 //   * warp roles: a producer (one TMA-issuing lane, or four warps of ordinary
 //     loads when TMA cannot describe the operands), one MMA-issuing lane, and
-//     four epilogue warps;
+//     eight epilogue warps (two per quarter of the accumulator's rows);
 //   * a 4-stage ring of 48 KB stages (A 128x64 K-major, B 64x256 N-major, both
 //     in the 128-byte swizzled layout) guarded by full/empty mbarriers;
 //   * tcgen05.mma (M=128, N=256, K=16) accumulating in tensor memory; two
@@ -53,7 +53,8 @@ template <bool kTma>
 struct Roles {
     static constexpr int kProducerWarps = kTma ? 1 : 4;
     static constexpr int kMmaWarp = kProducerWarps;
-    static constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;
+    static constexpr int kEpiWarp0 = kProducerWarps + 1;
+    static constexpr int kThreads = (kProducerWarps + 1 + kEpiWarps) * 32;
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks, int group_m,
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full_bar(b), 1);
-            mbar_init(acc_empty_bar(b), 128);
+            mbar_init(acc_empty_bar(b), kEpiWarps * 32);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -286,6 +287,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
+        const int half = (warp - R::kEpiWarp0) >> 2;  // which half of the 32-column chunks
         const int row_in_tile = quarter * 32 + lane;
         int it = 0;
         for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++it) {
@@ -298,16 +300,23 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             const int row = mb * kBM + row_in_tile;
             const int n0 = nb * kBN;
             const int chunks = min(kBN / 32, (args.N - n0 + 31) / 32);
+            constexpr int kChunksPerWarp = (kBN / 32) / (kEpiWarps / 4);
+            const int c_begin = half * kChunksPerWarp;
+            const int c_end = min(c_begin + kChunksPerWarp, chunks);
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kBN;
             __half* crow = args.C + static_cast<int64_t>(row) * args.N;
-            for (int c = 0; c < chunks; ++c) {
+            if (c_begin >= c_end) {  // no columns of this tile for this warp
+                tc_fence_before_sync();
+                mbar_arrive(acc_empty_bar(b));
+            }
+            for (int c = c_begin; c < c_end; ++c) {
                 uint32_t r[32];
                 __syncwarp();  // tcgen05.ld is warp-collective; lanes diverged on the row mask
                 tmem_ld_32x32b_x32(taddr + c * 32, r);
                 tmem_ld_wait();
-                if (c == chunks - 1) {
+                if (c == c_end - 1) {
                     tc_fence_before_sync();
-                    mbar_arrive(acc_empty_bar(b));  // TMEM buffer b may be overwritten
+                    mbar_arrive(acc_empty_bar(b));  // this warp is done with TMEM buffer b
                 }
                 if (row < args.M)
                     epilogue_row32(r, crow, args.bias, n0 + c * 32, args.N, args.gelu, args.c_vec, args.bias_vec);

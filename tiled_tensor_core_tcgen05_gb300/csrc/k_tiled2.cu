@@ -15,8 +15,9 @@
 // columns of B for each K block by TMA into its own 6-stage ring; the copies
 // of BOTH CTAs complete on the even CTA's "full" barrier (the pair form of the
 // TMA copy), which the even CTA arms with the bytes of both halves. Warp 1
-// lane 0 of the even CTA issues the pair MMAs; warps 2..5 are the epilogue,
-// each CTA reading its own 128 accumulator rows from its own tensor memory.
+// lane 0 of the even CTA issues the pair MMAs; warps 2..9 are the epilogue,
+// each CTA reading its own 128 accumulator rows from its own tensor memory
+// (two warps per quarter of the rows, each taking half of the columns).
 // MMA completion is committed to both CTAs at once (multicast), freeing the
 // stage in both rings and publishing the accumulator to both epilogues; both
 // epilogues release the accumulator to the issuer with one arrive per warp.
@@ -42,7 +43,8 @@ constexpr int kRingBytes = kPairStages * kStageBytes;
 constexpr int kBoxB = kBK * 64 * 2;
 constexpr int kAccBufs = TG_PAIR_ACC_BUFS;  // accumulators per CTA (256 fp32 columns each)
 constexpr int kTmemCols = kAccBufs * kPairBN;
-constexpr int kThreads = 6 * 32;
+constexpr int kEpiWarp0 = 2;
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
 
 constexpr int kBarFull = kRingBytes;
 constexpr int kBarEmpty = kBarFull + 8 * kPairStages;
@@ -94,7 +96,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full_bar(b), 1);
-            mbar_init(acc_empty_bar(b), 8);  // one arrive per epilogue warp, both CTAs
+            mbar_init(acc_empty_bar(b), 2 * kEpiWarps);  // one arrive per epilogue warp, both CTAs
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -187,6 +189,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int quarter = warp & 3;
+        const int half = (warp - kEpiWarp0) >> 2;
         const int row_in_tile = rank * kHalfM + quarter * 32 + lane;
         const uint32_t leader_acc_empty0 = mapa_shared(acc_empty_bar(0), 0);
         int it = 0;
@@ -200,14 +203,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int row = mb * kPairBM + row_in_tile;
             const int n0 = nb * kPairBN;
             const int chunks = min(kPairBN / 32, (args.N - n0 + 31) / 32);
+            constexpr int kChunksPerWarp = (kPairBN / 32) / (kEpiWarps / 4);
+            const int c_begin = half * kChunksPerWarp;
+            const int c_end = min(c_begin + kChunksPerWarp, chunks);
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kPairBN;
             __half* crow = args.C + static_cast<int64_t>(row) * args.N;
-            for (int c = 0; c < chunks; ++c) {
+            if (c_begin >= c_end) {  // no columns of this tile for this warp
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(leader_acc_empty0 + 8 * b);
+            }
+            for (int c = c_begin; c < c_end; ++c) {
                 uint32_t r[32];
                 __syncwarp();
                 tmem_ld_32x32b_x32(taddr + c * 32, r);
                 tmem_ld_wait();
-                if (c == chunks - 1) {
+                if (c == c_end - 1) {
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(leader_acc_empty0 + 8 * b);

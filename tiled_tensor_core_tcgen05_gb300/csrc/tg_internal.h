@@ -16,6 +16,14 @@ constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kStages = 4;
 constexpr int kGroupM = 16;  // tile rows per rasterisation group (L2 reuse)
+// Epilogue warps of the tiled kernels: two per TMEM lane quarter, each taking
+// half of a tile's 32-column chunks, so one warp's erf/convert/store work
+// overlaps the other's TMEM reads.
+#ifndef TG_EPI_WARPS
+#define TG_EPI_WARPS 8
+#endif
+constexpr int kEpiWarps = TG_EPI_WARPS;
+static_assert(kEpiWarps == 4 || kEpiWarps == 8, "epilogue warps: one or two per TMEM lane quarter");
 
 // ---- split-K (swap-AB) kernel geometry: one work unit is a 256-column slice of
 // N (two 128-row MMA halves) times a range of 64-wide K blocks; M (<= 128) is
