@@ -74,6 +74,9 @@ EXACT_SHAPES = [
     (127, 248, 192), (128, 256, 256), (129, 264, 200), (255, 512, 64), (257, 520, 128),
     (300, 1000, 256), (33, 40, 8), (128, 8, 256), (7, 13, 29), (129, 257, 31), (200, 3, 5),
     (5, 200, 3), (100, 96, 256), (16, 28672 // 16, 256),
+    # 2 x 43 = 86 tiles of 256 x 256: one wave of 76 CTA pairs plus 10 tiles that
+    # the pair kernel runs as 20 half-width units (whole, ragged, and an empty half)
+    (512, 11008, 64), (512, 10992, 72), (500, 10816, 64),
 ]
 
 

@@ -69,6 +69,10 @@ __device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks
 }
 
 // ---- ordinary-load staging into the same swizzled layout TMA produces ----
+//
+// 16- and 4-byte units go through cp.async (asynchronous, zero-filled when out
+// of range), so a producer thread issues a whole stage and moves on; operands
+// aligned to 2 bytes only are copied with ordinary loads and stores.
 
 template <int VEC>
 struct VecT;
@@ -76,36 +80,32 @@ template <> struct VecT<8> { using T = uint4; };
 template <> struct VecT<2> { using T = uint32_t; };
 template <> struct VecT<1> { using T = uint16_t; };
 
+template <int VEC>
+__device__ __forceinline__ void copy_unit(uint8_t* dst, const __half* src, bool valid, const __half* any_valid) {
+    if constexpr (VEC == 8) {
+        cp_async_16(smem_u32(dst), valid ? src : any_valid, valid ? 16u : 0u);
+    } else if constexpr (VEC == 2) {
+        cp_async_4(smem_u32(dst), valid ? src : any_valid, valid ? 4u : 0u);
+    } else {
+        *reinterpret_cast<uint16_t*>(dst) = valid ? *reinterpret_cast<const uint16_t*>(src) : uint16_t(0);
+    }
+}
+
 // A tile: rows m0..m0+127, k0..k0+63; byte (r, k) = r*128 + ((k/8) ^ (r%8))*16 + (k%8)*2.
 template <int VEC>
 __device__ __forceinline__ void stage_A(uint8_t* sA, const __half* __restrict__ A, int M, int K,
                                         int m0, int k0, int ptid) {
-    using T = typename VecT<VEC>::T;
     constexpr int kUnitsPerRow = kBK / VEC;
     constexpr int kPerThread = kBM * kUnitsPerRow / 128;
-    constexpr int kBatch = kPerThread < 8 ? kPerThread : 8;
-#pragma unroll 1
-    for (int i0 = 0; i0 < kPerThread; i0 += kBatch) {
-        T val[kBatch];
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            const int u = ptid + 128 * (i0 + j);
-            const int r = u / kUnitsPerRow;
-            const int k = (u % kUnitsPerRow) * VEC;
-            const int gm = m0 + r, gk = k0 + k;
-            if (gm < M && gk < K)
-                val[j] = *reinterpret_cast<const T*>(A + static_cast<int64_t>(gm) * K + gk);
-            else
-                val[j] = T{};
-        }
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            const int u = ptid + 128 * (i0 + j);
-            const int r = u / kUnitsPerRow;
-            const int k = (u % kUnitsPerRow) * VEC;
-            const int off = r * 128 + ((((k * 2) >> 4) ^ (r & 7)) << 4) + ((k * 2) & 15);
-            *reinterpret_cast<T*>(sA + off) = val[j];
-        }
+#pragma unroll 8
+    for (int i = 0; i < kPerThread; ++i) {
+        const int u = ptid + 128 * i;
+        const int r = u / kUnitsPerRow;
+        const int k = (u % kUnitsPerRow) * VEC;
+        const int gm = m0 + r, gk = k0 + k;
+        const int off = r * 128 + ((((k * 2) >> 4) ^ (r & 7)) << 4) + ((k * 2) & 15);
+        const bool valid = gm < M && gk < K;
+        copy_unit<VEC>(sA + off, A + (valid ? static_cast<int64_t>(gm) * K + gk : 0), valid, A);
     }
 }
 
@@ -113,33 +113,18 @@ __device__ __forceinline__ void stage_A(uint8_t* sA, const __half* __restrict__ 
 template <int VEC>
 __device__ __forceinline__ void stage_B(uint8_t* sB, const __half* __restrict__ B, int N, int K,
                                         int n0, int k0, int ptid) {
-    using T = typename VecT<VEC>::T;
     constexpr int kUnitsPerRow = kBN / VEC;
     constexpr int kPerThread = kBK * kUnitsPerRow / 128;
-    constexpr int kBatch = 8;
-#pragma unroll 1
-    for (int i0 = 0; i0 < kPerThread; i0 += kBatch) {
-        T val[kBatch];
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            const int u = ptid + 128 * (i0 + j);
-            const int k = u / kUnitsPerRow;
-            const int n = (u % kUnitsPerRow) * VEC;
-            const int gk = k0 + k, gn = n0 + n;
-            if (gk < K && gn < N)
-                val[j] = *reinterpret_cast<const T*>(B + static_cast<int64_t>(gk) * N + gn);
-            else
-                val[j] = T{};
-        }
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            const int u = ptid + 128 * (i0 + j);
-            const int k = u / kUnitsPerRow;
-            const int n = (u % kUnitsPerRow) * VEC;
-            const int nn = n & 63;
-            const int off = (n >> 6) * kBoxB + k * 128 + ((((nn * 2) >> 4) ^ (k & 7)) << 4) + ((nn * 2) & 15);
-            *reinterpret_cast<T*>(sB + off) = val[j];
-        }
+#pragma unroll 8
+    for (int i = 0; i < kPerThread; ++i) {
+        const int u = ptid + 128 * i;
+        const int k = u / kUnitsPerRow;
+        const int n = (u % kUnitsPerRow) * VEC;
+        const int gk = k0 + k, gn = n0 + n;
+        const int nn = n & 63;
+        const int off = (n >> 6) * kBoxB + k * 128 + ((((nn * 2) >> 4) ^ (k & 7)) << 4) + ((nn * 2) & 15);
+        const bool valid = gk < K && gn < N;
+        copy_unit<VEC>(sB + off, B + (valid ? static_cast<int64_t>(gk) * N + gn : 0), valid, B);
     }
 }
 
@@ -242,12 +227,13 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                     if (args.b_vec == 8) stage_B<8>(sB, args.B, args.N, args.K, n0, k0, ptid);
                     else if (args.b_vec == 2) stage_B<2>(sB, args.B, args.N, args.K, n0, k0, ptid);
                     else stage_B<1>(sB, args.B, args.N, args.K, n0, k0, ptid);
-                    fence_proxy_async_smem();
-                    mbar_arrive(full_bar(stage));
+                    fence_proxy_async_smem();      // this thread's ordinary stores, if any
+                    cp_async_arrive(full_bar(stage));  // fires once its cp.async copies land
                     if (++stage == kStages) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
             }
+            cp_async_wait_all();  // nothing of this thread is in flight when the CTA leaves
         }
     } else if (warp == R::kMmaWarp) {
         // ------------------------------------------------------------ MMA issue
@@ -265,6 +251,9 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                 for (int kb = 0; kb < args.num_kb; ++kb) {
                     if (!wait_phase(full_bar(stage), phase, wc, kSiteMmaFull)) { ok = false; break; }
                     tc_fence_after_sync();
+                    // stages filled by cp.async / ordinary stores (generic proxy) are read
+                    // by the tensor core (async proxy)
+                    if constexpr (!kTma) fence_proxy_async_smem();
                     const uint32_t sA = sbase + stage * kStageBytes;
                     const uint32_t sB = sA + kStageA;
                     const uint64_t a_desc = smem_desc_sw128(sA, 16, 1024);

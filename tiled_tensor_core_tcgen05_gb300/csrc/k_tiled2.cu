@@ -56,8 +56,25 @@ constexpr int kAbortSlot = kTmemSlot + 4;
 constexpr int kSmemUsed = kAbortSlot + 4;
 constexpr int kSmemAlloc = kSmemUsed + 1024;
 
-// M=256 (pair), N=256, A K-major, B N-major.
+// M=256 (pair), N=256, A K-major, B N-major; and the half-width form (N=128)
+// used for the split tiles of the last wave.
 constexpr uint32_t kIdesc = idesc_f16_f32(kPairBM, kPairBN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+constexpr uint32_t kIdescHalf = idesc_f16_f32(kPairBM, kPairBN / 2, /*a_mn_major=*/false, /*b_mn_major=*/true);
+
+// Work unit u -> tile and column range. Units below split_from are whole
+// 256x256 tiles; the rest are the two 256x128 halves of the last wave's tiles,
+// so that wave takes half as long when it would otherwise leave clusters idle.
+struct Unit {
+    int tile;
+    int col0;   // first column of the unit within the tile (0 or 128)
+    int width;  // 256 or 128
+};
+
+__device__ __forceinline__ Unit unit_of(int u, int split_from) {
+    if (u < split_from) return Unit{u, 0, kPairBN};
+    const int j = u - split_from;
+    return Unit{split_from + (j >> 1), (j & 1) * (kPairBN / 2), kPairBN / 2};
+}
 
 __device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks, int group_m, int& mb, int& nb) {
     const int per_group = group_m * n_blocks;
@@ -122,20 +139,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
-            for (int tile = cluster; tile < args.num_tiles && ok; tile += num_clusters) {
+            for (int u = cluster; u < args.num_units && ok; u += num_clusters) {
+                const Unit un = unit_of(u, args.split_from);
                 int mb, nb;
-                tile_coords(tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
+                tile_coords(un.tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
                 const int m0 = mb * kPairBM + rank * kHalfM;
-                const int n0 = nb * kPairBN + rank * kHalfN;
+                // this CTA's half of the unit's columns: 128 of a whole tile, 64 of a half tile
+                const int n0 = nb * kPairBN + un.col0 + rank * (un.width / 2);
+                const bool whole = un.width == kPairBN;
+                const uint32_t bytes = kStageA + (whole ? kStageB : kStageB / 2);
                 for (int kb = 0; kb < args.num_kb; ++kb) {
                     if (!wait_phase(empty_bar(stage), phase ^ 1, wc, kSiteProducerEmpty)) { ok = false; break; }
                     const uint32_t sA = sbase + stage * kStageBytes;
                     const uint32_t sB = sA + kStageA;
                     const uint32_t fb = leader_full0 + 8 * stage;
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytes);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * bytes);
                     tma_load_2d_pair(sA, &tmA, fb, kb * kBK, m0);
                     tma_load_2d_pair(sB, &tmB, fb, n0, kb * kBK);
-                    tma_load_2d_pair(sB + kBoxB, &tmB, fb, n0 + 64, kb * kBK);
+                    if (whole) tma_load_2d_pair(sB + kBoxB, &tmB, fb, n0 + 64, kb * kBK);
                     issued_mask |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == kPairStages) { stage = 0; phase ^= 1; }
@@ -158,7 +179,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            for (int tile = cluster; tile < args.num_tiles && ok; tile += num_clusters, ++it) {
+            for (int u = cluster; u < args.num_units && ok; u += num_clusters, ++it) {
+                const uint32_t idesc = unit_of(u, args.split_from).width == kPairBN ? kIdesc : kIdescHalf;
                 const int b = kAccBufs == 2 ? (it & 1) : 0;
                 const uint32_t acc_phase = kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
                 if (!wait_phase<true>(acc_empty_bar(b), acc_phase ^ 1, wc, kSiteMmaAccEmpty)) break;
@@ -174,7 +196,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k)
                         mma_f16_pair(d_tmem, a_desc + (uint64_t)((k * 32) >> 4), b_desc + (uint64_t)((k * 2048) >> 4),
-                                     kIdesc, (kb | k) != 0);
+                                     idesc, (kb | k) != 0);
                     mma_commit_pair(empty_bar(stage), 0x3);  // stage free in both CTAs
                     if (++stage == kPairStages) { stage = 0; phase ^= 1; }
                 }
@@ -193,16 +215,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int row_in_tile = rank * kHalfM + quarter * 32 + lane;
         const uint32_t leader_acc_empty0 = mapa_shared(acc_empty_bar(0), 0);
         int it = 0;
-        for (int tile = cluster; tile < args.num_tiles; tile += num_clusters, ++it) {
+        for (int u = cluster; u < args.num_units; u += num_clusters, ++it) {
+            const Unit un = unit_of(u, args.split_from);
             int mb, nb;
-            tile_coords(tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
+            tile_coords(un.tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
             const int b = kAccBufs == 2 ? (it & 1) : 0;
             const uint32_t acc_phase = kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
             if (!wait_phase(acc_full_bar(b), acc_phase, wc, kSiteEpilogueAccFull)) break;
             tc_fence_after_sync();
             const int row = mb * kPairBM + row_in_tile;
-            const int n0 = nb * kPairBN;
-            const int chunks = min(kPairBN / 32, (args.N - n0 + 31) / 32);
+            const int n0 = nb * kPairBN + un.col0;
+            const int chunks = max(0, min(un.width / 32, (args.N - n0 + 31) / 32));
             constexpr int kChunksPerWarp = (kPairBN / 32) / (kEpiWarps / 4);
             const int c_begin = half * kChunksPerWarp;
             const int c_end = min(c_begin + kChunksPerWarp, chunks);
@@ -273,7 +296,14 @@ cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const 
     if (clusters > max_clusters) clusters = max_clusters;
     if (clusters > a.num_tiles) clusters = a.num_tiles;
     if (clusters < 1) clusters = 1;
-    tiled_pair_kernel<<<2 * clusters, kThreads, kSmemAlloc, stream>>>(tmA, tmB, a);
+    TiledArgs args = a;
+    // a last wave of R < clusters tiles leaves clusters idle; when the halves
+    // of those tiles still fit in one wave (2R <= clusters), run them as halves
+    const int full_waves = a.num_tiles / clusters;
+    const int rest = a.num_tiles - full_waves * clusters;
+    args.split_from = (full_waves > 0 && rest > 0 && 2 * rest <= clusters) ? full_waves * clusters : a.num_tiles;
+    args.num_units = args.split_from + 2 * (a.num_tiles - args.split_from);
+    tiled_pair_kernel<<<2 * clusters, kThreads, kSmemAlloc, stream>>>(tmA, tmB, args);
     return cudaGetLastError();
 }
 

@@ -16,11 +16,11 @@ constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kStages = 4;
 constexpr int kGroupM = 16;  // tile rows per rasterisation group (L2 reuse)
-// Epilogue warps of the tiled kernels: two per TMEM lane quarter, each taking
-// half of a tile's 32-column chunks, so one warp's erf/convert/store work
-// overlaps the other's TMEM reads.
+// Epilogue warps of the tiled kernels: one per TMEM lane quarter (4), or two
+// per quarter each taking half of a tile's 32-column chunks (8). Measured on
+// GB300, 4 is as fast as 8 with erf-GELU and slightly faster without it.
 #ifndef TG_EPI_WARPS
-#define TG_EPI_WARPS 8
+#define TG_EPI_WARPS 4
 #endif
 constexpr int kEpiWarps = TG_EPI_WARPS;
 static_assert(kEpiWarps == 4 || kEpiWarps == 8, "epilogue warps: one or two per TMEM lane quarter");
@@ -64,6 +64,10 @@ struct TiledArgs {
     int bias_vec;  // bias 16-byte aligned: 16-byte loads
     int a_vec;     // ordinary-load staging width for A in elements: 8, 2 or 1
     int b_vec;     // same for B
+    // CTA-pair kernel only: tiles [split_from, num_tiles) of the last, partial
+    // wave run as two half-width units each; num_units = split_from +
+    // 2 * (num_tiles - split_from). Set by the launcher.
+    int split_from, num_units;
     Watchdog wd;
 };
 
