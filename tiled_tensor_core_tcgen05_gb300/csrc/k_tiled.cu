@@ -40,7 +40,8 @@ constexpr int kBarAccEmpty = kBarAccFull + 16;
 constexpr int kBarDrain = kBarAccEmpty + 16;
 constexpr int kTmemSlot = kBarDrain + 8;
 constexpr int kAbortSlot = kTmemSlot + 4;
-constexpr int kSmemUsed = kAbortSlot + 4;
+constexpr int kEpiStage = (kAbortSlot + 4 + 127) / 128 * 128;  // per-warp output staging
+constexpr int kSmemUsed = kEpiStage + kEpiWarps * kStageWarpBytes;
 constexpr int kSmemAlloc = kSmemUsed + 1024;  // slack to align the ring to 1024 B
 
 // Operand descriptors: A is K-major (8-row groups 1024 B apart); B is N-major
@@ -278,6 +279,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
         const int half = (warp - R::kEpiWarp0) >> 2;  // which half of the 32-column chunks
         const int row_in_tile = quarter * 32 + lane;
+        uint8_t* stage = smem + kEpiStage + (warp - R::kEpiWarp0) * kStageWarpBytes;
         int it = 0;
         for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++it) {
             int mb, nb;
@@ -293,7 +295,6 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             const int c_begin = half * kChunksPerWarp;
             const int c_end = min(c_begin + kChunksPerWarp, chunks);
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kBN;
-            __half* crow = args.C + static_cast<int64_t>(row) * args.N;
             if (c_begin >= c_end) {  // no columns of this tile for this warp
                 tc_fence_before_sync();
                 mbar_arrive(acc_empty_bar(b));
@@ -307,8 +308,8 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                     tc_fence_before_sync();
                     mbar_arrive(acc_empty_bar(b));  // this warp is done with TMEM buffer b
                 }
-                if (row < args.M)
-                    epilogue_row32(r, crow, args.bias, n0 + c * 32, args.N, args.gelu, args.c_vec, args.bias_vec);
+                epilogue_chunk(r, stage, args.C, args.bias, row - lane, n0 + c * 32, args.M, args.N, args.gelu,
+                               args.c_store, args.bias_vec);
             }
         }
     }

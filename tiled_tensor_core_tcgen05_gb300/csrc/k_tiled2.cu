@@ -38,7 +38,10 @@ constexpr int kPairBN = kBN;                // 256 columns of C per cluster tile
 constexpr int kStageA = kHalfM * kBK * 2;   // 16 KB
 constexpr int kStageB = kBK * kHalfN * 2;   // 16 KB: two 64x64 N-major boxes
 constexpr int kStageBytes = kStageA + kStageB;
-constexpr int kPairStages = 6;
+#ifndef TG_PAIR_STAGES
+#define TG_PAIR_STAGES 6
+#endif
+constexpr int kPairStages = TG_PAIR_STAGES;
 constexpr int kRingBytes = kPairStages * kStageBytes;
 constexpr int kBoxB = kBK * 64 * 2;
 constexpr int kAccBufs = TG_PAIR_ACC_BUFS;  // accumulators per CTA (256 fp32 columns each)
@@ -53,7 +56,8 @@ constexpr int kBarAccEmpty = kBarAccFull + 16;
 constexpr int kBarDrain = kBarAccEmpty + 16;
 constexpr int kTmemSlot = kBarDrain + 8;
 constexpr int kAbortSlot = kTmemSlot + 4;
-constexpr int kSmemUsed = kAbortSlot + 4;
+constexpr int kEpiStage = (kAbortSlot + 4 + 127) / 128 * 128;  // per-warp output staging
+constexpr int kSmemUsed = kEpiStage + kEpiWarps * kStageWarpBytes;
 constexpr int kSmemAlloc = kSmemUsed + 1024;
 
 // M=256 (pair), N=256, A K-major, B N-major; and the half-width form (N=128)
@@ -213,6 +217,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int half = (warp - kEpiWarp0) >> 2;
         const int row_in_tile = rank * kHalfM + quarter * 32 + lane;
+        uint8_t* stage = smem + kEpiStage + (warp - kEpiWarp0) * kStageWarpBytes;
         const uint32_t leader_acc_empty0 = mapa_shared(acc_empty_bar(0), 0);
         int it = 0;
         for (int u = cluster; u < args.num_units; u += num_clusters, ++it) {
@@ -230,7 +235,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int c_begin = half * kChunksPerWarp;
             const int c_end = min(c_begin + kChunksPerWarp, chunks);
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kPairBN;
-            __half* crow = args.C + static_cast<int64_t>(row) * args.N;
             if (c_begin >= c_end) {  // no columns of this tile for this warp
                 tc_fence_before_sync();
                 __syncwarp();
@@ -246,8 +250,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(leader_acc_empty0 + 8 * b);
                 }
-                if (row < args.M)
-                    epilogue_row32(r, crow, args.bias, n0 + c * 32, args.N, args.gelu, args.c_vec, args.bias_vec);
+                epilogue_chunk(r, stage, args.C, args.bias, row - lane, n0 + c * 32, args.M, args.N, args.gelu,
+                               args.c_store, args.bias_vec);
             }
         }
     }

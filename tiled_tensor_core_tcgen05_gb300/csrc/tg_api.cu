@@ -237,7 +237,7 @@ tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, 
     a.num_tiles = a.m_blocks * a.n_blocks;
     a.num_kb = (K + kBK - 1) / kBK;
     a.group_m = kGroupM;
-    a.c_vec = (N % 8 == 0 && aligned(C, 16)) ? 1 : 0;
+    a.c_store = (N % 8 == 0 && aligned(C, 16)) ? 2 : ((N % 2 == 0 && aligned(C, 4)) ? 1 : 0);
     a.bias_vec = (bias != nullptr && aligned(bias, 16)) ? 1 : 0;
     a.a_vec = vec_width(A, K);
     a.b_vec = vec_width(B, N);
@@ -266,8 +266,8 @@ tg_status run_tiled_pair(DeviceState& d, const __half* A, const __half* B, const
     a.n_blocks = (N + kBN - 1) / kBN;
     a.num_tiles = a.m_blocks * a.n_blocks;
     a.num_kb = (K + kBK - 1) / kBK;
-    a.group_m = kGroupM / 2;
-    a.c_vec = (N % 8 == 0 && aligned(C, 16)) ? 1 : 0;
+    a.group_m = kPairGroupM;
+    a.c_store = (N % 8 == 0 && aligned(C, 16)) ? 2 : ((N % 2 == 0 && aligned(C, 4)) ? 1 : 0);
     a.bias_vec = (bias != nullptr && aligned(bias, 16)) ? 1 : 0;
     a.a_vec = a.b_vec = 8;
     a.wd = watchdog(d);

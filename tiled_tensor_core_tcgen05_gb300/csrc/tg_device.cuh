@@ -77,12 +77,26 @@ __device__ __forceinline__ float epi_value(float acc, float b, int gelu) {
     return gelu ? gelu_erf(x) : x;
 }
 
-// 32 consecutive columns of one output row (col0..col0+31), held as fp32 bit
-// patterns by one thread: add bias, apply GELU, round to binary16, store.
-// Columns >= N are not written; rows are masked by the caller.
-__device__ __forceinline__ void epilogue_row32(const uint32_t (&r)[32], __half* __restrict__ crow,
-                                               const __half* __restrict__ bias, int col0, int N,
-                                               int gelu, int c_vec, int bias_vec) {
+// Bytes of shared memory each epilogue warp uses to stage one 32 x 32 chunk of
+// C: 32 rows of 64 bytes at an 80-byte pitch, so the lanes' 16-byte writes of
+// their own rows fall in distinct banks.
+constexpr int kStagePitch = 80;
+constexpr int kStageWarpBytes = 32 * kStagePitch;
+
+// How a warp may write C: 16-byte units (row starts 16-byte aligned, N % 8 == 0),
+// 4-byte units (4-byte aligned, N even) or single elements.
+enum CStoreMode : int { kStore16 = 2, kStore4 = 1, kStore2 = 0 };
+
+// One warp's 32 x 32 chunk of C, rows row0..row0+31 (lane l computed row
+// row0 + l), columns col0..col0+31. Each lane holds its row's 32 accumulator
+// values (fp32 bits): add bias, apply GELU, round once to binary16, stage the
+// row in this warp's shared buffer, then write the chunk back row by row so
+// each store instruction covers whole 64-byte row segments. Rows >= M and
+// columns >= N are not written.
+__device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], uint8_t* stage, __half* __restrict__ C,
+                                               const __half* __restrict__ bias, int row0, int col0, int M, int N,
+                                               int gelu, int store_mode, int bias_vec) {
+    const int lane = threadIdx.x & 31;
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
@@ -111,21 +125,56 @@ __device__ __forceinline__ void epilogue_row32(const uint32_t (&r)[32], __half* 
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
     }
-    if (full && c_vec) {
-        uint4* cp = reinterpret_cast<uint4*>(crow + col0);
+    // this lane's row into the staging buffer
+    uint4* mine = reinterpret_cast<uint4*>(stage + lane * kStagePitch);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint4 u;
-            __half2* h = reinterpret_cast<__half2*>(&u);
+    for (int q = 0; q < 4; ++q) {
+        uint4 u;
+        __half2* h = reinterpret_cast<__half2*>(&u);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(v[q * 8 + 2 * e], v[q * 8 + 2 * e + 1]);
-            cp[q] = u;
+        for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(v[q * 8 + 2 * e], v[q * 8 + 2 * e + 1]);
+        mine[q] = u;
+    }
+    __syncwarp();
+    if (store_mode == kStore16 && full) {
+        // 4 lanes per row, 8 rows per instruction
+#pragma unroll
+        for (int pass = 0; pass < 4; ++pass) {
+            const int rr = pass * 8 + (lane >> 2);
+            const int q = lane & 3;
+            const int row = row0 + rr;
+            if (row < M)
+                *reinterpret_cast<uint4*>(C + static_cast<int64_t>(row) * N + col0 + q * 8) =
+                    *reinterpret_cast<const uint4*>(stage + rr * kStagePitch + q * 16);
+        }
+    } else if (store_mode != kStore2) {
+        // 16 lanes per row, 2 rows per instruction, one or two elements per lane
+#pragma unroll 4
+        for (int pass = 0; pass < 16; ++pass) {
+            const int rr = pass * 2 + (lane >> 4);
+            const int c = col0 + 2 * (lane & 15);
+            const int row = row0 + rr;
+            if (row < M && c < N) {
+                __half* dst = C + static_cast<int64_t>(row) * N + c;
+                const __half* src = reinterpret_cast<const __half*>(stage + rr * kStagePitch) + 2 * (lane & 15);
+                if (c + 1 < N)
+                    *reinterpret_cast<__half2*>(dst) = *reinterpret_cast<const __half2*>(src);
+                else
+                    dst[0] = src[0];
+            }
         }
     } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (col0 + i < N) crow[col0 + i] = __float2half_rn(v[i]);
+        // one element per lane, one row per instruction
+#pragma unroll 4
+        for (int rr = 0; rr < 32; ++rr) {
+            const int row = row0 + rr;
+            const int c = col0 + lane;
+            if (row < M && c < N)
+                C[static_cast<int64_t>(row) * N + c] =
+                    reinterpret_cast<const __half*>(stage + rr * kStagePitch)[lane];
+        }
     }
+    __syncwarp();  // the buffer is rewritten by this warp's next chunk
 }
 
 }  // namespace tg

@@ -16,6 +16,10 @@ constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kStages = 4;
 constexpr int kGroupM = 16;  // tile rows per rasterisation group (L2 reuse)
+#ifndef TG_PAIR_GROUP_M
+#define TG_PAIR_GROUP_M 8
+#endif
+constexpr int kPairGroupM = TG_PAIR_GROUP_M;  // 256-row tile rows per group, CTA-pair kernel
 // Epilogue warps of the tiled kernels: one per TMEM lane quarter (4), or two
 // per quarter each taking half of a tile's 32-column chunks (8). Measured on
 // GB300, 4 is as fast as 8 with erf-GELU and slightly faster without it.
@@ -60,7 +64,8 @@ struct TiledArgs {
     int M, N, K;
     int gelu;
     int m_blocks, n_blocks, num_tiles, num_kb, group_m;
-    int c_vec;     // C rows start 16-byte aligned and N % 8 == 0: 16-byte stores
+    int c_store;   // how C may be written: 2 = 16-byte units (C 16-byte aligned, N % 8 == 0),
+                   // 1 = 4-byte units (C 4-byte aligned, N even), 0 = single elements
     int bias_vec;  // bias 16-byte aligned: 16-byte loads
     int a_vec;     // ordinary-load staging width for A in elements: 8, 2 or 1
     int b_vec;     // same for B
