@@ -213,30 +213,42 @@ def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sam
             "launch_ms": launch_ms, "clocks": clocks}
 
 
-def time_e2e(tg, w, steps: int, warmup: int):
+def time_e2e(tg, w, steps: int, warmup: int, n_streams: int = 2):
     """Same metric through the host-buffer entry point: every step copies the
-    inputs from pinned host memory, runs the GEMM and copies C back."""
+    step's inputs from pinned host memory, runs the GEMM and copies C back
+    (tg_gemm_staged). Steps alternate between `n_streams` streams, each with its
+    own device buffers, so one step's copies overlap another step's kernel."""
     import torch
     A, B, bias = w.inputs()
     hA, hB = A.pin_memory(), B.pin_memory()
     hb = bias.pin_memory() if bias is not None else None
-    hC = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
-    dA, dB = torch.empty_like(A, device="cuda"), torch.empty_like(B, device="cuda")
-    db = torch.empty_like(bias, device="cuda") if bias is not None else None
-    dC = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
-    stream = torch.cuda.current_stream()
+    hC = [torch.empty((w.M, w.N), dtype=torch.float16).pin_memory() for _ in range(n_streams)]
+    dev = [(torch.empty_like(A, device="cuda"), torch.empty_like(B, device="cuda"),
+            torch.empty_like(bias, device="cuda") if bias is not None else None,
+            torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")) for _ in range(n_streams)]
+    streams = [torch.cuda.Stream() for _ in range(n_streams)]
+    main = torch.cuda.current_stream()
 
-    def step():
-        tg.gemm_staged(hA, hB, hb, hC, dA, dB, db, dC, gelu=w.gelu, stream=stream)
+    def run(n):
+        start = torch.cuda.Event()
+        start.record(main)
+        for s in streams:
+            s.wait_event(start)
+        for i in range(n):
+            j = i % n_streams
+            dA, dB, db, dC = dev[j]
+            tg.gemm_staged(hA, hB, hb, hC[j], dA, dB, db, dC, gelu=w.gelu, stream=streams[j])
+        for s in streams:
+            done = torch.cuda.Event()
+            done.record(s)
+            main.wait_event(done)
 
-    for _ in range(warmup):
-        step()
+    run(warmup)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
+    e0.record(main)
+    run(steps)
+    e1.record(main)
     e1.synchronize()
     ms = e0.elapsed_time(e1)
     h2d = 2 * (w.M * w.K + w.K * w.N) + (2 * w.N if bias is not None else 0)
@@ -339,7 +351,8 @@ def run_gpu(args):
         ms, h2d, d2h = time_e2e(tg, main, e2e_steps, 2)
         out["e2e"] = {"value": round(main.flops() * e2e_steps / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                      "ms_per_step": round(ms / e2e_steps, 4), "api": "tg_gemm_staged (pinned host buffers)"}
+                      "ms_per_step": round(ms / e2e_steps, 4),
+                      "api": "tg_gemm_staged, pinned host buffers, steps alternating over 2 streams"}
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(main, args.cpu_budget_s, "TFLOP/s")
         print(json.dumps(out), flush=True)

@@ -1,0 +1,106 @@
+"""Host-side logic of bench.py, on CPU: max-over-ranks timing across a
+world_size-2 gloo group (the N>1 replicas path), roofline arithmetic, the
+staleness rule for recorded DRAM traffic, and the reference arm (the CPU
+oracle) producing its JSON line."""
+import importlib.util
+import io
+import json
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+from types import SimpleNamespace
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    m = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(m)
+    return m
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    b = _bench()
+    w, r, local, pg = b.dist_setup(world)
+    assert (w, r, local) == (world, rank, rank)
+    b.barrier(pg)
+    m = b.max_over_ranks(pg, 10.0 + rank)   # each rank times a different region
+    out[rank] = m
+    pg.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world_2():
+    port = _free_port()
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
+        assert dict(out) == {0: 11.0, 1: 11.0}
+
+
+def test_roofline_entry_math():
+    b = _bench()
+    import workloads
+    pk = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0}
+    w = workloads.SQUARE_8192
+    e = b.roofline_entry(w, 0.55, pk, "measured", "tensor", traffic=123)
+    assert e["achieved"] == pytest.approx(w.flops() / 0.55e-3 / 1e12, rel=1e-4)
+    assert e["frac"] == pytest.approx(e["achieved"] / 2000.0, abs=1e-4)
+    assert e["frac_of_sustained"] == pytest.approx(e["achieved"] / 1600.0, abs=1e-4)
+    assert e["traffic"] == 123 and e["unit"] == "TFLOP/s"
+    d = workloads.DECODE
+    e = b.roofline_entry(d, 0.0785, pk, "measured", "hbm")
+    assert e["unit"] == "GB/s" and e["achieved"] == pytest.approx(d.bytes() / 0.0785e-3 / 1e9, rel=1e-4)
+
+
+def test_recorded_traffic_is_dropped_when_kernels_change(tmp_path, monkeypatch):
+    b = _bench()
+    (tmp_path / "profiles").mkdir()
+    rec = {"square_8192": {"dram_bytes_per_launch": 42, "kernel_hash": "not-the-current-hash"}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(b, "ROOT", str(tmp_path))
+    monkeypatch.setattr(b, "kernel_source_hash", lambda: "current")
+    assert b.recorded_traffic("square_8192") is None
+    rec["square_8192"]["kernel_hash"] = "current"
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    assert b.recorded_traffic("square_8192") == 42
+    assert b.recorded_traffic("decode_16x28672x8192") is None
+
+
+def test_reference_arm_prints_its_line(monkeypatch):
+    b = _bench()
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    args = SimpleNamespace(workload="square_256", steps=2, warmup=1, ref_budget_s=0.5)
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        b.run_reference(args)
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_reference_arm_other_ranks_do_nothing(monkeypatch):
+    b = _bench()
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        b.run_reference(SimpleNamespace(workload="square_256", steps=1, warmup=1, ref_budget_s=0.1))
+    assert buf.getvalue() == ""
