@@ -139,9 +139,10 @@ tg_status tg_gemm_staged(const void* hA, const void* hB, const void* hbias, void
  * slice, the partial sums and arrival counters live in one fixed array of
  * TG_NOALLOC_SCRATCH_BYTES compiled into the library's device image: every
  * device that loads the library holds it until the process exits. A call whose
- * slices need more (4 * slices * M * N bytes of partials plus 4 bytes per
- * 256-column slice of N, rounded up to 256) returns TG_ERR_INVALID_ARG and
- * enqueues nothing. Nothing is allocated or freed by any call.
+ * slices need more (4 * slices * N * Mp bytes of partials, Mp = M rounded up to
+ * a multiple of 16, plus 4 bytes per 256-column slice of N, rounded up to 256)
+ * returns TG_ERR_INVALID_ARG and enqueues nothing. Nothing is allocated or
+ * freed by any call.
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before

@@ -206,15 +206,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive(acc_empty_bar(b));  // both accumulators of buffer b are read
                     }
                     if (!n_ok) continue;
+                    if (args.splits == 1) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = c * 16 + i;
-                        if (m >= args.M) break;
-                        const float v = __uint_as_float(r[i]);
-                        if (args.splits == 1)
-                            args.C[static_cast<int64_t>(m) * args.N + n] = __float2half_rn(epi_value(v, bias_n, args.gelu));
-                        else
-                            args.ws[(static_cast<int64_t>(sp) * args.M + m) * args.N + n] = v;
+                        for (int i = 0; i < 16; ++i) {
+                            const int m = c * 16 + i;
+                            if (m >= args.M) break;
+                            args.C[static_cast<int64_t>(m) * args.N + n] =
+                                __float2half_rn(epi_value(__uint_as_float(r[i]), bias_n, args.gelu));
+                        }
+                    } else {
+                        // partials as [slice][n][m_pad]: this thread's 16 rows are 64 contiguous bytes
+                        uint4* wp = reinterpret_cast<uint4*>(
+                            args.ws + (static_cast<int64_t>(sp) * args.N + n) * args.m_pad + c * 16);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) wp[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
                     }
                 }
             }
@@ -235,16 +240,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (n >= args.N) continue;
                         const float bias_n = args.bias != nullptr ? __half2float(args.bias[n]) : 0.0f;
                         for (int m0 = 0; m0 < args.M; m0 += 16) {
-                            // 16 rows at a time: 16 independent loads per slice in flight;
-                            // each row still sums its slices in order 0, 1, ... (deterministic)
+                            // this column's 16 rows m0..m0+15 of every slice: four 16-byte loads per
+                            // slice; each row sums its slices in order 0, 1, ... (deterministic)
                             float s[16];
 #pragma unroll
                             for (int i = 0; i < 16; ++i) s[i] = 0.0f;
                             for (int q = 0; q < args.splits; ++q) {
-                                const float* wq = args.ws + (static_cast<int64_t>(q) * args.M + m0) * args.N + n;
+                                const float4* wq = reinterpret_cast<const float4*>(
+                                    args.ws + (static_cast<int64_t>(q) * args.N + n) * args.m_pad + m0);
 #pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    if (m0 + i < args.M) s[i] += __ldcg(wq + static_cast<int64_t>(i) * args.N);
+                                for (int v4 = 0; v4 < 4; ++v4) {
+                                    const float4 p = __ldcg(wq + v4);
+                                    s[4 * v4] += p.x;
+                                    s[4 * v4 + 1] += p.y;
+                                    s[4 * v4 + 2] += p.z;
+                                    s[4 * v4 + 3] += p.w;
+                                }
                             }
 #pragma unroll
                             for (int i = 0; i < 16; ++i)

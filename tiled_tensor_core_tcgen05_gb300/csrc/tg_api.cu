@@ -130,6 +130,16 @@ Watchdog watchdog(const DeviceState& d) {
     return Watchdog{d.status_ptr, g_watchdog_ns.load(), g_skip_first_arrive.load()};
 }
 
+// Tile rows per rasterisation group: A strips of about kGroupBytes, at least 1,
+// at most all tile rows.
+int group_rows(int tile_rows, int K, int m_blocks) {
+    const int64_t strip = static_cast<int64_t>(tile_rows) * K * 2;
+    int64_t g = strip > 0 ? kGroupBytes / strip : m_blocks;
+    if (g < 1) g = 1;
+    if (g > m_blocks) g = m_blocks;
+    return static_cast<int>(g);
+}
+
 // Split count for the skinny kernel. Time is modelled in units of one K
 // block's transfer at one SM's streaming rate: a CTA's share is its waves of
 // work units, each costing its K blocks plus a fixed charge for refilling the
@@ -211,7 +221,7 @@ tg_status run_splitk(DeviceState& d, const __half* A, const __half* B, const __h
     a.wd = watchdog(d);
     if (a.splits > 1) {
         Scratch* sc = nullptr;
-        tg_status st = ensure_scratch(d, stream, static_cast<size_t>(a.splits) * M * N * sizeof(float),
+        tg_status st = ensure_scratch(d, stream, static_cast<size_t>(a.splits) * N * a.m_pad * sizeof(float),
                                       static_cast<size_t>(a.n_tiles), &sc);
         if (st != TG_OK) return st;
         a.ws = sc->ws;
@@ -236,7 +246,7 @@ tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, 
     a.n_blocks = (N + kBN - 1) / kBN;
     a.num_tiles = a.m_blocks * a.n_blocks;
     a.num_kb = (K + kBK - 1) / kBK;
-    a.group_m = kGroupM;
+    a.group_m = group_rows(kBM, K, a.m_blocks);
     a.c_store = (N % 8 == 0 && aligned(C, 16)) ? 2 : ((N % 2 == 0 && aligned(C, 4)) ? 1 : 0);
     a.bias_vec = (bias != nullptr && aligned(bias, 16)) ? 1 : 0;
     a.a_vec = vec_width(A, K);
@@ -266,7 +276,7 @@ tg_status run_tiled_pair(DeviceState& d, const __half* A, const __half* B, const
     a.n_blocks = (N + kBN - 1) / kBN;
     a.num_tiles = a.m_blocks * a.n_blocks;
     a.num_kb = (K + kBK - 1) / kBK;
-    a.group_m = kPairGroupM;
+    a.group_m = group_rows(2 * kBM, K, a.m_blocks);
     a.c_store = (N % 8 == 0 && aligned(C, 16)) ? 2 : ((N % 2 == 0 && aligned(C, 4)) ? 1 : 0);
     a.bias_vec = (bias != nullptr && aligned(bias, 16)) ? 1 : 0;
     a.a_vec = a.b_vec = 8;
@@ -465,7 +475,7 @@ void tg_shutdown(void) {
 namespace {
 
 // Layout: one arrival counter per 256-column slice of N (padded to 256 bytes),
-// then the fp32 partial sums [split][M][N]. Loaded with the library's device
+// then the fp32 partial sums [split][N][M rounded up to 16]. Loaded with the library's device
 // code, so every device that loads the library holds these bytes until exit.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[TG_NOALLOC_SCRATCH_BYTES];
 
@@ -537,7 +547,7 @@ extern "C" tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const 
     a.wd = watchdog(d);
     if (a.splits > 1) {
         const size_t counter_bytes = (static_cast<size_t>(a.n_tiles) * sizeof(unsigned int) + 255) / 256 * 256;
-        const size_t partial_bytes = static_cast<size_t>(a.splits) * a.M * a.N * sizeof(float);
+        const size_t partial_bytes = static_cast<size_t>(a.splits) * a.N * a.m_pad * sizeof(float);
         if (counter_bytes + partial_bytes > static_cast<size_t>(TG_NOALLOC_SCRATCH_BYTES))
             return fail(TG_ERR_INVALID_ARG,
                         "tg_gemm_splitk_noalloc: %d K slices of a %lld x %lld product need %zu bytes of scratch, "

@@ -15,11 +15,13 @@ constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kStages = 4;
-constexpr int kGroupM = 16;  // tile rows per rasterisation group (L2 reuse)
-#ifndef TG_PAIR_GROUP_M
-#define TG_PAIR_GROUP_M 8
-#endif
-constexpr int kPairGroupM = TG_PAIR_GROUP_M;  // 256-row tile rows per group, CTA-pair kernel
+// Rasterisation: tiles are visited in groups of G tile rows (all columns of a
+// group before the next), so the A strips of one group are re-read from L2
+// while B streams past. G is sized so that those strips (G x tile rows x K x 2
+// bytes) take about kGroupBytes: measured on GB300 for 8192^3, groups of
+// 8 x 256 rows (32 MB) read 1.06 GB from HBM per launch, 16 rows 1.25 GB and
+// 32 rows 2.09 GB.
+constexpr int64_t kGroupBytes = 32ll << 20;
 // Epilogue warps of the tiled kernels: one per TMEM lane quarter (4), or two
 // per quarter each taking half of a tile's 32-column chunks (8). Measured on
 // GB300, 4 is as fast as 8 with erf-GELU and slightly faster without it.
@@ -89,7 +91,7 @@ struct SplitArgs {
     int tmem_cols;     // TMEM columns allocated (2 * kSkHalves * tmem_stride, >= 32)
     int stages;        // ring depth
     int n_tiles, kb_total, kb_per_split, splits, num_units;
-    float* ws;               // splits * M * N fp32 partial sums (splits > 1)
+    float* ws;               // splits * N * m_pad fp32 partial sums, [slice][n][m] (splits > 1)
     unsigned int* counters;  // n_tiles arrival counters, zero between launches
     Watchdog wd;
 };
