@@ -256,6 +256,33 @@ def time_e2e(tg, w, steps: int, warmup: int, n_streams: int = 2):
     return ms, h2d, d2h
 
 
+def time_unfused(tg, w, steps: int, warmup: int):
+    """The unfused comparator for a workload with an epilogue: the GEMM with no
+    epilogue and no bias (C written to HBM), then tg_bias_gelu reading C back,
+    adding the bias, applying GELU and writing C again. Returns ms per step."""
+    import torch
+    A, B, bias = w.inputs()
+    dA, dB = A.cuda(), B.cuda()
+    db = bias.cuda() if bias is not None else None
+    dC = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
+    sh = torch.cuda.current_stream().cuda_stream
+
+    def step():
+        tg.tg_gemm(dA.data_ptr(), dB.data_ptr(), None, dC.data_ptr(), w.M, w.N, w.K, tg.EPI_NONE, sh)
+        tg.tg_bias_gelu(dC.data_ptr(), db.data_ptr() if db is not None else None, w.M, w.N, int(w.gelu), sh)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def roofline_entry(w, avg_launch_ms, pk, pk_kind, bound, traffic=None):
     t = avg_launch_ms / 1e3
     if bound == "tensor":
@@ -343,6 +370,12 @@ def run_gpu(args):
                  "TFLOP/s": round(w.flops() / (avg / 1e3) / 1e12, 2),
                  "GB/s": round(w.bytes() / (avg / 1e3) / 1e9, 1),
                  "roofline": roofline_entry(w, avg, pk, pk_kind, bound, recorded_traffic(w.name))}
+            if w.gelu or w.has_bias:
+                # unfused comparator, back to back (the fused figure above is per launch)
+                un_ms = time_unfused(tg, w, steps, max(3, args.warmup))
+                e["unfused_ms_per_step"] = round(un_ms, 5)
+                e["fusion_speedup"] = round(un_ms / avg, 3)
+                out["gpu_launches"] += 2 * steps
             extra.append(e)
             out["gpu_launches"] += steps
     out["workloads"] = extra

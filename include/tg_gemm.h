@@ -119,6 +119,19 @@ tg_status tg_gemm_staged(const void* hA, const void* hB, const void* hbias, void
                          void* dA, void* dB, void* dbias, void* dC,
                          int64_t M, int64_t N, int64_t K, int epilogue, tg_stream_t stream);
 
+/*
+ * The epilogue alone, in place: C[i,j] = epi(C[i,j] + bias[j]) on an M x N
+ * row-major binary16 DEVICE matrix (bias NULL = no bias; epilogue a
+ * tg_epilogue value), computed in fp32 and rounded once more to binary16.
+ * This is the unfused comparator for the fused epilogue described in
+ * "Designing high-performance GPU kernels with TileLang ...", section 3
+ * ("Epilogue Fusion and Memory Efficiency"): tg_gemm with TG_EPI_NONE and no
+ * bias, then this pass, computes the same function with the product rounded
+ * to binary16 in between and two extra HBM passes over C. Any alignment;
+ * stream-ordered; allocates nothing.
+ */
+tg_status tg_bias_gelu(void* C, const void* bias, int64_t M, int64_t N, int epilogue, tg_stream_t stream);
+
 /* Size of the fixed scratch array behind tg_gemm_splitk_noalloc (8 MiB). */
 #define TG_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
 

@@ -26,7 +26,7 @@ KERNEL_AUTO, KERNEL_TILED_TMA, KERNEL_TILED_LSU, KERNEL_SPLITK, KERNEL_TILED_PAI
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NO_MEMORY = range(6)
 
 # every symbol include/tg_gemm.h declares
-EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_device_status",
+EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_bias_gelu", "tg_device_status",
            "tg_set_watchdog_ns",
            "tg_debug_skip_first_arrive", "tg_status_string", "tg_last_error", "tg_version",
            "tg_ring_bytes", "tg_shutdown")
@@ -41,6 +41,7 @@ _lib.tg_gemm.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
 _lib.tg_gemm_ex.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp]
 _lib.tg_gemm_staged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
 _lib.tg_gemm_splitk_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
+_lib.tg_bias_gelu.argtypes = [_vp, _vp, _i64, _i64, _int, _vp]
 _lib.tg_device_status.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.tg_set_watchdog_ns.argtypes = [_u64]
 _lib.tg_debug_skip_first_arrive.argtypes = [_int]
@@ -53,7 +54,7 @@ _lib.tg_ring_bytes.argtypes = [_int]
 _lib.tg_ring_bytes.restype = _i64
 _lib.tg_shutdown.argtypes = []
 _lib.tg_shutdown.restype = None
-for _name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_device_status",
+for _name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_bias_gelu", "tg_device_status",
               "tg_set_watchdog_ns",
               "tg_debug_skip_first_arrive", "tg_version"):
     getattr(_lib, _name).restype = _int
@@ -96,6 +97,18 @@ def tg_gemm_splitk_noalloc(A: int, B: int, bias: int | None, C: int, M: int, N: 
     array, for callers that must not have the library allocate device memory
     (see include/tg_gemm.h for the size limit and the sharing rules)."""
     _check(_lib.tg_gemm_splitk_noalloc(A, B, bias, C, M, N, K, epilogue, split_k, stream))
+
+
+def tg_bias_gelu(C: int, bias: int | None, M: int, N: int, epilogue: int, stream: int | None) -> None:
+    _check(_lib.tg_bias_gelu(C, bias, M, N, epilogue, stream))
+
+
+def bias_gelu_(C, bias=None, gelu: bool = True, stream=None):
+    """In place C = epi(C + bias) on a CUDA float16 matrix (the unfused epilogue pass)."""
+    M, N = C.shape
+    tg_bias_gelu(_dev_fp16(C, "C"), _dev_fp16(bias, "bias") if bias is not None else None, M, N,
+                 EPI_GELU if gelu else EPI_NONE, _stream_handle(stream))
+    return C
 
 
 def tg_device_status(stream: int | None) -> tuple[int, int]:

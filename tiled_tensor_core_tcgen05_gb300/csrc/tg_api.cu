@@ -415,6 +415,26 @@ tg_status tg_device_status(tg_stream_t stream_, int* where) {
     return fail(TG_ERR_TIMEOUT, "a kernel wait expired (site %d)", v);
 }
 
+tg_status tg_bias_gelu(void* C, const void* bias, int64_t M, int64_t N, int epilogue, tg_stream_t stream_) {
+    t_last_error.clear();
+    const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_GELU)
+        return fail(TG_ERR_INVALID_ARG, "epilogue must be TG_EPI_NONE (0) or TG_EPI_GELU (1), got %d", epilogue);
+    if (M < 0 || N < 0 || M > 0x7FFFFFFFll || N > 0x7FFFFFFFll)
+        return fail(TG_ERR_INVALID_ARG, "sizes must be in [0, 2^31): M=%lld N=%lld", (long long)M, (long long)N);
+    if (M == 0 || N == 0) return TG_OK;
+    if (C == nullptr) return fail(TG_ERR_INVALID_ARG, "C is NULL");
+    if (overlaps(C, M * N * 2, bias, bias ? N * 2 : 0)) return fail(TG_ERR_INVALID_ARG, "C overlaps bias");
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    tg_status st = current_device(&dev);
+    if (st != TG_OK) return st;
+    const bool vec8 = N % 8 == 0 && aligned(C, 16) && (bias == nullptr || aligned(bias, 16));
+    cudaError_t e = launch_bias_gelu(static_cast<__half*>(C), static_cast<const __half*>(bias), M, N,
+                                     epilogue == TG_EPI_GELU ? 1 : 0, vec8, g_dev[dev].sm_count, stream);
+    return e == cudaSuccess ? TG_OK : cuda_fail(e, "epilogue kernel launch");
+}
+
 tg_status tg_set_watchdog_ns(uint64_t ns) {
     g_watchdog_ns.store(ns == 0 ? 2000000000ull : ns);
     return TG_OK;

@@ -110,6 +110,8 @@ cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const 
                               cudaStream_t stream);
 cudaError_t launch_splitk(const SplitArgs& a, const CUtensorMap& tmB, const CUtensorMap& tmA,
                           int grid, cudaStream_t stream);
+cudaError_t launch_bias_gelu(__half* C, const __half* bias, int64_t M, int64_t N, int gelu, bool vec8, int sm_count,
+                             cudaStream_t stream);
 cudaError_t launch_fill(const __half* bias, __half* C, int64_t M, int64_t N, int gelu,
                         int sm_count, cudaStream_t stream);
 
