@@ -61,6 +61,14 @@ def _bind(lib):
     lib.oracle_gemm_sampled.argtypes = [u16p, u16p, u16p, i64, i64, i64, ctypes.c_int,
                                         i64p, i64p, i64, u16p, f64p, ctypes.c_int]
     lib.oracle_gemm_sampled.restype = ctypes.c_int
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    lib.oracle_int4_value.argtypes = [ctypes.c_uint8, ctypes.c_int]
+    lib.oracle_int4_value.restype = ctypes.c_int
+    lib.oracle_dequant_w4.argtypes = [u8p, u16p, u16p, i64, i64, i64]
+    lib.oracle_dequant_w4.restype = ctypes.c_int
+    lib.oracle_gemm_w4_rows.argtypes = [u16p, u8p, u16p, u16p, u16p, f64p, i64, i64, i64, i64, ctypes.c_int,
+                                        i64, i64, ctypes.c_int]
+    lib.oracle_gemm_w4_rows.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -146,6 +154,43 @@ class Oracle:
         out = out.view(np.float16)
         return (out, out64) if want_f64 else out
 
+    def int4_value(self, byte: int, high: bool) -> int:
+        return int(self._lib.oracle_int4_value(int(byte) & 0xFF, 4 if high else 0))
+
+    def dequant_w4(self, Bq, scales, group: int = 128):
+        """W (K x N, np.float16): q * scale rounded once to binary16."""
+        q, sc = _u8(Bq), _bits(scales)
+        K, half_n = q.shape
+        N = 2 * half_n
+        W = np.empty((K, N), dtype=np.uint16)
+        rc = self._lib.oracle_dequant_w4(_ptr(q, ctypes.c_uint8), _ptr(sc, ctypes.c_uint16), _ptr(W, ctypes.c_uint16),
+                                         N, K, int(group))
+        if rc != 0:
+            raise RuntimeError("oracle_dequant_w4 failed")
+        return W.view(np.float16)
+
+    def gemm_w4(self, A, Bq, scales, bias=None, gelu: bool = False, group: int = 128,
+                rows: tuple[int, int] | None = None, want_f64: bool = False, threads: int = 0):
+        """C = epi(A @ W + bias) with W the dequantized 4-bit weights."""
+        a, q, sc, c = _bits(A), _u8(Bq), _bits(scales), _bits(bias)
+        M, K = a.shape
+        if q.shape[0] != K:
+            raise ValueError(f"packed weights have {q.shape[0]} rows, A has K={K}")
+        N = 2 * q.shape[1]
+        if sc.shape != ((K + group - 1) // group, N):
+            raise ValueError(f"scales must have shape ({(K + group - 1) // group}, {N}), got {sc.shape}")
+        r0, nr = (0, M) if rows is None else rows
+        out = np.empty((nr, N), dtype=np.uint16)
+        out64 = np.empty((nr, N), dtype=np.float64) if want_f64 else None
+        rc = self._lib.oracle_gemm_w4_rows(_ptr(a, ctypes.c_uint16), _ptr(q, ctypes.c_uint8),
+                                           _ptr(sc, ctypes.c_uint16), _ptr(c, ctypes.c_uint16),
+                                           _ptr(out, ctypes.c_uint16), _ptr(out64, ctypes.c_double),
+                                           M, N, K, int(group), int(bool(gelu)), r0, nr, int(threads))
+        if rc != 0:
+            raise RuntimeError("oracle_gemm_w4_rows failed")
+        out = out.view(np.float16)
+        return (out, out64) if want_f64 else out
+
     def gemm_sampled(self, A, B, bias, gelu: bool, rows, cols, want_f64: bool = False, threads: int = 0):
         """C[rows[t], cols[t]] for each t, each evaluated from the definition alone."""
         a, b, c = _bits(A), _bits(B), _bits(bias)
@@ -166,6 +211,17 @@ class Oracle:
             raise RuntimeError("oracle_gemm_sampled failed")
         out = out.view(np.float16)
         return (out, out64) if want_f64 else out
+
+
+def _u8(x) -> np.ndarray:
+    if hasattr(x, "numpy") and not isinstance(x, np.ndarray):
+        x = x.detach().contiguous().numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.int8:
+        x = x.view(np.uint8)
+    if x.dtype != np.uint8:
+        raise TypeError(f"expected packed bytes, got {x.dtype}")
+    return x
 
 
 def load_library(path: str) -> Oracle:
@@ -190,3 +246,6 @@ gelu = _default.gelu
 max_threads = _default.max_threads
 gemm = _default.gemm
 gemm_sampled = _default.gemm_sampled
+int4_value = _default.int4_value
+dequant_w4 = _default.dequant_w4
+gemm_w4 = _default.gemm_w4

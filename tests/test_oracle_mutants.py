@@ -11,7 +11,7 @@ import pytest
 pytestmark = pytest.mark.filterwarnings("ignore:overflow encountered in cast")
 
 import oracle
-from tests import test_oracle_codec, test_oracle_gemm
+from tests import test_oracle_codec, test_oracle_gemm, test_oracle_w4
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -36,12 +36,17 @@ MUTANTS = [
     ("fp32_accumulation", "double* acc = (double*)malloc((size_t)N * sizeof(double));",
      "float* acc = (float*)malloc((size_t)N * sizeof(float));"),
     ("sampled_wrong_index", "oracle_half_to_double(B[k * N + j])", "oracle_half_to_double(B[j * K + k])"),
+    ("int4_nibble_order", "row[n / 2], (n % 2) ? 4 : 0", "row[n / 2], (n % 2) ? 0 : 4"),
+    ("int4_unsigned", "return v >= 8 ? v - 16 : v;", "return v;"),
+    ("int4_group_index", "scales + (k / group) * N;", "scales + (k % group) * N;"),
+    ("int4_no_rounding_of_weights", "W[k * N + n] = oracle_double_to_half((double)q * oracle_half_to_double(srow[n]));",
+     "W[k * N + n] = oracle_double_to_half((double)q) ; (void)srow;"),
 ]
 
 
 def _pins():
     fns = []
-    for mod in (test_oracle_codec, test_oracle_gemm):
+    for mod in (test_oracle_codec, test_oracle_gemm, test_oracle_w4):
         for name, fn in inspect.getmembers(mod, inspect.isfunction):
             if name.startswith("test_") and "oracle_lib" in inspect.signature(fn).parameters:
                 fns.append(fn)

@@ -1,0 +1,86 @@
+"""Pins for the oracle's weight-only 4-bit GEMM: nibble decoding against
+numpy's two's-complement int8 shifts, dequantisation against numpy's fp64
+product rounded by numpy, hand-packed bytes, per-group scale indexing, a
+rank-1 closed form, and agreement with the (separately pinned) fp16 GEMM on
+the dequantised weights."""
+import numpy as np
+import pytest
+
+
+def f16(x):
+    return np.asarray(x, dtype=np.float64).astype(np.float16)
+
+
+def pack(q):
+    """q (K x N ints in [-8, 7]) -> K x N/2 bytes, low nibble = even column."""
+    u = (np.asarray(q, dtype=np.int64) & 0xF).astype(np.uint8)
+    return (u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8)
+
+
+def test_int4_decode_exhaustive(oracle_lib):
+    for b in range(256):
+        lo = int(np.right_shift(np.array((b << 4) & 0xFF, dtype=np.uint8).view(np.int8), 4))
+        hi = int(np.right_shift(np.array(b, dtype=np.uint8).view(np.int8), 4))
+        assert oracle_lib.int4_value(b, False) == lo, b
+        assert oracle_lib.int4_value(b, True) == hi, b
+
+
+def test_hand_packed_bytes(oracle_lib):
+    # row 0: 0x21 -> (1, 2); 0xF8 -> (-8, -1); row 1: 0x7F -> (-1, 7); 0x80 -> (0, -8)
+    Bq = np.array([[0x21, 0xF8], [0x7F, 0x80]], dtype=np.uint8)
+    s = f16([[1.0, 0.5, 2.0, -1.0]])
+    W = oracle_lib.dequant_w4(Bq, s, group=128).astype(np.float64)
+    assert np.array_equal(W, [[1.0, 1.0, -16.0, 1.0], [-1.0, 3.5, 0.0, 8.0]])
+
+
+def test_dequant_matches_numpy_rounding(oracle_lib):
+    rng = np.random.default_rng(0)
+    K, N, G = 300, 64, 128
+    q = rng.integers(-8, 8, size=(K, N))
+    s = f16(rng.uniform(-0.05, 0.05, size=((K + G - 1) // G, N)))
+    W = oracle_lib.dequant_w4(pack(q), s, group=G)
+    ref = (q.astype(np.float64) * s.astype(np.float64)[np.arange(K) // G, :]).astype(np.float16)
+    assert np.array_equal(W.view(np.uint16), ref.view(np.uint16))
+
+
+def test_group_boundaries(oracle_lib):
+    K, N, G = 256, 4, 128
+    q = np.ones((K, N), dtype=np.int64)
+    s = f16([[1.0] * N, [4.0] * N])
+    W = oracle_lib.dequant_w4(pack(q), s, group=G).astype(np.float64)
+    assert np.all(W[:128] == 1.0) and np.all(W[128:] == 4.0)
+
+
+def test_rank1_closed_form(oracle_lib):
+    # A rows constant u_i, all weights q = 3 with scale 2^-3: C[i,j] = K * u_i * 3/8
+    K, N, M = 512, 32, 5
+    u = np.array([1.0, -2.0, 0.5, 4.0, -0.25])
+    A = f16(np.repeat(u[:, None], K, axis=1))
+    Bq = pack(np.full((K, N), 3))
+    s = f16(np.full((K // 128, N), 0.125))
+    C = oracle_lib.gemm_w4(A, Bq, s, group=128)
+    assert np.array_equal(C.view(np.uint16), (K * 3 * 0.125 * np.outer(u, np.ones(N))).astype(np.float16).view(np.uint16))
+
+
+def test_agrees_with_fp16_gemm_on_dequantised_weights(oracle_lib):
+    rng = np.random.default_rng(2)
+    M, K, N = 7, 384, 48
+    A = f16(rng.uniform(-1, 1, size=(M, K)))
+    q = rng.integers(-8, 8, size=(K, N))
+    s = f16(rng.uniform(0.002, 0.006, size=(K // 128, N)))
+    bias = f16(rng.uniform(-0.1, 0.1, size=N))
+    W = oracle_lib.dequant_w4(pack(q), s)
+    for gelu in (False, True):
+        got = oracle_lib.gemm_w4(A, pack(q), s, bias, gelu=gelu)
+        ref = oracle_lib.gemm(A, W, bias, gelu=gelu)
+        assert np.array_equal(got.view(np.uint16), ref.view(np.uint16))
+    # and the product itself against numpy in fp64 on the numpy-dequantised weights
+    W64 = q.astype(np.float64) * s.astype(np.float64)[np.arange(K) // 128, :]
+    _, C64 = oracle_lib.gemm_w4(A, pack(q), s, want_f64=True)
+    np.testing.assert_allclose(C64, A.astype(np.float64) @ W64.astype(np.float16).astype(np.float64), rtol=1e-12,
+                               atol=1e-12)
+
+
+def test_bad_shapes_rejected(oracle_lib):
+    with pytest.raises(ValueError):
+        oracle_lib.gemm_w4(f16(np.zeros((2, 128))), np.zeros((128, 8), np.uint8), f16(np.zeros((2, 16))))

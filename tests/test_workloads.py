@@ -63,3 +63,14 @@ def test_integer_distribution_is_integer():
     A, B, _ = w.inputs()
     a = A.float().numpy()
     assert np.array_equal(a, np.round(a)) and a.min() >= -2 and a.max() <= 2
+
+
+def test_w4_workload_packing_and_bytes():
+    w = workloads.W4Workload("t", 3, 16, 256, seed=9)
+    A, Bq, s, b = w.inputs()
+    assert A.shape == (3, 256) and Bq.shape == (256, 8) and Bq.dtype == torch.uint8
+    assert s.shape == (2, 16) and s.dtype == torch.float16 and b is None
+    A2, Bq2, s2, _ = w.inputs()
+    assert torch.equal(Bq, Bq2) and torch.equal(s, s2)
+    d = workloads.DECODE_W4
+    assert d.bytes() == 2 * 16 * 8192 + 8192 * 28672 // 2 + 2 * 64 * 28672 + 2 * 16 * 28672

@@ -107,7 +107,67 @@ DECODE = Workload("decode_16x28672x8192", 16, 28672, 8192, seed=4,
                   note="decode-shaped skinny GEMM; HBM-bound on reading B")
 
 ALL = (SQUARE_256, RAGGED_GELU, SQUARE_8192, FFN_UP, DECODE)
-BY_NAME = {w.name: w for w in ALL}
+
+
+@dataclass(frozen=True)
+class W4Workload:
+    """A GEMM with 4-bit weights: A (M x K) fp16; B stored as K rows of N/2
+    bytes (two's-complement 4-bit values, low nibble = even column) plus one
+    fp16 scale per column and per group of `group` rows of K. The draws:
+    A, then the 4-bit values (uniform over [-8, 7]), then the scales, then the
+    bias, from one CPU torch.Generator seeded with `seed`."""
+    name: str
+    M: int
+    N: int
+    K: int
+    seed: int
+    group: int = 128
+    a_dist: Dist = Dist("normal", 0.0, 1.0)
+    scale_lo: float = 0.002
+    scale_hi: float = 0.006
+    bias_dist: Dist | None = None
+    gelu: bool = False
+
+    @property
+    def has_bias(self) -> bool:
+        return self.bias_dist is not None
+
+    def describe(self) -> str:
+        epi = ("bias+" if self.has_bias else "") + ("gelu" if self.gelu else ("none" if not self.has_bias else ""))
+        return (f"{self.name}: M={self.M} N={self.N} K={self.K} int4 weights, group {self.group}, "
+                f"epilogue={epi.rstrip('+')} seed={self.seed}")
+
+    def inputs(self, device: str = "cpu"):
+        """(A fp16, Bq uint8 K x N/2, scales fp16 ceil(K/group) x N, bias or None)."""
+        g = torch.Generator(device="cpu")
+        g.manual_seed(self.seed)
+        A = self.a_dist.draw((self.M, self.K), g)
+        q = torch.randint(-8, 8, (self.K, self.N), generator=g, dtype=torch.int16)
+        u = (q & 0xF).to(torch.uint8)
+        Bq = (u[:, 0::2] | (u[:, 1::2] << 4)).contiguous()
+        groups = (self.K + self.group - 1) // self.group
+        scales = (self.scale_lo + (self.scale_hi - self.scale_lo) *
+                  torch.rand((groups, self.N), generator=g, dtype=torch.float32)).to(torch.float16)
+        bias = self.bias_dist.draw((self.N,), g) if self.bias_dist is not None else None
+        out = [A, Bq, scales, bias]
+        if device != "cpu":
+            out = [t.to(device) if t is not None else None for t in out]
+        return tuple(out)
+
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    def bytes(self) -> int:
+        groups = (self.K + self.group - 1) // self.group
+        n = 2 * self.M * self.K + self.K * self.N // 2 + 2 * groups * self.N + 2 * self.M * self.N
+        if self.has_bias:
+            n += 2 * self.N
+        return n
+
+
+DECODE_W4 = W4Workload("decode_w4_16x28672x8192", 16, 28672, 8192, seed=5)
+W4_ALL = (DECODE_W4,)
+BY_NAME = {w.name: w for w in ALL + W4_ALL}
 
 
 def custom(M: int, N: int, K: int, seed: int, dist: Dist = U1, bias: Dist | None = None,
