@@ -158,10 +158,11 @@ class Oracle:
         return int(self._lib.oracle_int4_value(int(byte) & 0xFF, 4 if high else 0))
 
     def dequant_w4(self, Bq, scales, group: int = 128):
-        """W (K x N, np.float16): q * scale rounded once to binary16."""
+        """W (K x N, np.float16) from Bq (N x K/2 bytes, low nibble = even k):
+        q * scale rounded once to binary16."""
         q, sc = _u8(Bq), _bits(scales)
-        K, half_n = q.shape
-        N = 2 * half_n
+        N, half_k = q.shape
+        K = 2 * half_k
         W = np.empty((K, N), dtype=np.uint16)
         rc = self._lib.oracle_dequant_w4(_ptr(q, ctypes.c_uint8), _ptr(sc, ctypes.c_uint16), _ptr(W, ctypes.c_uint16),
                                          N, K, int(group))
@@ -174,9 +175,9 @@ class Oracle:
         """C = epi(A @ W + bias) with W the dequantized 4-bit weights."""
         a, q, sc, c = _bits(A), _u8(Bq), _bits(scales), _bits(bias)
         M, K = a.shape
-        if q.shape[0] != K:
-            raise ValueError(f"packed weights have {q.shape[0]} rows, A has K={K}")
-        N = 2 * q.shape[1]
+        if 2 * q.shape[1] != K:
+            raise ValueError(f"packed weights hold {2 * q.shape[1]} values per row, A has K={K}")
+        N = q.shape[0]
         if sc.shape != ((K + group - 1) // group, N):
             raise ValueError(f"scales must have shape ({(K + group - 1) // group}, {N}), got {sc.shape}")
         r0, nr = (0, M) if rows is None else rows

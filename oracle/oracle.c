@@ -195,9 +195,10 @@ int oracle_gemm_sampled(const uint16_t* A, const uint16_t* B, const uint16_t* bi
  * ("Quantized LLM inference"): weights are stored as 4-bit integers,
  * dequantized into a tile, and the tile is multiplied like an fp16 weight
  * matrix. The pages fix no format; the reading taken here:
- *   - Bq: K rows of N/2 bytes; byte j of row k holds q[k][2j] in its low 4 bits
- *     and q[k][2j+1] in its high 4 bits, each a two's-complement integer in
- *     [-8, 7];
+ *   - Bq: N rows of K/2 bytes, one row per output column n (the weight of
+ *     a linear layer, out x in); byte j of row n holds q[2j][n] in its low 4
+ *     bits and q[2j+1][n] in its high 4 bits, each a two's-complement integer
+ *     in [-8, 7];
  *   - scales: ceil(K/group) rows of N binary16 values; q[k][n] belongs to
  *     group k / group;
  *   - the dequantized weight is W[k][n] = q[k][n] * scale[k/group][n] rounded
@@ -213,12 +214,12 @@ int oracle_int4_value(uint8_t byte, int shift) {
 
 /* W (K x N binary16 bits) from the packed weights and scales. */
 int oracle_dequant_w4(const uint8_t* Bq, const uint16_t* scales, uint16_t* W, int64_t N, int64_t K, int64_t group) {
-    if (N < 0 || K < 0 || group <= 0 || (N % 2) != 0) return -1;
-    for (int64_t k = 0; k < K; ++k) {
-        const uint8_t* row = Bq + k * (N / 2);
-        const uint16_t* srow = scales + (k / group) * N;
-        for (int64_t n = 0; n < N; ++n) {
-            const int q = oracle_int4_value(row[n / 2], (n % 2) ? 4 : 0);
+    if (N < 0 || K < 0 || group <= 0 || (K % 2) != 0) return -1;
+    for (int64_t n = 0; n < N; ++n) {
+        const uint8_t* row = Bq + n * (K / 2);
+        for (int64_t k = 0; k < K; ++k) {
+            const uint16_t* srow = scales + (k / group) * N;
+            const int q = oracle_int4_value(row[k / 2], (k % 2) ? 4 : 0);
             W[k * N + n] = oracle_double_to_half((double)q * oracle_half_to_double(srow[n]));
         }
     }
@@ -229,7 +230,7 @@ int oracle_dequant_w4(const uint8_t* Bq, const uint16_t* scales, uint16_t* W, in
 int oracle_gemm_w4_rows(const uint16_t* A, const uint8_t* Bq, const uint16_t* scales, const uint16_t* bias,
                         uint16_t* C, double* C64, int64_t M, int64_t N, int64_t K, int64_t group, int gelu,
                         int64_t row0, int64_t nrows, int threads) {
-    if (N < 0 || K < 0 || (N % 2) != 0 || group <= 0) return -1;
+    if (N < 0 || K < 0 || (K % 2) != 0 || group <= 0) return -1;
     uint16_t* W = (uint16_t*)malloc((size_t)(K * N > 0 ? K * N : 1) * sizeof(uint16_t));
     if (!W) return -1;
     int rc = oracle_dequant_w4(Bq, scales, W, N, K, group);

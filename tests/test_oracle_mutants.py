@@ -36,7 +36,8 @@ MUTANTS = [
     ("fp32_accumulation", "double* acc = (double*)malloc((size_t)N * sizeof(double));",
      "float* acc = (float*)malloc((size_t)N * sizeof(float));"),
     ("sampled_wrong_index", "oracle_half_to_double(B[k * N + j])", "oracle_half_to_double(B[j * K + k])"),
-    ("int4_nibble_order", "row[n / 2], (n % 2) ? 4 : 0", "row[n / 2], (n % 2) ? 0 : 4"),
+    ("int4_nibble_order", "row[k / 2], (k % 2) ? 4 : 0", "row[k / 2], (k % 2) ? 0 : 4"),
+    ("int4_rows_along_k", "const uint8_t* row = Bq + n * (K / 2);", "const uint8_t* row = Bq + (n ^ 1) * (K / 2);"),
     ("int4_unsigned", "return v >= 8 ? v - 16 : v;", "return v;"),
     ("int4_group_index", "scales + (k / group) * N;", "scales + (k % group) * N;"),
     ("int4_no_rounding_of_weights", "W[k * N + n] = oracle_double_to_half((double)q * oracle_half_to_double(srow[n]));",

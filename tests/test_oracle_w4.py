@@ -12,9 +12,9 @@ def f16(x):
 
 
 def pack(q):
-    """q (K x N ints in [-8, 7]) -> K x N/2 bytes, low nibble = even column."""
-    u = (np.asarray(q, dtype=np.int64) & 0xF).astype(np.uint8)
-    return (u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8)
+    """q (K x N ints in [-8, 7]) -> N x K/2 bytes, low nibble = even k."""
+    u = (np.asarray(q, dtype=np.int64).T & 0xF).astype(np.uint8)
+    return np.ascontiguousarray(u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8)
 
 
 def test_int4_decode_exhaustive(oracle_lib):
@@ -26,11 +26,12 @@ def test_int4_decode_exhaustive(oracle_lib):
 
 
 def test_hand_packed_bytes(oracle_lib):
-    # row 0: 0x21 -> (1, 2); 0xF8 -> (-8, -1); row 1: 0x7F -> (-1, 7); 0x80 -> (0, -8)
+    # column n=0: 0x21 -> k0=1, k1=2; 0xF8 -> k2=-8, k3=-1
+    # column n=1: 0x7F -> k0=-1, k1=7; 0x80 -> k2=0, k3=-8
     Bq = np.array([[0x21, 0xF8], [0x7F, 0x80]], dtype=np.uint8)
-    s = f16([[1.0, 0.5, 2.0, -1.0]])
+    s = f16([[1.0, 0.5]])
     W = oracle_lib.dequant_w4(Bq, s, group=128).astype(np.float64)
-    assert np.array_equal(W, [[1.0, 1.0, -16.0, 1.0], [-1.0, 3.5, 0.0, 8.0]])
+    assert np.array_equal(W, [[1.0, -0.5], [2.0, 3.5], [-8.0, 0.0], [-1.0, -4.0]])
 
 
 def test_dequant_matches_numpy_rounding(oracle_lib):
@@ -83,4 +84,4 @@ def test_agrees_with_fp16_gemm_on_dequantised_weights(oracle_lib):
 
 def test_bad_shapes_rejected(oracle_lib):
     with pytest.raises(ValueError):
-        oracle_lib.gemm_w4(f16(np.zeros((2, 128))), np.zeros((128, 8), np.uint8), f16(np.zeros((2, 16))))
+        oracle_lib.gemm_w4(f16(np.zeros((2, 128))), np.zeros((16, 32), np.uint8), f16(np.zeros((1, 16))))

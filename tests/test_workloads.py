@@ -68,7 +68,7 @@ def test_integer_distribution_is_integer():
 def test_w4_workload_packing_and_bytes():
     w = workloads.W4Workload("t", 3, 16, 256, seed=9)
     A, Bq, s, b = w.inputs()
-    assert A.shape == (3, 256) and Bq.shape == (256, 8) and Bq.dtype == torch.uint8
+    assert A.shape == (3, 256) and Bq.shape == (16, 128) and Bq.dtype == torch.uint8
     assert s.shape == (2, 16) and s.dtype == torch.float16 and b is None
     A2, Bq2, s2, _ = w.inputs()
     assert torch.equal(Bq, Bq2) and torch.equal(s, s2)

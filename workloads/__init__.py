@@ -111,10 +111,11 @@ ALL = (SQUARE_256, RAGGED_GELU, SQUARE_8192, FFN_UP, DECODE)
 
 @dataclass(frozen=True)
 class W4Workload:
-    """A GEMM with 4-bit weights: A (M x K) fp16; B stored as K rows of N/2
-    bytes (two's-complement 4-bit values, low nibble = even column) plus one
-    fp16 scale per column and per group of `group` rows of K. The draws:
-    A, then the 4-bit values (uniform over [-8, 7]), then the scales, then the
+    """A GEMM with 4-bit weights: A (M x K) fp16; B stored as N rows of K/2
+    bytes, one row per output column (two's-complement 4-bit values, low
+    nibble = even k), plus one fp16 scale per column and per group of `group`
+    rows of K, stored ceil(K/group) x N. The draws: A, then the 4-bit values
+    q[n][k] (uniform over [-8, 7], drawn N x K), then the scales, then the
     bias, from one CPU torch.Generator seeded with `seed`."""
     name: str
     M: int
@@ -138,11 +139,11 @@ class W4Workload:
                 f"epilogue={epi.rstrip('+')} seed={self.seed}")
 
     def inputs(self, device: str = "cpu"):
-        """(A fp16, Bq uint8 K x N/2, scales fp16 ceil(K/group) x N, bias or None)."""
+        """(A fp16, Bq uint8 N x K/2, scales fp16 ceil(K/group) x N, bias or None)."""
         g = torch.Generator(device="cpu")
         g.manual_seed(self.seed)
         A = self.a_dist.draw((self.M, self.K), g)
-        q = torch.randint(-8, 8, (self.K, self.N), generator=g, dtype=torch.int16)
+        q = torch.randint(-8, 8, (self.N, self.K), generator=g, dtype=torch.int16)
         u = (q & 0xF).to(torch.uint8)
         Bq = (u[:, 0::2] | (u[:, 1::2] << 4)).contiguous()
         groups = (self.K + self.group - 1) // self.group
