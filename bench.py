@@ -162,20 +162,32 @@ def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sam
     """Time `steps` calls of tg_gemm on device-resident inputs. Returns the timed
     region (ms, max over ranks) and per-launch kernel durations."""
     import torch
-    A, B, bias = w.inputs()
-    dA, dB = A.cuda(), B.cuda()
-    db = bias.cuda() if bias is not None else None
-    dC = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
+    import workloads
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
-    args = (dA.data_ptr(), dB.data_ptr(), db.data_ptr() if db is not None else None, dC.data_ptr(),
-            w.M, w.N, w.K, int(w.gelu))
+    dC = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
+    if isinstance(w, workloads.W4Workload):
+        A, Bq, sc, bias = w.inputs()
+        dA, dB, ds = A.cuda(), Bq.cuda(), sc.cuda()
+        db = bias.cuda() if bias is not None else None
+        args = (dA.data_ptr(), dB.data_ptr(), ds.data_ptr(), db.data_ptr() if db is not None else None,
+                dC.data_ptr(), w.M, w.N, w.K, int(w.gelu), 0, sh)
+
+        def call():
+            tg.tg_gemm_w4(*args)
+    else:
+        A, B, bias = w.inputs()
+        dA, dB = A.cuda(), B.cuda()
+        db = bias.cuda() if bias is not None else None
+        args = (dA.data_ptr(), dB.data_ptr(), db.data_ptr() if db is not None else None, dC.data_ptr(),
+                w.M, w.N, w.K, int(w.gelu))
+
+        def call():
+            if kernel:
+                tg.tg_gemm_ex(*args, kernel, 0, sh)
+            else:
+                tg.tg_gemm(*args, sh)
     flush = torch.empty(flush_bytes, dtype=torch.uint8, device="cuda") if flush_bytes else None
-    def call():
-        if kernel:
-            tg.tg_gemm_ex(*args, kernel, 0, sh)
-        else:
-            tg.tg_gemm(*args, sh)
 
     for _ in range(warmup):
         call()
@@ -358,14 +370,14 @@ def run_gpu(args):
     # the rest of the suite, same rules, fewer steps
     extra = []
     if not args.only_main:
-        for w in workloads.ALL:
+        for w in workloads.ALL + workloads.W4_ALL:
             if w.name == main.name:
                 continue
             steps = max(5, min(args.steps, 50))  # secondary workloads: at most 50 timed launches
             r = time_workload(tg, w, steps, max(3, args.warmup), 0 if w.bytes() > 2 * l2 else 2 * l2 + (1 << 20),
                               pg=pg)
             avg = r["kernel_ms"] / steps
-            bound = "hbm" if w.name == workloads.DECODE.name else "tensor"
+            bound = "hbm" if w.M <= 128 else "tensor"  # the skinny (decode) shapes stream their weights
             e = {"workload": w.describe(), "ms_per_launch": round(avg, 5),
                  "TFLOP/s": round(w.flops() / (avg / 1e3) / 1e12, 2),
                  "GB/s": round(w.bytes() / (avg / 1e3) / 1e9, 1),

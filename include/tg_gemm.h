@@ -170,6 +170,34 @@ tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const void* bias,
                                  tg_stream_t stream);
 
 /*
+ * Weight-only 4-bit GEMM (decode shapes): C = epi(A @ W + bias) with W
+ * dequantized on chip, never written to memory. The form of the operation is
+ * that of "TileLang: writing LLM GPU kernels by thinking in tiles", section
+ * "Quantized LLM inference" (packed weights converted in a tile that feeds
+ * the tensor-core product); the pages fix no storage format, this is the
+ * library's:
+ *
+ *   A       M x K binary16, row-major, DEVICE, 16-byte aligned
+ *   Bq      N rows of K/2 bytes, DEVICE, 16-byte aligned: byte j of row n
+ *           holds q[2j][n] in bits 0-3 and q[2j+1][n] in bits 4-7, each a
+ *           two's-complement integer in [-8, 7] (the weight of a linear layer,
+ *           out x in, two values per byte along the input dimension)
+ *   scales  K/128 rows of N binary16 values, DEVICE, 16-byte aligned; q[k][n]
+ *           uses scales[k/128][n]
+ *   W       W[k][n] = q[k][n] * scales[k/128][n], rounded once to binary16
+ *   bias, C, epilogue, stream: as for tg_gemm.
+ *
+ * Needs M <= 128, K % 128 == 0 and N % 8 == 0 (TG_ERR_INVALID_ARG
+ * otherwise). M == 0 or N == 0 does nothing; K == 0 gives C = epi(bias).
+ * split_k: 0 = automatic, else the number of K slices (1..64, at most
+ * ceil(K / 256)); with more than one slice the library's per-stream scratch
+ * holds fp32 partial sums, reduced in slice order (deterministic). The
+ * tolerance is tg_gemm's, with W in place of B.
+ */
+tg_status tg_gemm_w4(const void* A, const void* Bq, const void* scales, const void* bias, void* C,
+                     int64_t M, int64_t N, int64_t K, int epilogue, int split_k, tg_stream_t stream);
+
+/*
  * Synchronises `stream`, then reports (and clears) the device-side status word
  * that kernels set when one of their bounded waits expires: TG_OK or
  * TG_ERR_TIMEOUT. `*where` (if not NULL) receives the code of the wait that

@@ -120,3 +120,30 @@ def test_product_package_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "oracle." not in text.replace("oracle.c", ""), f
                 assert "liboracle" not in text, f
+
+
+@pytest.mark.parametrize("args,msg", [
+    (dict(epilogue=3), "epilogue"),
+    (dict(M=129), "M <= 128"),
+    (dict(K=192), "K % 128"),
+    (dict(N=20), "N % 8"),
+    (dict(split_k=65), "split_k"),
+    (dict(C=0), "C is NULL"),
+    (dict(S=0), "A, Bq or scales"),
+    (dict(Bq=0x20000008), "16-byte aligned"),
+    (dict(C=0x20000000 + 64), "overlaps"),
+])
+def test_w4_invalid_arguments_rejected_on_host(tg, args, msg):
+    base = dict(A=0x10000, Bq=0x20000000, S=0x30000000, bias=None, C=0x40000000, M=16, N=64, K=256, epilogue=0,
+                split_k=0)
+    base.update(args)
+    with pytest.raises(tg.TgError) as ei:
+        tg.tg_gemm_w4(base["A"] or None, base["Bq"] or None, base["S"] or None, base["bias"], base["C"] or None,
+                      base["M"], base["N"], base["K"], base["epilogue"], base["split_k"], None)
+    assert ei.value.status == tg.ERR_INVALID_ARG
+    assert msg in str(ei.value)
+
+
+def test_w4_empty_products_need_no_device(tg):
+    tg.tg_gemm_w4(None, None, None, None, None, 0, 64, 256, 0, 0, None)
+    tg.tg_gemm_w4(None, None, None, None, None, 4, 0, 256, 1, 0, None)

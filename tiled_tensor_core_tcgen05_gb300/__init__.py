@@ -26,7 +26,8 @@ KERNEL_AUTO, KERNEL_TILED_TMA, KERNEL_TILED_LSU, KERNEL_SPLITK, KERNEL_TILED_PAI
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NO_MEMORY = range(6)
 
 # every symbol include/tg_gemm.h declares
-EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_bias_gelu", "tg_device_status",
+EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_bias_gelu",
+           "tg_device_status",
            "tg_set_watchdog_ns",
            "tg_debug_skip_first_arrive", "tg_status_string", "tg_last_error", "tg_version",
            "tg_ring_bytes", "tg_shutdown")
@@ -41,6 +42,7 @@ _lib.tg_gemm.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
 _lib.tg_gemm_ex.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp]
 _lib.tg_gemm_staged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
 _lib.tg_gemm_splitk_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
+_lib.tg_gemm_w4.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.tg_bias_gelu.argtypes = [_vp, _vp, _i64, _i64, _int, _vp]
 _lib.tg_device_status.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.tg_set_watchdog_ns.argtypes = [_u64]
@@ -54,7 +56,8 @@ _lib.tg_ring_bytes.argtypes = [_int]
 _lib.tg_ring_bytes.restype = _i64
 _lib.tg_shutdown.argtypes = []
 _lib.tg_shutdown.restype = None
-for _name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_bias_gelu", "tg_device_status",
+for _name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_bias_gelu",
+              "tg_device_status",
               "tg_set_watchdog_ns",
               "tg_debug_skip_first_arrive", "tg_version"):
     getattr(_lib, _name).restype = _int
@@ -97,6 +100,11 @@ def tg_gemm_splitk_noalloc(A: int, B: int, bias: int | None, C: int, M: int, N: 
     array, for callers that must not have the library allocate device memory
     (see include/tg_gemm.h for the size limit and the sharing rules)."""
     _check(_lib.tg_gemm_splitk_noalloc(A, B, bias, C, M, N, K, epilogue, split_k, stream))
+
+
+def tg_gemm_w4(A: int, Bq: int, scales: int, bias: int | None, C: int, M: int, N: int, K: int, epilogue: int,
+               split_k: int, stream: int | None) -> None:
+    _check(_lib.tg_gemm_w4(A, Bq, scales, bias, C, M, N, K, epilogue, split_k, stream))
 
 
 def tg_bias_gelu(C: int, bias: int | None, M: int, N: int, epilogue: int, stream: int | None) -> None:
@@ -187,6 +195,35 @@ def gemm(A, B, bias=None, gelu: bool = False, out=None, kernel: int = KERNEL_AUT
     pbias = _dev_fp16(bias, "bias") if bias is not None else None
     pc = _dev_fp16(out, "out") if out.numel() else None
     tg_gemm_ex(pa, pb, pbias, pc, M, N, K, EPI_GELU if gelu else EPI_NONE, kernel, split_k,
+               _stream_handle(stream))
+    return out
+
+
+def gemm_w4(A, Bq, scales, bias=None, gelu: bool = False, out=None, split_k: int = 0, stream=None):
+    """C = epi(A @ W + bias) with 4-bit weights: A (M, K) float16, Bq (N, K/2)
+    uint8 (low nibble = even k, two's complement), scales (K/128, N) float16,
+    W[k, n] = fp16(q[k, n] * scales[k // 128, n]). CUDA tensors, contiguous."""
+    import torch
+    if A.dim() != 2 or Bq.dim() != 2 or scales.dim() != 2:
+        raise ValueError("A, Bq and scales must be matrices")
+    M, K = A.shape
+    N = Bq.shape[0]
+    if 2 * Bq.shape[1] != K:
+        raise ValueError(f"Bq must have shape ({N}, {K // 2}), got {tuple(Bq.shape)}")
+    if tuple(scales.shape) != (K // 128, N):
+        raise ValueError(f"scales must have shape ({K // 128}, {N}), got {tuple(scales.shape)}")
+    if Bq.dtype != torch.uint8 or not Bq.is_cuda or not Bq.is_contiguous():
+        raise TypeError("Bq must be a contiguous CUDA uint8 tensor")
+    if bias is not None and tuple(bias.shape) != (N,):
+        raise ValueError(f"bias must have shape ({N},)")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    elif tuple(out.shape) != (M, N):
+        raise ValueError("out has the wrong shape")
+    tg_gemm_w4(_dev_fp16(A, "A") if A.numel() else None, Bq.data_ptr() if Bq.numel() else None,
+               _dev_fp16(scales, "scales") if scales.numel() else None,
+               _dev_fp16(bias, "bias") if bias is not None else None,
+               _dev_fp16(out, "out") if out.numel() else None, M, N, K, EPI_GELU if gelu else EPI_NONE, split_k,
                _stream_handle(stream))
     return out
 

@@ -23,6 +23,7 @@
 // no skinny-shape schedule, this one is designed for GB300's HBM.
 #include "tg_device.cuh"
 #include "tg_internal.h"
+#include "tg_skinny.cuh"
 
 namespace tg {
 namespace {
@@ -31,7 +32,6 @@ constexpr int kBoxB = kSkBK * 64 * 2;          // 64 (k) x 64 (n) N-major box, 8
 constexpr int kHalfBytes = 2 * kBoxB;          // one 128-column MMA half
 constexpr int kStageBBytes = kSkHalves * kHalfBytes;
 constexpr int kThreads = 6 * 32;            // producer, MMA, 4 epilogue warps
-constexpr int kEpiThreads = 128;
 
 struct Layout {
     int stage_bytes, ring, bar_full, bar_empty, bar_acc_full, bar_acc_empty, bar_drain, tmem_slot,
@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full_bar(b), 1);
-            mbar_init(acc_empty_bar(b), kEpiThreads);
+            mbar_init(acc_empty_bar(b), kSkEpiThreads);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -176,98 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        const int quarter = warp & 3;
-        const int ept = threadIdx.x - 64;  // 0..127
-        const int chunks = args.m_pad / 16;
-        int it = 0;
-        for (int u = blockIdx.x; u < args.num_units; u += gridDim.x, ++it) {
-            const int sp = u / args.n_tiles;
-            const int nt = u - sp * args.n_tiles;
-            const int b = it & 1;
-            const bool ok = wait_phase(acc_full_bar(b), (it >> 1) & 1, wc, kSiteEpilogueAccFull);
-            // all 128 epilogue threads stop together, so the named barriers below
-            // never wait for a thread that has left
-            if (named_barrier_or(1, kEpiThreads, !ok)) break;
-            tc_fence_after_sync();
-#pragma unroll 1
-            for (int h = 0; h < kSkHalves; ++h) {
-                const int n = nt * kSkBN + h * 128 + quarter * 32 + lane;  // this thread's output column
-                const bool n_ok = n < args.N;
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       (b * kSkHalves + h) * args.tmem_stride;
-                const float bias_n = (args.bias != nullptr && n_ok) ? __half2float(args.bias[n]) : 0.0f;
-                for (int c = 0; c < chunks; ++c) {
-                    uint32_t r[16];
-                    __syncwarp();  // tcgen05.ld is warp-collective; lanes diverged on the column mask
-                    tmem_ld_32x32b_x16(taddr + c * 16, r);
-                    tmem_ld_wait();
-                    if (h == kSkHalves - 1 && c == chunks - 1) {
-                        tc_fence_before_sync();
-                        mbar_arrive(acc_empty_bar(b));  // both accumulators of buffer b are read
-                    }
-                    if (!n_ok) continue;
-                    if (args.splits == 1) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int m = c * 16 + i;
-                            if (m >= args.M) break;
-                            args.C[static_cast<int64_t>(m) * args.N + n] =
-                                __float2half_rn(epi_value(__uint_as_float(r[i]), bias_n, args.gelu));
-                        }
-                    } else {
-                        // partials as [slice][n][m_pad]: this thread's 16 rows are 64 contiguous bytes
-                        uint4* wp = reinterpret_cast<uint4*>(
-                            args.ws + (static_cast<int64_t>(sp) * args.N + n) * args.m_pad + c * 16);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) wp[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
-                    }
-                }
-            }
-            if (args.splits > 1) {
-                // publish this slice's partials, then count arrivals for column slice nt
-                __threadfence();
-                named_barrier_sync(1, kEpiThreads);
-                if (ept == 0) {
-                    const unsigned int prev = atomicAdd(args.counters + nt, 1u);
-                    *last_flag = (prev == static_cast<unsigned int>(args.splits - 1)) ? 1 : 0;
-                }
-                named_barrier_sync(1, kEpiThreads);
-                if (*last_flag) {
-                    __threadfence();
-#pragma unroll 1
-                    for (int h = 0; h < kSkHalves; ++h) {
-                        const int n = nt * kSkBN + h * 128 + quarter * 32 + lane;
-                        if (n >= args.N) continue;
-                        const float bias_n = args.bias != nullptr ? __half2float(args.bias[n]) : 0.0f;
-                        for (int m0 = 0; m0 < args.M; m0 += 16) {
-                            // this column's 16 rows m0..m0+15 of every slice: four 16-byte loads per
-                            // slice; each row sums its slices in order 0, 1, ... (deterministic)
-                            float s[16];
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) s[i] = 0.0f;
-                            for (int q = 0; q < args.splits; ++q) {
-                                const float4* wq = reinterpret_cast<const float4*>(
-                                    args.ws + (static_cast<int64_t>(q) * args.N + n) * args.m_pad + m0);
-#pragma unroll
-                                for (int v4 = 0; v4 < 4; ++v4) {
-                                    const float4 p = __ldcg(wq + v4);
-                                    s[4 * v4] += p.x;
-                                    s[4 * v4 + 1] += p.y;
-                                    s[4 * v4 + 2] += p.z;
-                                    s[4 * v4 + 3] += p.w;
-                                }
-                            }
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (m0 + i < args.M)
-                                    args.C[static_cast<int64_t>(m0 + i) * args.N + n] =
-                                        __float2half_rn(epi_value(s[i], bias_n, args.gelu));
-                        }
-                    }
-                    if (ept == 0) atomicExch(args.counters + nt, 0u);
-                }
-            }
-        }
+        skinny_epilogue<kSkHalves>(args, tmem_base, acc_full_bar(0), acc_empty_bar(0), last_flag, wc, 64);
     }
 
     tc_fence_before_sync();

@@ -95,21 +95,30 @@ tg_status current_device(int* dev_out) {
     return TG_OK;
 }
 
-// Row-major [outer][inner] fp16 matrix, 128-byte-swizzled box of box_inner x box_outer,
-// out-of-bounds elements read as zero.
-tg_status make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                   uint32_t box_outer) {
+// Row-major [outer][inner] matrix of `elem_bytes`-byte elements, box of
+// box_inner x box_outer with the given swizzle; out-of-bounds elements read as
+// zero.
+tg_status make_map_ex(CUtensorMap* m, CUtensorMapDataType dtype, uint32_t elem_bytes, const void* base,
+                      uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                      CUtensorMapSwizzle swizzle) {
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * 2};
+    cuuint64_t strides[1] = {inner * elem_bytes};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    CUresult r = g_encode(m, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %llu x %llu matrix", (int)r,
                     (unsigned long long)outer, (unsigned long long)inner);
     return TG_OK;
+}
+
+// Row-major [outer][inner] fp16 matrix, 128-byte-swizzled box.
+tg_status make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                   uint32_t box_outer) {
+    return make_map_ex(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, inner, outer, box_inner, box_outer,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -140,16 +149,20 @@ int group_rows(int tile_rows, int K, int m_blocks) {
     return static_cast<int>(g);
 }
 
-// Split count for the skinny kernel. Time is modelled in units of one K
+// Split count for the skinny kernels. Time is modelled in units of one K
 // block's transfer at one SM's streaming rate: a CTA's share is its waves of
 // work units, each costing its K blocks plus a fixed charge for refilling the
-// pipeline and running the epilogue. HBM saturates before every SM streams, so
-// the job can never beat total / (kHbmFraction * SMs). Every split beyond the
-// first adds the partial-sum traffic of the final reduction. Ties keep fewer
-// splits.
-int choose_splits(int n_tiles, int kb_total, int sm_count) {
-    constexpr double kUnitOverhead = 6.0;    // pipeline refill + epilogue, in K blocks
-    constexpr double kReducePerSplit = 2.0;  // partial tile written and read back
+// pipeline and running the epilogue (unit_overhead, in K blocks). HBM
+// saturates before every SM streams, so the job can never beat
+// total / (kHbmFraction * SMs). Every split beyond the first adds the
+// partial-sum traffic of the final reduction (reduce_per_split, in K blocks).
+// Ties keep fewer splits. The fp16 kernel's block is 64 x 256 fp16 (32 KB);
+// the 4-bit kernel's is 256 x 128 packed (16 KB), so its fixed charges count
+// twice as many blocks.
+int choose_splits(int n_tiles, int kb_total, int sm_count, double unit_overhead = 6.0,
+                  double reduce_per_split = 2.0) {
+    const double kUnitOverhead = unit_overhead;
+    const double kReducePerSplit = reduce_per_split;
     constexpr double kHbmFraction = 0.7;     // share of SMs whose streams saturate HBM
     const double hbm_floor = static_cast<double>(n_tiles) * kb_total / (kHbmFraction * sm_count);
     int best_s = 1;
@@ -209,6 +222,7 @@ tg_status run_splitk(DeviceState& d, const __half* A, const __half* B, const __h
     a.m_pad = (M + 15) / 16 * 16;
     a.tmem_stride = 16;
     while (a.tmem_stride < a.m_pad) a.tmem_stride *= 2;
+    a.n_acc = 1;
     a.tmem_cols = 2 * kSkHalves * a.tmem_stride < 32 ? 32 : 2 * kSkHalves * a.tmem_stride;
     a.stages = split_stages_for(a.m_pad);
     a.n_tiles = (N + kSkBN - 1) / kSkBN;
@@ -555,6 +569,7 @@ extern "C" tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const 
     a.m_pad = (a.M + 15) / 16 * 16;
     a.tmem_stride = 16;
     while (a.tmem_stride < a.m_pad) a.tmem_stride *= 2;
+    a.n_acc = 1;
     a.tmem_cols = 2 * kSkHalves * a.tmem_stride < 32 ? 32 : 2 * kSkHalves * a.tmem_stride;
     a.stages = split_stages_for(a.m_pad);
     a.n_tiles = (a.N + kSkBN - 1) / kSkBN;
@@ -586,5 +601,97 @@ extern "C" tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const 
     const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
     cudaError_t e = launch_splitk(a, tmB, tmA, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "split-K kernel launch");
+    return TG_OK;
+}
+
+// ---------------------------------------------------------------------------
+// tg_gemm_w4: the skinny GEMM with 4-bit weights.
+
+extern "C" tg_status tg_gemm_w4(const void* A, const void* Bq, const void* scales, const void* bias, void* C,
+                                int64_t M, int64_t N, int64_t K, int epilogue, int split_k, tg_stream_t stream_) {
+    t_last_error.clear();
+    const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_GELU)
+        return fail(TG_ERR_INVALID_ARG, "epilogue must be TG_EPI_NONE (0) or TG_EPI_GELU (1), got %d", epilogue);
+    const int64_t kMax = 0x7FFFFFFFll;
+    if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax)
+        return fail(TG_ERR_INVALID_ARG, "sizes must be in [0, 2^31): M=%lld N=%lld K=%lld", (long long)M,
+                    (long long)N, (long long)K);
+    if (split_k < 0 || split_k > kSkMaxSplits)
+        return fail(TG_ERR_INVALID_ARG, "split_k must be 0 (automatic) or 1..%d, got %d", kSkMaxSplits, split_k);
+    if (M > kSkMaxM) return fail(TG_ERR_INVALID_ARG, "tg_gemm_w4 needs M <= %d, got %lld", kSkMaxM, (long long)M);
+    if (K % kW4Group != 0)
+        return fail(TG_ERR_INVALID_ARG, "tg_gemm_w4 needs K %% %d == 0, got K=%lld", kW4Group, (long long)K);
+    if (N % 8 != 0) return fail(TG_ERR_INVALID_ARG, "tg_gemm_w4 needs N %% 8 == 0, got N=%lld", (long long)N);
+    if (M == 0 || N == 0) return TG_OK;
+    if (C == nullptr) return fail(TG_ERR_INVALID_ARG, "C is NULL");
+    if (K > 0 && (A == nullptr || Bq == nullptr || scales == nullptr))
+        return fail(TG_ERR_INVALID_ARG, "A, Bq or scales is NULL");
+    if (K > 0 && !(aligned(A, 16) && aligned(Bq, 16) && aligned(scales, 16)))
+        return fail(TG_ERR_INVALID_ARG, "tg_gemm_w4 needs 16-byte aligned A, Bq and scales");
+    const int64_t c_bytes = M * N * 2;
+    if (overlaps(C, c_bytes, A, K > 0 ? M * K * 2 : 0) || overlaps(C, c_bytes, Bq, K > 0 ? N * K / 2 : 0) ||
+        overlaps(C, c_bytes, scales, K > 0 ? (K / kW4Group) * N * 2 : 0) ||
+        overlaps(C, c_bytes, bias, bias ? N * 2 : 0))
+        return fail(TG_ERR_INVALID_ARG, "C overlaps an input");
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    tg_status st = current_device(&dev);
+    if (st != TG_OK) return st;
+    DeviceState& d = g_dev[dev];
+    const int gelu = epilogue == TG_EPI_GELU ? 1 : 0;
+    if (K == 0) {
+        cudaError_t e = launch_fill(static_cast<const __half*>(bias), static_cast<__half*>(C), M, N, gelu,
+                                    d.sm_count, stream);
+        return e == cudaSuccess ? TG_OK : cuda_fail(e, "fill kernel launch");
+    }
+
+    W4Args w{};
+    SplitArgs& a = w.s;
+    a.A = static_cast<const __half*>(A);
+    a.bias = static_cast<const __half*>(bias);
+    a.C = static_cast<__half*>(C);
+    a.M = (int)M; a.N = (int)N; a.K = (int)K; a.gelu = gelu;
+    a.m_pad = (a.M + 15) / 16 * 16;
+    a.tmem_stride = 16;  // accumulator columns, a power of two >= m_pad
+    while (a.tmem_stride < a.m_pad) a.tmem_stride *= 2;
+    // independent accumulators per unit, so consecutive MMAs need not wait for
+    // one another: as many as fit in 64 columns, at most 4
+    a.n_acc = 64 / a.tmem_stride < 1 ? 1 : (64 / a.tmem_stride > 4 ? 4 : 64 / a.tmem_stride);
+    a.tmem_cols = 512;
+    w.a_col0 = (2 * a.n_acc * a.tmem_stride + 127) / 128 * 128;  // after the two accumulator buffers
+    w.a_slots = (512 - w.a_col0) / 128;
+    if (w.a_slots > 3) w.a_slots = 3;
+    a.stages = w4_stages_for(a.m_pad);
+    a.n_tiles = (a.N + kW4BN - 1) / kW4BN;
+    a.kb_total = (a.K + kW4BK - 1) / kW4BK;
+    int s = split_k > 0 ? split_k : choose_splits(a.n_tiles, a.kb_total, d.sm_count, 8.0, 1.0);
+    if (s > a.kb_total) s = a.kb_total;
+    a.kb_per_split = (a.kb_total + s - 1) / s;
+    a.splits = (a.kb_total + a.kb_per_split - 1) / a.kb_per_split;
+    a.num_units = a.n_tiles * a.splits;
+    a.wd = watchdog(d);
+    if (a.splits > 1) {
+        Scratch* sc = nullptr;
+        st = ensure_scratch(d, stream, static_cast<size_t>(a.splits) * a.N * a.m_pad * sizeof(float),
+                            static_cast<size_t>(a.n_tiles), &sc);
+        if (st != TG_OK) return st;
+        a.ws = sc->ws;
+        a.counters = sc->counters;
+    }
+    w.Bq = static_cast<const uint8_t*>(Bq);
+    w.scales = static_cast<const __half*>(scales);
+    CUtensorMap tmBq, tmA, tmS;
+    if ((st = make_map_ex(&tmBq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Bq, K / 2, N, kW4BK / 2, kW4BN,
+                          CU_TENSOR_MAP_SWIZZLE_128B)) != TG_OK)
+        return st;
+    if ((st = make_map(&tmA, A, K, M, 64, a.m_pad)) != TG_OK) return st;
+    if ((st = make_map_ex(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, scales, N, K / kW4Group, kW4BN,
+                          kW4BK / kW4Group, CU_TENSOR_MAP_SWIZZLE_NONE)) != TG_OK)
+        return st;
+    const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
+    cudaError_t e = launch_w4(w, tmBq, tmA, tmS, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "4-bit kernel launch");
     return TG_OK;
 }

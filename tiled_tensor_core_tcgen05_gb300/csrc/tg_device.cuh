@@ -18,18 +18,29 @@ struct WaitCtx {
 // returns false) when another wait of this CTA has already expired, or after
 // limit_ns, recording `site` as the first expired wait. kCluster: the barrier
 // receives arrives from another CTA of the cluster (acquire at cluster scope).
+// The abort flag and the clock are read once every kWaitCheckEvery polls, so
+// a phase that completes is noticed by the next poll rather than after a
+// clock read; every poll returns within its own hardware time limit, so the
+// wait stays bounded.
+constexpr uint32_t kWaitCheckEvery = 16;
+
 template <bool kCluster = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
     auto try_once = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
     if (try_once()) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
+    uint64_t t0 = 0;
+    for (uint32_t spin = 1;; ++spin) {
         if (try_once()) return true;
-        if (*w.abort) return false;
-        if (globaltimer_ns() - t0 > w.limit_ns) {
-            *w.abort = 1;
-            atomicCAS(w.status, 0, site);
-            return false;
+        if (spin % kWaitCheckEvery == 0) {
+            if (*w.abort) return false;
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > w.limit_ns) {
+                *w.abort = 1;
+                atomicCAS(w.status, 0, site);
+                return false;
+            }
         }
     }
 }

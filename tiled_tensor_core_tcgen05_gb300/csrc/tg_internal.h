@@ -41,6 +41,16 @@ constexpr int kSkMaxM = 128;
 constexpr int kSkMaxSplits = 64;
 constexpr int kSkSmemBudget = 200 * 1024;  // operand ring budget per CTA
 
+// ---- weight-only 4-bit kernel geometry: one work unit is a 128-column slice
+// of N (one 128-row MMA, swap-AB as above) times a range of 256-wide K
+// blocks. A stage holds that slice's packed weights (128 rows of 128 bytes),
+// the matching 256 columns of A and the two scale rows of the block.
+constexpr int kW4BN = 128;
+constexpr int kW4BK = 256;
+constexpr int kW4Group = 128;          // rows of K sharing one scale per column
+constexpr int kW4ConvGroups = 2;       // converter warp groups, taking stages in turn
+constexpr int kW4SmemBudget = 200 * 1024;
+
 // Watchdog plumbing handed to every kernel: where to record the first wait that
 // expired, the limit, and the test hook that withholds one producer arrival.
 struct Watchdog {
@@ -56,6 +66,8 @@ enum WaitSite : int {
     kSiteMmaAccEmpty = 3,
     kSiteEpilogueAccFull = 4,
     kSiteDrain = 5,
+    kSiteConvFull = 6,   // 4-bit kernel: a converter waiting for packed weights
+    kSiteConvEmpty = 7,  // 4-bit kernel: a converter waiting for a free TMEM slot
 };
 
 struct TiledArgs {
@@ -87,13 +99,27 @@ struct SplitArgs {
     int gelu;
     int m_pad;         // MMA N: M rounded up to a multiple of 16 (16..128)
     int tmem_stride;   // TMEM columns per accumulator (pow2 >= m_pad); a buffer holds
-                       // kSkHalves accumulators, two buffers alternate between units
+                       // kSkHalves x n_acc accumulators, two buffers alternate between units
+    int n_acc;         // accumulators per half, each taking every n_acc-th K step (summed
+                       // in order 0, 1, ... by the epilogue); lets independent MMAs overlap
     int tmem_cols;     // TMEM columns allocated (2 * kSkHalves * tmem_stride, >= 32)
     int stages;        // ring depth
     int n_tiles, kb_total, kb_per_split, splits, num_units;
     float* ws;               // splits * N * m_pad fp32 partial sums, [slice][n][m] (splits > 1)
     unsigned int* counters;  // n_tiles arrival counters, zero between launches
     Watchdog wd;
+};
+
+// The 4-bit kernel: the skinny fields above (A, bias, C, sizes, m_pad,
+// tmem_stride = accumulator columns, split bookkeeping) plus the packed
+// weights, their scales and the tensor-memory layout of the converted
+// operand.
+struct W4Args {
+    SplitArgs s;               // s.B unused; s.stages = ring depth; s.tmem_cols = 512
+    const uint8_t* Bq;         // N rows of K/2 bytes, low nibble = even k
+    const __half* scales;      // K/128 rows of N
+    int a_col0;                // first TMEM column of the converted-weight slots
+    int a_slots;               // number of 128-column slots (each one stage)
 };
 
 int split_stage_bytes(int m_pad);
@@ -110,6 +136,11 @@ cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const 
                               cudaStream_t stream);
 cudaError_t launch_splitk(const SplitArgs& a, const CUtensorMap& tmB, const CUtensorMap& tmA,
                           int grid, cudaStream_t stream);
+int w4_stage_bytes(int m_pad);
+int w4_smem_bytes(int m_pad, int stages);
+int w4_stages_for(int m_pad);
+cudaError_t launch_w4(const W4Args& a, const CUtensorMap& tmBq, const CUtensorMap& tmA, const CUtensorMap& tmS,
+                      int grid, cudaStream_t stream);
 cudaError_t launch_bias_gelu(__half* C, const __half* bias, int64_t M, int64_t N, int gelu, bool vec8, int sm_count,
                              cudaStream_t stream);
 cudaError_t launch_fill(const __half* bias, __half* C, int64_t M, int64_t N, int gelu,

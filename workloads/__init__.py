@@ -128,6 +128,10 @@ class W4Workload:
     scale_hi: float = 0.006
     bias_dist: Dist | None = None
     gelu: bool = False
+    # "uniform": scales uniform in [scale_lo, scale_hi]; "pow2": 2^e with e
+    # uniform over {-2, ..., 1} (with integer A, every product and partial sum
+    # is then exact in fp32)
+    scale_kind: str = "uniform"
 
     @property
     def has_bias(self) -> bool:
@@ -147,8 +151,14 @@ class W4Workload:
         u = (q & 0xF).to(torch.uint8)
         Bq = (u[:, 0::2] | (u[:, 1::2] << 4)).contiguous()
         groups = (self.K + self.group - 1) // self.group
-        scales = (self.scale_lo + (self.scale_hi - self.scale_lo) *
-                  torch.rand((groups, self.N), generator=g, dtype=torch.float32)).to(torch.float16)
+        if self.scale_kind == "pow2":
+            e = torch.randint(-2, 2, (groups, self.N), generator=g).to(torch.float32)
+            scales = torch.pow(2.0, e).to(torch.float16)
+        elif self.scale_kind == "uniform":
+            scales = (self.scale_lo + (self.scale_hi - self.scale_lo) *
+                      torch.rand((groups, self.N), generator=g, dtype=torch.float32)).to(torch.float16)
+        else:
+            raise ValueError(self.scale_kind)
         bias = self.bias_dist.draw((self.N,), g) if self.bias_dist is not None else None
         out = [A, Bq, scales, bias]
         if device != "cpu":
