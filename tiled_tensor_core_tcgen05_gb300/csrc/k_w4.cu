@@ -6,61 +6,90 @@
 // "Quantized LLM inference") lays out the shape of such a kernel. The packed
 // weights are brought on chip as a tile, converted there, and the converted
 // tile feeds the tensor-core product, so no fp16 copy of W ever goes through
-// memory. Here the converted tile lives in tensor memory, as the MMA's A
-// operand. The swap-AB schedule of the fp16 skinny kernel is kept:
-// C^T = W^T A^T, N on the 128-row side of the MMA and M (padded to 16) as its
-// N. With the weights stored as N rows of K/2 bytes, the thread that owns
-// TMEM lane n decodes row n's own contiguous bytes.
+// memory.
 //
-// One work unit is a 128-column slice of N times a range of 256-wide K
-// blocks. Roles, per CTA:
-//   warp 0      TMA producer: per stage, the slice's packed weights
-//               (128 x 128 bytes, 128-byte swizzle), A's 256 columns
-//               (four 64-wide K-major boxes) and the two scale rows;
-//   warp 1      allocates TMEM; one thread issues the MMAs (A from TMEM,
-//               A^T from shared memory) and the commits. Consecutive K steps
-//               go to up to four accumulators in turn, so an MMA need not
-//               wait for the one before it; the epilogue adds them;
-//   warps 2-5   epilogue (the skinny kernels' shared epilogue);
-//   warps 6-13  converters, two groups of four taking stages in turn. Warp w
-//               owns TMEM lanes 32 (w % 4) .. +31. Each thread reads its row's
-//               128 bytes and two scales, frees the raw stage, waits for a
-//               free TMEM slot, and writes 128 columns of fp16 pairs with
-//               tcgen05.st.
-// Barriers: raw_full (TMA bytes), raw_empty (4 converter warps + the MMA
-// commit), tfull (4 converter warps), tempty (MMA commit), plus the
-// accumulator pair of the skinny epilogue.
+// Orientation. A tcgen05 MMA costs about the same for any N up to 256 but
+// grows with its M rows, so the weights sit on the N side: the MMA is
+// 64 (tokens, M padded) x 256 (weight columns) x 16, A = the activations from
+// shared memory, B = the converted weights, written to shared memory by the
+// converter warps as a K-major tile (each weight column's 64 k contiguous,
+// 128-byte swizzle). Only M <= 64 runs per launch; the host runs larger M as
+// several row blocks. The activation boxes hold only the m_pad real rows; the
+// MMA's remaining rows read whatever follows in shared memory and land in
+// accumulator rows that are never stored.
+//
+// One work unit is a 256-column slice of N times a range of 256-wide K
+// blocks. Per CTA:
+//   warp 0      TMA producer, per 256-k stage: the slice's packed weights
+//               (256 rows x 128 bytes, 128-byte swizzle) and the two scale
+//               rows into a raw stage, A's 256 columns (four 64-wide boxes
+//               of m_pad rows) into an activation slot;
+//   warp 1      allocates TMEM (two 256-column accumulators); one thread
+//               issues four MMAs per 64-k sub-tile and the commits;
+//   warps 2-5   epilogue: TMEM lane 32q + i (i < 16) holds accumulator row
+//               16q + i; bias, GELU, C, or fp32 partials plus the
+//               deterministic last-arrival reduction for split K;
+//   warps 6-21  converters, two groups of 256 threads (one thread per weight
+//               column) taking alternate 64-k sub-tiles: read the column's
+//               bytes of its sub-tiles and two scales once per stage, then
+//               write the sub-tiles as fp16 into a ring of B slots.
+// Barriers: raw_full (TMA bytes), raw_empty (16 converter warps), afull (TMA
+// bytes), aempty (MMA commit after the stage's last sub-tile), bfull (the 8
+// warps of one converter group), bempty (MMA commit), acc_full / acc_empty
+// (MMA commit / 128 epilogue threads).
 #include "tg_device.cuh"
 #include "tg_internal.h"
-#include "tg_skinny.cuh"
 
 namespace tg {
 namespace {
 
-constexpr int kRawBytes = kW4BN * (kW4BK / 2);          // 16 KB of packed weights per stage
-constexpr int kScaleBytes = 2 * kW4BN * 2;              // two scale rows of 128 fp16
-constexpr int kConvWarps = 4 * kW4ConvGroups;
+constexpr int kRawBytes = kW4BN * (kW4BK / 2);   // 32 KB of packed weights per stage
+constexpr int kScaleBytes = 2 * kW4BN * 2;       // two scale rows of 256 fp16
+constexpr int kSubK = 64;                        // k per B sub-tile (one 128-byte row per column)
+constexpr int kSubs = kW4BK / kSubK;             // sub-tiles per stage
+constexpr int kSlotBytes = kW4BN * kSubK * 2;    // 32 KB of fp16 per B slot
+constexpr int kMmaM = 64;
+constexpr int kConvGroups = 2;                   // converter groups, taking alternate sub-tiles
+constexpr int kSubsPerGroup = 4 / kConvGroups;
+constexpr int kConvWarps = kConvGroups * kW4BN / 32;
+constexpr int kEpiThreads = 128;
 constexpr int kThreads = (6 + kConvWarps) * 32;
-constexpr int kMaxSlots = 3;
-constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemCols = 512;              // two 256-column accumulators
+constexpr int kMaxStages = 8;
+constexpr uint32_t kEpiSleepNs = 256;   // epilogue: waits about one work unit
+constexpr uint32_t kConvSleepNs = 32;   // converters: wait for a TMA stage or a free B slot
+constexpr int kPrefetchStages = 2;      // packed-weight boxes requested into L2 ahead of their load
+// The producer and MMA threads share schedulers with converter warps, so
+// their waits sleep too (briefly) instead of taking issue slots.
+constexpr uint32_t kProdSleepNs = 64;
+constexpr uint32_t kMmaSleepNs = 20;
 static_assert(kW4BK == 2 * kW4Group, "a stage spans two scale groups");
 
 struct Layout {
-    int stage_bytes, act_off, scale_off, ring, bar_raw_full, bar_raw_empty, bar_tfull, bar_tempty, bar_acc_full,
-        bar_acc_empty, bar_drain, tmem_slot, abort_slot, flag_slot, used, alloc;
+    int stage_bytes, scale_off, act_bytes, aring, bring, bar_raw_full, bar_raw_empty, bar_afull, bar_aempty,
+        bar_bfull, bar_bempty, bar_acc_full, bar_acc_empty, bar_drain, tmem_slot, abort_slot, flag_slot, used,
+        alloc;
 };
 
-__host__ __device__ inline Layout layout_for(int m_pad, int stages) {
+// [raw stages][activation slots][B slots][barriers]. Raw stages (packed
+// weights + scales) are freed as soon as the converters have read them;
+// activation slots (four 64-k boxes of m_pad rows) when the stage's MMAs are
+// done. A box's 64-row MMA window (8 KB) may run past its slot; the B ring
+// behind the activation slots keeps it inside the CTA's shared memory.
+__host__ __device__ inline Layout layout_for(int m_pad, int stages, int act_slots, int slots) {
     Layout L;
-    L.act_off = kRawBytes;                    // 1024-aligned
-    L.scale_off = kRawBytes + m_pad * 512;    // m_pad * 512 is a multiple of 8 KB
-    L.stage_bytes = (L.scale_off + kScaleBytes + 1023) / 1024 * 1024;
-    L.ring = stages * L.stage_bytes;
-    L.bar_raw_full = L.ring;
+    L.scale_off = kRawBytes;
+    L.stage_bytes = kRawBytes + kScaleBytes;  // multiple of 1024
+    L.act_bytes = kSubs * m_pad * 128;       // multiple of 8 KB
+    L.aring = stages * L.stage_bytes;
+    L.bring = L.aring + act_slots * L.act_bytes;
+    L.bar_raw_full = L.bring + slots * kSlotBytes;
     L.bar_raw_empty = L.bar_raw_full + 8 * stages;
-    L.bar_tfull = L.bar_raw_empty + 8 * stages;
-    L.bar_tempty = L.bar_tfull + 8 * kMaxSlots;
-    L.bar_acc_full = L.bar_tempty + 8 * kMaxSlots;
+    L.bar_afull = L.bar_raw_empty + 8 * stages;
+    L.bar_aempty = L.bar_afull + 8 * act_slots;
+    L.bar_bfull = L.bar_aempty + 8 * act_slots;
+    L.bar_bempty = L.bar_bfull + 8 * slots;
+    L.bar_acc_full = L.bar_bempty + 8 * slots;
     L.bar_acc_empty = L.bar_acc_full + 16;
     L.bar_drain = L.bar_acc_empty + 16;
     L.tmem_slot = L.bar_drain + 8;
@@ -93,6 +122,14 @@ __device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, uint32_t* o
     }
 }
 
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Accumulator row of TMEM lane (32 q + i) for a 64-row MMA: row 16 q + i for
+// i < 16; lanes 16..31 of each quarter hold no row (-1).
+__device__ __forceinline__ int acc_row(int quarter, int lane) { return lane < 16 ? quarter * 16 + lane : -1; }
+
 __global__ void __launch_bounds__(kThreads, 1)
     w4_gemm_kernel(const __grid_constant__ CUtensorMap tmBq, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmS, const W4Args wa) {
@@ -100,16 +137,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const SplitArgs& args = wa.s;
-    const Layout L = layout_for(args.m_pad, args.stages);
     const int R = args.stages;
-    const int T = wa.a_slots;
+    const int RA = wa.a_slots;
+    const int T = wa.b_slots;
+    const Layout L = layout_for(args.m_pad, R, RA, T);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     auto raw_full = [&](int s) { return sbase + L.bar_raw_full + 8 * s; };
     auto raw_empty = [&](int s) { return sbase + L.bar_raw_empty + 8 * s; };
-    auto tfull = [&](int t) { return sbase + L.bar_tfull + 8 * t; };
-    auto tempty = [&](int t) { return sbase + L.bar_tempty + 8 * t; };
+    auto afull = [&](int s) { return sbase + L.bar_afull + 8 * s; };
+    auto aempty = [&](int s) { return sbase + L.bar_aempty + 8 * s; };
+    auto bfull = [&](int t) { return sbase + L.bar_bfull + 8 * t; };
+    auto bempty = [&](int t) { return sbase + L.bar_bempty + 8 * t; };
     auto acc_full = [&](int b) { return sbase + L.bar_acc_full + 8 * b; };
     auto acc_empty = [&](int b) { return sbase + L.bar_acc_empty + 8 * b; };
     const uint32_t drain_bar = sbase + L.bar_drain;
@@ -120,15 +160,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < R; ++s) {
             mbar_init(raw_full(s), 1);
-            mbar_init(raw_empty(s), 4 + 1);
+            mbar_init(raw_empty(s), kConvWarps);
+        }
+        for (int s = 0; s < RA; ++s) {
+            mbar_init(afull(s), 1);
+            mbar_init(aempty(s), 1);
         }
         for (int t = 0; t < T; ++t) {
-            mbar_init(tfull(t), 4);
-            mbar_init(tempty(t), 1);
+            mbar_init(bfull(t), kConvWarps / kConvGroups);
+            mbar_init(bempty(t), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full(b), 1);
-            mbar_init(acc_empty(b), kSkEpiThreads);
+            mbar_init(acc_empty(b), kEpiThreads);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -153,41 +197,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint64_t pol_stream = l2_policy_evict_first();  // weights and scales: read once
             const uint64_t pol_keep = l2_policy_evict_last();     // A: re-read by every unit
-            const uint32_t tx = static_cast<uint32_t>(kRawBytes + args.m_pad * 512 + kScaleBytes);
-            int slot = 0;
-            uint32_t phase = 0;
-            uint32_t issued_mask = 0, issued_parity = 0;
+            int slot = 0, as = 0;
+            uint32_t phase = 0, aphase = 0;
+            uint32_t issued_mask = 0, issued_parity = 0, a_mask = 0, a_parity = 0;
             bool ok = true;
+            // L2 prefetch cursor, kPrefetchStages stages ahead of the loads in
+            // this CTA's sequence of (unit, K block) stages: the SMEM ring holds
+            // few stages, so HBM requests are issued earlier through L2
+            int pu = blockIdx.x, pkb = 0, pkb1 = 0;
+            auto pf_unit = [&](int u) {
+                const int sp = u / args.n_tiles;
+                pkb = sp * args.kb_per_split;
+                pkb1 = min(args.kb_total, pkb + args.kb_per_split);
+            };
+            auto pf_issue = [&]() {
+                if (pu >= args.num_units) return;
+                tma_prefetch_l2_2d(&tmBq, pkb * (kW4BK / 2), (pu % args.n_tiles) * kW4BN);
+                if (++pkb == pkb1) {
+                    pu += gridDim.x;
+                    if (pu < args.num_units) pf_unit(pu);
+                }
+            };
+            if (pu < args.num_units) pf_unit(pu);
+            for (int i = 0; i < kPrefetchStages; ++i) pf_issue();
             for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x) {
                 const int sp = u / args.n_tiles;
                 const int nt = u - sp * args.n_tiles;
                 const int kb0 = sp * args.kb_per_split;
                 const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_phase(raw_empty(slot), phase ^ 1, wc, kSiteProducerEmpty)) { ok = false; break; }
+                    if (!wait_phase_sleep(raw_empty(slot), phase ^ 1, wc, kSiteProducerEmpty, kProdSleepNs)) {
+                        ok = false;
+                        break;
+                    }
+                    pf_issue();
                     const uint32_t st = sbase + slot * L.stage_bytes;
-                    mbar_arrive_expect_tx(raw_full(slot), tx);
+                    mbar_arrive_expect_tx(raw_full(slot), kRawBytes + kScaleBytes);
                     tma_load_2d_hint(st, &tmBq, raw_full(slot), kb * (kW4BK / 2), nt * kW4BN, pol_stream);
-#pragma unroll
-                    for (int j = 0; j < kW4BK / 64; ++j)
-                        tma_load_2d_hint(st + L.act_off + j * args.m_pad * 128, &tmA, raw_full(slot),
-                                         kb * kW4BK + j * 64, 0, pol_keep);
                     tma_load_2d_hint(st + L.scale_off, &tmS, raw_full(slot), nt * kW4BN, kb * (kW4BK / kW4Group),
                                      pol_stream);
                     issued_mask |= 1u << slot;
                     issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
                     if (++slot == R) { slot = 0; phase ^= 1; }
+                    if (!wait_phase_sleep(aempty(as), aphase ^ 1, wc, kSiteProducerEmpty, kProdSleepNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = sbase + L.aring + as * L.act_bytes;
+                    mbar_arrive_expect_tx(afull(as), L.act_bytes);
+#pragma unroll
+                    for (int j = 0; j < kSubs; ++j)
+                        tma_load_2d_hint(sa + j * args.m_pad * 128, &tmA, afull(as), kb * kW4BK + j * kSubK, 0, pol_keep);
+                    a_mask |= 1u << as;
+                    a_parity = (a_parity & ~(1u << as)) | (aphase << as);
+                    if (++as == RA) { as = 0; aphase ^= 1; }
                 }
             }
             for (int s = 0; s < R; ++s)
                 if (issued_mask & (1u << s)) wait_phase_drain(raw_full(s), (issued_parity >> s) & 1, wc);
+            for (int s = 0; s < RA; ++s)
+                if (a_mask & (1u << s)) wait_phase_drain(afull(s), (a_parity >> s) & 1, wc);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16_f32(128, args.m_pad, /*a_mn_major=*/false, /*b_mn_major=*/false);
-            int slot = 0, ts = 0, ui = 0;
-            uint32_t phase = 0, tphase = 0;
+            const uint32_t idesc = idesc_f16_f32(kMmaM, kW4BN, /*a_mn_major=*/false, /*b_mn_major=*/false);
+            int as = 0, ts = 0, ui = 0;
+            uint32_t aphase = 0, tphase = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x, ++ui) {
                 const int sp = u / args.n_tiles;
@@ -196,28 +272,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = ui & 1;
                 if (!wait_phase(acc_empty(b), ((ui >> 1) & 1) ^ 1, wc, kSiteMmaAccEmpty)) break;
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + b * args.n_acc * args.tmem_stride;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_phase(raw_full(slot), phase, wc, kSiteMmaFull) ||
-                        !wait_phase(tfull(ts), tphase, wc, kSiteMmaFull)) {
-                        ok = false;
-                        break;
+                const uint32_t d_tmem = tmem_base + b * kW4BN;
+                for (int kb = kb0; kb < kb1 && ok; ++kb) {
+                    if (!wait_phase(afull(as), aphase, wc, kSiteMmaFull)) { ok = false; break; }
+                    const uint32_t act = sbase + L.aring + as * L.act_bytes;
+                    const int subs = min(kW4BK, args.K - kb * kW4BK) / kSubK;  // K % 128 == 0: 2 or 4
+                    for (int c = 0; c < kSubs; ++c) {
+                        if (!wait_phase_sleep(bfull(ts), tphase, wc, kSiteMmaFull, kMmaSleepNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        if (c < subs) {
+                            const uint64_t a_desc = smem_desc_sw128(act + c * args.m_pad * 128, 16, 1024);
+                            const uint64_t b_desc = smem_desc_sw128(sbase + L.bring + ts * kSlotBytes, 16, 1024);
+#pragma unroll
+                            for (int k = 0; k < kSubK / 16; ++k)
+                                mma_f16(d_tmem, a_desc + static_cast<uint64_t>((k * 32) >> 4),
+                                        b_desc + static_cast<uint64_t>((k * 32) >> 4), idesc,
+                                        (kb != kb0) || (c != 0) || (k != 0));
+                        }
+                        mma_commit(bempty(ts));
+                        if (++ts == T) { ts = 0; tphase ^= 1; }
                     }
-                    tc_fence_after_sync();
-                    const uint32_t act = sbase + slot * L.stage_bytes + L.act_off;
-                    const uint32_t a_tmem = tmem_base + wa.a_col0 + ts * 128;
-                    const int nk = min(kW4BK, args.K - kb * kW4BK) / 16;
-                    // K step j goes to accumulator j % n_acc: consecutive MMAs are independent
-                    for (int j = 0, acc = 0; j < nk; ++j, acc = (acc + 1 == args.n_acc) ? 0 : acc + 1) {
-                        const uint64_t b_desc = smem_desc_sw128(act + (j >> 2) * args.m_pad * 128, 16, 1024) +
-                                                static_cast<uint64_t>(((j & 3) * 32) >> 4);
-                        mma_f16_tmem_a(d_tmem + acc * args.tmem_stride, a_tmem + j * 8, b_desc, idesc,
-                                       (kb != kb0) || (j >= args.n_acc));
-                    }
-                    mma_commit(raw_empty(slot));
-                    mma_commit(tempty(ts));
-                    if (++slot == R) { slot = 0; phase ^= 1; }
-                    if (++ts == T) { ts = 0; tphase ^= 1; }
+                    if (!ok) break;
+                    mma_commit(aempty(as));
+                    if (++as == RA) { as = 0; aphase ^= 1; }
                 }
                 if (!ok) break;
                 mma_commit(acc_full(b));
@@ -228,52 +308,200 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue
-        skinny_epilogue<1>(args, tmem_base, acc_full(0), acc_empty(0), last_flag, wc, 64);
+        const int quarter = warp & 3;
+        const int ept = threadIdx.x - 64;
+        const int row = acc_row(quarter, lane);
+        const bool row_ok = row >= 0 && row < args.M;
+        const bool vec = wa.c_vec != 0;
+        int it = 0;
+        for (int u = blockIdx.x; u < args.num_units; u += gridDim.x, ++it) {
+            const int sp = u / args.n_tiles;
+            const int nt = u - sp * args.n_tiles;
+            const int n0 = nt * kW4BN;
+            const int b = it & 1;
+            const bool ok = wait_phase_sleep(acc_full(b), (it >> 1) & 1, wc, kSiteEpilogueAccFull, kEpiSleepNs);
+            if (named_barrier_or(1, kEpiThreads, !ok)) break;
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kW4BN;
+#pragma unroll 1
+            for (int c = 0; c < kW4BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + c * 32, r);
+                tmem_ld_wait();
+                if (c == kW4BN / 32 - 1) {
+                    tc_fence_before_sync();
+                    mbar_arrive(acc_empty(b));
+                }
+                const int col0 = n0 + c * 32;
+                if (!row_ok || col0 >= args.N) continue;
+                if (args.splits == 1) {
+                    __half* dst = args.C + static_cast<int64_t>(row) * args.N + col0;
+                    const bool whole = vec && col0 + 32 <= args.N;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {  // eight columns at a time
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int n = col0 + 8 * q + e;
+                            const float bi = (args.bias != nullptr && n < args.N) ? __half2float(args.bias[n]) : 0.0f;
+                            v[e] = epi_value(__uint_as_float(r[8 * q + e]), bi, args.gelu);
+                        }
+                        if (whole) {
+                            uint4 o;
+                            __half2* h = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
+                            reinterpret_cast<uint4*>(dst)[q] = o;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                if (col0 + 8 * q + e < args.N) dst[8 * q + e] = __float2half_rn(v[e]);
+                        }
+                    }
+                } else {
+                    // partials as [slice][m_pad][N] fp32: this thread's 32 columns are 128 contiguous bytes
+                    float* wp = args.ws + (static_cast<int64_t>(sp) * args.m_pad + row) * args.N + col0;
+                    if (col0 + 32 <= args.N) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            reinterpret_cast<uint4*>(wp)[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (col0 + i < args.N) wp[i] = __uint_as_float(r[i]);
+                    }
+                }
+            }
+            if (args.splits > 1) {
+                // publish this slice's partials, then count arrivals for column slice nt
+                __threadfence();
+                named_barrier_sync(1, kEpiThreads);
+                if (ept == 0) {
+                    const unsigned int prev = atomicAdd(args.counters + nt, 1u);
+                    *last_flag = (prev == static_cast<unsigned int>(args.splits - 1)) ? 1 : 0;
+                }
+                named_barrier_sync(1, kEpiThreads);
+                if (*last_flag) {
+                    __threadfence();
+                    // every (row, column) of the slice: thread t takes four adjacent
+                    // columns (float4) of rows t/64, t/64 + 2, ...; per batch of four rows
+                    // all slices' loads are issued before the sums, which run in slice
+                    // order 0, 1, ... (deterministic); then bias, GELU and C
+                    const int cq = ept & 63;
+                    const int n = n0 + 4 * cq;
+                    const int64_t slice_stride = static_cast<int64_t>(args.m_pad) * args.N;
+                    if (n < args.N) {
+                        float bi[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            bi[e] = (args.bias != nullptr && n + e < args.N) ? __half2float(args.bias[n + e]) : 0.0f;
+                        for (int m0 = ept >> 6; m0 < args.M; m0 += 8) {
+                            float4 acc[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            for (int q0 = 0; q0 < args.splits; q0 += 2) {
+                                float4 p[2][4];
+#pragma unroll
+                                for (int qq = 0; qq < 2; ++qq)
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        const int m = m0 + 2 * i;
+                                        p[qq][i] = (q0 + qq < args.splits && m < args.M)
+                                                       ? __ldcg(reinterpret_cast<const float4*>(
+                                                             args.ws + (q0 + qq) * slice_stride +
+                                                             static_cast<int64_t>(m) * args.N + n))
+                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+                                    }
+#pragma unroll
+                                for (int qq = 0; qq < 2; ++qq)
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i)
+                                        if (q0 + qq < args.splits) {
+                                            acc[i].x += p[qq][i].x;
+                                            acc[i].y += p[qq][i].y;
+                                            acc[i].z += p[qq][i].z;
+                                            acc[i].w += p[qq][i].w;
+                                        }
+                            }
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int m = m0 + 2 * i;
+                                if (m >= args.M) break;
+                                __half* dst = args.C + static_cast<int64_t>(m) * args.N + n;
+                                const float v[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    if (n + e < args.N) dst[e] = __float2half_rn(epi_value(v[e], bi[e], args.gelu));
+                            }
+                        }
+                    }
+                    if (ept == 0) atomicExch(args.counters + nt, 0u);
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------------ converters
-        const int group = (warp - 6) >> 2;
-        const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;  // TMEM lane = output column within the slice
-        const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + wa.a_col0;
-        int slot = 0, ts = 0, it = 0;
-        uint32_t phase = 0, tphase = 0;
+        // kConvGroups groups of kW4BN threads; group g converts sub-tiles
+        // c = g, g + kConvGroups, ... of every stage. Sub-tile c of the CTA's
+        // stage number it is the (4 it + c)-th B slot use, so with
+        // T % kConvGroups == 0 each slot is only ever filled by one group.
+        const int cidx = threadIdx.x - 6 * 32;
+        const int group = cidx / kW4BN;
+        const int col = cidx - group * kW4BN;  // weight column within the unit's slice (0..255)
+        const uint32_t swz = static_cast<uint32_t>(col & 7);
+        int slot = 0, it = 0;
+        uint32_t phase = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x) {
             const int sp = u / args.n_tiles;
             const int kb0 = sp * args.kb_per_split;
             const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                if (it % kW4ConvGroups == group) {
-                    ok = __all_sync(0xFFFFFFFFu, wait_phase(raw_full(slot), phase, wc, kSiteConvFull));
-                    if (!ok) break;
-                    const uint32_t st = sbase + slot * L.stage_bytes;
-                    // this row's 128 bytes: 16-byte chunk j sits at chunk j ^ (row % 8) (128-byte swizzle)
-                    uint4 w[8];
+                ok = __all_sync(0xFFFFFFFFu, wait_phase_sleep(raw_full(slot), phase, wc, kSiteConvFull, kConvSleepNs));
+                if (!ok) break;
+                const uint32_t st = sbase + slot * L.stage_bytes;
+                // this column's bytes of this group's sub-tiles: 16-byte chunk j of the
+                // 128-byte row sits at chunk j ^ (col % 8) (128-byte swizzle)
+                uint4 w[2 * kSubsPerGroup];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) w[j] = lds_v4(st + row * 128 + ((j ^ (row & 7)) << 4));
-                    const __half2 s_lo = __half2half2(__ushort_as_half(lds_u16(st + L.scale_off + 2 * row)));
-                    const __half2 s_hi = __half2half2(__ushort_as_half(lds_u16(st + L.scale_off + 2 * (kW4BN + row))));
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(raw_empty(slot));
-                    ok = __all_sync(0xFFFFFFFFu, wait_phase(tempty(ts), tphase ^ 1, wc, kSiteConvEmpty));
-                    if (!ok) break;
-                    tc_fence_after_sync();
+                for (int jj = 0; jj < kSubsPerGroup; ++jj)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {  // 64 k per chunk: 32 TMEM columns
-                        const __half2 s2 = c < 2 ? s_lo : s_hi;
-                        uint32_t r[32];
-                        const uint32_t* words = reinterpret_cast<const uint32_t*>(&w[2 * c]);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) dequant_word(words[i], s2, &r[4 * i]);
-                        tmem_st_32x32b_x32(lane_addr + ts * 128 + c * 32, r);
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t chunk = static_cast<uint32_t>(2 * (group + kConvGroups * jj) + h);
+                        w[2 * jj + h] = lds_v4(st + col * 128 + ((chunk ^ swz) << 4));
                     }
-                    tmem_st_wait();
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(tfull(ts));
+                const __half2 s_lo = __half2half2(__ushort_as_half(lds_u16(st + L.scale_off + 2 * col)));
+                const __half2 s_hi = __half2half2(__ushort_as_half(lds_u16(st + L.scale_off + 2 * (kW4BN + col))));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(raw_empty(slot));
+                // fully unrolled (no exit inside), so w[] stays in registers
+#pragma unroll
+                for (int jj = 0; jj < kSubsPerGroup; ++jj) {  // 64 k per sub-tile: this column's 128-byte row of B
+                    const int c = group + kConvGroups * jj;
+                    const int use = it * kSubs + c;  // B slot use number
+                    const int ts = use % T;
+                    const uint32_t tphase = static_cast<uint32_t>(use / T) & 1u;
+                    if (ok)
+                        ok = __all_sync(0xFFFFFFFFu,
+                                        wait_phase_sleep(bempty(ts), tphase ^ 1, wc, kSiteConvEmpty, kConvSleepNs));
+                    if (ok) {
+                        const __half2 s2 = (c * kSubK < kW4Group) ? s_lo : s_hi;
+                        const uint32_t dst = sbase + L.bring + ts * kSlotBytes + col * 128;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {  // word i: k = 8i .. 8i+7 -> 16-byte chunk i
+                            const uint4& q4 = w[2 * jj + (i >> 2)];
+                            const uint32_t word = (i & 3) == 0 ? q4.x : (i & 3) == 1 ? q4.y : (i & 3) == 2 ? q4.z : q4.w;
+                            uint32_t o[4];
+                            dequant_word(word, s2, o);
+                            sts_v4(dst + ((static_cast<uint32_t>(i) ^ swz) << 4), o[0], o[1], o[2], o[3]);
+                        }
+                        fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bfull(ts));
+                    }
                 }
+                if (!ok) break;
                 if (++slot == R) { slot = 0; phase ^= 1; }
-                if (++ts == T) { ts = 0; tphase ^= 1; }
             }
         }
     }
@@ -288,17 +516,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int w4_stage_bytes(int m_pad) { return layout_for(m_pad, 1).stage_bytes; }
-
-int w4_stages_for(int m_pad) {
-    int s = kW4SmemBudget / w4_stage_bytes(m_pad);
-    if (s > 16) s = 16;
-    s -= s % kW4ConvGroups;  // each converter group keeps the same ring slots
-    if (s < kW4ConvGroups) s = kW4ConvGroups;
-    return s;
+// Ring depths for a padded M within the shared-memory budget: B slots a
+// multiple of the converter groups (four when they fit: measured faster than
+// more raw stages), then the most raw stages, then activation slots; each
+// ring at least two deep.
+void w4_pipeline(int m_pad, int* stages, int* act_slots, int* slots) {
+    int best = -1;
+    for (int s = 2; s <= kMaxStages; ++s)
+        for (int t = kConvGroups; t <= 4; t += kConvGroups)
+            for (int a = 2; a <= 3; ++a) {
+                if (layout_for(m_pad, s, a, t).alloc > kW4SmemBudget) continue;
+                const int score = t * 100 + s * 10 + a;
+                if (score > best) {
+                    best = score;
+                    *stages = s;
+                    *slots = t;
+                    *act_slots = a;
+                }
+            }
 }
 
-int w4_smem_bytes(int m_pad, int stages) { return layout_for(m_pad, stages).alloc; }
+int w4_smem_bytes(int m_pad, int stages, int act_slots, int slots) {
+    return layout_for(m_pad, stages, act_slots, slots).alloc;
+}
 
 cudaError_t launch_w4(const W4Args& a, const CUtensorMap& tmBq, const CUtensorMap& tmA, const CUtensorMap& tmS,
                       int grid, cudaStream_t stream) {
@@ -311,7 +551,7 @@ cudaError_t launch_w4(const W4Args& a, const CUtensorMap& tmBq, const CUtensorMa
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    w4_gemm_kernel<<<grid, kThreads, w4_smem_bytes(a.s.m_pad, a.s.stages), stream>>>(tmBq, tmA, tmS, a);
+    w4_gemm_kernel<<<grid, kThreads, w4_smem_bytes(a.s.m_pad, a.s.stages, a.a_slots, a.b_slots), stream>>>(tmBq, tmA, tmS, a);
     return cudaGetLastError();
 }
 

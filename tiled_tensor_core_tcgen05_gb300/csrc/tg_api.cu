@@ -156,14 +156,15 @@ int group_rows(int tile_rows, int K, int m_blocks) {
 // saturates before every SM streams, so the job can never beat
 // total / (kHbmFraction * SMs). Every split beyond the first adds the
 // partial-sum traffic of the final reduction (reduce_per_split, in K blocks).
-// Ties keep fewer splits. The fp16 kernel's block is 64 x 256 fp16 (32 KB);
-// the 4-bit kernel's is 256 x 128 packed (16 KB), so its fixed charges count
-// twice as many blocks.
+// Ties keep fewer splits. The fp16 kernel streams HBM at full rate from 70%
+// of the SMs; the 4-bit kernel is limited per SM (decoding and staging the
+// weights), so every SM counts and its K block (256 x 256 packed, 32 KB) is
+// charged less fixed overhead.
 int choose_splits(int n_tiles, int kb_total, int sm_count, double unit_overhead = 6.0,
-                  double reduce_per_split = 2.0) {
+                  double reduce_per_split = 2.0, double hbm_fraction = 0.7) {
     const double kUnitOverhead = unit_overhead;
     const double kReducePerSplit = reduce_per_split;
-    constexpr double kHbmFraction = 0.7;     // share of SMs whose streams saturate HBM
+    const double kHbmFraction = hbm_fraction;  // share of SMs whose streams saturate HBM
     const double hbm_floor = static_cast<double>(n_tiles) * kb_total / (kHbmFraction * sm_count);
     int best_s = 1;
     double best = 1e300;
@@ -647,51 +648,48 @@ extern "C" tg_status tg_gemm_w4(const void* A, const void* Bq, const void* scale
         return e == cudaSuccess ? TG_OK : cuda_fail(e, "fill kernel launch");
     }
 
-    W4Args w{};
-    SplitArgs& a = w.s;
-    a.A = static_cast<const __half*>(A);
-    a.bias = static_cast<const __half*>(bias);
-    a.C = static_cast<__half*>(C);
-    a.M = (int)M; a.N = (int)N; a.K = (int)K; a.gelu = gelu;
-    a.m_pad = (a.M + 15) / 16 * 16;
-    a.tmem_stride = 16;  // accumulator columns, a power of two >= m_pad
-    while (a.tmem_stride < a.m_pad) a.tmem_stride *= 2;
-    // independent accumulators per unit, so consecutive MMAs need not wait for
-    // one another: as many as fit in 64 columns, at most 4
-    a.n_acc = 64 / a.tmem_stride < 1 ? 1 : (64 / a.tmem_stride > 4 ? 4 : 64 / a.tmem_stride);
-    a.tmem_cols = 512;
-    w.a_col0 = (2 * a.n_acc * a.tmem_stride + 127) / 128 * 128;  // after the two accumulator buffers
-    w.a_slots = (512 - w.a_col0) / 128;
-    if (w.a_slots > 3) w.a_slots = 3;
-    a.stages = w4_stages_for(a.m_pad);
-    a.n_tiles = (a.N + kW4BN - 1) / kW4BN;
-    a.kb_total = (a.K + kW4BK - 1) / kW4BK;
-    int s = split_k > 0 ? split_k : choose_splits(a.n_tiles, a.kb_total, d.sm_count, 8.0, 1.0);
-    if (s > a.kb_total) s = a.kb_total;
-    a.kb_per_split = (a.kb_total + s - 1) / s;
-    a.splits = (a.kb_total + a.kb_per_split - 1) / a.kb_per_split;
-    a.num_units = a.n_tiles * a.splits;
-    a.wd = watchdog(d);
-    if (a.splits > 1) {
-        Scratch* sc = nullptr;
-        st = ensure_scratch(d, stream, static_cast<size_t>(a.splits) * a.N * a.m_pad * sizeof(float),
-                            static_cast<size_t>(a.n_tiles), &sc);
-        if (st != TG_OK) return st;
-        a.ws = sc->ws;
-        a.counters = sc->counters;
+    // at most kW4MaxM rows of A per launch: larger M runs as row blocks (each
+    // reading the weights again)
+    for (int64_t r0 = 0; r0 < M; r0 += kW4MaxM) {
+        const int64_t rows = M - r0 < kW4MaxM ? M - r0 : kW4MaxM;
+        W4Args w{};
+        SplitArgs& a = w.s;
+        a.A = static_cast<const __half*>(A) + r0 * K;
+        a.bias = static_cast<const __half*>(bias);
+        a.C = static_cast<__half*>(C) + r0 * N;
+        a.M = (int)rows; a.N = (int)N; a.K = (int)K; a.gelu = gelu;
+        a.m_pad = (a.M + 15) / 16 * 16;
+        w4_pipeline(a.m_pad, &a.stages, &w.a_slots, &w.b_slots);
+        a.n_tiles = (a.N + kW4BN - 1) / kW4BN;
+        a.kb_total = (a.K + kW4BK - 1) / kW4BK;
+        int s = split_k > 0 ? split_k : choose_splits(a.n_tiles, a.kb_total, d.sm_count, 2.0, 1.0, 1.0);
+        if (s > a.kb_total) s = a.kb_total;
+        a.kb_per_split = (a.kb_total + s - 1) / s;
+        a.splits = (a.kb_total + a.kb_per_split - 1) / a.kb_per_split;
+        a.num_units = a.n_tiles * a.splits;
+        a.wd = watchdog(d);
+        if (a.splits > 1) {
+            Scratch* sc = nullptr;
+            st = ensure_scratch(d, stream, static_cast<size_t>(a.splits) * a.N * a.m_pad * sizeof(float),
+                                static_cast<size_t>(a.n_tiles), &sc);
+            if (st != TG_OK) return st;
+            a.ws = sc->ws;
+            a.counters = sc->counters;
+        }
+        w.Bq = static_cast<const uint8_t*>(Bq);
+        w.scales = static_cast<const __half*>(scales);
+        w.c_vec = aligned(a.C, 16) ? 1 : 0;  // N % 8 == 0 is required above
+        CUtensorMap tmBq, tmA, tmS;
+        if ((st = make_map_ex(&tmBq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Bq, K / 2, N, kW4BK / 2, kW4BN,
+                              CU_TENSOR_MAP_SWIZZLE_128B)) != TG_OK)
+            return st;
+        if ((st = make_map(&tmA, a.A, K, a.M, 64, a.m_pad)) != TG_OK) return st;
+        if ((st = make_map_ex(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, scales, N, K / kW4Group, kW4BN,
+                              kW4BK / kW4Group, CU_TENSOR_MAP_SWIZZLE_NONE)) != TG_OK)
+            return st;
+        const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
+        cudaError_t e = launch_w4(w, tmBq, tmA, tmS, grid, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "4-bit kernel launch");
     }
-    w.Bq = static_cast<const uint8_t*>(Bq);
-    w.scales = static_cast<const __half*>(scales);
-    CUtensorMap tmBq, tmA, tmS;
-    if ((st = make_map_ex(&tmBq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Bq, K / 2, N, kW4BK / 2, kW4BN,
-                          CU_TENSOR_MAP_SWIZZLE_128B)) != TG_OK)
-        return st;
-    if ((st = make_map(&tmA, A, K, M, 64, a.m_pad)) != TG_OK) return st;
-    if ((st = make_map_ex(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, scales, N, K / kW4Group, kW4BN,
-                          kW4BK / kW4Group, CU_TENSOR_MAP_SWIZZLE_NONE)) != TG_OK)
-        return st;
-    const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
-    cudaError_t e = launch_w4(w, tmBq, tmA, tmS, grid, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "4-bit kernel launch");
     return TG_OK;
 }

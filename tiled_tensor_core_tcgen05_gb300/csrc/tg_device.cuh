@@ -45,6 +45,26 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
     }
 }
 
+// wait_phase for waits whose latency matters little (a whole work unit, or a
+// ring slot refilled by a slower stage): between polls the thread sleeps
+// about sleep_ns, so a waiting warp takes few issue slots from the warps that
+// work beside it on the same scheduler. Same bound and abort rules.
+__device__ __forceinline__ bool wait_phase_sleep(uint32_t bar, uint32_t parity, const WaitCtx& w, int site,
+                                                 uint32_t sleep_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*w.abort) return false;
+        if (globaltimer_ns() - t0 > w.limit_ns) {
+            *w.abort = 1;
+            atomicCAS(w.status, 0, site);
+            return false;
+        }
+    }
+}
+
 // Wait used while draining at exit: ignores the abort flag (the point is to let
 // copies or MMAs already in flight land before shared/tensor memory is
 // released), but still bounded.

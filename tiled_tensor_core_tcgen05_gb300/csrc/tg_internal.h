@@ -41,15 +41,16 @@ constexpr int kSkMaxM = 128;
 constexpr int kSkMaxSplits = 64;
 constexpr int kSkSmemBudget = 200 * 1024;  // operand ring budget per CTA
 
-// ---- weight-only 4-bit kernel geometry: one work unit is a 128-column slice
-// of N (one 128-row MMA, swap-AB as above) times a range of 256-wide K
-// blocks. A stage holds that slice's packed weights (128 rows of 128 bytes),
-// the matching 256 columns of A and the two scale rows of the block.
-constexpr int kW4BN = 128;
+// ---- weight-only 4-bit kernel geometry: one work unit is a 256-column slice
+// of N (the MMA's N) times a range of 256-wide K blocks; tokens are the MMA's
+// M (64 rows, at most 64 real ones per launch). A stage holds the slice's
+// packed weights (256 rows of 128 bytes), the matching 256 columns of A and
+// the two scale rows of the block.
+constexpr int kW4BN = 256;
 constexpr int kW4BK = 256;
 constexpr int kW4Group = 128;          // rows of K sharing one scale per column
-constexpr int kW4ConvGroups = 2;       // converter warp groups, taking stages in turn
-constexpr int kW4SmemBudget = 200 * 1024;
+constexpr int kW4MaxM = 64;            // rows of A per launch
+constexpr int kW4SmemBudget = 224 * 1024;
 
 // Watchdog plumbing handed to every kernel: where to record the first wait that
 // expired, the limit, and the test hook that withholds one producer arrival.
@@ -111,15 +112,15 @@ struct SplitArgs {
 };
 
 // The 4-bit kernel: the skinny fields above (A, bias, C, sizes, m_pad,
-// tmem_stride = accumulator columns, split bookkeeping) plus the packed
-// weights, their scales and the tensor-memory layout of the converted
-// operand.
+// split bookkeeping, stages = raw ring depth) plus the packed weights, their
+// scales and the depth of the converted-weight ring.
 struct W4Args {
-    SplitArgs s;               // s.B unused; s.stages = ring depth; s.tmem_cols = 512
+    SplitArgs s;               // s.B, s.tmem_* and s.n_acc unused
     const uint8_t* Bq;         // N rows of K/2 bytes, low nibble = even k
     const __half* scales;      // K/128 rows of N
-    int a_col0;                // first TMEM column of the converted-weight slots
-    int a_slots;               // number of 128-column slots (each one stage)
+    int a_slots;               // activation slots (one 256-k stage of A each)
+    int b_slots;               // converted 64-k sub-tiles in flight
+    int c_vec;                 // C 16-byte aligned and N % 8 == 0: 16-byte stores
 };
 
 int split_stage_bytes(int m_pad);
@@ -136,9 +137,8 @@ cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const 
                               cudaStream_t stream);
 cudaError_t launch_splitk(const SplitArgs& a, const CUtensorMap& tmB, const CUtensorMap& tmA,
                           int grid, cudaStream_t stream);
-int w4_stage_bytes(int m_pad);
-int w4_smem_bytes(int m_pad, int stages);
-int w4_stages_for(int m_pad);
+void w4_pipeline(int m_pad, int* stages, int* act_slots, int* slots);
+int w4_smem_bytes(int m_pad, int stages, int act_slots, int slots);
 cudaError_t launch_w4(const W4Args& a, const CUtensorMap& tmBq, const CUtensorMap& tmA, const CUtensorMap& tmS,
                       int grid, cudaStream_t stream);
 cudaError_t launch_bias_gelu(__half* C, const __half* bias, int64_t M, int64_t N, int gelu, bool vec8, int sm_count,
