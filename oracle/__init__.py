@@ -69,6 +69,9 @@ def _bind(lib):
     lib.oracle_gemm_w4_rows.argtypes = [u16p, u8p, u16p, u16p, u16p, f64p, i64, i64, i64, i64, ctypes.c_int,
                                         i64, i64, ctypes.c_int]
     lib.oracle_gemm_w4_rows.restype = ctypes.c_int
+    lib.oracle_attention_rows.argtypes = [u16p, u16p, u16p, u16p, f64p, i64, i64, i64, i64, ctypes.c_int,
+                                          ctypes.c_double, i64p, i64, ctypes.c_int]
+    lib.oracle_attention_rows.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -192,6 +195,31 @@ class Oracle:
         out = out.view(np.float16)
         return (out, out64) if want_f64 else out
 
+    def attention(self, Q, K, V, causal: bool = False, rows=None, want_f64: bool = False, threads: int = 0):
+        """Attention forward O = softmax(Q K^T / sqrt(D)) V on (B, S, H, D)
+        binary16 tensors (bshd). rows: flat query indices (b * S + s) * H + h to
+        evaluate (default all, returned as (B, S, H, D)); else (len(rows), D)."""
+        q, k, v = _bits(Q), _bits(K), _bits(V)
+        if q.ndim != 4 or q.shape != k.shape or q.shape != v.shape:
+            raise ValueError(f"Q, K, V must share one (B, S, H, D) shape, got {q.shape} {k.shape} {v.shape}")
+        B, S, H, D = q.shape
+        full = rows is None
+        r = np.arange(B * S * H, dtype=np.int64) if full else np.ascontiguousarray(rows, dtype=np.int64)
+        out = np.empty((len(r), D), dtype=np.uint16)
+        out64 = np.empty((len(r), D), dtype=np.float64) if want_f64 else None
+        rc = self._lib.oracle_attention_rows(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                             _ptr(v, ctypes.c_uint16), _ptr(out, ctypes.c_uint16),
+                                             _ptr(out64, ctypes.c_double), B, S, H, D, int(bool(causal)),
+                                             1.0 / np.sqrt(D) if D > 0 else 1.0, _ptr(r, ctypes.c_int64), len(r),
+                                             int(threads))
+        if rc != 0:
+            raise RuntimeError("oracle_attention_rows failed")
+        out = out.view(np.float16)
+        if full:
+            out = out.reshape(B, S, H, D)
+            out64 = out64.reshape(B, S, H, D) if want_f64 else None
+        return (out, out64) if want_f64 else out
+
     def gemm_sampled(self, A, B, bias, gelu: bool, rows, cols, want_f64: bool = False, threads: int = 0):
         """C[rows[t], cols[t]] for each t, each evaluated from the definition alone."""
         a, b, c = _bits(A), _bits(B), _bits(bias)
@@ -250,3 +278,4 @@ gemm_sampled = _default.gemm_sampled
 int4_value = _default.int4_value
 dequant_w4 = _default.dequant_w4
 gemm_w4 = _default.gemm_w4
+attention = _default.attention

@@ -239,6 +239,91 @@ int oracle_gemm_w4_rows(const uint16_t* A, const uint8_t* Bq, const uint16_t* sc
     return rc;
 }
 
+/* ---- Attention forward ----
+ *
+ * "TileLang: writing LLM GPU kernels by thinking in tiles", section 5 ("Why
+ * this matters specifically for LLMs", FlashAttention): S = Q K^T / sqrt(d),
+ * P = softmax(S) along each row, O = P V. "Designing high-performance GPU
+ * kernels with TileLang ..." (section 5, FlashAttention) adds the causal mask.
+ * Readings taken here: tensors are (batch, sequence, head, dim) row-major, the
+ * layout of the bshd example the pages walk through; with the causal mask,
+ * query position i sees key positions 0..i; softmax over the visible keys.
+ *
+ * The definition, one query row at a time, in fp64: every visible score, the
+ * row maximum subtracted before exp (softmax is unchanged by a shift of its
+ * inputs; the shift only keeps exp finite), exp, their sum, the weighted sum of
+ * V rows divided by that sum, rounded once to binary16. No tiling and no
+ * online rescaling: those are the kernel's business.
+ *
+ * rows[t] is a flat query row index (b * S + s) * H + h; output row t of O
+ * (nrows x D binary16, and O64 in fp64 if not NULL) is that query's result.
+ */
+int oracle_attention_rows(const uint16_t* Q, const uint16_t* K, const uint16_t* V, uint16_t* O, double* O64,
+                          int64_t B, int64_t S, int64_t H, int64_t D, int causal, double scale,
+                          const int64_t* rows, int64_t nrows, int threads) {
+    if (B < 0 || S < 0 || H < 0 || D < 0 || nrows < 0) return -1;
+    for (int64_t t = 0; t < nrows; ++t)
+        if (rows[t] < 0 || rows[t] >= B * S * H) return -1;
+    double* lut = decode_table();
+    if (!lut) return -1;
+    int rc = 0;
+#ifdef _OPENMP
+    if (threads > 0) omp_set_num_threads(threads);
+#pragma omp parallel
+#endif
+    {
+        double* sc = (double*)malloc((size_t)(S > 0 ? S : 1) * sizeof(double));
+        double* acc = (double*)malloc((size_t)(D > 0 ? D : 1) * sizeof(double));
+        double* q = (double*)malloc((size_t)(D > 0 ? D : 1) * sizeof(double));
+        const int have = sc && acc && q;
+        if (!have) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            rc = -1;
+        }
+        /* every thread reaches the work-sharing loop; one without buffers skips its rows */
+        {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 4)
+#endif
+            for (int64_t t = 0; t < nrows; ++t) {
+                if (!have) continue;
+                const int64_t r = rows[t];
+                const int64_t h = r % H, bs = r / H, si = bs % S, b = bs / S;
+                for (int64_t d = 0; d < D; ++d) q[d] = lut[Q[r * D + d]];
+                const int64_t visible = causal ? si + 1 : S;
+                double m = -INFINITY;
+                for (int64_t j = 0; j < visible; ++j) {
+                    const uint16_t* kr = K + ((b * S + j) * H + h) * D;
+                    double dot = 0.0;
+                    for (int64_t d = 0; d < D; ++d) dot += q[d] * lut[kr[d]];
+                    sc[j] = dot * scale;
+                    if (sc[j] > m) m = sc[j];
+                }
+                double l = 0.0;
+                for (int64_t d = 0; d < D; ++d) acc[d] = 0.0;
+                for (int64_t j = 0; j < visible; ++j) {
+                    const double pj = exp(sc[j] - m);
+                    l += pj;
+                    const uint16_t* vr = V + ((b * S + j) * H + h) * D;
+                    for (int64_t d = 0; d < D; ++d) acc[d] += pj * lut[vr[d]];
+                }
+                for (int64_t d = 0; d < D; ++d) {
+                    const double y = acc[d] / l;
+                    if (O64) O64[t * D + d] = y;
+                    if (O) O[t * D + d] = oracle_double_to_half(y);
+                }
+            }
+        }
+        free(sc);
+        free(acc);
+        free(q);
+    }
+    free(lut);
+    return rc;
+}
+
 /* Number of threads an OpenMP parallel region of this library uses. */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

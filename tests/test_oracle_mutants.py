@@ -11,7 +11,7 @@ import pytest
 pytestmark = pytest.mark.filterwarnings("ignore:overflow encountered in cast")
 
 import oracle
-from tests import test_oracle_codec, test_oracle_gemm, test_oracle_w4
+from tests import test_oracle_attention, test_oracle_codec, test_oracle_gemm, test_oracle_w4
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -42,12 +42,23 @@ MUTANTS = [
     ("int4_group_index", "scales + (k / group) * N;", "scales + (k % group) * N;"),
     ("int4_no_rounding_of_weights", "W[k * N + n] = oracle_double_to_half((double)q * oracle_half_to_double(srow[n]));",
      "W[k * N + n] = oracle_double_to_half((double)q) ; (void)srow;"),
+    ("attn_no_max_shift", "const double pj = exp(sc[j] - m);", "const double pj = exp(sc[j]);"),
+    ("attn_causal_drops_diagonal", "const int64_t visible = causal ? si + 1 : S;",
+     "const int64_t visible = causal ? (si > 0 ? si : 1) : S;"),
+    ("attn_causal_sees_next", "const int64_t visible = causal ? si + 1 : S;",
+     "const int64_t visible = causal ? (si + 2 < S ? si + 2 : S) : S;"),
+    ("attn_wrong_scale", "sc[j] = dot * scale;", "sc[j] = dot * scale * scale;"),
+    ("attn_no_normalisation", "const double y = acc[d] / l;", "const double y = acc[d];"),
+    ("attn_value_of_query_row", "const uint16_t* vr = V + ((b * S + j) * H + h) * D;",
+     "const uint16_t* vr = V + ((b * S + si) * H + h) * D;"),
+    ("attn_key_of_head_zero", "const uint16_t* kr = K + ((b * S + j) * H + h) * D;",
+     "const uint16_t* kr = K + ((b * S + j) * H + 0) * D;"),
 ]
 
 
 def _pins():
     fns = []
-    for mod in (test_oracle_codec, test_oracle_gemm, test_oracle_w4):
+    for mod in (test_oracle_codec, test_oracle_gemm, test_oracle_w4, test_oracle_attention):
         for name, fn in inspect.getmembers(mod, inspect.isfunction):
             if name.startswith("test_") and "oracle_lib" in inspect.signature(fn).parameters:
                 fns.append(fn)

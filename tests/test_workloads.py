@@ -74,3 +74,15 @@ def test_w4_workload_packing_and_bytes():
     assert torch.equal(Bq, Bq2) and torch.equal(s, s2)
     d = workloads.DECODE_W4
     assert d.bytes() == 2 * 16 * 8192 + 8192 * 28672 // 2 + 2 * 64 * 28672 + 2 * 16 * 28672
+
+
+def test_attention_workloads_are_seeded_and_sized():
+    w = workloads.ATTN_SMALL
+    Q, K, V = w.inputs()
+    assert Q.shape == K.shape == V.shape == (1, 256, 2, 128) and Q.dtype == torch.float16
+    Q2, K2, V2 = w.inputs()
+    assert torch.equal(Q, Q2) and torch.equal(V, V2) and not torch.equal(Q, K)
+    big = workloads.ATTN_4096
+    assert big.flops() == 4 * 32 * 128 * 4096 * 4096
+    assert workloads.ATTN_4096_CAUSAL.flops() == 4 * 32 * 128 * (4096 * 4097 // 2)
+    assert big.bytes() == 8 * 4096 * 32 * 128

@@ -181,6 +181,55 @@ W4_ALL = (DECODE_W4,)
 BY_NAME = {w.name: w for w in ALL + W4_ALL}
 
 
+@dataclass(frozen=True)
+class AttnWorkload:
+    """Attention forward O = softmax(Q K^T / sqrt(D)) V (optionally causal) on
+    (batch, sequence, head, dim) fp16 tensors, the layout of the bshd example
+    in the pages. Q, K, V are drawn in that order from one CPU torch.Generator
+    seeded with `seed`, each normal(0, 1) then rounded to fp16."""
+    name: str
+    B: int
+    S: int
+    H: int
+    D: int
+    seed: int
+    causal: bool = False
+    dist: Dist = Dist("normal", 0.0, 1.0)
+
+    def describe(self) -> str:
+        return (f"{self.name}: batch={self.B} seq={self.S} heads={self.H} dim={self.D} "
+                f"{'causal' if self.causal else 'non-causal'} seed={self.seed}")
+
+    def inputs(self, device: str = "cpu"):
+        g = torch.Generator(device="cpu")
+        g.manual_seed(self.seed)
+        shape = (self.B, self.S, self.H, self.D)
+        out = [self.dist.draw(shape, g) for _ in range(3)]
+        if device != "cpu":
+            out = [t.to(device) for t in out]
+        return tuple(out)
+
+    def visible_pairs(self) -> int:
+        return self.S * (self.S + 1) // 2 if self.causal else self.S * self.S
+
+    # algorithmic work: two products over the visible (query, key) pairs
+    def flops(self) -> int:
+        return 4 * self.B * self.H * self.D * self.visible_pairs()
+
+    def bytes(self) -> int:
+        return 2 * 4 * self.B * self.S * self.H * self.D  # Q, K, V read once, O written once
+
+
+ATTN_SMALL = AttnWorkload("attn_1x256x2x128", 1, 256, 2, 128, seed=20)
+ATTN_SMALL_CAUSAL = AttnWorkload("attn_1x256x2x128_causal", 1, 256, 2, 128, seed=21, causal=True)
+ATTN_RAGGED = AttnWorkload("attn_2x1000x3x128_causal", 2, 1000, 3, 128, seed=22, causal=True)
+# the pages' attention benchmark shape: batch 1, 32 heads, head dim 128, sequence 512..4096
+ATTN_4096 = AttnWorkload("attn_1x4096x32x128", 1, 4096, 32, 128, seed=23)
+ATTN_4096_CAUSAL = AttnWorkload("attn_1x4096x32x128_causal", 1, 4096, 32, 128, seed=24, causal=True)
+ATTN_ALL = (ATTN_SMALL, ATTN_SMALL_CAUSAL, ATTN_RAGGED, ATTN_4096, ATTN_4096_CAUSAL)
+BY_NAME.update({w.name: w for w in ATTN_ALL})
+
+
 def custom(M: int, N: int, K: int, seed: int, dist: Dist = U1, bias: Dist | None = None,
            gelu: bool = False) -> Workload:
     """An ad-hoc workload (edge-shape tests) with the same generator recipe."""
