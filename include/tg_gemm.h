@@ -198,6 +198,29 @@ tg_status tg_gemm_w4(const void* A, const void* Bq, const void* scales, const vo
                      int64_t M, int64_t N, int64_t K, int epilogue, int split_k, tg_stream_t stream);
 
 /*
+ * Attention forward (FlashAttention), the fused attention kernel of
+ * "TileLang: writing LLM GPU kernels by thinking in tiles", section 5, with
+ * the causal option of "Designing high-performance GPU kernels with TileLang
+ * ...", section 5:
+ *
+ *     S = Q K^T / sqrt(D),  P = softmax(S) along each query row,  O = P V
+ *
+ *   Q, K, V, O  B x S x H x D binary16, row-major in that order (batch,
+ *               sequence, head, dim: the bshd layout), DEVICE, 16-byte aligned
+ *   causal      0: every query sees every key; 1: query position i sees key
+ *               positions 0..i
+ *
+ * D must be 128 (TG_ERR_INVALID_ARG otherwise). B, S or H == 0 does nothing.
+ * Scores, the softmax and the accumulation are fp32 (the exponentials in base
+ * 2 with log2(e) folded into the scale; P is rounded to binary16 for the P V
+ * product); O is rounded once to binary16. Results agree with the exact
+ * definition within |O - ref| <= 1e-2 + 1e-2 |ref| per element. O must not
+ * overlap Q, K or V. Stream-ordered; allocates nothing.
+ */
+tg_status tg_attention_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t S,
+                           int64_t H, int64_t D, int causal, tg_stream_t stream);
+
+/*
  * Synchronises `stream`, then reports (and clears) the device-side status word
  * that kernels set when one of their bounded waits expires: TG_OK or
  * TG_ERR_TIMEOUT. `*where` (if not NULL) receives the code of the wait that

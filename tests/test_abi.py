@@ -147,3 +147,27 @@ def test_w4_invalid_arguments_rejected_on_host(tg, args, msg):
 def test_w4_empty_products_need_no_device(tg):
     tg.tg_gemm_w4(None, None, None, None, None, 0, 64, 256, 0, 0, None)
     tg.tg_gemm_w4(None, None, None, None, None, 4, 0, 256, 1, 0, None)
+
+
+@pytest.mark.parametrize("args,msg", [
+    (dict(D=64), "head dimension"),
+    (dict(causal=2), "causal"),
+    (dict(S=-1), "out of range"),
+    (dict(Q=0), "NULL"),
+    (dict(K=0x20000008), "16-byte aligned"),
+    (dict(O=0x10000 + 256), "overlaps"),
+])
+def test_attention_invalid_arguments_rejected_on_host(tg, args, msg):
+    base = dict(Q=0x10000, K=0x20000000, V=0x30000000, O=0x40000000, B=1, S=64, H=2, D=128, causal=0)
+    base.update(args)
+    with pytest.raises(tg.TgError) as ei:
+        tg.library().tg_attention_fwd and tg._check(tg.library().tg_attention_fwd(
+            base["Q"] or None, base["K"] or None, base["V"] or None, base["O"] or None, base["B"], base["S"],
+            base["H"], base["D"], base["causal"], None))
+    assert ei.value.status == tg.ERR_INVALID_ARG
+    assert msg in str(ei.value)
+
+
+def test_attention_empty_needs_no_device(tg):
+    tg.tg_attention_fwd(None, None, None, None, 0, 64, 2, 128, False, None)
+    tg.tg_attention_fwd(None, None, None, None, 1, 0, 2, 128, True, None)

@@ -26,7 +26,8 @@ KERNEL_AUTO, KERNEL_TILED_TMA, KERNEL_TILED_LSU, KERNEL_SPLITK, KERNEL_TILED_PAI
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NO_MEMORY = range(6)
 
 # every symbol include/tg_gemm.h declares
-EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_bias_gelu",
+EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_attention_fwd",
+           "tg_bias_gelu",
            "tg_device_status",
            "tg_set_watchdog_ns",
            "tg_debug_skip_first_arrive", "tg_status_string", "tg_last_error", "tg_version",
@@ -43,6 +44,7 @@ _lib.tg_gemm_ex.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _i
 _lib.tg_gemm_staged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
 _lib.tg_gemm_splitk_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.tg_gemm_w4.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
+_lib.tg_attention_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _vp]
 _lib.tg_bias_gelu.argtypes = [_vp, _vp, _i64, _i64, _int, _vp]
 _lib.tg_device_status.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.tg_set_watchdog_ns.argtypes = [_u64]
@@ -56,7 +58,8 @@ _lib.tg_ring_bytes.argtypes = [_int]
 _lib.tg_ring_bytes.restype = _i64
 _lib.tg_shutdown.argtypes = []
 _lib.tg_shutdown.restype = None
-for _name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_bias_gelu",
+for _name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_attention_fwd",
+              "tg_bias_gelu",
               "tg_device_status",
               "tg_set_watchdog_ns",
               "tg_debug_skip_first_arrive", "tg_version"):
@@ -105,6 +108,29 @@ def tg_gemm_splitk_noalloc(A: int, B: int, bias: int | None, C: int, M: int, N: 
 def tg_gemm_w4(A: int, Bq: int, scales: int, bias: int | None, C: int, M: int, N: int, K: int, epilogue: int,
                split_k: int, stream: int | None) -> None:
     _check(_lib.tg_gemm_w4(A, Bq, scales, bias, C, M, N, K, epilogue, split_k, stream))
+
+
+def tg_attention_fwd(Q: int, K: int, V: int, O: int, B: int, S: int, H: int, D: int, causal: bool,
+                     stream: int | None) -> None:
+    _check(_lib.tg_attention_fwd(Q, K, V, O, B, S, H, D, 1 if causal else 0, stream))
+
+
+def attention(Q, K, V, causal: bool = False, out=None, stream=None):
+    """O = softmax(Q K^T / sqrt(D)) V for CUDA float16 tensors of shape
+    (batch, sequence, heads, 128), contiguous; optional causal mask."""
+    import torch
+    if Q.dim() != 4 or Q.shape != K.shape or Q.shape != V.shape:
+        raise ValueError(f"Q, K, V must share one (B, S, H, D) shape: {tuple(Q.shape)} {tuple(K.shape)} {tuple(V.shape)}")
+    B, S, H, D = Q.shape
+    if out is None:
+        out = torch.empty_like(Q)
+    elif out.shape != Q.shape:
+        raise ValueError("out has the wrong shape")
+    if Q.numel() == 0:
+        return out
+    tg_attention_fwd(_dev_fp16(Q, "Q"), _dev_fp16(K, "K"), _dev_fp16(V, "V"), _dev_fp16(out, "out"), B, S, H, D,
+                     causal, _stream_handle(stream))
+    return out
 
 
 def tg_bias_gelu(C: int, bias: int | None, M: int, N: int, epilogue: int, stream: int | None) -> None:

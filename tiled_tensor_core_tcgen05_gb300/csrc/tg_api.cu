@@ -114,6 +114,23 @@ tg_status make_map_ex(CUtensorMap* m, CUtensorMapDataType dtype, uint32_t elem_b
     return TG_OK;
 }
 
+// (batch, sequence, head, dim) fp16 tensor as a 4-D map, innermost first:
+// {dim, head, sequence, batch}; box {64, 1, 128, 1} with the 128-byte swizzle
+// (one 64-column slice of 128 consecutive positions of one head).
+tg_status make_map_bshd(CUtensorMap* m, const void* base, uint64_t B, uint64_t S, uint64_t H, uint64_t D) {
+    cuuint64_t dims[4] = {D, H, S, B};
+    cuuint64_t strides[3] = {D * 2, H * D * 2, S * H * D * 2};
+    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %llu x %llu x %llu x %llu tensor", (int)r,
+                    (unsigned long long)B, (unsigned long long)S, (unsigned long long)H, (unsigned long long)D);
+    return TG_OK;
+}
+
 // Row-major [outer][inner] fp16 matrix, 128-byte-swizzled box.
 tg_status make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                    uint32_t box_outer) {
@@ -691,5 +708,47 @@ extern "C" tg_status tg_gemm_w4(const void* A, const void* Bq, const void* scale
         cudaError_t e = launch_w4(w, tmBq, tmA, tmS, grid, stream);
         if (e != cudaSuccess) return cuda_fail(e, "4-bit kernel launch");
     }
+    return TG_OK;
+}
+
+// ---------------------------------------------------------------------------
+// tg_attention_fwd: FlashAttention forward on (batch, sequence, head, dim).
+
+extern "C" tg_status tg_attention_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t S,
+                                      int64_t H, int64_t D, int causal, tg_stream_t stream_) {
+    t_last_error.clear();
+    const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (causal != 0 && causal != 1) return fail(TG_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
+    if (B < 0 || S < 0 || H < 0 || D < 0 || B > 0xFFFF || S > 0x7FFFFFFFll || H > 0xFFFF)
+        return fail(TG_ERR_INVALID_ARG, "sizes out of range: B=%lld S=%lld H=%lld D=%lld", (long long)B, (long long)S,
+                    (long long)H, (long long)D);
+    if (D != kAttnD) return fail(TG_ERR_INVALID_ARG, "tg_attention_fwd supports head dimension %d, got %lld", kAttnD,
+                                 (long long)D);
+    if (B == 0 || S == 0 || H == 0) return TG_OK;
+    if (!Q || !K || !V || !O) return fail(TG_ERR_INVALID_ARG, "Q, K, V or O is NULL");
+    if (!(aligned(Q, 16) && aligned(K, 16) && aligned(V, 16) && aligned(O, 16)))
+        return fail(TG_ERR_INVALID_ARG, "tg_attention_fwd needs 16-byte aligned Q, K, V and O");
+    const int64_t bytes = B * S * H * D * 2;
+    if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) || overlaps(O, bytes, V, bytes))
+        return fail(TG_ERR_INVALID_ARG, "O overlaps an input");
+    const int64_t n_qt = (S + 127) / 128;
+    if (B * H * n_qt > 0x7FFFFFFFll) return fail(TG_ERR_INVALID_ARG, "too many query blocks");
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    tg_status st = current_device(&dev);
+    if (st != TG_OK) return st;
+    AttnArgs a{};
+    a.O = static_cast<__half*>(O);
+    a.S = (int)S; a.H = (int)H; a.causal = causal;
+    a.n_qt = (int)n_qt;
+    a.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
+    a.wd = watchdog(g_dev[dev]);
+    CUtensorMap tmQ, tmK, tmV;
+    if ((st = make_map_bshd(&tmQ, Q, B, S, H, D)) != TG_OK) return st;
+    if ((st = make_map_bshd(&tmK, K, B, S, H, D)) != TG_OK) return st;
+    if ((st = make_map_bshd(&tmV, V, B, S, H, D)) != TG_OK) return st;
+    cudaError_t e = launch_attn(a, tmQ, tmK, tmV, (int)(B * H * n_qt), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
     return TG_OK;
 }

@@ -123,6 +123,17 @@ struct W4Args {
     int c_vec;                 // C 16-byte aligned and N % 8 == 0: 16-byte stores
 };
 
+// Attention forward: (batch, sequence, head, dim) fp16, dim = kAttnD.
+constexpr int kAttnD = 128;
+struct AttnArgs {
+    __half* O;
+    int S, H;
+    int causal;
+    int n_qt;            // 128-query blocks per (batch, head)
+    float scale_log2;    // log2(e) / sqrt(dim): scores in base-2 exponent units
+    Watchdog wd;
+};
+
 int split_stage_bytes(int m_pad);
 int split_smem_bytes(int m_pad, int stages);
 int split_stages_for(int m_pad);
@@ -141,6 +152,9 @@ void w4_pipeline(int m_pad, int* stages, int* act_slots, int* slots);
 int w4_smem_bytes(int m_pad, int stages, int act_slots, int slots);
 cudaError_t launch_w4(const W4Args& a, const CUtensorMap& tmBq, const CUtensorMap& tmA, const CUtensorMap& tmS,
                       int grid, cudaStream_t stream);
+int attn_smem_bytes();
+cudaError_t launch_attn(const AttnArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                        int grid, cudaStream_t stream);
 cudaError_t launch_bias_gelu(__half* C, const __half* bias, int64_t M, int64_t N, int gelu, bool vec8, int sm_count,
                              cudaStream_t stream);
 cudaError_t launch_fill(const __half* bias, __half* C, int64_t M, int64_t N, int gelu,
