@@ -165,8 +165,17 @@ def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sam
     import workloads
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
-    dC = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
-    if isinstance(w, workloads.W4Workload):
+    dC = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda") if hasattr(w, "M") else None
+    if isinstance(w, workloads.AttnWorkload):
+        dC = None
+        Q, K, V = w.inputs()
+        dA, dB, ds = Q.cuda(), K.cuda(), V.cuda()
+        db = torch.empty_like(dA)
+        args = (dA.data_ptr(), dB.data_ptr(), ds.data_ptr(), db.data_ptr(), w.B, w.S, w.H, w.D, bool(w.causal), sh)
+
+        def call():
+            tg.tg_attention_fwd(*args)
+    elif isinstance(w, workloads.W4Workload):
         A, Bq, sc, bias = w.inputs()
         dA, dB, ds = A.cuda(), Bq.cuda(), sc.cuda()
         db = bias.cuda() if bias is not None else None
@@ -370,19 +379,20 @@ def run_gpu(args):
     # the rest of the suite, same rules, fewer steps
     extra = []
     if not args.only_main:
-        for w in workloads.ALL + workloads.W4_ALL:
+        for w in workloads.ALL + workloads.W4_ALL + (workloads.ATTN_4096, workloads.ATTN_4096_CAUSAL):
             if w.name == main.name:
                 continue
             steps = max(5, min(args.steps, 50))  # secondary workloads: at most 50 timed launches
             r = time_workload(tg, w, steps, max(3, args.warmup), 0 if w.bytes() > 2 * l2 else 2 * l2 + (1 << 20),
                               pg=pg)
             avg = r["kernel_ms"] / steps
-            bound = "hbm" if w.M <= 128 else "tensor"  # the skinny (decode) shapes stream their weights
+            # the skinny (decode) shapes stream their weights; attention and the big GEMMs are contractions
+            bound = "hbm" if getattr(w, "M", 1 << 30) <= 128 else "tensor"
             e = {"workload": w.describe(), "ms_per_launch": round(avg, 5),
                  "TFLOP/s": round(w.flops() / (avg / 1e3) / 1e12, 2),
                  "GB/s": round(w.bytes() / (avg / 1e3) / 1e9, 1),
                  "roofline": roofline_entry(w, avg, pk, pk_kind, bound, recorded_traffic(w.name))}
-            if w.gelu or w.has_bias:
+            if getattr(w, "gelu", False) or getattr(w, "has_bias", False):
                 # unfused comparator, back to back (the fused figure above is per launch)
                 un_ms = time_unfused(tg, w, steps, max(3, args.warmup))
                 e["unfused_ms_per_step"] = round(un_ms, 5)

@@ -72,6 +72,8 @@ def _bind(lib):
     lib.oracle_attention_rows.argtypes = [u16p, u16p, u16p, u16p, f64p, i64, i64, i64, i64, ctypes.c_int,
                                           ctypes.c_double, i64p, i64, ctypes.c_int]
     lib.oracle_attention_rows.restype = ctypes.c_int
+    lib.oracle_softmax_rows.argtypes = [u16p, u16p, f64p, i64, i64, i64, i64, ctypes.c_int]
+    lib.oracle_softmax_rows.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -220,6 +222,22 @@ class Oracle:
             out64 = out64.reshape(B, S, H, D) if want_f64 else None
         return (out, out64) if want_f64 else out
 
+    def softmax(self, X, rows: tuple[int, int] | None = None, want_f64: bool = False, threads: int = 0):
+        """Row softmax of an M x N binary16 matrix, rows [r0, r0 + n) (default all)."""
+        x = _bits(X)
+        if x.ndim != 2:
+            raise ValueError(f"X must be a matrix, got shape {x.shape}")
+        M, N = x.shape
+        r0, nr = (0, M) if rows is None else rows
+        out = np.empty((nr, N), dtype=np.uint16)
+        out64 = np.empty((nr, N), dtype=np.float64) if want_f64 else None
+        rc = self._lib.oracle_softmax_rows(_ptr(x, ctypes.c_uint16), _ptr(out, ctypes.c_uint16),
+                                           _ptr(out64, ctypes.c_double), M, N, r0, nr, int(threads))
+        if rc != 0:
+            raise RuntimeError("oracle_softmax_rows failed")
+        out = out.view(np.float16)
+        return (out, out64) if want_f64 else out
+
     def gemm_sampled(self, A, B, bias, gelu: bool, rows, cols, want_f64: bool = False, threads: int = 0):
         """C[rows[t], cols[t]] for each t, each evaluated from the definition alone."""
         a, b, c = _bits(A), _bits(B), _bits(bias)
@@ -279,3 +297,4 @@ int4_value = _default.int4_value
 dequant_w4 = _default.dequant_w4
 gemm_w4 = _default.gemm_w4
 attention = _default.attention
+softmax = _default.softmax

@@ -324,6 +324,43 @@ int oracle_attention_rows(const uint16_t* Q, const uint16_t* K, const uint16_t* 
     return rc;
 }
 
+/* ---- Row softmax ----
+ *
+ * "Designing high-performance GPU kernels with TileLang ..." (scrapefeed),
+ * section 4 "Advanced Reductions and Softmax": row-wise softmax, a maximum
+ * over the row for numerical stability, then the sum of exponentials.
+ * Y[i,j] = exp(X[i,j] - max_j X[i,:]) / sum_j exp(X[i,j] - max_j X[i,:]) in
+ * fp64, rounded once to binary16. X and Y are M x N binary16, row-major.
+ * Rows [row0, row0 + nrows) are computed; Y holds those rows (Y64 in fp64 if
+ * not NULL). A row whose maximum is -inf (every entry -inf) has no defined
+ * softmax; the arithmetic gives NaN, which is what is stored.
+ */
+int oracle_softmax_rows(const uint16_t* X, uint16_t* Y, double* Y64, int64_t M, int64_t N, int64_t row0,
+                        int64_t nrows, int threads) {
+    if (M < 0 || N < 0 || row0 < 0 || nrows < 0 || row0 + nrows > M) return -1;
+    double* lut = decode_table();
+    if (!lut) return -1;
+#ifdef _OPENMP
+    if (threads > 0) omp_set_num_threads(threads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t r = 0; r < nrows; ++r) {
+        const uint16_t* x = X + (row0 + r) * N;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < N; ++j)
+            if (lut[x[j]] > m) m = lut[x[j]];
+        double l = 0.0;
+        for (int64_t j = 0; j < N; ++j) l += exp(lut[x[j]] - m);
+        for (int64_t j = 0; j < N; ++j) {
+            const double y = exp(lut[x[j]] - m) / l;
+            if (Y64) Y64[r * N + j] = y;
+            if (Y) Y[r * N + j] = oracle_double_to_half(y);
+        }
+    }
+    free(lut);
+    return 0;
+}
+
 /* Number of threads an OpenMP parallel region of this library uses. */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

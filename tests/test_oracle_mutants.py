@@ -11,7 +11,7 @@ import pytest
 pytestmark = pytest.mark.filterwarnings("ignore:overflow encountered in cast")
 
 import oracle
-from tests import test_oracle_attention, test_oracle_codec, test_oracle_gemm, test_oracle_w4
+from tests import test_oracle_attention, test_oracle_codec, test_oracle_gemm, test_oracle_softmax, test_oracle_w4
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -51,6 +51,13 @@ MUTANTS = [
     ("attn_no_normalisation", "const double y = acc[d] / l;", "const double y = acc[d];"),
     ("attn_value_of_query_row", "const uint16_t* vr = V + ((b * S + j) * H + h) * D;",
      "const uint16_t* vr = V + ((b * S + si) * H + h) * D;"),
+    ("softmax_no_max_shift", "for (int64_t j = 0; j < N; ++j) l += exp(lut[x[j]] - m);",
+     "m = 0.0; for (int64_t j = 0; j < N; ++j) l += exp(lut[x[j]] - m);"),
+    ("softmax_max_skips_last", "for (int64_t j = 0; j < N; ++j)\n            if (lut[x[j]] > m) m = lut[x[j]];",
+     "for (int64_t j = 0; j + 1 < N; ++j)\n            if (lut[x[j]] > m) m = lut[x[j]];"),
+    ("softmax_sum_skips_first", "for (int64_t j = 0; j < N; ++j) l += exp(lut[x[j]] - m);",
+     "for (int64_t j = 1; j < N; ++j) l += exp(lut[x[j]] - m);"),
+    ("softmax_wrong_row", "const uint16_t* x = X + (row0 + r) * N;", "const uint16_t* x = X + r * N;"),
     ("attn_key_of_head_zero", "const uint16_t* kr = K + ((b * S + j) * H + h) * D;",
      "const uint16_t* kr = K + ((b * S + j) * H + 0) * D;"),
 ]
@@ -58,7 +65,7 @@ MUTANTS = [
 
 def _pins():
     fns = []
-    for mod in (test_oracle_codec, test_oracle_gemm, test_oracle_w4, test_oracle_attention):
+    for mod in (test_oracle_codec, test_oracle_gemm, test_oracle_w4, test_oracle_attention, test_oracle_softmax):
         for name, fn in inspect.getmembers(mod, inspect.isfunction):
             if name.startswith("test_") and "oracle_lib" in inspect.signature(fn).parameters:
                 fns.append(fn)

@@ -86,3 +86,11 @@ def test_attention_workloads_are_seeded_and_sized():
     assert big.flops() == 4 * 32 * 128 * 4096 * 4096
     assert workloads.ATTN_4096_CAUSAL.flops() == 4 * 32 * 128 * (4096 * 4097 // 2)
     assert big.bytes() == 8 * 4096 * 32 * 128
+
+
+def test_softmax_workloads():
+    w = workloads.SOFTMAX_RAGGED
+    (X,) = w.inputs()
+    (X2,) = w.inputs()
+    assert X.shape == (1000, 1030) and X.dtype == torch.float16 and torch.equal(X, X2)
+    assert workloads.SOFTMAX_4096.bytes() == 4 * 32768 * 4096

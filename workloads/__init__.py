@@ -230,6 +230,37 @@ ATTN_ALL = (ATTN_SMALL, ATTN_SMALL_CAUSAL, ATTN_RAGGED, ATTN_4096, ATTN_4096_CAU
 BY_NAME.update({w.name: w for w in ATTN_ALL})
 
 
+@dataclass(frozen=True)
+class SoftmaxWorkload:
+    """Row softmax Y = softmax(X) along each row of an M x N fp16 matrix; X is
+    drawn normal(0, sigma) (logit-like) from a CPU torch.Generator seeded with
+    `seed`, then rounded to fp16."""
+    name: str
+    M: int
+    N: int
+    seed: int
+    dist: Dist = Dist("normal", 0.0, 3.0)
+
+    def describe(self) -> str:
+        return f"{self.name}: M={self.M} N={self.N} seed={self.seed}"
+
+    def inputs(self, device: str = "cpu"):
+        g = torch.Generator(device="cpu")
+        g.manual_seed(self.seed)
+        X = self.dist.draw((self.M, self.N), g)
+        return (X.to(device) if device != "cpu" else X,)
+
+    def bytes(self) -> int:
+        return 2 * 2 * self.M * self.N  # X read once, Y written once
+
+
+SOFTMAX_RAGGED = SoftmaxWorkload("softmax_1000x1030", 1000, 1030, seed=30)
+SOFTMAX_4096 = SoftmaxWorkload("softmax_32768x4096", 32768, 4096, seed=31)
+SOFTMAX_VOCAB = SoftmaxWorkload("softmax_4096x32768", 4096, 32768, seed=32)
+SOFTMAX_ALL = (SOFTMAX_RAGGED, SOFTMAX_4096, SOFTMAX_VOCAB)
+BY_NAME.update({w.name: w for w in SOFTMAX_ALL})
+
+
 def custom(M: int, N: int, K: int, seed: int, dist: Dist = U1, bias: Dist | None = None,
            gelu: bool = False) -> Workload:
     """An ad-hoc workload (edge-shape tests) with the same generator recipe."""
