@@ -166,7 +166,16 @@ def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sam
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
     dC = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda") if hasattr(w, "M") else None
-    if isinstance(w, workloads.AttnWorkload):
+    if isinstance(w, workloads.SoftmaxWorkload):
+        (X,) = w.inputs()
+        dA = X.cuda()
+        dB = ds = None
+        db = torch.empty_like(dA)
+        args = (dA.data_ptr(), db.data_ptr(), w.M, w.N, sh)
+
+        def call():
+            tg.tg_softmax_rows(*args)
+    elif isinstance(w, workloads.AttnWorkload):
         dC = None
         Q, K, V = w.inputs()
         dA, dB, ds = Q.cuda(), K.cuda(), V.cuda()
@@ -379,7 +388,8 @@ def run_gpu(args):
     # the rest of the suite, same rules, fewer steps
     extra = []
     if not args.only_main:
-        for w in workloads.ALL + workloads.W4_ALL + (workloads.ATTN_4096, workloads.ATTN_4096_CAUSAL):
+        for w in (workloads.ALL + workloads.W4_ALL + (workloads.ATTN_4096, workloads.ATTN_4096_CAUSAL) +
+                  (workloads.SOFTMAX_4096, workloads.SOFTMAX_VOCAB)):
             if w.name == main.name:
                 continue
             steps = max(5, min(args.steps, 50))  # secondary workloads: at most 50 timed launches
@@ -387,11 +397,13 @@ def run_gpu(args):
                               pg=pg)
             avg = r["kernel_ms"] / steps
             # the skinny (decode) shapes stream their weights; attention and the big GEMMs are contractions
-            bound = "hbm" if getattr(w, "M", 1 << 30) <= 128 else "tensor"
+            bound = ("hbm" if getattr(w, "M", 1 << 30) <= 128 or isinstance(w, workloads.SoftmaxWorkload)
+                     else "tensor")
             e = {"workload": w.describe(), "ms_per_launch": round(avg, 5),
-                 "TFLOP/s": round(w.flops() / (avg / 1e3) / 1e12, 2),
                  "GB/s": round(w.bytes() / (avg / 1e3) / 1e9, 1),
                  "roofline": roofline_entry(w, avg, pk, pk_kind, bound, recorded_traffic(w.name))}
+            if hasattr(w, "flops"):
+                e["TFLOP/s"] = round(w.flops() / (avg / 1e3) / 1e12, 2)
             if getattr(w, "gelu", False) or getattr(w, "has_bias", False):
                 # unfused comparator, back to back (the fused figure above is per launch)
                 un_ms = time_unfused(tg, w, steps, max(3, args.warmup))

@@ -221,6 +221,22 @@ tg_status tg_attention_fwd(const void* Q, const void* K, const void* V, void* O,
                            int64_t H, int64_t D, int causal, tg_stream_t stream);
 
 /*
+ * Row softmax, the reduction kernel of "Designing high-performance GPU kernels
+ * with TileLang ...", section 4: for every row i of the M x N row-major
+ * binary16 DEVICE matrix X,
+ *
+ *     Y[i,j] = exp(X[i,j] - max_j X[i,:]) / sum_j exp(X[i,j] - max_j X[i,:])
+ *
+ * computed in fp32 (the exponentials in base 2) and rounded once to binary16.
+ * Entries of -inf give 0; a row that is entirely -inf gives NaN. Y may be X
+ * itself (in place) but must not otherwise overlap it. Any alignment; rows
+ * that start 16-byte aligned with N <= 32768 and N % 8 == 0 take the
+ * register-resident path (one HBM read and one write per element).
+ * Stream-ordered; allocates nothing.
+ */
+tg_status tg_softmax_rows(const void* X, void* Y, int64_t M, int64_t N, tg_stream_t stream);
+
+/*
  * Synchronises `stream`, then reports (and clears) the device-side status word
  * that kernels set when one of their bounded waits expires: TG_OK or
  * TG_ERR_TIMEOUT. `*where` (if not NULL) receives the code of the wait that

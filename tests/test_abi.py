@@ -171,3 +171,13 @@ def test_attention_invalid_arguments_rejected_on_host(tg, args, msg):
 def test_attention_empty_needs_no_device(tg):
     tg.tg_attention_fwd(None, None, None, None, 0, 64, 2, 128, False, None)
     tg.tg_attention_fwd(None, None, None, None, 1, 0, 2, 128, True, None)
+
+
+def test_softmax_argument_checks(tg):
+    tg.tg_softmax_rows(None, None, 0, 10, None)
+    tg.tg_softmax_rows(None, None, 10, 0, None)
+    for args, msg in [((0x1000, 0x2000, -1, 4), "sizes"), ((None, 0x2000, 4, 4), "NULL"),
+                      ((0x1000, 0x1004, 4, 4), "overlaps")]:
+        with pytest.raises(tg.TgError) as ei:
+            tg.tg_softmax_rows(*args, None)
+        assert ei.value.status == tg.ERR_INVALID_ARG and msg in str(ei.value)

@@ -27,7 +27,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NO_MEMOR
 
 # every symbol include/tg_gemm.h declares
 EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_attention_fwd",
-           "tg_bias_gelu",
+           "tg_softmax_rows", "tg_bias_gelu",
            "tg_device_status",
            "tg_set_watchdog_ns",
            "tg_debug_skip_first_arrive", "tg_status_string", "tg_last_error", "tg_version",
@@ -45,6 +45,7 @@ _lib.tg_gemm_staged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i
 _lib.tg_gemm_splitk_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.tg_gemm_w4.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.tg_attention_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _vp]
+_lib.tg_softmax_rows.argtypes = [_vp, _vp, _i64, _i64, _vp]
 _lib.tg_bias_gelu.argtypes = [_vp, _vp, _i64, _i64, _int, _vp]
 _lib.tg_device_status.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.tg_set_watchdog_ns.argtypes = [_u64]
@@ -59,7 +60,7 @@ _lib.tg_ring_bytes.restype = _i64
 _lib.tg_shutdown.argtypes = []
 _lib.tg_shutdown.restype = None
 for _name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_attention_fwd",
-              "tg_bias_gelu",
+              "tg_softmax_rows", "tg_bias_gelu",
               "tg_device_status",
               "tg_set_watchdog_ns",
               "tg_debug_skip_first_arrive", "tg_version"):
@@ -130,6 +131,24 @@ def attention(Q, K, V, causal: bool = False, out=None, stream=None):
         return out
     tg_attention_fwd(_dev_fp16(Q, "Q"), _dev_fp16(K, "K"), _dev_fp16(V, "V"), _dev_fp16(out, "out"), B, S, H, D,
                      causal, _stream_handle(stream))
+    return out
+
+
+def tg_softmax_rows(X: int, Y: int, M: int, N: int, stream: int | None) -> None:
+    _check(_lib.tg_softmax_rows(X, Y, M, N, stream))
+
+
+def softmax(X, out=None, stream=None):
+    """Row softmax of a CUDA float16 matrix (contiguous); ``out`` may be X."""
+    import torch
+    if X.dim() != 2:
+        raise ValueError("X must be a matrix")
+    if out is None:
+        out = torch.empty_like(X)
+    elif out.shape != X.shape:
+        raise ValueError("out has the wrong shape")
+    if X.numel():
+        tg_softmax_rows(_dev_fp16(X, "X"), _dev_fp16(out, "out"), X.shape[0], X.shape[1], _stream_handle(stream))
     return out
 
 

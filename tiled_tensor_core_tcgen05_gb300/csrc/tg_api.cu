@@ -752,3 +752,25 @@ extern "C" tg_status tg_attention_fwd(const void* Q, const void* K, const void* 
     if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
     return TG_OK;
 }
+
+// ---------------------------------------------------------------------------
+// tg_softmax_rows: row softmax of an M x N fp16 matrix.
+
+extern "C" tg_status tg_softmax_rows(const void* X, void* Y, int64_t M, int64_t N, tg_stream_t stream_) {
+    t_last_error.clear();
+    const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (M < 0 || N < 0 || M > 0x7FFFFFFFll || N > 0x7FFFFFFFll)
+        return fail(TG_ERR_INVALID_ARG, "sizes must be in [0, 2^31): M=%lld N=%lld", (long long)M, (long long)N);
+    if (M == 0 || N == 0) return TG_OK;
+    if (!X || !Y) return fail(TG_ERR_INVALID_ARG, "X or Y is NULL");
+    if (X != Y && overlaps(Y, M * N * 2, X, M * N * 2))
+        return fail(TG_ERR_INVALID_ARG, "Y overlaps X without being the same buffer");
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    tg_status st = current_device(&dev);
+    if (st != TG_OK) return st;
+    const bool vec = N % 8 == 0 && aligned(X, 16) && aligned(Y, 16);
+    cudaError_t e = launch_softmax(static_cast<const __half*>(X), static_cast<__half*>(Y), (int)M, (int)N, vec,
+                                   g_dev[dev].sm_count, stream);
+    return e == cudaSuccess ? TG_OK : cuda_fail(e, "softmax kernel launch");
+}

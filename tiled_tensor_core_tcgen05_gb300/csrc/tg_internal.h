@@ -152,6 +152,7 @@ void w4_pipeline(int m_pad, int* stages, int* act_slots, int* slots);
 int w4_smem_bytes(int m_pad, int stages, int act_slots, int slots);
 cudaError_t launch_w4(const W4Args& a, const CUtensorMap& tmBq, const CUtensorMap& tmA, const CUtensorMap& tmS,
                       int grid, cudaStream_t stream);
+cudaError_t launch_softmax(const __half* X, __half* Y, int M, int N, bool vec, int sm_count, cudaStream_t stream);
 int attn_smem_bytes();
 cudaError_t launch_attn(const AttnArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                         int grid, cudaStream_t stream);
