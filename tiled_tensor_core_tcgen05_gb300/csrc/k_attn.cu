@@ -10,24 +10,25 @@
 // maximum rescaling the accumulator and the running sum, exponentials in base
 // 2 with log2(e) folded into the scale; 128 x 128 blocks with d = 128.
 //
-// GB300 mapping. One CTA per (batch, head, 128-query block).
-//   warp 0      TMA producer: Q once (two 64-column boxes), then K and V
-//               blocks of 128 keys into a two-stage ring;
-//   warp 1      allocates TMEM; one thread issues S_j = Q K_j^T (M = N = 128,
-//               K = d) into one of two TMEM score buffers, and O += P_j V_j
-//               with P_j read from TMEM as the A operand. S_{j+1} is issued
-//               before O += P_j V_j, so the tensor core works while the
-//               softmax of block j runs;
-//   warps 2-5   softmax, one thread per query row (its TMEM lane): read the
-//               row of S_j, mask, row maximum, exponentials, running sum;
-//               write P_j (fp16) to TMEM; rescale the O row when needed; at
-//               the end divide by the sum and write O.
+// GB300 mapping. One CTA per (batch, head, 128-query block), two CTAs per SM,
+// so that one CTA's tensor-core work overlaps the other's softmax.
+//   warp 0      TMA producer: Q once (two 64-column boxes), then each block of
+//               128 keys: K into its slot as soon as the previous K has been
+//               read, V likewise;
+//   warp 1      allocates 256 TMEM columns; one thread issues, per key block,
+//               S_j = Q K_j^T (M = N = 128, K = d) and, once P_j is written,
+//               O += P_j V_j with P_j read from TMEM as the A operand;
+//   warps 2-5   softmax, one thread per query row (its TMEM lane): a pass over
+//               the row of S_j in 32-column chunks for the maximum, then a pass
+//               that forms the exponentials and writes P_j (fp16 pairs) over
+//               the score columns already read; at the end O / sum.
 // The accumulator is only rescaled when a row's maximum grows by more than
 // 2^8 (in the base-2 domain); otherwise the old maximum stays the reference,
 // so the exponentials are at most 2^8 and the final O / sum is unchanged.
 //
-// TMEM columns: S buffers [0, 256), O [256, 384), P buffers [384, 512)
-// (fp16 pairs of keys, 64 columns each).
+// TMEM columns: S [0, 128) with P over its first 64 columns, O [128, 256).
+// S_{j+1} is issued only after O += P_j V_j has completed, since it
+// overwrites P_j.
 #include "tg_device.cuh"
 #include "tg_internal.h"
 
@@ -37,28 +38,29 @@ namespace {
 constexpr int kD = kAttnD;
 constexpr int kBM = 128;                       // queries per CTA
 constexpr int kBN = 128;                       // keys per block
-constexpr int kStages = 2;
 constexpr int kBoxBytes = 128 * 64 * 2;        // 128 rows x 64 columns fp16
 constexpr int kTileBytes = 2 * kBoxBytes;      // 128 rows x 128 columns
 constexpr int kThreads = 6 * 32;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+constexpr int kCtasPerSm = 2;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0, kColP = 0, kColO = 128;
 constexpr float kRescaleLog2 = 8.0f;           // lazy rescale threshold (base-2 exponent)
 static_assert(kD == 128, "head dimension 128");
 
-// shared memory: Q, then per stage K and V, then barriers
+// shared memory: Q, K, V, then barriers (about 97 KB: two CTAs fit on an SM)
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kTileBytes;
-constexpr int kOffBar = kOffKV + kStages * 2 * kTileBytes;
+constexpr int kOffK = kTileBytes;
+constexpr int kOffV = 2 * kTileBytes;
+constexpr int kOffBar = 3 * kTileBytes;
 constexpr int kBarQ = kOffBar;
 constexpr int kBarKFull = kBarQ + 8;
-constexpr int kBarVFull = kBarKFull + 8 * kStages;
-constexpr int kBarKVEmpty = kBarVFull + 8 * kStages;
-constexpr int kBarSFull = kBarKVEmpty + 8 * kStages;
-constexpr int kBarSFree = kBarSFull + 16;
-constexpr int kBarPFull = kBarSFree + 16;
-constexpr int kBarPFree = kBarPFull + 16;
-constexpr int kBarDrain = kBarPFree + 16;
+constexpr int kBarKEmpty = kBarKFull + 8;
+constexpr int kBarVFull = kBarKEmpty + 8;
+constexpr int kBarVEmpty = kBarVFull + 8;
+constexpr int kBarSFull = kBarVEmpty + 8;
+constexpr int kBarPFull = kBarSFull + 8;
+constexpr int kBarODone = kBarPFull + 8;
+constexpr int kBarDrain = kBarODone + 8;
 constexpr int kTmemSlot = kBarDrain + 8;
 constexpr int kAbortSlot = kTmemSlot + 4;
 constexpr int kSmemUsed = kAbortSlot + 4;
@@ -78,7 +80,7 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
         : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnArgs args) {
     extern __shared__ uint8_t smem_raw[];
@@ -95,33 +97,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_kt = (args.S + kBN - 1) / kBN;
     const int j_last = args.causal ? min(qt, n_kt - 1) : n_kt - 1;  // key blocks 0..j_last
 
-    const uint32_t bar_q = sbase + kBarQ;
-    auto k_full = [&](int s) { return sbase + kBarKFull + 8 * s; };
-    auto v_full = [&](int s) { return sbase + kBarVFull + 8 * s; };
-    auto kv_empty = [&](int s) { return sbase + kBarKVEmpty + 8 * s; };
-    auto s_full = [&](int i) { return sbase + kBarSFull + 8 * i; };
-    auto s_free = [&](int i) { return sbase + kBarSFree + 8 * i; };
-    auto p_full = [&](int i) { return sbase + kBarPFull + 8 * i; };
-    auto p_free = [&](int i) { return sbase + kBarPFree + 8 * i; };
-    auto k_tile = [&](int s) { return sbase + kOffKV + s * 2 * kTileBytes; };
-    auto v_tile = [&](int s) { return sbase + kOffKV + s * 2 * kTileBytes + kTileBytes; };
-    const uint32_t drain_bar = sbase + kBarDrain;
+    const uint32_t bar_q = sbase + kBarQ, k_full = sbase + kBarKFull, k_empty = sbase + kBarKEmpty;
+    const uint32_t v_full = sbase + kBarVFull, v_empty = sbase + kBarVEmpty, s_full = sbase + kBarSFull;
+    const uint32_t p_full = sbase + kBarPFull, o_done = sbase + kBarODone, drain_bar = sbase + kBarDrain;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortSlot);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
 
     if (threadIdx.x == 0) {
         mbar_init(bar_q, 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(k_full(s), 1);
-            mbar_init(v_full(s), 1);
-            mbar_init(kv_empty(s), 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(s_full(i), 1);
-            mbar_init(s_free(i), 4);  // one arrival per softmax warp
-            mbar_init(p_full(i), 4);
-            mbar_init(p_free(i), 1);
-        }
+        mbar_init(k_full, 1);
+        mbar_init(k_empty, 1);
+        mbar_init(v_full, 1);
+        mbar_init(v_empty, 1);
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 4);  // one arrival per softmax warp
+        mbar_init(o_done, 1);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -145,26 +135,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(bar_q, kTileBytes);
             for (int i = 0; i < 2; ++i)
                 tma_load_4d(sbase + kOffQ + i * kBoxBytes, &tmQ, bar_q, 64 * i, h, qt * kBM, b);
-            uint32_t issued = 0, parity = 0;
+            int k_issued = 0, v_issued = 0;
             for (int j = 0; j <= j_last; ++j) {
-                const int s = j % kStages;
-                const uint32_t ph = static_cast<uint32_t>(j / kStages) & 1u;
-                if (!wait_phase_sleep(kv_empty(s), ph ^ 1, wc, kSiteProducerEmpty, 64)) break;
-                mbar_arrive_expect_tx(k_full(s), kTileBytes);
+                const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+                if (!wait_phase_sleep(k_empty, ph ^ 1, wc, kSiteProducerEmpty, 64)) break;
+                mbar_arrive_expect_tx(k_full, kTileBytes);
                 for (int i = 0; i < 2; ++i)
-                    tma_load_4d(k_tile(s) + i * kBoxBytes, &tmK, k_full(s), 64 * i, h, j * kBN, b);
-                mbar_arrive_expect_tx(v_full(s), kTileBytes);
+                    tma_load_4d(sbase + kOffK + i * kBoxBytes, &tmK, k_full, 64 * i, h, j * kBN, b);
+                ++k_issued;
+                if (!wait_phase_sleep(v_empty, ph ^ 1, wc, kSiteProducerEmpty, 64)) break;
+                mbar_arrive_expect_tx(v_full, kTileBytes);
                 for (int i = 0; i < 2; ++i)
-                    tma_load_4d(v_tile(s) + i * kBoxBytes, &tmV, v_full(s), 64 * i, h, j * kBN, b);
-                issued |= 1u << s;
-                parity = (parity & ~(1u << s)) | (ph << s);
+                    tma_load_4d(sbase + kOffV + i * kBoxBytes, &tmV, v_full, 64 * i, h, j * kBN, b);
+                ++v_issued;
             }
+            // let every copy in flight land before the CTA exits
             wait_phase_drain(bar_q, 0, wc);
-            for (int s = 0; s < kStages; ++s)
-                if (issued & (1u << s)) {
-                    wait_phase_drain(k_full(s), (parity >> s) & 1, wc);
-                    wait_phase_drain(v_full(s), (parity >> s) & 1, wc);
-                }
+            if (k_issued > 0) wait_phase_drain(k_full, static_cast<uint32_t>(k_issued - 1) & 1u, wc);
+            if (v_issued > 0) wait_phase_drain(v_full, static_cast<uint32_t>(v_issued - 1) & 1u, wc);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
@@ -172,47 +160,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc_s = idesc_f16_f32(kBM, kBN, /*a_mn_major=*/false, /*b_mn_major=*/false);
             const uint32_t idesc_o = idesc_f16_f32(kBM, kD, /*a_mn_major=*/false, /*b_mn_major=*/true);
             bool ok = wait_phase(bar_q, 0, wc, kSiteMmaFull);
-            tc_fence_after_sync();
-            // S_j = Q K_j^T: both operands K-major (d contiguous), two 64-column boxes
-            auto issue_s = [&](int j) -> bool {
-                const int s = j % kStages;
-                const int sb = j & 1;
-                if (!wait_phase(k_full(s), static_cast<uint32_t>(j / kStages) & 1u, wc, kSiteMmaFull)) return false;
-                if (j >= 2 && !wait_phase(s_free(sb), static_cast<uint32_t>((j >> 1) - 1) & 1u, wc, kSiteMmaAccEmpty))
-                    return false;
+            for (int j = 0; ok && j <= j_last; ++j) {
+                const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+                // S_j = Q K_j^T (both operands K-major, d contiguous, two 64-column boxes); it
+                // overwrites P_{j-1}, so O += P_{j-1} V_{j-1} must have completed
+                if (!wait_phase(k_full, ph, wc, kSiteMmaFull) ||
+                    (j > 0 && !wait_phase(o_done, ph ^ 1, wc, kSiteMmaAccEmpty))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint64_t a = smem_desc_sw128(sbase + kOffQ + (kk >> 2) * kBoxBytes, 16, 1024) +
                                        static_cast<uint64_t>(((kk & 3) * 32) >> 4);
-                    const uint64_t bd = smem_desc_sw128(k_tile(s) + (kk >> 2) * kBoxBytes, 16, 1024) +
+                    const uint64_t bd = smem_desc_sw128(sbase + kOffK + (kk >> 2) * kBoxBytes, 16, 1024) +
                                         static_cast<uint64_t>(((kk & 3) * 32) >> 4);
-                    mma_f16(tmem_base + kColS + sb * kBN, a, bd, idesc_s, kk != 0);
+                    mma_f16(tmem_base + kColS, a, bd, idesc_s, kk != 0);
                 }
-                mma_commit(s_full(sb));
-                return true;
-            };
-            // O += P_j V_j: P from TMEM (8 columns per 16 keys), V N-major (d contiguous)
-            auto issue_o = [&](int j) -> bool {
-                const int s = j % kStages;
-                const int sb = j & 1;
-                if (!wait_phase(v_full(s), static_cast<uint32_t>(j / kStages) & 1u, wc, kSiteMmaFull)) return false;
-                if (!wait_phase(p_full(sb), static_cast<uint32_t>(j >> 1) & 1u, wc, kSiteMmaFull)) return false;
+                mma_commit(s_full);
+                mma_commit(k_empty);
+                // O += P_j V_j: P from TMEM (8 columns per 16 keys), V N-major (d contiguous)
+                if (!wait_phase_sleep(p_full, ph, wc, kSiteMmaFull, 20) || !wait_phase(v_full, ph, wc, kSiteMmaFull)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t bd = smem_desc_sw128(v_tile(s), kBoxBytes, 1024) +
+                    const uint64_t bd = smem_desc_sw128(sbase + kOffV, kBoxBytes, 1024) +
                                         static_cast<uint64_t>((kk * 2048) >> 4);
-                    mma_f16_tmem_a(tmem_base + kColO, tmem_base + kColP + sb * (kBN / 2) + kk * 8, bd, idesc_o,
-                                   (j != 0) || (kk != 0));
+                    mma_f16_tmem_a(tmem_base + kColO, tmem_base + kColP + kk * 8, bd, idesc_o, (j != 0) || (kk != 0));
                 }
-                mma_commit(p_free(sb));
-                mma_commit(kv_empty(s));
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            for (int j = 1; ok && j <= j_last; ++j) ok = issue_s(j) && issue_o(j - 1);
-            if (ok) issue_o(j_last);
+                mma_commit(o_done);
+                mma_commit(v_empty);
+            }
             mma_commit(drain_bar);
             wait_phase_drain(drain_bar, 0, wc);
         }
@@ -224,36 +206,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q_pos = qt * kBM + row;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
         const float scale = args.scale_log2;
+        const int limit = args.causal ? min(args.S, q_pos + 1) : args.S;  // visible keys: < limit
         float m_run = 0.0f, l_run = 0.0f;
         bool ok = true;
         for (int j = 0; j <= j_last; ++j) {
-            const int sb = j & 1;
-            const uint32_t use = static_cast<uint32_t>(j >> 1);
-            ok = __all_sync(0xFFFFFFFFu, wait_phase(s_full(sb), use & 1u, wc, kSiteEpilogueAccFull));
+            const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+            ok = __all_sync(0xFFFFFFFFu, wait_phase(s_full, ph, wc, kSiteEpilogueAccFull));
             if (!ok) break;
             tc_fence_after_sync();
-            uint32_t r[kBN];
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c)
-                tmem_ld_32x32b_x32(lane_base + kColS + sb * kBN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c]));
-            tmem_ld_wait();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free(sb));  // the MMA may now write S_{j+2} here
-
-            // mask (keys past the sequence, keys after the query when causal) and row maximum
             const int key0 = j * kBN;
-            const int limit = args.causal ? min(args.S, q_pos + 1) : args.S;  // visible keys: < limit
+            const bool masked = key0 + kBN > limit;
+            // pass 1: row maximum over the visible keys (two 32-column chunks per TMEM wait)
             float mx = -INFINITY;
-            if (key0 + kBN > limit) {
+#pragma unroll 1
+            for (int c = 0; c < kBN / 32; c += 2) {
+                uint32_t ra[32], rb[32];
+                tmem_ld_32x32b_x32(lane_base + kColS + c * 32, ra);
+                tmem_ld_32x32b_x32(lane_base + kColS + (c + 1) * 32, rb);
+                tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    if (key0 + c >= limit) r[c] = __float_as_uint(-INFINITY);
-                    mx = fmaxf(mx, __uint_as_float(r[c]));
+                for (int e = 0; e < 32; ++e) {
+                    const float va = (masked && key0 + c * 32 + e >= limit) ? -INFINITY : __uint_as_float(ra[e]);
+                    const float vb = (masked && key0 + (c + 1) * 32 + e >= limit) ? -INFINITY : __uint_as_float(rb[e]);
+                    mx = fmaxf(mx, fmaxf(va, vb));
                 }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, __uint_as_float(r[c]));
             }
             const float m_tile = mx * scale;
             float alpha = 1.0f;
@@ -265,34 +241,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_run = m_tile;
                 rescale = true;
             }
-            // P buffer sb was last read by O += P_{j-2} V_{j-2}
-            if (j >= 2) {
-                ok = __all_sync(0xFFFFFFFFu, wait_phase(p_free(sb), (use - 1) & 1u, wc, kSiteEpilogueAccFull));
-                if (!ok) break;
-                tc_fence_after_sync();
-            }
-            // exponentials, running sum, P (fp16 pairs) into TMEM, 32 keys at a time
+            // pass 2: exponentials and their sum, two chunks per TMEM wait; P chunk c (16
+            // columns at 16c) lands on score columns already read (chunk c / 2)
             float sum = 0.0f;
+#pragma unroll 1
+            for (int c = 0; c < kBN / 32; c += 2) {
+                uint32_t r[2][32];
+                tmem_ld_32x32b_x32(lane_base + kColS + c * 32, r[0]);
+                tmem_ld_32x32b_x32(lane_base + kColS + (c + 1) * 32, r[1]);
+                tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t pk[16];
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(r[32 * c + 2 * e]), scale, -m_run));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(r[32 * c + 2 * e + 1]), scale, -m_run));
-                    sum += p0 + p1;
-                    pk[e] = pack_half2(p0, p1);
+                    for (int e = 0; e < 16; ++e) {
+                        const int k0 = key0 + (c + h) * 32 + 2 * e;
+                        const float s0 = (masked && k0 >= limit) ? -INFINITY : __uint_as_float(r[h][2 * e]);
+                        const float s1 = (masked && k0 + 1 >= limit) ? -INFINITY : __uint_as_float(r[h][2 * e + 1]);
+                        const float p0 = ex2_approx(fmaf(s0, scale, -m_run));
+                        const float p1 = ex2_approx(fmaf(s1, scale, -m_run));
+                        sum += p0 + p1;
+                        pk[e] = pack_half2(p0, p1);
+                    }
+                    tmem_st_32x32b_x16(lane_base + kColP + (c + h) * 16, pk);
                 }
-                tmem_st_32x32b_x16(lane_base + kColP + sb * (kBN / 2) + c * 16, pk);
             }
             l_run = l_run * alpha + sum;
-            // O row *= alpha once O += P_{j-1} V_{j-1} has landed (any lane of the warp needing it)
+            // O row *= alpha (O already holds P_{j-1} V_{j-1}: S_j was issued after it completed)
             if (j >= 1 && __any_sync(0xFFFFFFFFu, rescale)) {
-                ok = __all_sync(0xFFFFFFFFu,
-                                wait_phase(p_free((j - 1) & 1), static_cast<uint32_t>((j - 1) >> 1) & 1u, wc,
-                                           kSiteEpilogueAccFull));
-                if (!ok) break;
-                tc_fence_after_sync();
 #pragma unroll 1
                 for (int c = 0; c < kD / 32; ++c) {
                     uint32_t o[32];
@@ -306,11 +282,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(sb));
+            if (lane == 0) mbar_arrive(p_full);
         }
         // O / sum, written as fp16 once the last O += P V has landed
-        if (ok && __all_sync(0xFFFFFFFFu, wait_phase(p_free(j_last & 1), static_cast<uint32_t>(j_last >> 1) & 1u, wc,
-                                                     kSiteEpilogueAccFull))) {
+        if (ok && __all_sync(0xFFFFFFFFu, wait_phase_sleep(o_done, static_cast<uint32_t>(j_last) & 1u, wc,
+                                                           kSiteEpilogueAccFull, 64))) {
             tc_fence_after_sync();
             const float inv = 1.0f / l_run;
             __half* dst = args.O + ((static_cast<int64_t>(b) * args.S + q_pos) * args.H + h) * kD;
