@@ -18,15 +18,17 @@
 //   warp 1      allocates 256 TMEM columns; one thread issues, per key block,
 //               S_j = Q K_j^T (M = N = 128, K = d) and, once P_j is written,
 //               O += P_j V_j with P_j read from TMEM as the A operand;
-//   warps 2-5   softmax, one thread per query row (its TMEM lane): a pass over
-//               the row of S_j in 32-column chunks for the maximum, then a pass
-//               that forms the exponentials and writes P_j (fp16 pairs) over
-//               the score columns already read; at the end O / sum.
+//   warps 2-9   softmax, two threads per query row (its TMEM lane), each with
+//               half of the keys: read its 64 scores of S_j, the row maximum
+//               (halves exchanged through shared memory), the exponentials,
+//               P_j (fp16 pairs) written over the scores just read; each half
+//               rescales and finally writes 64 of O's columns.
 // The accumulator is only rescaled when a row's maximum grows by more than
 // 2^8 (in the base-2 domain); otherwise the old maximum stays the reference,
 // so the exponentials are at most 2^8 and the final O / sum is unchanged.
 //
-// TMEM columns: S [0, 128) with P over its first 64 columns, O [128, 256).
+// TMEM columns: S [0, 128) with each half's P over the first 32 of its 64
+// score columns (keys 64g.. -> columns 64g..64g+31), O [128, 256).
 // S_{j+1} is issued only after O += P_j V_j has completed, since it
 // overwrites P_j.
 #include "tg_device.cuh"
@@ -40,7 +42,9 @@ constexpr int kBM = 128;                       // queries per CTA
 constexpr int kBN = 128;                       // keys per block
 constexpr int kBoxBytes = 128 * 64 * 2;        // 128 rows x 64 columns fp16
 constexpr int kTileBytes = 2 * kBoxBytes;      // 128 rows x 128 columns
-constexpr int kThreads = 6 * 32;
+constexpr int kSoftmaxWarps = 8;                // two per TMEM lane quarter, each half the keys
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kThreads = (2 + kSoftmaxWarps) * 32;
 constexpr int kCtasPerSm = 2;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0, kColP = 0, kColO = 128;
@@ -61,7 +65,9 @@ constexpr int kBarSFull = kBarVEmpty + 8;
 constexpr int kBarPFull = kBarSFull + 8;
 constexpr int kBarODone = kBarPFull + 8;
 constexpr int kBarDrain = kBarODone + 8;
-constexpr int kTmemSlot = kBarDrain + 8;
+constexpr int kOffRedMax = kBarDrain + 8;                 // [2 (key-block parity)][2 halves][128 rows] floats
+constexpr int kOffRedSum = kOffRedMax + 2 * 2 * 128 * 4;  // [2 halves][128 rows] floats
+constexpr int kTmemSlot = kOffRedSum + 2 * 128 * 4;
 constexpr int kAbortSlot = kTmemSlot + 4;
 constexpr int kSmemUsed = kAbortSlot + 4;
 constexpr int kSmemAlloc = kSmemUsed + 1024;
@@ -110,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         mbar_init(v_full, 1);
         mbar_init(v_empty, 1);
         mbar_init(s_full, 1);
-        mbar_init(p_full, 4);  // one arrival per softmax warp
+        mbar_init(p_full, kSoftmaxWarps);  // one arrival per softmax warp
         mbar_init(o_done, 1);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -190,7 +196,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int kk = 0; kk < kBN / 16; ++kk) {
                     const uint64_t bd = smem_desc_sw128(sbase + kOffV, kBoxBytes, 1024) +
                                         static_cast<uint64_t>((kk * 2048) >> 4);
-                    mma_f16_tmem_a(tmem_base + kColO, tmem_base + kColP + kk * 8, bd, idesc_o, (j != 0) || (kk != 0));
+                    // keys 64 g .. 64 g + 63 (softmax half g) are P columns 64 g .. 64 g + 31
+                    const uint32_t a_col = kColP + (kk >> 2) * 64 + (kk & 3) * 8;
+                    mma_f16_tmem_a(tmem_base + kColO, tmem_base + a_col, bd, idesc_o, (j != 0) || (kk != 0));
                 }
                 mma_commit(o_done);
                 mma_commit(v_empty);
@@ -201,36 +209,50 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + output
+        // warp w handles the rows of TMEM lane quarter w % 4 and, with half g = (w - 2) / 4,
+        // keys 64 g .. 64 g + 63 of each block and O columns 64 g .. 64 g + 63; the two halves
+        // of a row exchange their maxima through shared memory every key block (named barrier
+        // 1, all softmax warps) and their sums at the end.
         const int quarter = warp & 3;
+        const int g = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;  // query row within the block = TMEM lane
         const int q_pos = qt * kBM + row;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+        const uint32_t s_cols = kColS + g * 64;  // this half's 64 score columns; its P goes to the first 32
+        float* red_max = reinterpret_cast<float*>(smem + kOffRedMax);
+        float* red_sum = reinterpret_cast<float*>(smem + kOffRedSum);
         const float scale = args.scale_log2;
         const int limit = args.causal ? min(args.S, q_pos + 1) : args.S;  // visible keys: < limit
         float m_run = 0.0f, l_run = 0.0f;
         bool ok = true;
         for (int j = 0; j <= j_last; ++j) {
             const uint32_t ph = static_cast<uint32_t>(j) & 1u;
-            ok = __all_sync(0xFFFFFFFFu, wait_phase(s_full, ph, wc, kSiteEpilogueAccFull));
-            if (!ok) break;
+            ok = wait_phase(s_full, ph, wc, kSiteEpilogueAccFull);
+            // every softmax warp stops together, so the named barriers below never wait for a
+            // thread that has left
+            if (named_barrier_or(1, kSoftmaxThreads, !ok)) {
+                ok = false;
+                break;
+            }
             tc_fence_after_sync();
-            const int key0 = j * kBN;
-            const bool masked = key0 + kBN > limit;
-            // pass 1: row maximum over the visible keys (two 32-column chunks per TMEM wait)
+            const int key0 = j * kBN + g * 64;
+            const bool masked = key0 + 64 > limit;
+            uint32_t r[2][32];
+            tmem_ld_32x32b_x32(lane_base + s_cols, r[0]);
+            tmem_ld_32x32b_x32(lane_base + s_cols + 32, r[1]);
+            tmem_ld_wait();
             float mx = -INFINITY;
-#pragma unroll 1
-            for (int c = 0; c < kBN / 32; c += 2) {
-                uint32_t ra[32], rb[32];
-                tmem_ld_32x32b_x32(lane_base + kColS + c * 32, ra);
-                tmem_ld_32x32b_x32(lane_base + kColS + (c + 1) * 32, rb);
-                tmem_ld_wait();
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float va = (masked && key0 + c * 32 + e >= limit) ? -INFINITY : __uint_as_float(ra[e]);
-                    const float vb = (masked && key0 + (c + 1) * 32 + e >= limit) ? -INFINITY : __uint_as_float(rb[e]);
-                    mx = fmaxf(mx, fmaxf(va, vb));
+                    if (masked && key0 + hc * 32 + e >= limit) r[hc][e] = __float_as_uint(-INFINITY);
+                    mx = fmaxf(mx, __uint_as_float(r[hc][e]));
                 }
-            }
+            // the row maximum over both halves
+            red_max[(j & 1) * 256 + g * 128 + row] = mx;
+            named_barrier_sync(1, kSoftmaxThreads);
+            mx = fmaxf(mx, red_max[(j & 1) * 256 + (g ^ 1) * 128 + row]);
             const float m_tile = mx * scale;
             float alpha = 1.0f;
             bool rescale = false;
@@ -241,42 +263,32 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 m_run = m_tile;
                 rescale = true;
             }
-            // pass 2: exponentials and their sum, two chunks per TMEM wait; P chunk c (16
-            // columns at 16c) lands on score columns already read (chunk c / 2)
+            // exponentials, this half's sum, P (fp16 pairs) over the scores just read
             float sum = 0.0f;
-#pragma unroll 1
-            for (int c = 0; c < kBN / 32; c += 2) {
-                uint32_t r[2][32];
-                tmem_ld_32x32b_x32(lane_base + kColS + c * 32, r[0]);
-                tmem_ld_32x32b_x32(lane_base + kColS + (c + 1) * 32, r[1]);
-                tmem_ld_wait();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[16];
+            for (int hc = 0; hc < 2; ++hc) {
+                uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int k0 = key0 + (c + h) * 32 + 2 * e;
-                        const float s0 = (masked && k0 >= limit) ? -INFINITY : __uint_as_float(r[h][2 * e]);
-                        const float s1 = (masked && k0 + 1 >= limit) ? -INFINITY : __uint_as_float(r[h][2 * e + 1]);
-                        const float p0 = ex2_approx(fmaf(s0, scale, -m_run));
-                        const float p1 = ex2_approx(fmaf(s1, scale, -m_run));
-                        sum += p0 + p1;
-                        pk[e] = pack_half2(p0, p1);
-                    }
-                    tmem_st_32x32b_x16(lane_base + kColP + (c + h) * 16, pk);
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(r[hc][2 * e]), scale, -m_run));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(r[hc][2 * e + 1]), scale, -m_run));
+                    sum += p0 + p1;
+                    pk[e] = pack_half2(p0, p1);
                 }
+                tmem_st_32x32b_x16(lane_base + s_cols + hc * 16, pk);
             }
             l_run = l_run * alpha + sum;
-            // O row *= alpha (O already holds P_{j-1} V_{j-1}: S_j was issued after it completed)
+            // this half's O columns *= alpha (O already holds P_{j-1} V_{j-1}: S_j was issued after
+            // it completed); both halves of a row take the same decision
             if (j >= 1 && __any_sync(0xFFFFFFFFu, rescale)) {
 #pragma unroll 1
-                for (int c = 0; c < kD / 32; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     uint32_t o[32];
-                    tmem_ld_32x32b_x32(lane_base + kColO + c * 32, o);
+                    tmem_ld_32x32b_x32(lane_base + kColO + g * 64 + c * 32, o);
                     tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st_32x32b_x32(lane_base + kColO + c * 32, o);
+                    tmem_st_32x32b_x32(lane_base + kColO + g * 64 + c * 32, o);
                 }
             }
             tmem_st_wait();
@@ -284,25 +296,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
         }
-        // O / sum, written as fp16 once the last O += P V has landed
-        if (ok && __all_sync(0xFFFFFFFFu, wait_phase_sleep(o_done, static_cast<uint32_t>(j_last) & 1u, wc,
-                                                           kSiteEpilogueAccFull, 64))) {
-            tc_fence_after_sync();
-            const float inv = 1.0f / l_run;
-            __half* dst = args.O + ((static_cast<int64_t>(b) * args.S + q_pos) * args.H + h) * kD;
+        // O / (sum of both halves), written as fp16 once the last O += P V has landed
+        if (!named_barrier_or(1, kSoftmaxThreads, !ok)) {
+            red_sum[g * 128 + row] = l_run;
+            const bool done = wait_phase_sleep(o_done, static_cast<uint32_t>(j_last) & 1u, wc, kSiteEpilogueAccFull, 64);
+            if (!named_barrier_or(1, kSoftmaxThreads, !done)) {
+                tc_fence_after_sync();
+                const float inv = 1.0f / (l_run + red_sum[(g ^ 1) * 128 + row]);
+                __half* dst = args.O + ((static_cast<int64_t>(b) * args.S + q_pos) * args.H + h) * kD + g * 64;
 #pragma unroll 1
-            for (int c = 0; c < kD / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld_32x32b_x32(lane_base + kColO + c * 32, o);
-                tmem_ld_wait();
-                if (q_pos < args.S) {
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(lane_base + kColO + g * 64 + c * 32, o);
+                    tmem_ld_wait();
+                    if (q_pos < args.S) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        reinterpret_cast<uint4*>(dst + c * 32)[q] =
-                            make_uint4(pack_half2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
-                                       pack_half2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
-                                       pack_half2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
-                                       pack_half2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
+                        for (int q = 0; q < 4; ++q)
+                            reinterpret_cast<uint4*>(dst + c * 32)[q] = make_uint4(
+                                pack_half2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
+                                pack_half2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
+                                pack_half2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
+                                pack_half2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
+                    }
                 }
             }
         }
