@@ -240,7 +240,6 @@ tg_status run_splitk(DeviceState& d, const __half* A, const __half* B, const __h
     a.m_pad = (M + 15) / 16 * 16;
     a.tmem_stride = 16;
     while (a.tmem_stride < a.m_pad) a.tmem_stride *= 2;
-    a.n_acc = 1;
     a.tmem_cols = 2 * kSkHalves * a.tmem_stride < 32 ? 32 : 2 * kSkHalves * a.tmem_stride;
     a.stages = split_stages_for(a.m_pad);
     a.n_tiles = (N + kSkBN - 1) / kSkBN;
@@ -587,7 +586,6 @@ extern "C" tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const 
     a.m_pad = (a.M + 15) / 16 * 16;
     a.tmem_stride = 16;
     while (a.tmem_stride < a.m_pad) a.tmem_stride *= 2;
-    a.n_acc = 1;
     a.tmem_cols = 2 * kSkHalves * a.tmem_stride < 32 ? 32 : 2 * kSkHalves * a.tmem_stride;
     a.stages = split_stages_for(a.m_pad);
     a.n_tiles = (a.N + kSkBN - 1) / kSkBN;

@@ -100,9 +100,7 @@ struct SplitArgs {
     int gelu;
     int m_pad;         // MMA N: M rounded up to a multiple of 16 (16..128)
     int tmem_stride;   // TMEM columns per accumulator (pow2 >= m_pad); a buffer holds
-                       // kSkHalves x n_acc accumulators, two buffers alternate between units
-    int n_acc;         // accumulators per half, each taking every n_acc-th K step (summed
-                       // in order 0, 1, ... by the epilogue); lets independent MMAs overlap
+                       // kSkHalves accumulators, two buffers alternate between units
     int tmem_cols;     // TMEM columns allocated (2 * kSkHalves * tmem_stride, >= 32)
     int stages;        // ring depth
     int n_tiles, kb_total, kb_per_split, splits, num_units;
@@ -115,7 +113,7 @@ struct SplitArgs {
 // split bookkeeping, stages = raw ring depth) plus the packed weights, their
 // scales and the depth of the converted-weight ring.
 struct W4Args {
-    SplitArgs s;               // s.B, s.tmem_* and s.n_acc unused
+    SplitArgs s;               // s.B and s.tmem_* unused
     const uint8_t* Bq;         // N rows of K/2 bytes, low nibble = even k
     const __half* scales;      // K/128 rows of N
     int a_slots;               // activation slots (one 256-k stage of A each)

@@ -23,9 +23,7 @@ constexpr int kSkEpiThreads = 128;
 // Runs the epilogue role for every unit this CTA owns (units blockIdx.x,
 // blockIdx.x + gridDim.x, ...; unit u is column slice u % n_tiles of K slice
 // u / n_tiles). Accumulator buffer b = (i-th unit of this CTA) & 1 starts at
-// TMEM column b * kHalves * n_acc * tmem_stride; half h at
-// + h * n_acc * tmem_stride, and its n_acc partial accumulators follow one
-// another, tmem_stride columns apart; they are added in order 0, 1, ....
+// TMEM column b * kHalves * tmem_stride; half h at + h * tmem_stride.
 // acc_full0 / acc_empty0: the first of two consecutive mbarriers each (8 bytes
 // apart); acc_empty counts kSkEpiThreads arrivals. epi_thread0: the first
 // thread of the four epilogue warps. Named barrier 1 is used.
@@ -54,20 +52,13 @@ __device__ __forceinline__ void skinny_epilogue(const SplitArgs& args, uint32_t 
             const int n = nt * kUnitCols + h * 128 + quarter * 32 + lane;  // this thread's output column
             const bool n_ok = n < args.N;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   (b * kHalves + h) * args.n_acc * args.tmem_stride;
+                                   (b * kHalves + h) * args.tmem_stride;
             const float bias_n = (args.bias != nullptr && n_ok) ? __half2float(args.bias[n]) : 0.0f;
             for (int c = 0; c < chunks; ++c) {
                 uint32_t r[16];
                 __syncwarp();  // tcgen05.ld is warp-collective; lanes diverged on the column mask
                 tmem_ld_32x32b_x16(taddr + c * 16, r);
                 tmem_ld_wait();
-                for (int a = 1; a < args.n_acc; ++a) {
-                    uint32_t r2[16];
-                    tmem_ld_32x32b_x16(taddr + a * args.tmem_stride + c * 16, r2);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
-                }
                 if (h == kHalves - 1 && c == chunks - 1) {
                     tc_fence_before_sync();
                     mbar_arrive(acc_empty0 + 8 * b);  // every accumulator of buffer b is read
