@@ -95,9 +95,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // block -> (query block, head, batch); the longest causal blocks first
-    const int qt = args.n_qt - 1 - static_cast<int>(blockIdx.x % args.n_qt);
-    const int bh = static_cast<int>(blockIdx.x / args.n_qt);
+    // block -> (query block, head, batch): all heads' last query block first, then the one
+    // before, ... so with the causal mask the longest CTAs start first (and the shortest
+    // fill the tail)
+    const int n_bh = static_cast<int>(gridDim.x) / args.n_qt;
+    const int qt = args.n_qt - 1 - static_cast<int>(blockIdx.x) / n_bh;
+    const int bh = static_cast<int>(blockIdx.x) % n_bh;
     const int h = bh % args.H;
     const int b = bh / args.H;
     const int n_kt = (args.S + kBN - 1) / kBN;
