@@ -8,14 +8,16 @@
 // in "Designing high-performance GPU kernels with TileLang ...", section 3.
 //
 // GB300 design (not the pages' Ampere/Hopper schedule):
-//   * one CTA per SM, persistent over 128 x 256 output tiles in grouped order;
+//   * one CTA per SM, persistent over 128 x BN output tiles in grouped order
+//     (BN = 256; 128 or 64 when 256-wide tiles would leave most SMs idle);
 //   * warp roles: a producer (one TMA-issuing lane, or four warps of ordinary
 //     loads when TMA cannot describe the operands), one MMA-issuing lane, and
-//     eight epilogue warps (two per quarter of the accumulator's rows);
-//   * a 4-stage ring of 48 KB stages (A 128x64 K-major, B 64x256 N-major, both
-//     in the 128-byte swizzled layout) guarded by full/empty mbarriers;
-//   * tcgen05.mma (M=128, N=256, K=16) accumulating in tensor memory; two
-//     256-column accumulators so the epilogue of one tile overlaps the
+//     four epilogue warps (one per quarter of the accumulator's rows);
+//   * a ~192 KB ring (4 stages of A 128x64 K-major + B 64x256 N-major, or 6 / 8
+//     of the narrower stages, all in the 128-byte swizzled layout) guarded by
+//     full/empty mbarriers;
+//   * tcgen05.mma (M=128, N=BN, K=16) accumulating in tensor memory; two
+//     BN-column accumulators so the epilogue of one tile overlaps the
 //     mainloop of the next;
 //   * the epilogue reads TMEM with tcgen05.ld, adds bias, applies GELU in fp32,
 //     rounds once to binary16 and stores with masking for ragged M/N.
@@ -25,30 +27,37 @@
 namespace tg {
 namespace {
 
-constexpr int kStageA = kBM * kBK * 2;  // 16 KB: 128 rows x 128 B
-constexpr int kStageB = kBK * kBN * 2;  // 32 KB: four 64x64 N-major boxes of 8 KB
-constexpr int kStageBytes = kStageA + kStageB;
-constexpr int kRingBytes = kStages * kStageBytes;
 constexpr int kBoxB = kBK * 64 * 2;  // one 64 (k) x 64 (n) box, 8 KB
-constexpr int kTmemCols = 2 * kBN;   // two accumulators of 256 fp32 columns
 
-// Barrier block after the ring: full[S], empty[S], acc_full[2], acc_empty[2], drain.
-constexpr int kBarFull = kRingBytes;
-constexpr int kBarEmpty = kBarFull + 8 * kStages;
-constexpr int kBarAccFull = kBarEmpty + 8 * kStages;
-constexpr int kBarAccEmpty = kBarAccFull + 16;
-constexpr int kBarDrain = kBarAccEmpty + 16;
-constexpr int kTmemSlot = kBarDrain + 8;
-constexpr int kAbortSlot = kTmemSlot + 4;
-constexpr int kEpiStage = (kAbortSlot + 4 + 127) / 128 * 128;  // per-warp output staging
-constexpr int kSmemUsed = kEpiStage + kEpiWarps * kStageWarpBytes;
-constexpr int kSmemAlloc = kSmemUsed + 1024;  // slack to align the ring to 1024 B
-
-// Operand descriptors: A is K-major (8-row groups 1024 B apart); B is N-major
-// with 64-column atoms 8 KB apart (one TMA box each) and 8-row K groups 1024 B
-// apart. One K=16 step advances A by 32 B within the swizzled row and B by 16
-// rows (2048 B).
-constexpr uint32_t kIdesc = idesc_f16_f32(kBM, kBN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+// Geometry for a tile width BN (256, or 128 / 64 for problems with few tiles):
+// a ring of ~192 KB (4, 6 or 8 stages), two BN-column fp32 accumulators in
+// TMEM, and the barrier block after the ring: full[S], empty[S], acc_full[2],
+// acc_empty[2], drain; then the per-warp output staging.
+template <int BN>
+struct Geom {
+    static constexpr int kStageA = kBM * kBK * 2;  // 16 KB: 128 rows x 128 B
+    static constexpr int kStageB = kBK * BN * 2;   // BN / 64 N-major boxes of 8 KB
+    static constexpr int kStageBytes = kStageA + kStageB;
+    static constexpr int kStagesN = (kStages * (kBM * kBK + kBK * kBN) * 2) / kStageBytes;
+    static constexpr int kRingBytes = kStagesN * kStageBytes;
+    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kBarFull = kRingBytes;
+    static constexpr int kBarEmpty = kBarFull + 8 * kStagesN;
+    static constexpr int kBarAccFull = kBarEmpty + 8 * kStagesN;
+    static constexpr int kBarAccEmpty = kBarAccFull + 16;
+    static constexpr int kBarDrain = kBarAccEmpty + 16;
+    static constexpr int kTmemSlot = kBarDrain + 8;
+    static constexpr int kAbortSlot = kTmemSlot + 4;
+    static constexpr int kEpiStage = (kAbortSlot + 4 + 127) / 128 * 128;
+    static constexpr int kSmemUsed = kEpiStage + kEpiWarps * kStageWarpBytes;
+    static constexpr int kSmemAlloc = kSmemUsed + 1024;  // slack to align the ring to 1024 B
+    // Operand descriptors: A is K-major (8-row groups 1024 B apart); B is N-major
+    // with 64-column atoms 8 KB apart (one TMA box each) and 8-row K groups 1024 B
+    // apart. One K=16 step advances A by 32 B within the swizzled row and B by 16
+    // rows (2048 B).
+    static constexpr uint32_t kIdesc = idesc_f16_f32(kBM, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+    static_assert(kStagesN >= 4 && kStagesN <= 8, "ring depth");
+};
 
 template <bool kTma>
 struct Roles {
@@ -110,11 +119,11 @@ __device__ __forceinline__ void stage_A(uint8_t* sA, const __half* __restrict__ 
     }
 }
 
-// B tile: k0..k0+63, n0..n0+255; byte (k, n) = (n/64)*8192 + k*128 + (((n%64)/8) ^ (k%8))*16 + (n%8)*2.
-template <int VEC>
+// B tile: k0..k0+63, n0..n0+BN-1; byte (k, n) = (n/64)*8192 + k*128 + (((n%64)/8) ^ (k%8))*16 + (n%8)*2.
+template <int BN, int VEC>
 __device__ __forceinline__ void stage_B(uint8_t* sB, const __half* __restrict__ B, int N, int K,
                                         int n0, int k0, int ptid) {
-    constexpr int kUnitsPerRow = kBN / VEC;
+    constexpr int kUnitsPerRow = BN / VEC;
     constexpr int kPerThread = kBK * kUnitsPerRow / 128;
 #pragma unroll 8
     for (int i = 0; i < kPerThread; ++i) {
@@ -129,27 +138,30 @@ __device__ __forceinline__ void stage_B(uint8_t* sB, const __half* __restrict__ 
     }
 }
 
-template <bool kTma>
+template <bool kTma, int BN>
 __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
     tiled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const TiledArgs args) {
     using R = Roles<kTma>;
+    using G = Geom<BN>;
+    constexpr int kStageA = G::kStageA, kStageBytes = G::kStageBytes, kStagesN = G::kStagesN;
+    constexpr int kBN_ = BN;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    auto full_bar = [&](int s) { return sbase + kBarFull + 8 * s; };
-    auto empty_bar = [&](int s) { return sbase + kBarEmpty + 8 * s; };
-    auto acc_full_bar = [&](int b) { return sbase + kBarAccFull + 8 * b; };
-    auto acc_empty_bar = [&](int b) { return sbase + kBarAccEmpty + 8 * b; };
-    const uint32_t drain_bar = sbase + kBarDrain;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortSlot);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
+    auto full_bar = [&](int s) { return sbase + G::kBarFull + 8 * s; };
+    auto empty_bar = [&](int s) { return sbase + G::kBarEmpty + 8 * s; };
+    auto acc_full_bar = [&](int b) { return sbase + G::kBarAccFull + 8 * b; };
+    auto acc_empty_bar = [&](int b) { return sbase + G::kBarAccEmpty + 8 * b; };
+    const uint32_t drain_bar = sbase + G::kBarDrain;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::kAbortSlot);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kTmemSlot);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kStagesN; ++s) {
             mbar_init(full_bar(s), kTma ? 1 : R::kProducerWarps * 32);
             mbar_init(empty_bar(s), 1);
         }
@@ -166,7 +178,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == R::kMmaWarp) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_alloc(smem_u32(tmem_slot), G::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -196,17 +208,17 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                             mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
                             tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, mb * kBM);
 #pragma unroll
-                            for (int j = 0; j < kBN / 64; ++j)
-                                tma_load_2d(sB + j * kBoxB, &tmB, full_bar(stage), nb * kBN + j * 64, kb * kBK);
+                            for (int j = 0; j < kBN_ / 64; ++j)
+                                tma_load_2d(sB + j * kBoxB, &tmB, full_bar(stage), nb * kBN_ + j * 64, kb * kBK);
                             issued_mask |= 1u << stage;
                             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                         }
-                        if (++stage == kStages) { stage = 0; phase ^= 1; }
+                        if (++stage == kStagesN) { stage = 0; phase ^= 1; }
                     }
                     if (!ok) break;
                 }
                 // let every copy this thread started land before the CTA can exit
-                for (int s = 0; s < kStages; ++s)
+                for (int s = 0; s < kStagesN; ++s)
                     if (issued_mask & (1u << s)) wait_phase_drain(full_bar(s), (issued_parity >> s) & 1, wc);
             }
         } else {
@@ -221,16 +233,16 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                     if (!wait_phase(empty_bar(stage), phase ^ 1, wc, kSiteProducerEmpty)) { ok = false; break; }
                     uint8_t* sA = smem + stage * kStageBytes;
                     uint8_t* sB = sA + kStageA;
-                    const int m0 = mb * kBM, n0 = nb * kBN, k0 = kb * kBK;
+                    const int m0 = mb * kBM, n0 = nb * kBN_, k0 = kb * kBK;
                     if (args.a_vec == 8) stage_A<8>(sA, args.A, args.M, args.K, m0, k0, ptid);
                     else if (args.a_vec == 2) stage_A<2>(sA, args.A, args.M, args.K, m0, k0, ptid);
                     else stage_A<1>(sA, args.A, args.M, args.K, m0, k0, ptid);
-                    if (args.b_vec == 8) stage_B<8>(sB, args.B, args.N, args.K, n0, k0, ptid);
-                    else if (args.b_vec == 2) stage_B<2>(sB, args.B, args.N, args.K, n0, k0, ptid);
-                    else stage_B<1>(sB, args.B, args.N, args.K, n0, k0, ptid);
+                    if (args.b_vec == 8) stage_B<BN, 8>(sB, args.B, args.N, args.K, n0, k0, ptid);
+                    else if (args.b_vec == 2) stage_B<BN, 2>(sB, args.B, args.N, args.K, n0, k0, ptid);
+                    else stage_B<BN, 1>(sB, args.B, args.N, args.K, n0, k0, ptid);
                     fence_proxy_async_smem();      // this thread's ordinary stores, if any
                     cp_async_arrive(full_bar(stage));  // fires once its cp.async copies land
-                    if (++stage == kStages) { stage = 0; phase ^= 1; }
+                    if (++stage == kStagesN) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
             }
@@ -248,7 +260,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!wait_phase(acc_empty_bar(b), acc_phase ^ 1, wc, kSiteMmaAccEmpty)) break;
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + b * kBN;
+                const uint32_t d_tmem = tmem_base + b * kBN_;
                 for (int kb = 0; kb < args.num_kb; ++kb) {
                     if (!wait_phase(full_bar(stage), phase, wc, kSiteMmaFull)) { ok = false; break; }
                     tc_fence_after_sync();
@@ -262,9 +274,9 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k)
                         mma_f16(d_tmem, a_desc + (uint64_t)((k * 32) >> 4), b_desc + (uint64_t)((k * 2048) >> 4),
-                                kIdesc, (kb | k) != 0);
+                                G::kIdesc, (kb | k) != 0);
                     mma_commit(empty_bar(stage));  // frees the stage once these MMAs finish
-                    if (++stage == kStages) { stage = 0; phase ^= 1; }
+                    if (++stage == kStagesN) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
                 mma_commit(acc_full_bar(b));  // accumulator b is complete
@@ -279,7 +291,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
         const int half = (warp - R::kEpiWarp0) >> 2;  // which half of the 32-column chunks
         const int row_in_tile = quarter * 32 + lane;
-        uint8_t* stage = smem + kEpiStage + (warp - R::kEpiWarp0) * kStageWarpBytes;
+        uint8_t* stage = smem + G::kEpiStage + (warp - R::kEpiWarp0) * kStageWarpBytes;
         int it = 0;
         for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++it) {
             int mb, nb;
@@ -289,12 +301,12 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             if (!wait_phase(acc_full_bar(b), acc_phase, wc, kSiteEpilogueAccFull)) break;
             tc_fence_after_sync();
             const int row = mb * kBM + row_in_tile;
-            const int n0 = nb * kBN;
-            const int chunks = min(kBN / 32, (args.N - n0 + 31) / 32);
-            constexpr int kChunksPerWarp = (kBN / 32) / (kEpiWarps / 4);
+            const int n0 = nb * kBN_;
+            const int chunks = min(kBN_ / 32, (args.N - n0 + 31) / 32);
+            constexpr int kChunksPerWarp = (kBN_ / 32) / (kEpiWarps / 4);
             const int c_begin = half * kChunksPerWarp;
             const int c_end = min(c_begin + kChunksPerWarp, chunks);
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kBN;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kBN_;
             if (c_begin >= c_end) {  // no columns of this tile for this warp
                 tc_fence_before_sync();
                 mbar_arrive(acc_empty_bar(b));
@@ -318,40 +330,49 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
     __syncthreads();
     if (warp == R::kMmaWarp) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc(tmem_base, G::kTmemCols);
     }
 }
 
-template <bool kTma>
+template <bool kTma, int BN>
 cudaError_t launch(const TiledArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB, int grid,
                    cudaStream_t stream) {
     using R = Roles<kTma>;
+    constexpr int kSmem = Geom<BN>::kSmemAlloc;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_done[dev]) {
-        e = cudaFuncSetAttribute(tiled_gemm_kernel<kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+        e = cudaFuncSetAttribute(tiled_gemm_kernel<kTma, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
     CUtensorMap dummy{};
-    tiled_gemm_kernel<kTma><<<grid, R::kThreads, kSmemAlloc, stream>>>(tmA ? *tmA : dummy, tmB ? *tmB : dummy, a);
+    tiled_gemm_kernel<kTma, BN><<<grid, R::kThreads, kSmem, stream>>>(tmA ? *tmA : dummy, tmB ? *tmB : dummy, a);
     return cudaGetLastError();
+}
+
+template <bool kTma>
+cudaError_t launch_bn(const TiledArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB, int grid,
+                      cudaStream_t stream) {
+    if (a.bn == 64) return launch<kTma, 64>(a, tmA, tmB, grid, stream);
+    if (a.bn == 128) return launch<kTma, 128>(a, tmA, tmB, grid, stream);
+    return launch<kTma, 256>(a, tmA, tmB, grid, stream);
 }
 
 }  // namespace
 
-int tiled_smem_bytes(bool) { return kSmemAlloc; }
+int tiled_smem_bytes(bool) { return Geom<kBN>::kSmemAlloc; }
 int tiled_threads(bool tma) { return tma ? Roles<true>::kThreads : Roles<false>::kThreads; }
 
 cudaError_t launch_tiled_tma(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                              cudaStream_t stream) {
-    return launch<true>(a, &tmA, &tmB, grid, stream);
+    return launch_bn<true>(a, &tmA, &tmB, grid, stream);
 }
 
 cudaError_t launch_tiled_lsu(const TiledArgs& a, int grid, cudaStream_t stream) {
-    return launch<false>(a, nullptr, nullptr, grid, stream);
+    return launch_bn<false>(a, nullptr, nullptr, grid, stream);
 }
 
 }  // namespace tg

@@ -274,7 +274,11 @@ tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, 
     a.A = A; a.B = B; a.bias = bias; a.C = C;
     a.M = M; a.N = N; a.K = K; a.gelu = gelu;
     a.m_blocks = (M + kBM - 1) / kBM;
-    a.n_blocks = (N + kBN - 1) / kBN;
+    // narrower tiles (128, then 64 columns) while 256-wide ones would leave more than half
+    // of the SMs idle: small and ragged problems are latency-bound, more CTAs finish sooner
+    a.bn = kBN;
+    while (a.bn > 64 && static_cast<int64_t>(a.m_blocks) * ((N + a.bn - 1) / a.bn) < d.sm_count / 2) a.bn /= 2;
+    a.n_blocks = (N + a.bn - 1) / a.bn;
     a.num_tiles = a.m_blocks * a.n_blocks;
     a.num_kb = (K + kBK - 1) / kBK;
     a.group_m = group_rows(kBM, K, a.m_blocks);
@@ -304,6 +308,7 @@ tg_status run_tiled_pair(DeviceState& d, const __half* A, const __half* B, const
     a.A = A; a.B = B; a.bias = bias; a.C = C;
     a.M = M; a.N = N; a.K = K; a.gelu = gelu;
     a.m_blocks = (M + 2 * kBM - 1) / (2 * kBM);
+    a.bn = kBN;
     a.n_blocks = (N + kBN - 1) / kBN;
     a.num_tiles = a.m_blocks * a.n_blocks;
     a.num_kb = (K + kBK - 1) / kBK;

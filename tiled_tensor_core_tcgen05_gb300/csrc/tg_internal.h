@@ -88,6 +88,8 @@ struct TiledArgs {
     // wave run as two half-width units each; num_units = split_from +
     // 2 * (num_tiles - split_from). Set by the launcher.
     int split_from, num_units;
+    int bn;        // single-CTA kernel: tile width (256, or 128 / 64 when 256-wide tiles would
+                   // leave most SMs idle)
     Watchdog wd;
 };
 
