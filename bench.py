@@ -47,9 +47,33 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+# The sources each kernel is built from (its translation unit and the headers it
+# includes); recorded traffic stays valid while these files are unchanged.
+_COMMON_SOURCES = ("tg_ptx.cuh", "tg_device.cuh", "tg_internal.h")
+KERNEL_SOURCES = {
+    "tiled_pair_kernel": ("k_tiled2.cu",),
+    "tiled_gemm_kernel": ("k_tiled.cu",),
+    "splitk_gemm_kernel": ("k_splitk.cu", "tg_skinny.cuh"),
+    "w4_gemm_kernel": ("k_w4.cu",),
+    "attn_fwd_kernel": ("k_attn.cu",),
+    "softmax_rows": ("k_softmax.cu",),
+}
+
+
+def kernel_source_hash(kernel: str | None = None) -> str:
+    """Hash of the sources of `kernel` (a key of KERNEL_SOURCES or a name starting
+    with one), or of every source file when kernel is None or unknown."""
+    csrc = os.path.join(ROOT, "tiled_tensor_core_tcgen05_gb300", "csrc")
+    files = None
+    if kernel is not None:
+        for k, own in KERNEL_SOURCES.items():
+            if kernel.startswith(k):
+                files = [os.path.join(csrc, f) for f in own + _COMMON_SOURCES]
+                break
+    if files is None:
+        files = glob.glob(os.path.join(csrc, "*"))
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "tiled_tensor_core_tcgen05_gb300", "csrc", "*"))):
+    for f in sorted(files):
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode())
             h.update(fh.read())
@@ -65,7 +89,7 @@ def recorded_traffic(workload: str):
     with open(p) as fh:
         d = json.load(fh)
     e = d.get(workload)
-    if not e or e.get("kernel_hash") != kernel_source_hash():
+    if not e or e.get("kernel_hash") != kernel_source_hash(e.get("kernel")):
         return None
     return e.get("dram_bytes_per_launch")
 

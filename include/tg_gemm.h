@@ -188,7 +188,8 @@ tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const void* bias,
  *   bias, C, epilogue, stream: as for tg_gemm.
  *
  * Needs M <= 128, K % 128 == 0 and N % 8 == 0 (TG_ERR_INVALID_ARG
- * otherwise). M == 0 or N == 0 does nothing; K == 0 gives C = epi(bias).
+ * otherwise); M > 64 runs as row blocks of 64, each reading the weights once.
+ * M == 0 or N == 0 does nothing; K == 0 gives C = epi(bias).
  * split_k: 0 = automatic, else the number of K slices (1..64, at most
  * ceil(K / 256)); with more than one slice the library's per-stream scratch
  * holds fp32 partial sums, reduced in slice order (deterministic). The

@@ -74,12 +74,25 @@ def test_recorded_traffic_is_dropped_when_kernels_change(tmp_path, monkeypatch):
     rec = {"square_8192": {"dram_bytes_per_launch": 42, "kernel_hash": "not-the-current-hash"}}
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(b, "ROOT", str(tmp_path))
-    monkeypatch.setattr(b, "kernel_source_hash", lambda: "current")
+    monkeypatch.setattr(b, "kernel_source_hash", lambda kernel=None: "current")
     assert b.recorded_traffic("square_8192") is None
     rec["square_8192"]["kernel_hash"] = "current"
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     assert b.recorded_traffic("square_8192") == 42
     assert b.recorded_traffic("decode_16x28672x8192") is None
+
+
+def test_kernel_hash_follows_only_that_kernels_sources():
+    b = _bench()
+    assert set(b.KERNEL_SOURCES) >= {"tiled_pair_kernel", "tiled_gemm_kernel", "splitk_gemm_kernel",
+                                     "w4_gemm_kernel", "attn_fwd_kernel", "softmax_rows"}
+    csrc = os.path.join(b.ROOT, "tiled_tensor_core_tcgen05_gb300", "csrc")
+    for files in b.KERNEL_SOURCES.values():
+        for f in files + b._COMMON_SOURCES:
+            assert os.path.exists(os.path.join(csrc, f)), f
+    # a template instance name maps to its kernel's sources, and kernels differ
+    assert b.kernel_source_hash("softmax_rows_reg<32, 16>") == b.kernel_source_hash("softmax_rows")
+    assert b.kernel_source_hash("attn_fwd_kernel") != b.kernel_source_hash("softmax_rows")
 
 
 def test_reference_arm_prints_its_line(monkeypatch):
