@@ -361,10 +361,12 @@ def cpu_baseline(w, budget_s: float, metric_unit: str):
     import oracle
     A, B, bias = w.inputs()
     threads = oracle.max_threads()
+    # calibrate on one row per thread (the oracle spreads rows over its threads)
+    cal = max(1, min(w.M, threads))
     t0 = time.perf_counter()
-    oracle.gemm(A, B, bias, gelu=w.gelu, rows=(0, 1))
-    t1 = time.perf_counter() - t0
-    rows = max(1, min(w.M, int(budget_s / max(t1, 1e-4))))
+    oracle.gemm(A, B, bias, gelu=w.gelu, rows=(0, cal))
+    t_cal = time.perf_counter() - t0
+    rows = max(1, min(w.M, int(budget_s / max(t_cal, 1e-4)) * cal))
     t0 = time.perf_counter()
     oracle.gemm(A, B, bias, gelu=w.gelu, rows=(0, rows))
     dt = time.perf_counter() - t0
@@ -471,11 +473,13 @@ def run_reference(args):
     w = workloads.BY_NAME[args.workload]
     A, B, bias = w.inputs()
     threads = oracle.max_threads()
+    # calibrate on one row per thread (the oracle spreads rows over its threads)
+    cal = max(1, min(w.M, threads))
     t0 = time.perf_counter()
-    oracle.gemm(A, B, bias, gelu=w.gelu, rows=(0, 1))
-    t_row = time.perf_counter() - t0
+    oracle.gemm(A, B, bias, gelu=w.gelu, rows=(0, cal))
+    t_cal = time.perf_counter() - t0
     total_budget = args.ref_budget_s
-    rows = max(1, min(w.M, int(total_budget / max(1, args.steps + args.warmup) / max(t_row, 1e-4))))
+    rows = max(1, min(w.M, int(total_budget / max(1, args.steps + args.warmup) / max(t_cal, 1e-4)) * cal))
     for i in range(args.warmup):
         oracle.gemm(A, B, bias, gelu=w.gelu, rows=((i * rows) % w.M, min(rows, w.M - (i * rows) % w.M)))
     t0 = time.perf_counter()

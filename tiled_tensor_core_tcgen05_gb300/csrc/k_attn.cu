@@ -23,6 +23,12 @@
 //               (halves exchanged through shared memory), the exponentials,
 //               P_j (fp16 pairs) written over the scores just read; each half
 //               rescales and finally writes 64 of O's columns.
+// The softmax warps sit on the critical path of each key block (scores ->
+// P -> second product), and their time is instruction issue rather than the
+// exponential unit, so their arithmetic is kept lean: masking only in blocks
+// that reach past a row's last visible key, the maximum by three-input max,
+// scaling and sums in paired fp32 instructions, and one named barrier per
+// block (the maximum exchange, which also carries the abort vote).
 // The accumulator is only rescaled when a row's maximum grows by more than
 // 2^8 (in the base-2 domain); otherwise the old maximum stays the reference,
 // so the exponentials are at most 2^8 and the final O / sum is unchanged.
@@ -75,6 +81,12 @@ constexpr int kSmemAlloc = kSmemUsed + 1024;
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t* r) {
@@ -190,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 mma_commit(s_full);
                 mma_commit(k_empty);
                 // O += P_j V_j: P from TMEM (8 columns per 16 keys), V N-major (d contiguous)
-                if (!wait_phase_sleep(p_full, ph, wc, kSiteMmaFull, 20) || !wait_phase(v_full, ph, wc, kSiteMmaFull)) {
+                if (!wait_phase(p_full, ph, wc, kSiteMmaFull) || !wait_phase(v_full, ph, wc, kSiteMmaFull)) {
                     ok = false;
                     break;
                 }
@@ -230,13 +242,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         bool ok = true;
         for (int j = 0; j <= j_last; ++j) {
             const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+            // a wait that gave up still reads the scores (allocated columns: harmless values) and
+            // reaches the barrier of the maximum exchange, where every softmax warp learns of it and
+            // all stop together, so no named barrier ever waits for a thread that has left
             ok = wait_phase(s_full, ph, wc, kSiteEpilogueAccFull);
-            // every softmax warp stops together, so the named barriers below never wait for a
-            // thread that has left
-            if (named_barrier_or(1, kSoftmaxThreads, !ok)) {
-                ok = false;
-                break;
-            }
             tc_fence_after_sync();
             const int key0 = j * kBN + g * 64;
             const bool masked = key0 + 64 > limit;
@@ -244,17 +253,31 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             tmem_ld_32x32b_x32(lane_base + s_cols, r[0]);
             tmem_ld_32x32b_x32(lane_base + s_cols + 32, r[1]);
             tmem_ld_wait();
-            float mx = -INFINITY;
+            if (masked) {  // only blocks that reach past a row's last visible key
 #pragma unroll
-            for (int hc = 0; hc < 2; ++hc)
+                for (int hc = 0; hc < 2; ++hc)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    if (masked && key0 + hc * 32 + e >= limit) r[hc][e] = __float_as_uint(-INFINITY);
-                    mx = fmaxf(mx, __uint_as_float(r[hc][e]));
-                }
+                    for (int e = 0; e < 32; ++e)
+                        if (key0 + hc * 32 + e >= limit) r[hc][e] = __float_as_uint(-INFINITY);
+            }
+            auto score = [&](int i) { return __uint_as_float(r[i >> 5][i & 31]); };
+            // this half's maximum: four independent chains of three-input maxima
+            float acc[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[c] = score(c);
+#pragma unroll
+            for (int i = 4; i < 60; i += 8)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[c] = fmax3(acc[c], score(i + 2 * c), score(i + 2 * c + 1));
+            acc[0] = fmax3(acc[0], score(60), score(61));
+            acc[1] = fmax3(acc[1], score(62), score(63));
+            float mx = fmaxf(fmax3(acc[0], acc[1], acc[2]), acc[3]);
             // the row maximum over both halves
             red_max[(j & 1) * 256 + g * 128 + row] = mx;
-            named_barrier_sync(1, kSoftmaxThreads);
+            if (named_barrier_or(1, kSoftmaxThreads, !ok)) {
+                ok = false;
+                break;
+            }
             mx = fmaxf(mx, red_max[(j & 1) * 256 + (g ^ 1) * 128 + row]);
             const float m_tile = mx * scale;
             float alpha = 1.0f;
@@ -266,20 +289,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 m_run = m_tile;
                 rescale = true;
             }
-            // exponentials, this half's sum, P (fp16 pairs) over the scores just read
-            float sum = 0.0f;
+            // exponentials in pairs, this half's sum, P (fp16 pairs) over the scores just read
+            const float2 scale2 = make_float2(scale, scale);
+            const float2 neg_m2 = make_float2(-m_run, -m_run);
+            float2 sum2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
             for (int hc = 0; hc < 2; ++hc) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(r[hc][2 * e]), scale, -m_run));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(r[hc][2 * e + 1]), scale, -m_run));
-                    sum += p0 + p1;
-                    pk[e] = pack_half2(p0, p1);
+                    const float2 x2 = __ffma2_rn(make_float2(score(hc * 32 + 2 * e), score(hc * 32 + 2 * e + 1)),
+                                                 scale2, neg_m2);
+                    const float2 p2 = make_float2(ex2_approx(x2.x), ex2_approx(x2.y));
+                    sum2[e & 1] = __fadd2_rn(sum2[e & 1], p2);
+                    pk[e] = pack_half2(p2.x, p2.y);
                 }
                 tmem_st_32x32b_x16(lane_base + s_cols + hc * 16, pk);
             }
+            const float2 s2 = __fadd2_rn(sum2[0], sum2[1]);
+            const float sum = s2.x + s2.y;
             l_run = l_run * alpha + sum;
             // this half's O columns *= alpha (O already holds P_{j-1} V_{j-1}: S_j was issued after
             // it completed); both halves of a row take the same decision
