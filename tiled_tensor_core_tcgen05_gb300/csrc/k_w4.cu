@@ -102,24 +102,39 @@ __host__ __device__ inline Layout layout_for(int m_pad, int stages, int act_slot
 
 // One 32-bit word of packed weights (eight consecutive k of one column, byte
 // p holding k = 2p in its low and 2p + 1 in its high nibble) into four fp16
-// pairs, pair p = (w[2p], w[2p+1]) * scale, each product rounded once.
-// Byte p is copied under the exponent byte 0x64 in both halves; the masks keep
-// the low nibble in the low half and the high nibble (times 16) in the high
-// half, and the XOR with 8 maps the two's-complement value q to q + 8. The
-// halves then read 1024 + (q_lo + 8) and 1024 + 16 (q_hi + 8), which one fp16
-// fused multiply-add maps exactly to (q_lo, q_hi); the scale multiply is the
-// only rounding.
+// pairs (w[k] * scale, each product rounded once), in the order
+// (k0, k4), (k1, k5), (k2, k6), (k3, k7): the order in which masks that keep
+// one nibble of each 16-bit half deliver them. The activations' 16-byte
+// chunks are permuted the same way (permute_chunk), so the dot product over
+// k is unchanged.
+// A nibble masked under the exponent bits 0x64 and XORed with 8 (two's
+// complement q -> q + 8) reads 1024 + (q + 8) in the low nibble position and
+// 1024 + 16 (q + 8) in the high one; one fp16 fused multiply-add maps either
+// exactly to q, and the scale multiply is the only rounding.
 __device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, uint32_t* out) {
-    const __half2 mul = __halves2half2(__ushort_as_half(0x3C00), __ushort_as_half(0x2C00));  // (1, 1/16)
-    const __half2 add = __halves2half2(__ushort_as_half(0xE408), __ushort_as_half(0xD480));  // (-1032, -72)
+    const __half2 one = __halves2half2(__ushort_as_half(0x3C00), __ushort_as_half(0x3C00));        // 1
+    const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
+    const __half2 off_lo = __halves2half2(__ushort_as_half(0xE408), __ushort_as_half(0xE408));     // -1032
+    const __half2 off_hi = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));     // -72
+    const uint32_t w8 = w >> 8;
+    uint32_t x[4] = {(w & 0x000F000Fu) ^ 0x64086408u, (w & 0x00F000F0u) ^ 0x64806480u,
+                     (w8 & 0x000F000Fu) ^ 0x64086408u, (w8 & 0x00F000F0u) ^ 0x64806480u};
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        uint32_t x = __byte_perm(w, 0x64u, 0x4040u | (0x101u * p));
-        x = (x & 0xFFF0FF0Fu) ^ 0x00800008u;
-        __half2 h = *reinterpret_cast<__half2*>(&x);
-        h = __hmul2(__hfma2(h, mul, add), s2);
+        __half2 h = *reinterpret_cast<__half2*>(&x[p]);
+        h = __hmul2((p & 1) ? __hfma2(h, sixteenth, off_hi) : __hfma2(h, one, off_lo), s2);
         out[p] = *reinterpret_cast<uint32_t*>(&h);
     }
+}
+
+// In-place reorder of one 16-byte chunk of activations (eight consecutive k)
+// to the order dequant_word gives the weights: (a0, a4, a1, a5, a2, a6, a3, a7).
+__device__ __forceinline__ void permute_chunk(uint32_t addr) {
+    const uint4 v = lds_v4(addr);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(__byte_perm(v.x, v.z, 0x5410)),
+                 "r"(__byte_perm(v.x, v.z, 0x7632)), "r"(__byte_perm(v.y, v.w, 0x5410)),
+                 "r"(__byte_perm(v.y, v.w, 0x7632))
+                 : "memory");
 }
 
 __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -474,6 +489,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __half2 s_hi = __half2half2(__ushort_as_half(lds_u16(st + L.scale_off + 2 * (kW4BN + col))));
                 __syncwarp();
                 if (lane == 0) mbar_arrive(raw_empty(slot));
+                // this group's activation boxes of the stage, permuted like the weights; the MMA
+                // reads a box only after this group's bfull arrive for its sub-tile
+                {
+                    const int as = it % RA;
+                    ok = __all_sync(0xFFFFFFFFu, wait_phase_sleep(afull(as), static_cast<uint32_t>(it / RA) & 1u, wc,
+                                                                  kSiteConvFull, kConvSleepNs));
+                    if (!ok) break;
+                    const uint32_t sa = sbase + L.aring + as * L.act_bytes;
+                    const int chunks = args.m_pad * 8;  // 16-byte chunks per 64-k box
+#pragma unroll
+                    for (int jj = 0; jj < kSubsPerGroup; ++jj) {
+                        const uint32_t box = sa + (group + kConvGroups * jj) * args.m_pad * 128;
+                        for (int t = col; t < chunks; t += kW4BN) permute_chunk(box + 16 * t);
+                    }
+                }
                 // fully unrolled (no exit inside), so w[] stays in registers
 #pragma unroll
                 for (int jj = 0; jj < kSubsPerGroup; ++jj) {  // 64 k per sub-tile: this column's 128-byte row of B
