@@ -1,7 +1,8 @@
 """GPU parity of the attention forward (tg_attention_fwd), through the C ABI,
 against the fp64 CPU oracle on the same seeded (batch, sequence, head, dim)
 inputs: every element of the small workloads and of ragged lengths, sampled
-query rows (all heads, first and last positions) of the 4096-token ones.
+query rows (all heads, first and last positions) of the 4096-token ones and of
+shapes whose heads are scheduled in several groups.
 Tolerance per element: |gpu - ref| <= 1e-2 + 1e-2 |ref|."""
 import numpy as np
 import pytest
@@ -78,6 +79,23 @@ def test_full_size_sampled_rows(tg, w):
     pos = np.concatenate([[0, 1, 127, 128, w.S - 1], rng.integers(0, w.S, 27)])
     rows = np.array([(b * w.S + s) * w.H + h for b in range(w.B) for s in pos for h in range(w.H)])
     ref = oracle.attention(Q, K, V, causal=w.causal, rows=rows)
+    _check(got.reshape(-1, w.D)[rows], ref, w.name)
+    _status_ok(tg)
+
+
+# (batch, head) pairs whose keys and values exceed 64 MB run as several groups of heads
+# (the last one smaller): sampled rows of every head, first and last positions included
+GROUPED = [(1, 8192, 20, True), (3, 4096, 12, False)]
+
+
+@pytest.mark.parametrize("B,S,H,causal", GROUPED, ids=[f"{b}x{s}x{h}{'c' if c else ''}" for b, s, h, c in GROUPED])
+def test_head_groups_sampled_rows(tg, B, S, H, causal):
+    w = workloads.AttnWorkload(f"g_{B}x{S}x{H}", B, S, H, 128, seed=7 * B + H, causal=causal)
+    (Q, K, V), got = _run(tg, w)
+    rng = np.random.default_rng(w.seed)
+    pos = np.concatenate([[0, 127, 128, S - 1], rng.integers(0, S, 6)])
+    rows = np.array([(b * S + s) * H + h for b in range(B) for s in pos for h in range(H)])
+    ref = oracle.attention(Q, K, V, causal=causal, rows=rows)
     _check(got.reshape(-1, w.D)[rows], ref, w.name)
     _status_ok(tg)
 

@@ -55,6 +55,7 @@ constexpr int kCtasPerSm = 2;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0, kColP = 0, kColO = 128;
 constexpr float kRescaleLog2 = 8.0f;           // lazy rescale threshold (base-2 exponent)
+constexpr long long kL2Budget = 64LL << 20;     // K and V bytes of the heads in flight: half of L2
 static_assert(kD == 128, "head dimension 128");
 
 // shared memory: Q, K, V, then barriers (about 97 KB: two CTAs fit on an SM)
@@ -107,12 +108,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // block -> (query block, head, batch): all heads' last query block first, then the one
-    // before, ... so with the causal mask the longest CTAs start first (and the shortest
-    // fill the tail)
+    // block -> (query block, head, batch). The (batch, head) pairs are taken in groups whose K
+    // and V (4 S d bytes each) fit in kL2Budget, so the blocks in flight re-read keys and values
+    // from L2; within a group, every head's last query block first, then the one before, ...
+    // so with the causal mask the longest CTAs start first (and the shortest fill the tail),
+    // and the CTAs in flight spread over many heads rather than queueing on one head's blocks
     const int n_bh = static_cast<int>(gridDim.x) / args.n_qt;
-    const int qt = args.n_qt - 1 - static_cast<int>(blockIdx.x) / n_bh;
-    const int bh = static_cast<int>(blockIdx.x) % n_bh;
+    const long long kv_bytes = 4LL * args.S * kD;
+    const int gsz = static_cast<int>(max(1LL, min(static_cast<long long>(n_bh), kL2Budget / kv_bytes)));
+    const int per_group = gsz * args.n_qt;
+    const int grp = static_cast<int>(blockIdx.x) / per_group;
+    const int first = grp * gsz;
+    const int this_gsz = min(gsz, n_bh - first);
+    const int local = static_cast<int>(blockIdx.x) - grp * per_group;
+    const int qt = args.n_qt - 1 - local / this_gsz;
+    const int bh = first + local % this_gsz;
     const int h = bh % args.H;
     const int b = bh / args.H;
     const int n_kt = (args.S + kBN - 1) / kBN;
