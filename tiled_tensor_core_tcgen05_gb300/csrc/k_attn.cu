@@ -21,8 +21,10 @@
 //   warps 2-9   softmax, two threads per query row (its TMEM lane), each with
 //               half of the keys: read its 64 scores of S_j, the row maximum
 //               (halves exchanged through shared memory), the exponentials,
-//               P_j (fp16 pairs) written over the scores just read; each half
-//               rescales and finally writes 64 of O's columns.
+//               P_j (fp16 pairs) written over the scores just read and handed
+//               over 32 keys at a time, so the MMA thread starts O += P_j V_j
+//               on keys 0-31 and 64-95 while the rest are still exponentiated;
+//               each half rescales and finally writes 64 of O's columns.
 // The softmax warps sit on the critical path of each key block (scores ->
 // P -> second product), and their time is instruction issue rather than the
 // exponential unit, so their arithmetic is kept lean: masking only in blocks
@@ -69,8 +71,8 @@ constexpr int kBarKEmpty = kBarKFull + 8;
 constexpr int kBarVFull = kBarKEmpty + 8;
 constexpr int kBarVEmpty = kBarVFull + 8;
 constexpr int kBarSFull = kBarVEmpty + 8;
-constexpr int kBarPFull = kBarSFull + 8;
-constexpr int kBarODone = kBarPFull + 8;
+constexpr int kBarPFull = kBarSFull + 8;       // two: P of keys 0-31 and 64-95, then of the rest
+constexpr int kBarODone = kBarPFull + 16;
 constexpr int kBarDrain = kBarODone + 8;
 constexpr int kOffRedMax = kBarDrain + 8;                 // [2 (key-block parity)][2 halves][128 rows] floats
 constexpr int kOffRedSum = kOffRedMax + 2 * 2 * 128 * 4;  // [2 halves][128 rows] floats
@@ -130,7 +132,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     const uint32_t bar_q = sbase + kBarQ, k_full = sbase + kBarKFull, k_empty = sbase + kBarKEmpty;
     const uint32_t v_full = sbase + kBarVFull, v_empty = sbase + kBarVEmpty, s_full = sbase + kBarSFull;
-    const uint32_t p_full = sbase + kBarPFull, o_done = sbase + kBarODone, drain_bar = sbase + kBarDrain;
+    const uint32_t p_full0 = sbase + kBarPFull, p_full1 = sbase + kBarPFull + 8;
+    const uint32_t o_done = sbase + kBarODone, drain_bar = sbase + kBarDrain;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortSlot);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
 
@@ -141,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         mbar_init(v_full, 1);
         mbar_init(v_empty, 1);
         mbar_init(s_full, 1);
-        mbar_init(p_full, kSoftmaxWarps);  // one arrival per softmax warp
+        mbar_init(p_full0, kSoftmaxWarps);  // one arrival per softmax warp
+        mbar_init(p_full1, kSoftmaxWarps);
         mbar_init(o_done, 1);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -211,20 +215,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
                 mma_commit(s_full);
                 mma_commit(k_empty);
-                // O += P_j V_j: P from TMEM (8 columns per 16 keys), V N-major (d contiguous)
-                if (!wait_phase(p_full, ph, wc, kSiteMmaFull) || !wait_phase(v_full, ph, wc, kSiteMmaFull)) {
+                // O += P_j V_j: P from TMEM (8 columns per 16 keys), V N-major (d contiguous); the
+                // key steps whose P the softmax wrote first (keys 0-31 and 64-95) go first
+                if (!wait_phase(p_full0, ph, wc, kSiteMmaFull) || !wait_phase(v_full, ph, wc, kSiteMmaFull)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
+                auto pv_step = [&](int kk) {
                     const uint64_t bd = smem_desc_sw128(sbase + kOffV, kBoxBytes, 1024) +
                                         static_cast<uint64_t>((kk * 2048) >> 4);
                     // keys 64 g .. 64 g + 63 (softmax half g) are P columns 64 g .. 64 g + 31
                     const uint32_t a_col = kColP + (kk >> 2) * 64 + (kk & 3) * 8;
                     mma_f16_tmem_a(tmem_base + kColO, tmem_base + a_col, bd, idesc_o, (j != 0) || (kk != 0));
+                };
+                pv_step(0);
+                pv_step(1);
+                pv_step(4);
+                pv_step(5);
+                if (!wait_phase(p_full1, ph, wc, kSiteMmaFull)) {
+                    ok = false;
+                    break;
                 }
+                tc_fence_after_sync();
+                pv_step(2);
+                pv_step(3);
+                pv_step(6);
+                pv_step(7);
                 mma_commit(o_done);
                 mma_commit(v_empty);
             }
@@ -299,7 +316,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 m_run = m_tile;
                 rescale = true;
             }
-            // exponentials in pairs, this half's sum, P (fp16 pairs) over the scores just read
+            // exponentials in pairs, this half's sum, P (fp16 pairs) over the scores just read,
+            // handed to the MMA thread 32 keys at a time
             const float2 scale2 = make_float2(scale, scale);
             const float2 neg_m2 = make_float2(-m_run, -m_run);
             float2 sum2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
@@ -315,27 +333,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     pk[e] = pack_half2(p2.x, p2.y);
                 }
                 tmem_st_32x32b_x16(lane_base + s_cols + hc * 16, pk);
+                // this half's O columns *= alpha before the first hand-off: O holds
+                // P_{j-1} V_{j-1} (S_j was issued after it completed) and O += P_j V_j starts
+                // at the first hand-off; both halves of a row take the same decision
+                if (hc == 0 && j >= 1 && __any_sync(0xFFFFFFFFu, rescale)) {
+#pragma unroll 1
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t o[32];
+                        tmem_ld_32x32b_x32(lane_base + kColO + g * 64 + c * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st_32x32b_x32(lane_base + kColO + g * 64 + c * 32, o);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hc == 0 ? p_full0 : p_full1);
             }
             const float2 s2 = __fadd2_rn(sum2[0], sum2[1]);
             const float sum = s2.x + s2.y;
             l_run = l_run * alpha + sum;
-            // this half's O columns *= alpha (O already holds P_{j-1} V_{j-1}: S_j was issued after
-            // it completed); both halves of a row take the same decision
-            if (j >= 1 && __any_sync(0xFFFFFFFFu, rescale)) {
-#pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t o[32];
-                    tmem_ld_32x32b_x32(lane_base + kColO + g * 64 + c * 32, o);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st_32x32b_x32(lane_base + kColO + g * 64 + c * 32, o);
-                }
-            }
-            tmem_st_wait();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
         }
         // O / (sum of both halves), written as fp16 once the last O += P V has landed
         if (!named_barrier_or(1, kSoftmaxThreads, !ok)) {
