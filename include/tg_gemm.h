@@ -88,9 +88,15 @@ typedef enum {
  * tg_epilogue value. A, B may be NULL only when the product is empty.
  *
  * Kernel choice (TMA-compatible means K % 8 == 0, N % 8 == 0 and 16-byte
- * aligned A and B): not TMA-compatible -> TG_KERNEL_TILED_LSU; M <= 128 ->
- * TG_KERNEL_SPLITK; at least one 256x256 tile per pair of SMs ->
- * TG_KERNEL_TILED_PAIR; otherwise TG_KERNEL_TILED_TMA.
+ * aligned A and B): not TMA-compatible and (M <= 128 or 2 M N K < 2^32) ->
+ * TG_KERNEL_TILED_LSU; not TMA-compatible, M > 128 and 2 M N K >= 2^32 ->
+ * each operand TMA cannot describe is first
+ * copied (on `stream`) into a library-owned buffer with its row stride rounded
+ * up to 8 elements (one buffer per stream, grown as needed, freed by
+ * tg_shutdown; TG_ERR_NO_MEMORY if it cannot be allocated), then the TMA
+ * kernels below run on the copy; M <= 128 -> TG_KERNEL_SPLITK; at least one
+ * 256x256 tile per pair of SMs -> TG_KERNEL_TILED_PAIR; otherwise
+ * TG_KERNEL_TILED_TMA.
  */
 tg_status tg_gemm(const void* A, const void* B, const void* bias, void* C,
                   int64_t M, int64_t N, int64_t K, int epilogue, tg_stream_t stream);

@@ -77,6 +77,9 @@ EXACT_SHAPES = [
     # 2 x 43 = 86 tiles of 256 x 256: one wave of 76 CTA pairs plus 10 tiles that
     # the pair kernel runs as 20 half-width units (whole, ragged, and an empty half)
     (512, 11008, 64), (512, 10992, 72), (500, 10816, 64),
+    # neither K nor N a multiple of 8, at least 2^32 flops and enough tiles for CTA pairs: the
+    # automatic choice copies A and B to aligned strides and runs the pair kernel on the copies
+    (2048, 10990, 103),
 ]
 
 
@@ -139,9 +142,11 @@ def test_ragged_bias_gelu_full(tg):
     A, B, bias = w.inputs()
     ref = oracle.gemm(A, B, bias, gelu=True)
     dA, dB, dbias = _to_dev(A, B, bias)
-    C = tg.gemm(dA, dB, dbias, gelu=True)
-    _check_tol(C.cpu().float().numpy(), ref.astype(np.float64), w.name)
-    # the same problem with the operands at TMA-friendly strides goes through TMA
+    # N = 1030 gives B a stride TMA cannot describe: at this size the automatic choice is the
+    # ordinary-load kernel, reading B in place
+    for kernel in (tg.KERNEL_AUTO, tg.KERNEL_TILED_LSU):
+        C = tg.gemm(dA, dB, dbias, gelu=True, kernel=kernel)
+        _check_tol(C.cpu().float().numpy(), ref.astype(np.float64), f"{w.name} kernel {kernel}")
     _status_ok(tg)
 
 
@@ -239,6 +244,32 @@ def test_unaligned_pointers_take_the_load_path(tg):
         tg.gemm(dA, dB, db, gelu=True, out=dC, kernel=tg.KERNEL_TILED_TMA)
     tg.gemm(dA, dB, db, gelu=True, out=dC)
     _check_tol(dC.cpu().float().numpy(), ref, "unaligned")
+    _status_ok(tg)
+
+
+def test_unaligned_large_products_take_the_copy_path(tg):
+    # 2 M N K >= 2^32 with 2-byte-aligned A, B, bias and C (and odd strides): A and B are
+    # copied to aligned strides and the TMA kernels run on the copies; bias and C are used
+    # in place. Checked on sampled rows and columns of every tile.
+    for M, N, K in ((1536, 1400, 1008), (1040, 2050, 1031)):
+        w = workloads.custom(M, N, K, seed=78 + K, bias=workloads.Dist("uniform", -0.1, 0.1), gelu=True)
+        A, B, bias = w.inputs()
+        bufA = torch.zeros(M * K + 1, dtype=torch.float16, device="cuda")
+        bufB = torch.zeros(K * N + 1, dtype=torch.float16, device="cuda")
+        bufb = torch.zeros(N + 1, dtype=torch.float16, device="cuda")
+        bufC = torch.zeros(M * N + 1, dtype=torch.float16, device="cuda")
+        dA = bufA[1:].view(M, K); dA.copy_(A)
+        dB = bufB[1:].view(K, N); dB.copy_(B)
+        db = bufb[1:]; db.copy_(bias)
+        dC = bufC[1:].view(M, N)
+        tg.gemm(dA, dB, db, gelu=True, out=dC)
+        rows, cols = _tile_samples(M, N, 128, 128, 4, seed=M + N)
+        got = dC[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].cpu().float().numpy()
+        _check_tol(got, oracle.gemm_sampled(A, B, bias, True, rows, cols).astype(np.float64),
+                   f"unaligned {M}x{N}x{K}")
+        # the inputs are untouched and nothing is written outside C
+        assert torch.equal(dA.cpu(), A) and torch.equal(dB.cpu(), B)
+        assert bufC[0].item() == 0
     _status_ok(tg)
 
 

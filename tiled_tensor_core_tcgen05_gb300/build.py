@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtg_gemm.so")
-SOURCES = ["tg_api.cu", "k_tiled.cu", "k_tiled2.cu", "k_splitk.cu", "k_w4.cu", "k_attn.cu", "k_softmax.cu", "k_fill.cu", "k_epilogue.cu"]
+SOURCES = ["tg_api.cu", "k_tiled.cu", "k_tiled2.cu", "k_splitk.cu", "k_w4.cu", "k_attn.cu", "k_softmax.cu", "k_fill.cu", "k_epilogue.cu", "k_pad.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
           "--expt-relaxed-constexpr"]

@@ -42,6 +42,8 @@ struct Scratch {
     size_t ws_bytes = 0;
     unsigned int* counters = nullptr;
     size_t n_counters = 0;
+    __half* pad = nullptr;  // aligned-stride copies of operands TMA cannot describe
+    size_t pad_bytes = 0;
 };
 
 struct DeviceState {
@@ -131,11 +133,27 @@ tg_status make_map_bshd(CUtensorMap* m, const void* base, uint64_t B, uint64_t S
     return TG_OK;
 }
 
+// Row-major [outer][inner] fp16 matrix with a row stride of `ld` elements
+// (a multiple of 8), 128-byte-swizzled box.
+tg_status make_map_ld(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                      uint32_t box_inner, uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %llu x %llu matrix (row stride %llu)",
+                    (int)r, (unsigned long long)outer, (unsigned long long)inner, (unsigned long long)ld);
+    return TG_OK;
+}
+
 // Row-major [outer][inner] fp16 matrix, 128-byte-swizzled box.
 tg_status make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                    uint32_t box_outer) {
-    return make_map_ex(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, inner, outer, box_inner, box_outer,
-                       CU_TENSOR_MAP_SWIZZLE_128B);
+    return make_map_ld(m, base, inner, outer, inner, box_inner, box_outer);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -269,7 +287,7 @@ tg_status run_splitk(DeviceState& d, const __half* A, const __half* B, const __h
 }
 
 tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, const __half* bias, __half* C, int M,
-                    int N, int K, int gelu, cudaStream_t stream) {
+                    int N, int K, int gelu, cudaStream_t stream, int64_t lda = 0, int64_t ldb = 0) {
     TiledArgs a{};
     a.A = A; a.B = B; a.bias = bias; a.C = C;
     a.M = M; a.N = N; a.K = K; a.gelu = gelu;
@@ -291,9 +309,9 @@ tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, 
     cudaError_t e;
     if (tma) {
         CUtensorMap tmA, tmB;
-        tg_status st = make_map(&tmA, A, K, M, kBK, kBM);
+        tg_status st = make_map_ld(&tmA, A, K, M, lda ? lda : K, kBK, kBM);
         if (st != TG_OK) return st;
-        if ((st = make_map(&tmB, B, N, K, 64, kBK)) != TG_OK) return st;
+        if ((st = make_map_ld(&tmB, B, N, K, ldb ? ldb : N, 64, kBK)) != TG_OK) return st;
         e = launch_tiled_tma(a, tmA, tmB, grid, stream);
     } else {
         e = launch_tiled_lsu(a, grid, stream);
@@ -303,7 +321,7 @@ tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, 
 }
 
 tg_status run_tiled_pair(DeviceState& d, const __half* A, const __half* B, const __half* bias, __half* C, int M,
-                         int N, int K, int gelu, cudaStream_t stream) {
+                         int N, int K, int gelu, cudaStream_t stream, int64_t lda = 0, int64_t ldb = 0) {
     TiledArgs a{};
     a.A = A; a.B = B; a.bias = bias; a.C = C;
     a.M = M; a.N = N; a.K = K; a.gelu = gelu;
@@ -318,12 +336,64 @@ tg_status run_tiled_pair(DeviceState& d, const __half* A, const __half* B, const
     a.a_vec = a.b_vec = 8;
     a.wd = watchdog(d);
     CUtensorMap tmA, tmB;
-    tg_status st = make_map(&tmA, A, K, M, kBK, kBM);
+    tg_status st = make_map_ld(&tmA, A, K, M, lda ? lda : K, kBK, kBM);
     if (st != TG_OK) return st;
-    if ((st = make_map(&tmB, B, N, K, 64, kBK)) != TG_OK) return st;
+    if ((st = make_map_ld(&tmB, B, N, K, ldb ? ldb : N, 64, kBK)) != TG_OK) return st;
     cudaError_t e = launch_tiled_pair(a, tmA, tmB, d.sm_count / 2, stream);
     if (e != cudaSuccess) return cuda_fail(e, "pair tiled kernel launch");
     return TG_OK;
+}
+
+// Unaligned operands: products of at least this many flops take the aligned-copy path.
+constexpr double kCopyPathFlops = 4294967296.0;  // 2^32
+
+// True when the CTA-pair kernel has at least one wave of 256x256 tiles.
+bool pair_pays(const DeviceState& d, int64_t M, int64_t N) {
+    const int64_t pair_tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kBN - 1) / kBN);
+    return pair_tiles >= d.sm_count / 2;
+}
+
+// A GEMM whose A or B TMA cannot describe (row stride not a multiple of 16
+// bytes, or base not 16-byte aligned): each such operand is first copied into
+// the stream's aligned-stride buffer (row stride rounded up to 8 elements),
+// then the TMA kernels run on the copies with the original logical extents.
+tg_status run_padded(DeviceState& d, const __half* A, const __half* B, const __half* bias, __half* C, int M, int N,
+                     int K, int gelu, cudaStream_t stream) {
+    const bool pad_a = K % 8 != 0 || !aligned(A, 16);
+    const bool pad_b = N % 8 != 0 || !aligned(B, 16);
+    const int64_t lda = pad_a ? (static_cast<int64_t>(K) + 7) / 8 * 8 : K;
+    const int64_t ldb = pad_b ? (static_cast<int64_t>(N) + 7) / 8 * 8 : N;
+    const size_t a_bytes = pad_a ? static_cast<size_t>(M) * lda * 2 : 0;  // multiple of 16
+    const size_t b_bytes = pad_b ? static_cast<size_t>(K) * ldb * 2 : 0;
+    Scratch& s = d.scratch[stream];
+    if (s.pad_bytes < a_bytes + b_bytes) {
+        if (s.pad) cudaFree(s.pad);
+        s.pad = nullptr;
+        s.pad_bytes = 0;
+        cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&s.pad), a_bytes + b_bytes);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(TG_ERR_NO_MEMORY, "aligned operand copies of %zu bytes: %s", a_bytes + b_bytes,
+                        cudaGetErrorString(e));
+        }
+        s.pad_bytes = a_bytes + b_bytes;
+    }
+    const __half* a = A;
+    const __half* b = B;
+    cudaError_t e;
+    if (pad_a) {
+        if ((e = launch_pad_rows(A, s.pad, M, K, lda, d.sm_count, stream)) != cudaSuccess)
+            return cuda_fail(e, "copy of A to an aligned stride");
+        a = s.pad;
+    }
+    if (pad_b) {
+        __half* pb = s.pad + a_bytes / 2;
+        if ((e = launch_pad_rows(B, pb, K, N, ldb, d.sm_count, stream)) != cudaSuccess)
+            return cuda_fail(e, "copy of B to an aligned stride");
+        b = pb;
+    }
+    if (pair_pays(d, M, N)) return run_tiled_pair(d, a, b, bias, C, M, N, K, gelu, stream, lda, ldb);
+    return run_tiled(d, true, a, b, bias, C, M, N, K, gelu, stream, lda, ldb);
 }
 
 }  // namespace
@@ -380,14 +450,20 @@ tg_status tg_gemm_ex(const void* A, const void* B, const void* bias, void* C, in
     int k = kernel;
     if (k == TG_KERNEL_AUTO) {
         if (!tma_ok) {
+            // large problems: an aligned copy of the operand plus the TMA kernels beats
+            // staging it by 4- or 2-byte loads (4096 x 4094 x 4096: 3.6x); small ones are
+            // latency-bound and the copy's launch costs more than it saves (1000 x 1030 x 520:
+            // 19.3 vs 17.3 us); skinny M keeps the loads (a copy would double the weight
+            // traffic that bounds it)
+            if (M > kSkMaxM && 2.0 * M * N * K >= kCopyPathFlops)
+                return run_padded(d, a, b, bi, c, (int)M, (int)N, (int)K, gelu, stream);
             k = TG_KERNEL_TILED_LSU;
         } else if (M <= kSkMaxM) {
             k = TG_KERNEL_SPLITK;
         } else {
             // CTA pairs once there is at least one wave of 256x256 tiles for them;
             // smaller problems keep more, smaller 128x256 tiles on single CTAs
-            const int64_t pair_tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kBN - 1) / kBN);
-            k = pair_tiles >= d.sm_count / 2 ? TG_KERNEL_TILED_PAIR : TG_KERNEL_TILED_TMA;
+            k = pair_pays(d, M, N) ? TG_KERNEL_TILED_PAIR : TG_KERNEL_TILED_TMA;
         }
     }
     if (k == TG_KERNEL_SPLITK)
@@ -517,6 +593,7 @@ void tg_shutdown(void) {
         for (auto& kv : d.scratch) {
             if (kv.second.ws) cudaFree(kv.second.ws);
             if (kv.second.counters) cudaFree(kv.second.counters);
+            if (kv.second.pad) cudaFree(kv.second.pad);
         }
         d.scratch.clear();
     }

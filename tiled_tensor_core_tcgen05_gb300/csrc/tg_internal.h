@@ -158,6 +158,8 @@ cudaError_t launch_attn(const AttnArgs& a, const CUtensorMap& tmQ, const CUtenso
                         int grid, cudaStream_t stream);
 cudaError_t launch_bias_gelu(__half* C, const __half* bias, int64_t M, int64_t N, int gelu, bool vec8, int sm_count,
                              cudaStream_t stream);
+cudaError_t launch_pad_rows(const __half* src, __half* dst, int64_t rows, int64_t cols, int64_t dst_ld,
+                            int sm_count, cudaStream_t stream);
 cudaError_t launch_fill(const __half* bias, __half* C, int64_t M, int64_t N, int gelu,
                         int sm_count, cudaStream_t stream);
 
