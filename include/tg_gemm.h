@@ -147,9 +147,9 @@ tg_status tg_bias_gelu(void* C, const void* bias, int64_t M, int64_t N, int epil
  * nearly all device memory to its own pool allocator at start-up, where a
  * cudaMalloc from inside a library fails or fragments that pool; and a
  * latency-bound serving loop, where cudaMalloc/cudaFree would synchronise the
- * device and stall unrelated streams. The paper (the TileLang pages) has no
- * counterpart to this entry point: it changes only where the scratch memory
- * comes from, not what is computed.
+ * device and stall unrelated streams. The TileLang pages have no counterpart
+ * to this entry point: it changes only where the scratch memory comes from,
+ * not what is computed.
  *
  * Same arguments and result as tg_gemm_ex(..., TG_KERNEL_SPLITK, split_k, ...):
  * M <= 128, K % 8 == 0, N % 8 == 0, A and B 16-byte aligned; split_k 0 picks
