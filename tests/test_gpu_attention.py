@@ -84,8 +84,9 @@ def test_full_size_sampled_rows(tg, w):
 
 
 # (batch, head) pairs whose keys and values exceed 64 MB run as several groups of heads
-# (the last one smaller): sampled rows of every head, first and last positions included
-GROUPED = [(1, 8192, 20, True), (3, 4096, 12, False)]
+# (the last one smaller), and a 16384-position sequence: sampled rows of every head, first and
+# last positions included
+GROUPED = [(1, 8192, 20, True), (3, 4096, 12, False), (1, 16384, 2, True)]
 
 
 @pytest.mark.parametrize("B,S,H,causal", GROUPED, ids=[f"{b}x{s}x{h}{'c' if c else ''}" for b, s, h, c in GROUPED])

@@ -273,6 +273,20 @@ def test_unaligned_large_products_take_the_copy_path(tg):
     _status_ok(tg)
 
 
+def test_copy_path_pads_only_the_operand_that_needs_it(tg):
+    # K = 519: A's rows are not 16-byte multiples (A is copied), B (519 x 2048) is used in place;
+    # no bias, no GELU
+    M, N, K = 2048, 2048, 519
+    w = workloads.custom(M, N, K, seed=91)
+    A, B, _ = w.inputs()
+    dA, dB, _ = _to_dev(A, B, None)
+    C = tg.gemm(dA, dB)
+    rows, cols = _tile_samples(M, N, 128, 128, 2, seed=91)
+    got = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].cpu().float().numpy()
+    _check_tol(got, oracle.gemm_sampled(A, B, None, False, rows, cols).astype(np.float64), "pad A only")
+    _status_ok(tg)
+
+
 def test_repeatable_bit_for_bit(tg):
     for M, N, K, kernel in [(300, 520, 1000, 1), (16, 2048, 4096, 3), (70, 131, 67, 2)]:
         w = workloads.custom(M, N, K, seed=5, bias=workloads.Dist("uniform", -0.1, 0.1), gelu=True)
