@@ -287,6 +287,18 @@ def test_copy_path_pads_only_the_operand_that_needs_it(tg):
     _status_ok(tg)
 
 
+@pytest.mark.parametrize("M,N,K", [(3, 24, 1 << 22), (5, 7, (1 << 20) + 3)], ids=["splitk_K4M", "loads_K1M_odd"])
+def test_very_long_k(tg, M, N, K):
+    # K in the millions: the skinny path's K slices and the ordinary-load path's 64-bit offsets;
+    # inputs uniform[-1/4, 1/4] keep |C| moderate for the fp16 output
+    w = workloads.custom(M, N, K, seed=K % 1000, dist=workloads.Dist("uniform", -0.25, 0.25))
+    A, B, _ = w.inputs()
+    dA, dB, _ = _to_dev(A, B, None)
+    C = tg.gemm(dA, dB)
+    _check_tol(C.cpu().float().numpy(), oracle.gemm(A, B, None).astype(np.float64), f"{M}x{N}x{K}")
+    _status_ok(tg)
+
+
 def test_repeatable_bit_for_bit(tg):
     for M, N, K, kernel in [(300, 520, 1000, 1), (16, 2048, 4096, 3), (70, 131, 67, 2)]:
         w = workloads.custom(M, N, K, seed=5, bias=workloads.Dist("uniform", -0.1, 0.1), gelu=True)
