@@ -36,6 +36,10 @@ METRIC = "fp16 GEMM TFLOP/s & % of GB300 tensor peak; decode-GEMM HBM GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # fp16 and bf16 share the same dense tensor-core rate on this part (2.25 PFLOP/s nominal each)
 FP16_PER_BF16 = 1.0
+# the GB300's datasheet dense fp16 tensor rate (without sparsity), TFLOP/s
+SKU_FP16_DENSE_TFLOPS = 2250.0
+# nominal HBM3e bandwidth of the part, GB/s
+SKU_HBM_GBS = 8000.0
 
 
 def peaks():
@@ -99,7 +103,7 @@ class ClockSampler:
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -146,9 +150,24 @@ class ClockSampler:
         pw = [num(r[3]) for r in rows if num(r[3]) is not None]
         # "under load": samples drawing well above idle power
         loaded = [s for s, p in zip(sm, pw) if p is not None and pw and p > 0.5 * max(pw)] or sm
+        self.timed = []  # (host time of the sample, SM MHz)
+        for r in rows:
+            if len(r) >= 10 and num(r[1]) is not None:
+                t = _smi_time(r[9])
+                if t is not None:
+                    self.timed.append((t, num(r[1])))
         return {"sm_mhz": statistics.median(loaded) if loaded else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
-                "power_w_max": max(pw) if pw else None}
+                "samples_under_load": len(loaded), "power_w_max": max(pw) if pw else None}
+
+
+def _smi_time(text: str):
+    """nvidia-smi's timestamp ("2026/12/03 05:30:36.123", local time) as seconds since the epoch."""
+    import datetime
+    try:
+        return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+    except ValueError:
+        return None
 
 
 def dist_setup(n_gpus: int):
@@ -180,6 +199,8 @@ def barrier(pg):
 # ------------------------------------------------------------------ GPU arm
 
 KERNELS = {"auto": 0, "tiled": 1, "lsu": 2, "splitk": 3, "pair": 4}
+# one-thread oracle timings: the whole product (None) or its first rows
+ONE_THREAD_ROWS = {"square_256": None, "ragged_1000x1030x520_bias_gelu": None, "decode_16x28672x8192": 2}
 
 
 def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sampler=None, kernel: int = 0):
@@ -192,6 +213,8 @@ def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sam
     dC = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda") if hasattr(w, "M") else None
     if isinstance(w, workloads.SoftmaxWorkload):
         (X,) = w.inputs()
+        host_inputs = (X,)
+        dC = None
         dA = X.cuda()
         dB = ds = None
         db = torch.empty_like(dA)
@@ -202,6 +225,7 @@ def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sam
     elif isinstance(w, workloads.AttnWorkload):
         dC = None
         Q, K, V = w.inputs()
+        host_inputs = (Q, K, V)
         dA, dB, ds = Q.cuda(), K.cuda(), V.cuda()
         db = torch.empty_like(dA)
         args = (dA.data_ptr(), dB.data_ptr(), ds.data_ptr(), db.data_ptr(), w.B, w.S, w.H, w.D, bool(w.causal), sh)
@@ -210,6 +234,7 @@ def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sam
             tg.tg_attention_fwd(*args)
     elif isinstance(w, workloads.W4Workload):
         A, Bq, sc, bias = w.inputs()
+        host_inputs = (A, Bq, sc, bias)
         dA, dB, ds = A.cuda(), Bq.cuda(), sc.cuda()
         db = bias.cuda() if bias is not None else None
         args = (dA.data_ptr(), dB.data_ptr(), ds.data_ptr(), db.data_ptr() if db is not None else None,
@@ -219,6 +244,7 @@ def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sam
             tg.tg_gemm_w4(*args)
     else:
         A, B, bias = w.inputs()
+        host_inputs = (A, B, bias)
         dA, dB = A.cuda(), B.cuda()
         db = bias.cuda() if bias is not None else None
         args = (dA.data_ptr(), dB.data_ptr(), db.data_ptr() if db is not None else None, dC.data_ptr(),
@@ -262,9 +288,82 @@ def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sam
     st, where = tg.tg_device_status(None)
     if st != tg.OK:
         raise RuntimeError(f"watchdog status {st} (site {where}) during timing of {w.name}")
+    # the last timed launch's output, for the parity check against the oracle
+    out = (dC if dC is not None else db).cpu()
     del dA, dB, db, dC, flush
     return {"region_ms": max_over_ranks(pg, region_ms), "kernel_ms": max_over_ranks(pg, kernel_ms),
-            "launch_ms": launch_ms, "clocks": clocks}
+            "launch_ms": launch_ms, "clocks": clocks, "output": out, "inputs": host_inputs, "call": None}
+
+
+def time_sustained(tg, w, seconds: float, sampler, chunk: int = 50):
+    """Back-to-back launches of `w` for about `seconds`, in chunks of `chunk`
+    launches each timed with CUDA events between two host timestamps, while
+    nvidia-smi samples the SM clock. Each chunk gets the median clock of the
+    samples inside its host window; chunks are binned by that clock (50 MHz
+    bins), so the rate can be read against the clock the power limit allowed."""
+    import torch
+    A, B, bias = w.inputs()
+    dA, dB = A.cuda(), B.cuda()
+    db = bias.cuda() if bias is not None else None
+    dC = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
+    stream = torch.cuda.current_stream()
+    args = (dA.data_ptr(), dB.data_ptr(), db.data_ptr() if db is not None else None, dC.data_ptr(),
+            w.M, w.N, w.K, int(w.gelu), stream.cuda_stream)
+    for _ in range(10):
+        tg.tg_gemm(*args)
+    torch.cuda.synchronize()
+    sampler.start()
+    chunks = []
+    t_stop = time.time() + seconds
+    while time.time() < t_stop:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h0 = time.time()
+        e0.record(stream)
+        for _ in range(chunk):
+            tg.tg_gemm(*args)
+        e1.record(stream)
+        e1.synchronize()
+        chunks.append((h0, time.time(), e0.elapsed_time(e1)))
+    clocks = sampler.stop()
+    st, where = tg.tg_device_status(None)
+    if st != tg.OK:
+        raise RuntimeError(f"watchdog status {st} (site {where}) during the sustained run of {w.name}")
+    total_ms = sum(c[2] for c in chunks)
+    launches = chunk * len(chunks)
+    bins = {}
+    for h0, h1, ms in chunks:
+        mhz = [m for t, m in getattr(sampler, "timed", []) if h0 <= t <= h1]
+        if not mhz:
+            continue
+        b = int(round(statistics.median(mhz) / 50.0) * 50)
+        n, t = bins.get(b, (0, 0.0))
+        bins[b] = (n + 1, t + ms)
+    by_clock = [{"sm_mhz": b, "chunks": n, "TFLOP/s": round(w.flops() * chunk * n / (t / 1e3) / 1e12, 1)}
+                for b, (n, t) in sorted(bins.items())]
+    return {"seconds": round(total_ms / 1e3, 3), "launches": launches, "chunk": chunk,
+            "ms_per_launch": round(total_ms / launches, 5),
+            "TFLOP/s": round(w.flops() * launches / (total_ms / 1e3) / 1e12, 2),
+            "by_clock": by_clock, "clocks": clocks}
+
+
+def host_call_us(tg, w, calls: int = 200):
+    """Host time to enqueue one tg_gemm call (argument checks, kernel choice,
+    tensor maps, launch), averaged over `calls` back-to-back calls."""
+    import torch
+    A, B, bias = w.inputs()
+    dA, dB = A.cuda(), B.cuda()
+    db = bias.cuda() if bias is not None else None
+    dC = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
+    args = (dA.data_ptr(), dB.data_ptr(), db.data_ptr() if db is not None else None, dC.data_ptr(),
+            w.M, w.N, w.K, int(w.gelu), torch.cuda.current_stream().cuda_stream)
+    tg.tg_gemm(*args)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        tg.tg_gemm(*args)
+    dt = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    return round(dt / calls * 1e6, 2)
 
 
 def time_e2e(tg, w, steps: int, warmup: int, n_streams: int = 2):
@@ -351,33 +450,159 @@ def roofline_entry(w, avg_launch_ms, pk, pk_kind, bound, traffic=None):
         peak_note = f"hbm_gbs of {pk_kind}"
     e = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
          "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_note}
-    if bound == "tensor" and "bf16_tflops_sustained" in pk:
-        e["frac_of_sustained"] = round(achieved / (pk["bf16_tflops_sustained"] * FP16_PER_BF16), 4)
+    if bound == "tensor":
+        if "bf16_tflops_sustained" in pk:
+            e["frac_of_sustained"] = round(achieved / (pk["bf16_tflops_sustained"] * FP16_PER_BF16), 4)
+        e["frac_of_sku"] = round(achieved / SKU_FP16_DENSE_TFLOPS, 4)
+        e["sku_peak"] = SKU_FP16_DENSE_TFLOPS
+    else:
+        e["frac_of_sku"] = round(achieved / SKU_HBM_GBS, 4)
+        e["sku_peak"] = SKU_HBM_GBS
     return e
 
 
-def cpu_baseline(w, budget_s: float, metric_unit: str):
-    """The oracle as it stands, on the host cores, on whole rows of C."""
+def _oracle_unit(w, inputs, n: int, first: int = 0, threads: int = 0, rng=None):
+    """Run the oracle on `n` units of workload `w` (rows of C, or query rows for
+    attention) and return (flops, algorithmic bytes) of that sample."""
+    import numpy as np
+    import oracle
+    import workloads
+    if isinstance(w, workloads.Workload):
+        A, B, bias = inputs
+        oracle.gemm(A, B, bias, gelu=w.gelu, rows=(first, n), threads=threads)
+        return 2.0 * n * w.N * w.K, 2.0 * (n * w.K + w.K * w.N + n * w.N)
+    if isinstance(w, workloads.W4Workload):
+        A, Bq, sc, bias = inputs
+        oracle.gemm_w4(A, Bq, sc, bias, gelu=w.gelu, rows=(first, n), threads=threads)
+        groups = (w.K + w.group - 1) // w.group
+        return 2.0 * n * w.N * w.K, 2.0 * n * w.K + w.K * w.N / 2 + 2.0 * groups * w.N + 2.0 * n * w.N
+    if isinstance(w, workloads.AttnWorkload):
+        Q, K, V = inputs
+        rng = rng or np.random.default_rng(0)
+        rows = rng.integers(0, w.B * w.S * w.H, n)
+        oracle.attention(Q, K, V, causal=w.causal, rows=rows, threads=threads)
+        pos = (rows // w.H) % w.S
+        keys = (pos + 1).sum() if w.causal else n * w.S
+        return 4.0 * w.D * float(keys), 8.0 * w.D * n  # this query's q, o; its share of k, v
+    (X,) = inputs
+    oracle.softmax(X, rows=(first, n), threads=threads)
+    return 0.0, 4.0 * n * w.N
+
+
+def cpu_baseline(w, budget_s: float, metric_unit: str, inputs=None):
+    """The oracle as it stands, on all host cores, on a bounded sample of the
+    workload's units (whole rows of C, or query rows), about `budget_s` of work."""
+    import oracle
+    import workloads
+    if inputs is None:
+        inputs = w.inputs()
+    threads = oracle.max_threads()
+    total = w.B * w.S * w.H if isinstance(w, workloads.AttnWorkload) else w.M
+    # calibrate on one unit per thread (the oracle spreads units over its threads)
+    cal = max(1, min(total, threads))
+    t0 = time.perf_counter()
+    _oracle_unit(w, inputs, cal)
+    t_cal = time.perf_counter() - t0
+    n = max(1, min(total, int(budget_s / max(t_cal, 1e-4)) * cal))
+    t0 = time.perf_counter()
+    flops, nbytes = _oracle_unit(w, inputs, n)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9 if metric_unit == "GB/s" else flops / dt / 1e12
+    unit_name = "query rows" if isinstance(w, workloads.AttnWorkload) else "rows"
+    return {"value": value, "unit": metric_unit, "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {total} {unit_name} of {w.name} ({flops / 2:.3g} fp64 FMAs, {dt:.2f} s)"}
+
+
+PARITY_TOL = {"default": (1e-2, 1e-2), "softmax": (1e-6, 2e-3)}  # (abs, rel) per element
+
+
+def parity_check(w, inputs, out, n_samples: int = 4096, seed: int = 12345):
+    """The timed launch's output against the oracle, on sampled outputs the
+    oracle evaluates one by one from the definition (GEMMs: single elements;
+    4-bit GEMM, attention and softmax: whole rows). Returns the element count,
+    the largest absolute and relative errors and the number of elements outside
+    |gpu - ref| <= atol + rtol |ref|."""
+    import numpy as np
+    import oracle
+    import workloads
+    rng = np.random.default_rng(seed)
+    got_all = out.numpy()
+    if isinstance(w, workloads.Workload):
+        A, B, bias = inputs
+        if w.M * w.N <= n_samples:
+            rows, cols = np.divmod(np.arange(w.M * w.N), w.N)
+        else:
+            rows = np.concatenate([[0, w.M - 1, 0, w.M - 1], rng.integers(0, w.M, n_samples - 4)])
+            cols = np.concatenate([[0, 0, w.N - 1, w.N - 1], rng.integers(0, w.N, n_samples - 4)])
+        ref = oracle.gemm_sampled(A, B, bias, w.gelu, rows, cols)
+        got = got_all[rows, cols]
+        what = "sampled elements (first and last rows and columns included)"
+    elif isinstance(w, workloads.W4Workload):
+        A, Bq, sc, bias = inputs
+        picks = sorted({0, w.M - 1})
+        ref = np.concatenate([oracle.gemm_w4(A, Bq, sc, bias, gelu=w.gelu, rows=(r, 1)) for r in picks])
+        got = got_all[picks]
+        what = f"rows {picks} (every column)"
+    elif isinstance(w, workloads.AttnWorkload):
+        Q, K, V = inputs
+        pos = np.concatenate([[0, w.S - 1], rng.integers(0, w.S, 14)])
+        rows = np.array([(b * w.S + s) * w.H + h for b in range(w.B) for s in pos for h in (0, w.H - 1)])
+        ref = oracle.attention(Q, K, V, causal=w.causal, rows=rows)
+        got = got_all.reshape(-1, w.D)[rows]
+        what = f"{len(rows)} query rows (first and last positions, first and last heads)"
+    else:
+        (X,) = inputs
+        picks = sorted({0, w.M - 1, *rng.integers(0, w.M, 6).tolist()})
+        ref = np.concatenate([oracle.softmax(X, rows=(r, 1)) for r in picks])
+        got = got_all[picks]
+        what = f"{len(picks)} rows"
+    atol, rtol = PARITY_TOL["softmax" if isinstance(w, workloads.SoftmaxWorkload) else "default"]
+    got = np.asarray(got, dtype=np.float64).ravel()
+    ref = np.asarray(ref, dtype=np.float64).ravel()
+    err = np.abs(got - ref)
+    bad = ~(err <= atol + rtol * np.abs(ref))  # NaN counts as a violation
+    rel = err / np.maximum(np.abs(ref), 1e-30)
+    return {"checked": int(got.size), "what": what, "max_abs_err": float(np.nanmax(err)),
+            "max_rel_err": float(np.nanmax(rel)), "violations": int(bad.sum()),
+            "tolerance": f"|gpu - ref| <= {atol:g} + {rtol:g} |ref|", "oracle": "fp64 CPU oracle"}
+
+
+def host_cpu():
+    """Host CPU model and logical core count (for the oracle timings)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as fh:
+                for line in fh:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"model": model or "unknown", "logical_cpus": os.cpu_count()}
+
+
+def cpu_baseline_one_thread(w, row_budget: int | None = None):
+    """The oracle on one host thread: the whole product when `row_budget` is None,
+    else its first `row_budget` rows, with the time scaled to the whole product."""
     import oracle
     A, B, bias = w.inputs()
-    threads = oracle.max_threads()
-    # calibrate on one row per thread (the oracle spreads rows over its threads)
-    cal = max(1, min(w.M, threads))
+    rows = w.M if row_budget is None else max(1, min(w.M, row_budget))
     t0 = time.perf_counter()
-    oracle.gemm(A, B, bias, gelu=w.gelu, rows=(0, cal))
-    t_cal = time.perf_counter() - t0
-    rows = max(1, min(w.M, int(budget_s / max(t_cal, 1e-4)) * cal))
-    t0 = time.perf_counter()
-    oracle.gemm(A, B, bias, gelu=w.gelu, rows=(0, rows))
+    oracle.gemm(A, B, bias, gelu=w.gelu, rows=(0, rows), threads=1)
     dt = time.perf_counter() - t0
-    flops = 2.0 * rows * w.N * w.K
-    if metric_unit == "GB/s":
-        value = (2.0 * rows * w.K + 2.0 * w.K * w.N + 2.0 * rows * w.N) / dt / 1e9
-    else:
-        value = flops / dt / 1e12
-    return {"value": value, "unit": metric_unit, "cores": threads, "kind": "oracle",
-            "sample": f"rows 0..{rows - 1} of {w.M} of the {w.name} product ({rows * w.N * w.K:.3g} fp64 FMAs, "
-                      f"{dt:.2f} s)"}
+    full_s = dt * w.M / rows
+    return {"threads": 1, "seconds": round(dt, 4), "rows": f"0..{rows - 1} of {w.M}",
+            "seconds_whole_product": round(full_s, 4), "fp64_fmas": rows * w.N * w.K,
+            "GFLOP/s": round(2.0 * rows * w.N * w.K / dt / 1e9, 3)}
 
 
 def run_gpu(args):
@@ -418,6 +643,17 @@ def run_gpu(args):
     }
     out["roofline"] = roofline_entry(main, avg_launch, pk, pk_kind, main_bound, recorded_traffic(main.name))
     out["clocks"] = res["clocks"]
+    cpu_ok = rank == 0 and world == 1 and not args.no_cpu_baseline
+    if rank == 0:
+        out["parity"] = parity_check(main, res["inputs"], res["output"])
+    if cpu_ok:
+        out["host_cpu"] = host_cpu()
+    if rank == 0 and gemm_main and args.sustained_s > 0:
+        s = time_sustained(tg, main, args.sustained_s, ClockSampler(local))
+        s["frac_of_sustained_peak"] = round(s["TFLOP/s"] / (pk["bf16_tflops_sustained"] * FP16_PER_BF16), 4)
+        s["peak_source"] = f"bf16_tflops_sustained of {pk_kind}; fp16 dense rate = bf16 dense rate"
+        out["sustained"] = s
+        out["gpu_launches"] += s["launches"]
     # the rest of the suite, same rules, fewer steps
     extra = []
     if not args.only_main:
@@ -437,6 +673,14 @@ def run_gpu(args):
                  "roofline": roofline_entry(w, avg, pk, pk_kind, bound, recorded_traffic(w.name))}
             if hasattr(w, "flops"):
                 e["TFLOP/s"] = round(w.flops() / (avg / 1e3) / 1e12, 2)
+            if rank == 0:
+                e["parity"] = parity_check(w, r["inputs"], r["output"])
+            if cpu_ok:
+                e["cpu_baseline"] = cpu_baseline(w, args.cpu_budget_other_s, e["roofline"]["unit"], r["inputs"])
+                if w.name in ONE_THREAD_ROWS:
+                    e["cpu_one_thread"] = cpu_baseline_one_thread(w, ONE_THREAD_ROWS[w.name])
+            if rank == 0 and isinstance(w, workloads.Workload) and w.M <= 256:
+                e["host_us_per_call"] = host_call_us(tg, w)
             if getattr(w, "gelu", False) or getattr(w, "has_bias", False):
                 # unfused comparator, back to back (the fused figure above is per launch)
                 un_ms = time_unfused(tg, w, steps, max(3, args.warmup))
@@ -454,8 +698,9 @@ def run_gpu(args):
                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                           "ms_per_step": round(ms / e2e_steps, 4),
                           "api": "tg_gemm_staged, pinned host buffers, steps alternating over 2 streams"}
-            if world == 1 and not args.no_cpu_baseline:
-                out["cpu_baseline"] = cpu_baseline(main, args.cpu_budget_s, "TFLOP/s")
+            if cpu_ok:
+                out["cpu_baseline"] = cpu_baseline(main, args.cpu_budget_s, "TFLOP/s", res["inputs"])
+                out["cpu_baseline"]["cpu_model"] = out["host_cpu"]["model"]
         print(json.dumps(out), flush=True)
     if pg is not None:
         pg.destroy_process_group()
@@ -514,7 +759,10 @@ def main():
     ap.add_argument("--kernel", choices=sorted(KERNELS), default="auto",
                     help="pin the kernel of the headline workload (profiling); default: the library's choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--cpu-budget-s", type=float, default=10.0, help="oracle seconds for the headline workload")
+    ap.add_argument("--cpu-budget-other-s", type=float, default=2.0, help="oracle seconds for each other workload")
+    ap.add_argument("--sustained-s", type=float, default=2.0,
+                    help="seconds of back-to-back headline launches with binned clocks (0: skip)")
     ap.add_argument("--ref-budget-s", type=float, default=60.0)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -153,7 +153,9 @@ tg_status tg_bias_gelu(void* C, const void* bias, int64_t M, int64_t N, int epil
  *
  * Same arguments and result as tg_gemm_ex(..., TG_KERNEL_SPLITK, split_k, ...):
  * M <= 128, K % 8 == 0, N % 8 == 0, A and B 16-byte aligned; split_k 0 picks
- * the number of K slices automatically, 1..64 fixes it. The caller still
+ * the number of K slices automatically, never more than fit in the fixed
+ * array (one slice needs none, so an automatic call is never refused for
+ * size), 1..64 fixes it. The caller still
  * passes A, B, bias and C (device pointers it owns). With more than one K
  * slice, the partial sums and arrival counters live in one fixed array of
  * TG_NOALLOC_SCRATCH_BYTES compiled into the library's device image: every
@@ -281,7 +283,12 @@ int tg_version(void);
  */
 int64_t tg_ring_bytes(int kernel);
 
-/* Frees the library's per-device scratch buffers. Call with no work in flight. */
+/*
+ * Frees the library's per-device scratch buffers and forgets its per-device
+ * caches (tensor maps, device addresses of its own arrays, kernel attributes).
+ * Call with no work in flight. After a cudaDeviceReset, call tg_shutdown before
+ * the next library call: the caches would otherwise refer to the old context.
+ */
 void tg_shutdown(void);
 
 #ifdef __cplusplus

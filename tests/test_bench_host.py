@@ -117,3 +117,73 @@ def test_reference_arm_other_ranks_do_nothing(monkeypatch):
     with redirect_stdout(buf):
         b.run_reference(SimpleNamespace(workload="square_256", steps=1, warmup=1, ref_budget_s=0.1))
     assert buf.getvalue() == ""
+
+
+def test_roofline_entry_reports_the_sku_fractions():
+    b = _bench()
+    import workloads
+    pk = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0}
+    e = b.roofline_entry(workloads.SQUARE_8192, 0.55, pk, "measured", "tensor")
+    assert e["sku_peak"] == 2250.0 and e["frac_of_sku"] == pytest.approx(e["achieved"] / 2250.0, abs=1e-4)
+    e = b.roofline_entry(workloads.DECODE, 0.0785, pk, "measured", "hbm")
+    assert e["sku_peak"] == 8000.0 and e["frac_of_sku"] == pytest.approx(e["achieved"] / 8000.0, abs=1e-4)
+
+
+def _small_cases():
+    import workloads
+    return [workloads.custom(40, 72, 64, seed=3, bias=workloads.Dist("uniform", -0.1, 0.1), gelu=True),
+            workloads.W4Workload("w4_small", 3, 64, 256, seed=4),
+            workloads.AttnWorkload("attn_small", 1, 40, 2, 128, seed=5, causal=True),
+            workloads.SoftmaxWorkload("softmax_small", 5, 24, seed=6)]
+
+
+def _oracle_output(w, inputs):
+    import oracle
+    import workloads
+    if isinstance(w, workloads.Workload):
+        A, B, bias = inputs
+        return oracle.gemm(A, B, bias, gelu=w.gelu)
+    if isinstance(w, workloads.W4Workload):
+        return oracle.gemm_w4(*inputs, gelu=w.gelu)
+    if isinstance(w, workloads.AttnWorkload):
+        return oracle.attention(*inputs, causal=w.causal)
+    return oracle.softmax(*inputs)
+
+
+@pytest.mark.parametrize("k", range(4), ids=["gemm", "w4", "attention", "softmax"])
+def test_parity_check_passes_the_oracle_and_counts_a_planted_error(k):
+    b = _bench()
+    w = _small_cases()[k]
+    inputs = w.inputs()
+    out = torch.from_numpy(_oracle_output(w, inputs).copy())
+    p = b.parity_check(w, inputs, out, n_samples=64)
+    assert p["violations"] == 0 and p["max_abs_err"] == 0.0 and p["checked"] > 0
+    bad = out.clone().view(-1)
+    bad[:] = bad + 0.5  # every element off by 0.5: well outside the tolerance everywhere
+    p = b.parity_check(w, inputs, bad.view(out.shape), n_samples=64)
+    assert p["violations"] == p["checked"]
+
+
+@pytest.mark.parametrize("k", range(4), ids=["gemm", "w4", "attention", "softmax"])
+def test_cpu_baseline_leg_for_every_workload_kind(k):
+    b = _bench()
+    w = _small_cases()[k]
+    unit = "GB/s" if k in (1, 3) else "TFLOP/s"
+    e = b.cpu_baseline(w, 0.05, unit)
+    assert e["kind"] == "oracle" and e["unit"] == unit and e["value"] > 0 and e["cores"] >= 1
+
+
+def test_one_thread_oracle_timing_and_host_cpu():
+    b = _bench()
+    import workloads
+    e = b.cpu_baseline_one_thread(workloads.custom(32, 64, 48, seed=7), row_budget=8)
+    assert e["threads"] == 1 and e["rows"] == "0..7 of 32" and e["seconds_whole_product"] >= e["seconds"]
+    c = b.host_cpu()
+    assert c["logical_cpus"] >= 1 and isinstance(c["model"], str)
+
+
+def test_smi_timestamps_parse():
+    b = _bench()
+    t = b._smi_time("2026/12/03 05:30:36.250")
+    assert t is not None and abs((t % 1) - 0.25) < 1e-6
+    assert b._smi_time("not a time") is None

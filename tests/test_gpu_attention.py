@@ -114,3 +114,110 @@ def test_repeatable(tg):
     b = tg.attention(Q, K, V, causal=True).cpu()
     assert torch.equal(a, b)
     _status_ok(tg)
+
+
+# ---------------------------------------------------------------- the online-softmax rescale
+#
+# The kernel keeps a running maximum m per query row (in base-2 units, the scores times
+# log2(e) / sqrt(D)) and rescales the output accumulator and the running sum by 2^(m - m_new)
+# only when a key block's row maximum m_new exceeds m by more than 8; smaller rises leave m as
+# the reference, so the block's exponentials reach up to 2^8 before the fp16 rounding of P.
+# These inputs make the rises happen (keys that grow along the sequence, wide score
+# distributions, one huge score late in the sequence), including in the blocks whose keys are
+# partly masked (the causal diagonal block, a ragged last block). Before the GPU runs, each
+# case proves on the host, from fp64 scores, that the rule fires: the test then pins the
+# rescale branch, not only its inputs. (A masked block is always the last block of its row, so
+# a rescale after a masked block cannot occur; the rescale inside one can, and is counted.)
+
+def _rescale_events(Q, K, causal):
+    """(rescales, rescales inside a partly masked block, rises of at most 2^8) over all query
+    rows, following the kernel's rule on fp64 scores."""
+    q = Q.numpy().astype(np.float64)
+    k = K.numpy().astype(np.float64)
+    B, S, H, D = q.shape
+    s = np.einsum("bqhd,bkhd->bhqk", q, k) * (np.log2(np.e) / np.sqrt(D))
+    pos = np.arange(S)
+    if causal:
+        s = np.where(pos[None, None, None, :] <= pos[None, None, :, None], s, -np.inf)
+    n_kt = (S + 127) // 128
+    bm = np.stack([s[..., j * 128:min(S, (j + 1) * 128)].max(-1) for j in range(n_kt)], -1)
+    m = bm[..., 0].copy()
+    qblk = pos // 128
+    rescales = masked = small = 0
+    for j in range(1, n_kt):
+        seen = (qblk >= j)[None, None, :] if causal else np.ones((1, 1, S), bool)
+        part = (qblk == j)[None, None, :] if causal else np.full((1, 1, S), j == n_kt - 1 and S % 128 != 0)
+        rise = (bm[..., j] > m + 8) & seen
+        small += int(((bm[..., j] > m) & (bm[..., j] <= m + 8) & seen).sum())
+        rescales += int(rise.sum())
+        masked += int((rise & part).sum())
+        m = np.where(rise, bm[..., j], m)
+    return rescales, masked, small
+
+
+RESCALE = [  # (B, S, H, causal, k_ramp, sigma)
+    (1, 1000, 2, False, 1.5, 1.0),
+    (1, 1000, 2, True, 1.5, 1.0),
+    (2, 777, 1, True, 2.5, 1.0),
+    (1, 1000, 2, False, 0.0, 2.0),
+    (1, 1000, 2, True, 0.0, 2.0),
+    (1, 384, 3, False, 2.5, 1.0),
+]
+
+
+@pytest.mark.parametrize("B,S,H,causal,ramp,sigma", RESCALE,
+                         ids=[f"{b}x{s}x{h}{'c' if c else ''}_ramp{r}_sd{sd}" for b, s, h, c, r, sd in RESCALE])
+def test_rising_maxima_force_the_rescale(tg, B, S, H, causal, ramp, sigma):
+    w = workloads.AttnWorkload(f"r_{B}x{S}x{H}", B, S, H, 128, seed=900 + S + H + int(10 * ramp), causal=causal,
+                               dist=workloads.Dist("normal", 0.0, sigma), k_ramp=ramp)
+    Q, K, V = w.inputs()
+    rescales, masked, small = _rescale_events(Q, K, causal)
+    assert rescales >= 50, f"only {rescales} rescales: the inputs do not exercise the branch"
+    assert small >= 50, f"only {small} rises below the threshold"
+    if S % 128 != 0 or causal:
+        assert masked >= 5, f"only {masked} rescales inside a partly masked block"
+    (Q, K, V), got = _run(tg, w)
+    _check(got, oracle.attention(Q, K, V, causal=causal), w.name)
+    _status_ok(tg)
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["noncausal", "causal"])
+def test_huge_late_score_takes_over_the_row(tg, causal):
+    """Head 0: every query has 100 in dimension 0 and key 700 (block 5, followed by a ragged
+    block of 9 keys) has 100 there too, so its score is about 10^4 / sqrt(128) = 884 while
+    the others stay within a few tens: the rescale factor underflows to 0 and each query
+    that sees key 700 returns V[700]. Head 1 is left N(0, 1)."""
+    B, S, H, s_dom = 1, 777, 2, 700
+    w = workloads.AttnWorkload("dominant", B, S, H, 128, seed=960 + int(causal), causal=causal)
+    Q, K, V = w.inputs()
+    Q[:, :, 0, 0] = 100.0
+    K[:, s_dom, 0, 0] = 100.0
+    rescales, masked, _ = _rescale_events(Q, K, causal)
+    rows_seeing = S - s_dom if causal else S
+    assert rescales >= rows_seeing, f"{rescales} rescales for {rows_seeing} rows that see the huge score"
+    if causal:
+        assert masked >= S - s_dom  # key 700 sits in the diagonal block of queries 640..767
+    got = tg.attention(Q.cuda(), K.cuda(), V.cuda(), causal=causal).cpu().numpy()
+    ref = oracle.attention(Q, K, V, causal=causal)
+    _check(got, ref, "dominant key")
+    first = s_dom if causal else 0
+    np.testing.assert_allclose(got[0, first:, 0].astype(np.float64),
+                               np.broadcast_to(V.numpy()[0, s_dom, 0].astype(np.float64), (S - first, 128)),
+                               rtol=1e-3, atol=1e-3)
+    _status_ok(tg)
+
+
+def test_rescale_at_full_length_sampled_rows(tg):
+    """4096 positions, 8 heads, keys ramping slowly (every block rises a little, some by more
+    than 2^8): sampled rows of every head, first and last positions included."""
+    w = workloads.AttnWorkload("ramp_1x4096x8", 1, 4096, 8, 128, seed=970, causal=True, k_ramp=0.3)
+    Q, K, V = w.inputs()
+    rescales, masked, small = _rescale_events(Q[:, :, :2], K[:, :, :2], True)
+    assert rescales >= 50 and small >= 50
+    got = tg.attention(Q.cuda(), K.cuda(), V.cuda(), causal=True).cpu().numpy()
+    rng = np.random.default_rng(970)
+    pos = np.concatenate([[0, 127, 128, 129, 4095], rng.integers(0, 4096, 11)])
+    rows = np.array([s * w.H + h for s in pos for h in range(w.H)])
+    ref = oracle.attention(Q, K, V, causal=True, rows=rows)
+    _check(got.reshape(-1, w.D)[rows], ref, w.name)
+    _status_ok(tg)

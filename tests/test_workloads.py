@@ -94,3 +94,14 @@ def test_softmax_workloads():
     (X2,) = w.inputs()
     assert X.shape == (1000, 1030) and X.dtype == torch.float16 and torch.equal(X, X2)
     assert workloads.SOFTMAX_4096.bytes() == 4 * 32768 * 4096
+
+
+def test_key_ramp_scales_keys_by_position_and_leaves_q_v_alone():
+    plain = workloads.AttnWorkload("p", 1, 300, 2, 128, seed=77)
+    ramp = workloads.AttnWorkload("r", 1, 300, 2, 128, seed=77, k_ramp=2.0)
+    Qp, Kp, Vp = plain.inputs()
+    Qr, Kr, Vr = ramp.inputs()
+    assert torch.equal(Qp, Qr) and torch.equal(Vp, Vr)
+    scale = 1.0 + 2.0 * torch.arange(300, dtype=torch.float32) / 128.0
+    expect = (Kp.to(torch.float32) * scale.view(1, 300, 1, 1)).to(torch.float16)
+    assert torch.equal(Kr, expect)

@@ -397,14 +397,14 @@ int attn_smem_bytes() { return kSmemAlloc; }
 
 cudaError_t launch_attn(const AttnArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                         int grid, cudaStream_t stream) {
-    static bool attr_done[64] = {};
+    static int attr_gen[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !attr_done[dev]) {
+    if (dev < 64 && attr_gen[dev] != g_generation) {
         e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
         if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+        attr_gen[dev] = g_generation;
     }
     attn_fwd_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(tmQ, tmK, tmV, a);
     return cudaGetLastError();

@@ -202,14 +202,14 @@ int split_smem_bytes(int m_pad, int stages) { return layout_for(m_pad, stages).a
 
 cudaError_t launch_splitk(const SplitArgs& a, const CUtensorMap& tmB, const CUtensorMap& tmA, int grid,
                           cudaStream_t stream) {
-    static bool attr_done[64] = {};
+    static int attr_gen[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !attr_done[dev]) {
+    if (dev < 64 && attr_gen[dev] != g_generation) {
         e = cudaFuncSetAttribute(splitk_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+        attr_gen[dev] = g_generation;
     }
     const int smem = split_smem_bytes(a.m_pad, a.stages);
     splitk_gemm_kernel<<<grid, kThreads, smem, stream>>>(tmB, tmA, a);

@@ -339,14 +339,14 @@ cudaError_t launch(const TiledArgs& a, const CUtensorMap* tmA, const CUtensorMap
                    cudaStream_t stream) {
     using R = Roles<kTma>;
     constexpr int kSmem = Geom<BN>::kSmemAlloc;
-    static bool attr_done[64] = {};
+    static int attr_gen[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !attr_done[dev]) {
+    if (dev < 64 && attr_gen[dev] != g_generation) {
         e = cudaFuncSetAttribute(tiled_gemm_kernel<kTma, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+        attr_gen[dev] = g_generation;
     }
     CUtensorMap dummy{};
     tiled_gemm_kernel<kTma, BN><<<grid, R::kThreads, kSmem, stream>>>(tmA ? *tmA : dummy, tmB ? *tmB : dummy, a);

@@ -271,12 +271,12 @@ int tiled_pair_smem_bytes() { return kSmemAlloc; }
 
 cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, int max_clusters,
                               cudaStream_t stream) {
-    static bool attr_done[64] = {};
+    static int attr_gen[64] = {};
     static int active_clusters[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !attr_done[dev]) {
+    if (dev < 64 && attr_gen[dev] != g_generation) {
         e = cudaFuncSetAttribute(tiled_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
@@ -294,7 +294,7 @@ cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const 
         e = cudaOccupancyMaxActiveClusters(&n, tiled_pair_kernel, &cfg);
         if (e != cudaSuccess) return e;
         active_clusters[dev] = n > 0 ? n : 1;
-        attr_done[dev] = true;
+        attr_gen[dev] = g_generation;
     }
     int clusters = dev < 64 ? active_clusters[dev] : 1;
     if (clusters > max_clusters) clusters = max_clusters;

@@ -572,14 +572,14 @@ int w4_smem_bytes(int m_pad, int stages, int act_slots, int slots) {
 
 cudaError_t launch_w4(const W4Args& a, const CUtensorMap& tmBq, const CUtensorMap& tmA, const CUtensorMap& tmS,
                       int grid, cudaStream_t stream) {
-    static bool attr_done[64] = {};
+    static int attr_gen[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !attr_done[dev]) {
+    if (dev < 64 && attr_gen[dev] != g_generation) {
         e = cudaFuncSetAttribute(w4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+        attr_gen[dev] = g_generation;
     }
     w4_gemm_kernel<<<grid, kThreads, w4_smem_bytes(a.s.m_pad, a.s.stages, a.a_slots, a.b_slots), stream>>>(tmBq, tmA, tmS, a);
     return cudaGetLastError();

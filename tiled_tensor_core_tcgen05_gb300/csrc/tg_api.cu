@@ -12,6 +12,10 @@
 #include "tg_gemm.h"
 #include "tg_internal.h"
 
+namespace tg {
+int g_generation = 1;
+}
+
 namespace {
 
 using namespace tg;
@@ -62,6 +66,55 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
+// Encoded tensor maps by (device, element type, rank, base address, extents,
+// strides, box, swizzle). A map only describes an address range and its
+// layout, so a hit is valid even if the memory behind the address was freed
+// and allocated again; the cache saves the host cost of re-encoding on every
+// call (decode-sized calls are host-latency-bound). Bounded: cleared when it
+// reaches kMapCacheMax entries, and by tg_shutdown. Guarded by g_mu.
+struct MapKey {
+    uint64_t v[16];
+    bool operator==(const MapKey& o) const { return std::memcmp(v, o.v, sizeof v) == 0; }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        uint64_t h = 1469598103934665603ull;
+        for (uint64_t x : k.v) h = (h ^ x) * 1099511628211ull;
+        return static_cast<size_t>(h);
+    }
+};
+constexpr size_t kMapCacheMax = 4096;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+int g_map_dev = 0;  // device the current call runs on (set by current_device)
+
+CUresult encode_cached(CUtensorMap* m, CUtensorMapDataType dtype, uint32_t rank, const void* base,
+                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                       CUtensorMapSwizzle swizzle) {
+    MapKey k{};
+    k.v[0] = static_cast<uint64_t>(g_map_dev) | (static_cast<uint64_t>(dtype) << 16) |
+             (static_cast<uint64_t>(rank) << 32) | (static_cast<uint64_t>(swizzle) << 40);
+    k.v[1] = reinterpret_cast<uint64_t>(base);
+    for (uint32_t i = 0; i < rank; ++i) {
+        k.v[2 + i] = dims[i];
+        k.v[6 + i] = box[i];
+        if (i + 1 < rank) k.v[10 + i] = strides[i];
+    }
+    auto it = g_maps.find(k);
+    if (it != g_maps.end()) {
+        *m = it->second;
+        return CUDA_SUCCESS;
+    }
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, dtype, rank, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) {
+        if (g_maps.size() >= kMapCacheMax) g_maps.clear();
+        g_maps.emplace(k, *m);
+    }
+    return r;
+}
+
 // Current device, checked to be compute capability 10.3; fills the per-device
 // state on first use. Caller holds g_mu.
 tg_status current_device(int* dev_out) {
@@ -93,6 +146,7 @@ tg_status current_device(int* dev_out) {
         }
         d.ready = true;
     }
+    g_map_dev = dev;
     *dev_out = dev;
     return TG_OK;
 }
@@ -106,10 +160,7 @@ tg_status make_map_ex(CUtensorMap* m, CUtensorMapDataType dtype, uint32_t elem_b
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner * elem_bytes};
     cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(m, dtype, 2, base, dims, strides, box, swizzle);
     if (r != CUDA_SUCCESS)
         return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %llu x %llu matrix", (int)r,
                     (unsigned long long)outer, (unsigned long long)inner);
@@ -123,10 +174,8 @@ tg_status make_map_bshd(CUtensorMap* m, const void* base, uint64_t B, uint64_t S
     cuuint64_t dims[4] = {D, H, S, B};
     cuuint64_t strides[3] = {D * 2, H * D * 2, S * H * D * 2};
     cuuint32_t box[4] = {64, 1, 128, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, base, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS)
         return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %llu x %llu x %llu x %llu tensor", (int)r,
                     (unsigned long long)B, (unsigned long long)S, (unsigned long long)H, (unsigned long long)D);
@@ -140,10 +189,8 @@ tg_status make_map_ld(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {ld * 2};
     cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS)
         return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %llu x %llu matrix (row stride %llu)",
                     (int)r, (unsigned long long)outer, (unsigned long long)inner, (unsigned long long)ld);
@@ -250,9 +297,12 @@ tg_status ensure_scratch(DeviceState& d, cudaStream_t stream, size_t ws_bytes, s
     return TG_OK;
 }
 
-tg_status run_splitk(DeviceState& d, const __half* A, const __half* B, const __half* bias, __half* C, int M, int N,
-                     int K, int gelu, int split_k, cudaStream_t stream) {
-    SplitArgs a{};
+// The skinny kernel's arguments for one call, all but its scratch pointers.
+// split_k > 0 fixes the number of K slices; 0 takes the cost model's choice,
+// capped at max_splits (at least 1).
+void splitk_args(const DeviceState& d, const __half* A, const __half* B, const __half* bias, __half* C, int M, int N,
+                 int K, int gelu, int split_k, int max_splits, SplitArgs& a) {
+    a = SplitArgs{};
     a.A = A; a.B = B; a.bias = bias; a.C = C;
     a.M = M; a.N = N; a.K = K; a.gelu = gelu;
     a.m_pad = (M + 15) / 16 * 16;
@@ -262,12 +312,35 @@ tg_status run_splitk(DeviceState& d, const __half* A, const __half* B, const __h
     a.stages = split_stages_for(a.m_pad);
     a.n_tiles = (N + kSkBN - 1) / kSkBN;
     a.kb_total = (K + kSkBK - 1) / kSkBK;
-    int s = split_k > 0 ? split_k : choose_splits(a.n_tiles, a.kb_total, d.sm_count);
+    int s = split_k;
+    if (s <= 0) {
+        s = choose_splits(a.n_tiles, a.kb_total, d.sm_count);
+        if (s > max_splits) s = max_splits;
+    }
     if (s > a.kb_total) s = a.kb_total;
+    if (s < 1) s = 1;
     a.kb_per_split = (a.kb_total + s - 1) / s;
     a.splits = (a.kb_total + a.kb_per_split - 1) / a.kb_per_split;
     a.num_units = a.n_tiles * a.splits;
     a.wd = watchdog(d);
+}
+
+// Tensor maps and launch of the skinny kernel, its scratch already in `a`.
+tg_status splitk_launch(const DeviceState& d, const SplitArgs& a, cudaStream_t stream) {
+    CUtensorMap tmB, tmA;
+    tg_status st = make_map(&tmB, a.B, a.N, a.K, 64, kSkBK);
+    if (st != TG_OK) return st;
+    if ((st = make_map(&tmA, a.A, a.K, a.M, kSkBK, a.m_pad)) != TG_OK) return st;
+    const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
+    cudaError_t e = launch_splitk(a, tmB, tmA, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "split-K kernel launch");
+    return TG_OK;
+}
+
+tg_status run_splitk(DeviceState& d, const __half* A, const __half* B, const __half* bias, __half* C, int M, int N,
+                     int K, int gelu, int split_k, cudaStream_t stream) {
+    SplitArgs a;
+    splitk_args(d, A, B, bias, C, M, N, K, gelu, split_k, kSkMaxSplits, a);
     if (a.splits > 1) {
         Scratch* sc = nullptr;
         tg_status st = ensure_scratch(d, stream, static_cast<size_t>(a.splits) * N * a.m_pad * sizeof(float),
@@ -276,14 +349,7 @@ tg_status run_splitk(DeviceState& d, const __half* A, const __half* B, const __h
         a.ws = sc->ws;
         a.counters = sc->counters;
     }
-    CUtensorMap tmB, tmA;
-    tg_status st = make_map(&tmB, B, N, K, 64, kSkBK);
-    if (st != TG_OK) return st;
-    if ((st = make_map(&tmA, A, K, M, kSkBK, a.m_pad)) != TG_OK) return st;
-    const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
-    cudaError_t e = launch_splitk(a, tmB, tmA, grid, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "split-K kernel launch");
-    return TG_OK;
+    return splitk_launch(d, a, stream);
 }
 
 tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, const __half* bias, __half* C, int M,
@@ -395,6 +461,19 @@ tg_status run_padded(DeviceState& d, const __half* A, const __half* B, const __h
     if (pair_pays(d, M, N)) return run_tiled_pair(d, a, b, bias, C, M, N, K, gelu, stream, lda, ldb);
     return run_tiled(d, true, a, b, bias, C, M, N, K, gelu, stream, lda, ldb);
 }
+
+// ---------------------------------------------------------------------------
+// tg_gemm_splitk_noalloc: the skinny split-K path with its scratch in a fixed
+// array of the library's own device image instead of library-allocated memory.
+
+// Layout: one arrival counter per 256-column slice of N (padded to 256 bytes),
+// then the fp32 partial sums [split][N][M rounded up to 16]. Loaded with the library's device
+// code, so every device that loads the library holds these bytes until exit.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TG_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch for each device, looked up on the first
+// call on that device (with that device current).
+unsigned char* g_noalloc_ptr[kMaxDevices] = {};
 
 }  // namespace
 
@@ -596,27 +675,16 @@ void tg_shutdown(void) {
             if (kv.second.pad) cudaFree(kv.second.pad);
         }
         d.scratch.clear();
+        d.ready = false;  // the status word's address is looked up again
     }
+    // device addresses and per-context kernel attributes are looked up again on the
+    // next call, so the library keeps working after a cudaDeviceReset that follows this
+    for (auto& p : g_noalloc_ptr) p = nullptr;
+    g_maps.clear();
+    ++g_generation;
 }
 
 }  // extern "C"
-
-// ---------------------------------------------------------------------------
-// tg_gemm_splitk_noalloc: the skinny split-K path with its scratch in a fixed
-// array of the library's own device image instead of library-allocated memory.
-
-namespace {
-
-// Layout: one arrival counter per 256-column slice of N (padded to 256 bytes),
-// then the fp32 partial sums [split][N][M rounded up to 16]. Loaded with the library's device
-// code, so every device that loads the library holds these bytes until exit.
-static __device__ __align__(256) unsigned char g_noalloc_scratch[TG_NOALLOC_SCRATCH_BYTES];
-
-// Device address of g_noalloc_scratch for each device, looked up on the first
-// call on that device (with that device current).
-unsigned char* g_noalloc_ptr[kMaxDevices] = {};
-
-}  // namespace
 
 extern "C" tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const void* bias, void* C, int64_t M,
                                             int64_t N, int64_t K, int epilogue, int split_k, tg_stream_t stream_) {
@@ -659,32 +727,25 @@ extern "C" tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const 
         g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
     }
 
-    SplitArgs a{};
-    a.A = static_cast<const __half*>(A);
-    a.B = static_cast<const __half*>(B);
-    a.bias = static_cast<const __half*>(bias);
-    a.C = static_cast<__half*>(C);
-    a.M = (int)M; a.N = (int)N; a.K = (int)K; a.gelu = gelu;
-    a.m_pad = (a.M + 15) / 16 * 16;
-    a.tmem_stride = 16;
-    while (a.tmem_stride < a.m_pad) a.tmem_stride *= 2;
-    a.tmem_cols = 2 * kSkHalves * a.tmem_stride < 32 ? 32 : 2 * kSkHalves * a.tmem_stride;
-    a.stages = split_stages_for(a.m_pad);
-    a.n_tiles = (a.N + kSkBN - 1) / kSkBN;
-    a.kb_total = (a.K + kSkBK - 1) / kSkBK;
-    int s = split_k > 0 ? split_k : choose_splits(a.n_tiles, a.kb_total, d.sm_count);
-    if (s > a.kb_total) s = a.kb_total;
-    a.kb_per_split = (a.kb_total + s - 1) / s;
-    a.splits = (a.kb_total + a.kb_per_split - 1) / a.kb_per_split;
-    a.num_units = a.n_tiles * a.splits;
-    a.wd = watchdog(d);
+    // the most K slices whose partials fit in the array beside the counters (one slice needs
+    // no scratch, so the automatic choice always fits)
+    const int m_pad = (static_cast<int>(M) + 15) / 16 * 16;
+    const int n_tiles = static_cast<int>((N + kSkBN - 1) / kSkBN);
+    const size_t counter_bytes = (static_cast<size_t>(n_tiles) * sizeof(unsigned int) + 255) / 256 * 256;
+    const size_t per_split = static_cast<size_t>(N) * m_pad * sizeof(float);
+    const size_t room = TG_NOALLOC_SCRATCH_BYTES > counter_bytes ? TG_NOALLOC_SCRATCH_BYTES - counter_bytes : 0;
+    const int fit = static_cast<int>(room / per_split < static_cast<size_t>(kSkMaxSplits) ? room / per_split
+                                                                                          : kSkMaxSplits);
+    SplitArgs a;
+    splitk_args(d, static_cast<const __half*>(A), static_cast<const __half*>(B), static_cast<const __half*>(bias),
+                static_cast<__half*>(C), static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), gelu, split_k,
+                fit < 1 ? 1 : fit, a);
     if (a.splits > 1) {
-        const size_t counter_bytes = (static_cast<size_t>(a.n_tiles) * sizeof(unsigned int) + 255) / 256 * 256;
-        const size_t partial_bytes = static_cast<size_t>(a.splits) * a.N * a.m_pad * sizeof(float);
+        const size_t partial_bytes = static_cast<size_t>(a.splits) * per_split;
         if (counter_bytes + partial_bytes > static_cast<size_t>(TG_NOALLOC_SCRATCH_BYTES))
             return fail(TG_ERR_INVALID_ARG,
                         "tg_gemm_splitk_noalloc: %d K slices of a %lld x %lld product need %zu bytes of scratch, "
-                        "more than the %zu-byte static scratch (use fewer slices or tg_gemm)",
+                        "more than the %zu-byte static scratch (use fewer slices, 0 for automatic, or tg_gemm)",
                         a.splits, (long long)M, (long long)N, counter_bytes + partial_bytes,
                         static_cast<size_t>(TG_NOALLOC_SCRATCH_BYTES));
         // the arrival counters must start at zero; the partials are written before they are read
@@ -693,13 +754,7 @@ extern "C" tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const 
         a.counters = reinterpret_cast<unsigned int*>(g_noalloc_ptr[dev]);
         a.ws = reinterpret_cast<float*>(g_noalloc_ptr[dev] + counter_bytes);
     }
-    CUtensorMap tmB, tmA;
-    if ((st = make_map(&tmB, B, N, K, 64, kSkBK)) != TG_OK) return st;
-    if ((st = make_map(&tmA, A, K, M, kSkBK, a.m_pad)) != TG_OK) return st;
-    const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
-    cudaError_t e = launch_splitk(a, tmB, tmA, grid, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "split-K kernel launch");
-    return TG_OK;
+    return splitk_launch(d, a, stream);
 }
 
 // ---------------------------------------------------------------------------

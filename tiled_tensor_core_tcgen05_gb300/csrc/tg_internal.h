@@ -134,6 +134,13 @@ struct AttnArgs {
     Watchdog wd;
 };
 
+// Incremented by tg_shutdown. Launchers cache per-device, per-context state
+// (kernel attributes such as the dynamic shared-memory limit) together with
+// the generation they were made in, and make them again when it has changed,
+// so the library keeps working after tg_shutdown and a cudaDeviceReset.
+// Read and written with the front end's lock held.
+extern int g_generation;
+
 int split_stage_bytes(int m_pad);
 int split_smem_bytes(int m_pad, int stages);
 int split_stages_for(int m_pad);

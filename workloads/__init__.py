@@ -186,7 +186,13 @@ class AttnWorkload:
     """Attention forward O = softmax(Q K^T / sqrt(D)) V (optionally causal) on
     (batch, sequence, head, dim) fp16 tensors, the layout of the bshd example
     in the pages. Q, K, V are drawn in that order from one CPU torch.Generator
-    seeded with `seed`, each normal(0, 1) then rounded to fp16."""
+    seeded with `seed`, each normal(0, 1) then rounded to fp16.
+
+    ``k_ramp`` > 0 draws keys whose scale grows along the sequence: the drawn
+    fp16 key at position s is multiplied by (1 + k_ramp * s / 128) in float32
+    and rounded to fp16 again, so later blocks of 128 keys score higher than
+    earlier ones (inputs that make a running row maximum rise from block to
+    block)."""
     name: str
     B: int
     S: int
@@ -195,6 +201,7 @@ class AttnWorkload:
     seed: int
     causal: bool = False
     dist: Dist = Dist("normal", 0.0, 1.0)
+    k_ramp: float = 0.0
 
     def describe(self) -> str:
         return (f"{self.name}: batch={self.B} seq={self.S} heads={self.H} dim={self.D} "
@@ -204,7 +211,14 @@ class AttnWorkload:
         g = torch.Generator(device="cpu")
         g.manual_seed(self.seed)
         shape = (self.B, self.S, self.H, self.D)
-        out = [self.dist.draw(shape, g) for _ in range(3)]
+        if self.k_ramp:
+            q = self.dist.draw(shape, g)
+            k = self.dist.draw(shape, g).to(torch.float32)
+            ramp = 1.0 + self.k_ramp * torch.arange(self.S, dtype=torch.float32) / 128.0
+            k = (k * ramp.view(1, self.S, 1, 1)).to(torch.float16)
+            out = [q, k, self.dist.draw(shape, g)]
+        else:
+            out = [self.dist.draw(shape, g) for _ in range(3)]
         if device != "cpu":
             out = [t.to(device) for t in out]
         return tuple(out)
