@@ -461,6 +461,19 @@ def roofline_entry(w, avg_launch_ms, pk, pk_kind, bound, traffic=None):
     return e
 
 
+_ALL_THREADS = []
+
+
+def oracle_threads() -> int:
+    """Threads of the oracle's parallel regions on this host: taken once, before
+    any one-thread timing (the oracle's thread setting persists in the process),
+    and passed explicitly to every all-core call."""
+    if not _ALL_THREADS:
+        import oracle
+        _ALL_THREADS.append(max(1, oracle.max_threads()))
+    return _ALL_THREADS[0]
+
+
 def _oracle_unit(w, inputs, n: int, first: int = 0, threads: int = 0, rng=None):
     """Run the oracle on `n` units of workload `w` (rows of C, or query rows for
     attention) and return (flops, algorithmic bytes) of that sample."""
@@ -496,16 +509,16 @@ def cpu_baseline(w, budget_s: float, metric_unit: str, inputs=None):
     import workloads
     if inputs is None:
         inputs = w.inputs()
-    threads = oracle.max_threads()
+    threads = oracle_threads()
     total = w.B * w.S * w.H if isinstance(w, workloads.AttnWorkload) else w.M
     # calibrate on one unit per thread (the oracle spreads units over its threads)
     cal = max(1, min(total, threads))
     t0 = time.perf_counter()
-    _oracle_unit(w, inputs, cal)
+    _oracle_unit(w, inputs, cal, threads=threads)
     t_cal = time.perf_counter() - t0
     n = max(1, min(total, int(budget_s / max(t_cal, 1e-4)) * cal))
     t0 = time.perf_counter()
-    flops, nbytes = _oracle_unit(w, inputs, n)
+    flops, nbytes = _oracle_unit(w, inputs, n, threads=threads)
     dt = time.perf_counter() - t0
     value = nbytes / dt / 1e9 if metric_unit == "GB/s" else flops / dt / 1e12
     unit_name = "query rows" if isinstance(w, workloads.AttnWorkload) else "rows"
@@ -534,26 +547,27 @@ def parity_check(w, inputs, out, n_samples: int = 4096, seed: int = 12345):
         else:
             rows = np.concatenate([[0, w.M - 1, 0, w.M - 1], rng.integers(0, w.M, n_samples - 4)])
             cols = np.concatenate([[0, 0, w.N - 1, w.N - 1], rng.integers(0, w.N, n_samples - 4)])
-        ref = oracle.gemm_sampled(A, B, bias, w.gelu, rows, cols)
+        ref = oracle.gemm_sampled(A, B, bias, w.gelu, rows, cols, threads=oracle_threads())
         got = got_all[rows, cols]
         what = "sampled elements (first and last rows and columns included)"
     elif isinstance(w, workloads.W4Workload):
         A, Bq, sc, bias = inputs
         picks = sorted({0, w.M - 1})
-        ref = np.concatenate([oracle.gemm_w4(A, Bq, sc, bias, gelu=w.gelu, rows=(r, 1)) for r in picks])
+        ref = np.concatenate([oracle.gemm_w4(A, Bq, sc, bias, gelu=w.gelu, rows=(r, 1), threads=oracle_threads())
+                              for r in picks])
         got = got_all[picks]
         what = f"rows {picks} (every column)"
     elif isinstance(w, workloads.AttnWorkload):
         Q, K, V = inputs
         pos = np.concatenate([[0, w.S - 1], rng.integers(0, w.S, 14)])
         rows = np.array([(b * w.S + s) * w.H + h for b in range(w.B) for s in pos for h in (0, w.H - 1)])
-        ref = oracle.attention(Q, K, V, causal=w.causal, rows=rows)
+        ref = oracle.attention(Q, K, V, causal=w.causal, rows=rows, threads=oracle_threads())
         got = got_all.reshape(-1, w.D)[rows]
         what = f"{len(rows)} query rows (first and last positions, first and last heads)"
     else:
         (X,) = inputs
         picks = sorted({0, w.M - 1, *rng.integers(0, w.M, 6).tolist()})
-        ref = np.concatenate([oracle.softmax(X, rows=(r, 1)) for r in picks])
+        ref = np.concatenate([oracle.softmax(X, rows=(r, 1), threads=oracle_threads()) for r in picks])
         got = got_all[picks]
         what = f"{len(picks)} rows"
     atol, rtol = PARITY_TOL["softmax" if isinstance(w, workloads.SoftmaxWorkload) else "default"]
@@ -615,6 +629,7 @@ def run_gpu(args):
     pk, pk_kind = peaks()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     main = workloads.BY_NAME[args.workload]
+    oracle_threads()
     sampler = ClockSampler(local) if rank == 0 else None
     res = time_workload(tg, main, args.steps, args.warmup, 0 if main.bytes() > 2 * l2 else 2 * l2 + (1 << 20),
                         pg=pg, sampler=sampler, kernel=KERNELS[args.kernel])

@@ -187,3 +187,14 @@ def test_smi_timestamps_parse():
     t = b._smi_time("2026/12/03 05:30:36.250")
     assert t is not None and abs((t % 1) - 0.25) < 1e-6
     assert b._smi_time("not a time") is None
+
+
+def test_all_core_baselines_survive_a_one_thread_timing():
+    b = _bench()
+    import oracle
+    import workloads
+    n = b.oracle_threads()
+    assert n == max(1, oracle.max_threads()) or n >= 1
+    b.cpu_baseline_one_thread(workloads.custom(8, 16, 16, seed=8))  # leaves the oracle at one thread
+    e = b.cpu_baseline(workloads.custom(32, 64, 48, seed=9), 0.05, "TFLOP/s")
+    assert e["cores"] == n
