@@ -69,6 +69,13 @@ def _bind(lib):
     lib.oracle_gemm_w4_rows.argtypes = [u16p, u8p, u16p, u16p, u16p, f64p, i64, i64, i64, i64, ctypes.c_int,
                                         i64, i64, ctypes.c_int]
     lib.oracle_gemm_w4_rows.restype = ctypes.c_int
+    lib.oracle_e2m1_value.argtypes = [ctypes.c_uint8, ctypes.c_int]
+    lib.oracle_e2m1_value.restype = ctypes.c_double
+    lib.oracle_dequant_w4f.argtypes = [u8p, u16p, u16p, i64, i64, i64, ctypes.c_int]
+    lib.oracle_dequant_w4f.restype = ctypes.c_int
+    lib.oracle_gemm_w4f_rows.argtypes = [u16p, u8p, u16p, u16p, u16p, f64p, i64, i64, i64, i64, ctypes.c_int,
+                                         ctypes.c_int, i64, i64, ctypes.c_int]
+    lib.oracle_gemm_w4f_rows.restype = ctypes.c_int
     lib.oracle_attention_rows.argtypes = [u16p, u16p, u16p, u16p, f64p, i64, i64, i64, i64, ctypes.c_int,
                                           ctypes.c_double, i64p, i64, ctypes.c_int]
     lib.oracle_attention_rows.restype = ctypes.c_int
@@ -162,22 +169,27 @@ class Oracle:
     def int4_value(self, byte: int, high: bool) -> int:
         return int(self._lib.oracle_int4_value(int(byte) & 0xFF, 4 if high else 0))
 
-    def dequant_w4(self, Bq, scales, group: int = 128):
+    def e2m1_value(self, byte: int, high: bool) -> float:
+        """Value of the FP4 (E2M1) field in the low (or high) nibble of `byte`."""
+        return float(self._lib.oracle_e2m1_value(int(byte) & 0xFF, 4 if high else 0))
+
+    def dequant_w4(self, Bq, scales, group: int = 128, fmt: int = 0):
         """W (K x N, np.float16) from Bq (N x K/2 bytes, low nibble = even k):
-        q * scale rounded once to binary16."""
+        value * scale rounded once to binary16; fmt 0 = INT4, 1 = FP4 (E2M1)."""
         q, sc = _u8(Bq), _bits(scales)
         N, half_k = q.shape
         K = 2 * half_k
         W = np.empty((K, N), dtype=np.uint16)
-        rc = self._lib.oracle_dequant_w4(_ptr(q, ctypes.c_uint8), _ptr(sc, ctypes.c_uint16), _ptr(W, ctypes.c_uint16),
-                                         N, K, int(group))
+        rc = self._lib.oracle_dequant_w4f(_ptr(q, ctypes.c_uint8), _ptr(sc, ctypes.c_uint16),
+                                          _ptr(W, ctypes.c_uint16), N, K, int(group), int(fmt))
         if rc != 0:
-            raise RuntimeError("oracle_dequant_w4 failed")
+            raise RuntimeError("oracle_dequant_w4f failed")
         return W.view(np.float16)
 
     def gemm_w4(self, A, Bq, scales, bias=None, gelu: bool = False, group: int = 128,
-                rows: tuple[int, int] | None = None, want_f64: bool = False, threads: int = 0):
-        """C = epi(A @ W + bias) with W the dequantized 4-bit weights."""
+                rows: tuple[int, int] | None = None, want_f64: bool = False, threads: int = 0, fmt: int = 0):
+        """C = epi(A @ W + bias) with W the dequantized 4-bit weights (fmt 0 =
+        INT4, 1 = FP4 E2M1)."""
         a, q, sc, c = _bits(A), _u8(Bq), _bits(scales), _bits(bias)
         M, K = a.shape
         if 2 * q.shape[1] != K:
@@ -188,12 +200,12 @@ class Oracle:
         r0, nr = (0, M) if rows is None else rows
         out = np.empty((nr, N), dtype=np.uint16)
         out64 = np.empty((nr, N), dtype=np.float64) if want_f64 else None
-        rc = self._lib.oracle_gemm_w4_rows(_ptr(a, ctypes.c_uint16), _ptr(q, ctypes.c_uint8),
-                                           _ptr(sc, ctypes.c_uint16), _ptr(c, ctypes.c_uint16),
-                                           _ptr(out, ctypes.c_uint16), _ptr(out64, ctypes.c_double),
-                                           M, N, K, int(group), int(bool(gelu)), r0, nr, int(threads))
+        rc = self._lib.oracle_gemm_w4f_rows(_ptr(a, ctypes.c_uint16), _ptr(q, ctypes.c_uint8),
+                                            _ptr(sc, ctypes.c_uint16), _ptr(c, ctypes.c_uint16),
+                                            _ptr(out, ctypes.c_uint16), _ptr(out64, ctypes.c_double),
+                                            M, N, K, int(group), int(fmt), int(bool(gelu)), r0, nr, int(threads))
         if rc != 0:
-            raise RuntimeError("oracle_gemm_w4_rows failed")
+            raise RuntimeError("oracle_gemm_w4f_rows failed")
         out = out.view(np.float16)
         return (out, out64) if want_f64 else out
 
@@ -294,6 +306,7 @@ max_threads = _default.max_threads
 gemm = _default.gemm
 gemm_sampled = _default.gemm_sampled
 int4_value = _default.int4_value
+e2m1_value = _default.e2m1_value
 dequant_w4 = _default.dequant_w4
 gemm_w4 = _default.gemm_w4
 attention = _default.attention

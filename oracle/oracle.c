@@ -212,31 +212,67 @@ int oracle_int4_value(uint8_t byte, int shift) {
     return v >= 8 ? v - 16 : v;
 }
 
+/*
+ * FP4 weights. The same section names 4-bit floating point (FP4) beside INT4
+ * as a weight format. Reading taken: FP4 is the E2M1 element of the OCP
+ * microscaling formats, each 4-bit field being
+ *   bit 3      sign s
+ *   bits 2..1  exponent e, bias 1
+ *   bit 0      mantissa m
+ * with value (-1)^s * 2^(e-1) * (1 + m/2) for e > 0 and (-1)^s * m/2 for e = 0
+ * (zero and the one subnormal, 0.5); there are no infinities or NaN. Storage,
+ * scales and rounding are those of the INT4 format above: the dequantized
+ * weight is W[k][n] = v * scale[k/group][n] rounded once to binary16.
+ */
+double oracle_e2m1_value(uint8_t byte, int shift) {
+    const int v = (byte >> shift) & 0xF;
+    const int s = (v >> 3) & 1, e = (v >> 1) & 3, m = v & 1;
+    const double x = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -x : x;
+}
+
+/* Value of the 4-bit field at bit `shift` of `byte` in weight format `format`
+ * (0: two's-complement INT4, 1: FP4 E2M1). */
+static double field_value(uint8_t byte, int shift, int format) {
+    return format == 1 ? oracle_e2m1_value(byte, shift) : (double)oracle_int4_value(byte, shift);
+}
+
 /* W (K x N binary16 bits) from the packed weights and scales. */
-int oracle_dequant_w4(const uint8_t* Bq, const uint16_t* scales, uint16_t* W, int64_t N, int64_t K, int64_t group) {
-    if (N < 0 || K < 0 || group <= 0 || (K % 2) != 0) return -1;
+int oracle_dequant_w4f(const uint8_t* Bq, const uint16_t* scales, uint16_t* W, int64_t N, int64_t K, int64_t group,
+                       int format) {
+    if (N < 0 || K < 0 || group <= 0 || (K % 2) != 0 || format < 0 || format > 1) return -1;
     for (int64_t n = 0; n < N; ++n) {
         const uint8_t* row = Bq + n * (K / 2);
         for (int64_t k = 0; k < K; ++k) {
             const uint16_t* srow = scales + (k / group) * N;
-            const int q = oracle_int4_value(row[k / 2], (k % 2) ? 4 : 0);
-            W[k * N + n] = oracle_double_to_half((double)q * oracle_half_to_double(srow[n]));
+            const double q = field_value(row[k / 2], (k % 2) ? 4 : 0, format);
+            W[k * N + n] = oracle_double_to_half(q * oracle_half_to_double(srow[n]));
         }
     }
     return 0;
 }
 
-/* Rows [row0, row0 + nrows) of C = epi(A @ W + bias), W from oracle_dequant_w4. */
-int oracle_gemm_w4_rows(const uint16_t* A, const uint8_t* Bq, const uint16_t* scales, const uint16_t* bias,
-                        uint16_t* C, double* C64, int64_t M, int64_t N, int64_t K, int64_t group, int gelu,
-                        int64_t row0, int64_t nrows, int threads) {
+int oracle_dequant_w4(const uint8_t* Bq, const uint16_t* scales, uint16_t* W, int64_t N, int64_t K, int64_t group) {
+    return oracle_dequant_w4f(Bq, scales, W, N, K, group, 0);
+}
+
+/* Rows [row0, row0 + nrows) of C = epi(A @ W + bias), W from oracle_dequant_w4f. */
+int oracle_gemm_w4f_rows(const uint16_t* A, const uint8_t* Bq, const uint16_t* scales, const uint16_t* bias,
+                         uint16_t* C, double* C64, int64_t M, int64_t N, int64_t K, int64_t group, int format,
+                         int gelu, int64_t row0, int64_t nrows, int threads) {
     if (N < 0 || K < 0 || (K % 2) != 0 || group <= 0) return -1;
     uint16_t* W = (uint16_t*)malloc((size_t)(K * N > 0 ? K * N : 1) * sizeof(uint16_t));
     if (!W) return -1;
-    int rc = oracle_dequant_w4(Bq, scales, W, N, K, group);
+    int rc = oracle_dequant_w4f(Bq, scales, W, N, K, group, format);
     if (rc == 0) rc = oracle_gemm_rows(A, W, bias, C, C64, M, N, K, gelu, row0, nrows, threads);
     free(W);
     return rc;
+}
+
+int oracle_gemm_w4_rows(const uint16_t* A, const uint8_t* Bq, const uint16_t* scales, const uint16_t* bias,
+                        uint16_t* C, double* C64, int64_t M, int64_t N, int64_t K, int64_t group, int gelu,
+                        int64_t row0, int64_t nrows, int threads) {
+    return oracle_gemm_w4f_rows(A, Bq, scales, bias, C, C64, M, N, K, group, 0, gelu, row0, nrows, threads);
 }
 
 /* ---- Attention forward ----

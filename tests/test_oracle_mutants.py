@@ -40,8 +40,13 @@ MUTANTS = [
     ("int4_rows_along_k", "const uint8_t* row = Bq + n * (K / 2);", "const uint8_t* row = Bq + (n ^ 1) * (K / 2);"),
     ("int4_unsigned", "return v >= 8 ? v - 16 : v;", "return v;"),
     ("int4_group_index", "scales + (k / group) * N;", "scales + (k % group) * N;"),
-    ("int4_no_rounding_of_weights", "W[k * N + n] = oracle_double_to_half((double)q * oracle_half_to_double(srow[n]));",
-     "W[k * N + n] = oracle_double_to_half((double)q) ; (void)srow;"),
+    ("int4_no_rounding_of_weights", "W[k * N + n] = oracle_double_to_half(q * oracle_half_to_double(srow[n]));",
+     "W[k * N + n] = oracle_double_to_half(q) ; (void)srow;"),
+    ("e2m1_exponent_bias", "ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e)"),
+    ("e2m1_subnormal_as_normal", "(e == 0) ? 0.5 * m :", "(e == 0) ? ldexp(1.0 + 0.5 * m, -1) :"),
+    ("e2m1_mantissa_weight", "ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.25 * m, e - 1)"),
+    ("e2m1_sign_bit", "const int s = (v >> 3) & 1, e", "const int s = v & 1, e"),
+    ("fp4_format_ignored", "return format == 1 ? oracle_e2m1_value", "return format == 2 ? oracle_e2m1_value"),
     ("attn_no_max_shift", "const double pj = exp(sc[j] - m);", "const double pj = exp(sc[j]);"),
     ("attn_causal_drops_diagonal", "const int64_t visible = causal ? si + 1 : S;",
      "const int64_t visible = causal ? (si > 0 ? si : 1) : S;"),

@@ -85,3 +85,77 @@ def test_agrees_with_fp16_gemm_on_dequantised_weights(oracle_lib):
 def test_bad_shapes_rejected(oracle_lib):
     with pytest.raises(ValueError):
         oracle_lib.gemm_w4(f16(np.zeros((2, 128))), np.zeros((16, 32), np.uint8), f16(np.zeros((1, 16))))
+
+
+# ---------------------------------------------------------------- FP4 (E2M1) weights
+
+def _e2m1_table():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "e2m1_values.txt")
+    vals = {}
+    for line in open(path):
+        line = line.split("#")[0].strip()
+        if line:
+            code, v = line.split()
+            vals[int(code, 16)] = float(v)
+    assert sorted(vals) == list(range(16))
+    return vals
+
+
+def test_e2m1_decode_exhaustive_against_the_table(oracle_lib):
+    table = _e2m1_table()
+    for b in range(256):
+        lo, hi = oracle_lib.e2m1_value(b, False), oracle_lib.e2m1_value(b, True)
+        assert lo == table[b & 0xF] and np.signbit(lo) == np.signbit(table[b & 0xF]), (b, lo)
+        assert hi == table[b >> 4] and np.signbit(hi) == np.signbit(table[b >> 4]), (b, hi)
+
+
+def test_e2m1_invariants(oracle_lib):
+    mags = [oracle_lib.e2m1_value(c, False) for c in range(8)]
+    assert all(a < b for a, b in zip(mags, mags[1:]))          # codes 0..7 ordered by magnitude
+    for c in range(8):
+        assert oracle_lib.e2m1_value(c | 8, False) == -mags[c]  # bit 3 is the sign
+        assert float(np.float16(mags[c])) == mags[c]           # every value exact in binary16
+    # consecutive codes of one binade differ by half a unit of that binade
+    assert [mags[3] - mags[2], mags[5] - mags[4], mags[7] - mags[6]] == [0.5, 1.0, 2.0]
+
+
+def test_fp4_hand_packed_bytes(oracle_lib):
+    # column n=0: 0x72 -> k0 = code 2 (1.0), k1 = code 7 (6.0); 0x9F -> k2 = -6.0, k3 = -0.5
+    # column n=1: 0x0B -> k0 = -1.5, k1 = 0.0;  0x45 -> k2 = 3.0,  k3 = 2.0
+    Bq = np.array([[0x72, 0x9F], [0x0B, 0x45]], dtype=np.uint8)
+    s = f16([[1.0, 0.25]])
+    W = oracle_lib.dequant_w4(Bq, s, group=128, fmt=1).astype(np.float64)
+    assert np.array_equal(W, [[1.0, -0.375], [6.0, 0.0], [-6.0, 0.75], [-0.5, 0.5]])
+
+
+def _pack_codes(codes):
+    """codes (K x N ints in 0..15) -> N x K/2 bytes, low nibble = even k."""
+    u = np.asarray(codes, dtype=np.uint8).T
+    return np.ascontiguousarray(u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8)
+
+
+def test_fp4_dequant_matches_numpy_rounding(oracle_lib):
+    table = _e2m1_table()
+    rng = np.random.default_rng(5)
+    K, N, G = 384, 40, 128
+    codes = rng.integers(0, 16, size=(K, N))
+    s = f16(rng.uniform(0.001, 3.0, size=(K // G, N)))
+    W = oracle_lib.dequant_w4(_pack_codes(codes), s, group=G, fmt=1)
+    vals = np.vectorize(table.get)(codes).astype(np.float64)
+    ref = (vals * np.repeat(s.astype(np.float64), G, axis=0)).astype(np.float16)  # numpy's rounding
+    assert np.array_equal(W.view(np.uint16), ref.view(np.uint16))
+
+
+def test_fp4_gemm_matches_numpy(oracle_lib):
+    table = _e2m1_table()
+    rng = np.random.default_rng(6)
+    M, K, N, G = 7, 256, 24, 128
+    A = f16(rng.standard_normal((M, K)))
+    codes = rng.integers(0, 16, size=(K, N))
+    s = f16(rng.uniform(0.01, 0.1, size=(K // G, N)))
+    bias = f16(rng.standard_normal(N) * 0.1)
+    W = (np.vectorize(table.get)(codes) * np.repeat(s.astype(np.float64), G, axis=0)).astype(np.float16)
+    ref = (A.astype(np.float64) @ W.astype(np.float64) + bias.astype(np.float64)).astype(np.float16)
+    got = oracle_lib.gemm_w4(A, _pack_codes(codes), s, bias, fmt=1)
+    assert np.array_equal(got.view(np.uint16), ref.view(np.uint16))

@@ -105,3 +105,18 @@ def test_key_ramp_scales_keys_by_position_and_leaves_q_v_alone():
     scale = 1.0 + 2.0 * torch.arange(300, dtype=torch.float32) / 128.0
     expect = (Kp.to(torch.float32) * scale.view(1, 300, 1, 1)).to(torch.float16)
     assert torch.equal(Kr, expect)
+
+
+def test_fp4_workload_draws_every_code_and_int4_draws_are_unchanged():
+    w = workloads.W4Workload("f", 4, 64, 256, seed=3, fmt="fp4")
+    A, Bq, s, bias = w.inputs()
+    codes = np.concatenate([(Bq.numpy() & 0xF).ravel(), (Bq.numpy() >> 4).ravel()])
+    assert set(codes.tolist()) == set(range(16)) and w.fmt_code == 1
+    i = workloads.W4Workload("i", 4, 64, 256, seed=3)
+    A2, Bq2, _, _ = i.inputs()
+    assert torch.equal(A, A2) and i.fmt_code == 0
+    g = torch.Generator().manual_seed(3)
+    workloads.Dist("normal", 0.0, 1.0).draw((4, 256), g)
+    q = torch.randint(-8, 8, (64, 256), generator=g, dtype=torch.int16)
+    u = (q & 0xF).to(torch.uint8)
+    assert torch.equal(Bq2, (u[:, 0::2] | (u[:, 1::2] << 4)).contiguous())

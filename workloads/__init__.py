@@ -132,6 +132,13 @@ class W4Workload:
     # uniform over {-2, ..., 1} (with integer A, every product and partial sum
     # is then exact in fp32)
     scale_kind: str = "uniform"
+    # weight format: "int4" (two's complement, q drawn uniform over [-8, 7]) or
+    # "fp4" (E2M1 codes drawn uniform over all 16 codes)
+    fmt: str = "int4"
+
+    @property
+    def fmt_code(self) -> int:
+        return {"int4": 0, "fp4": 1}[self.fmt]
 
     @property
     def has_bias(self) -> bool:
@@ -139,7 +146,7 @@ class W4Workload:
 
     def describe(self) -> str:
         epi = ("bias+" if self.has_bias else "") + ("gelu" if self.gelu else ("none" if not self.has_bias else ""))
-        return (f"{self.name}: M={self.M} N={self.N} K={self.K} int4 weights, group {self.group}, "
+        return (f"{self.name}: M={self.M} N={self.N} K={self.K} {self.fmt} weights, group {self.group}, "
                 f"epilogue={epi.rstrip('+')} seed={self.seed}")
 
     def inputs(self, device: str = "cpu"):
@@ -147,8 +154,11 @@ class W4Workload:
         g = torch.Generator(device="cpu")
         g.manual_seed(self.seed)
         A = self.a_dist.draw((self.M, self.K), g)
-        q = torch.randint(-8, 8, (self.N, self.K), generator=g, dtype=torch.int16)
-        u = (q & 0xF).to(torch.uint8)
+        if self.fmt == "fp4":
+            u = torch.randint(0, 16, (self.N, self.K), generator=g, dtype=torch.int16).to(torch.uint8)
+        else:
+            q = torch.randint(-8, 8, (self.N, self.K), generator=g, dtype=torch.int16)
+            u = (q & 0xF).to(torch.uint8)
         Bq = (u[:, 0::2] | (u[:, 1::2] << 4)).contiguous()
         groups = (self.K + self.group - 1) // self.group
         if self.scale_kind == "pow2":
@@ -177,7 +187,8 @@ class W4Workload:
 
 
 DECODE_W4 = W4Workload("decode_w4_16x28672x8192", 16, 28672, 8192, seed=5)
-W4_ALL = (DECODE_W4,)
+DECODE_FP4 = W4Workload("decode_fp4_16x28672x8192", 16, 28672, 8192, seed=6, fmt="fp4")
+W4_ALL = (DECODE_W4, DECODE_FP4)
 BY_NAME = {w.name: w for w in ALL + W4_ALL}
 
 
