@@ -238,10 +238,10 @@ def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sam
         dA, dB, ds = A.cuda(), Bq.cuda(), sc.cuda()
         db = bias.cuda() if bias is not None else None
         args = (dA.data_ptr(), dB.data_ptr(), ds.data_ptr(), db.data_ptr() if db is not None else None,
-                dC.data_ptr(), w.M, w.N, w.K, int(w.gelu), 0, sh)
+                dC.data_ptr(), w.M, w.N, w.K, int(w.gelu), w.fmt_code, 0, sh)
 
         def call():
-            tg.tg_gemm_w4(*args)
+            tg.tg_gemm_w4_ex(*args)
     else:
         A, B, bias = w.inputs()
         host_inputs = (A, B, bias)
@@ -486,7 +486,7 @@ def _oracle_unit(w, inputs, n: int, first: int = 0, threads: int = 0, rng=None):
         return 2.0 * n * w.N * w.K, 2.0 * (n * w.K + w.K * w.N + n * w.N)
     if isinstance(w, workloads.W4Workload):
         A, Bq, sc, bias = inputs
-        oracle.gemm_w4(A, Bq, sc, bias, gelu=w.gelu, rows=(first, n), threads=threads)
+        oracle.gemm_w4(A, Bq, sc, bias, gelu=w.gelu, rows=(first, n), threads=threads, fmt=w.fmt_code)
         groups = (w.K + w.group - 1) // w.group
         return 2.0 * n * w.N * w.K, 2.0 * n * w.K + w.K * w.N / 2 + 2.0 * groups * w.N + 2.0 * n * w.N
     if isinstance(w, workloads.AttnWorkload):
@@ -553,7 +553,8 @@ def parity_check(w, inputs, out, n_samples: int = 4096, seed: int = 12345):
     elif isinstance(w, workloads.W4Workload):
         A, Bq, sc, bias = inputs
         picks = sorted({0, w.M - 1})
-        ref = np.concatenate([oracle.gemm_w4(A, Bq, sc, bias, gelu=w.gelu, rows=(r, 1), threads=oracle_threads())
+        ref = np.concatenate([oracle.gemm_w4(A, Bq, sc, bias, gelu=w.gelu, rows=(r, 1), threads=oracle_threads(),
+                                              fmt=w.fmt_code)
                               for r in picks])
         got = got_all[picks]
         what = f"rows {picks} (every column)"

@@ -206,6 +206,25 @@ tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const void* bias,
 tg_status tg_gemm_w4(const void* A, const void* Bq, const void* scales, const void* bias, void* C,
                      int64_t M, int64_t N, int64_t K, int epilogue, int split_k, tg_stream_t stream);
 
+/* Weight formats of the 4-bit GEMM. */
+typedef enum {
+    TG_W4_INT4 = 0,     /* two's-complement integers in [-8, 7] */
+    TG_W4_FP4_E2M1 = 1  /* FP4 E2M1: bit 3 sign, bits 2-1 exponent (bias 1), bit 0 mantissa;
+                           values +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}, no infinities or NaN */
+} tg_w4_format;
+
+/*
+ * tg_gemm_w4 with the format of the 4-bit fields given: the same section
+ * ("Quantized LLM inference") names INT4 and FP4 weights. `weight_format` is a
+ * tg_w4_format value; storage, scales, W[k][n] = value(q[k][n]) *
+ * scales[k/128][n] rounded once to binary16, sizes, splits, errors and
+ * tolerance are those of tg_gemm_w4 (which is this call with TG_W4_INT4).
+ * An unknown format is TG_ERR_INVALID_ARG.
+ */
+tg_status tg_gemm_w4_ex(const void* A, const void* Bq, const void* scales, const void* bias, void* C,
+                        int64_t M, int64_t N, int64_t K, int epilogue, int weight_format, int split_k,
+                        tg_stream_t stream);
+
 /*
  * Attention forward (FlashAttention), the fused attention kernel of
  * "TileLang: writing LLM GPU kernels by thinking in tiles", section 5, with

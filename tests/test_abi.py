@@ -181,3 +181,13 @@ def test_softmax_argument_checks(tg):
         with pytest.raises(tg.TgError) as ei:
             tg.tg_softmax_rows(*args, None)
         assert ei.value.status == tg.ERR_INVALID_ARG and msg in str(ei.value)
+
+
+def test_w4_ex_rejects_an_unknown_format_and_shares_the_checks(tg):
+    with pytest.raises(tg.TgError) as ei:
+        tg.tg_gemm_w4_ex(0x10000, 0x20000000, 0x30000000, None, 0x40000000, 16, 64, 256, 0, 2, 0, None)
+    assert ei.value.status == tg.ERR_INVALID_ARG and "weight_format" in str(ei.value)
+    with pytest.raises(tg.TgError) as ei:
+        tg.tg_gemm_w4_ex(0x10000, 0x20000000, 0x30000000, None, 0x40000000, 16, 64, 192, 0, tg.W4_FP4_E2M1, 0, None)
+    assert ei.value.status == tg.ERR_INVALID_ARG and "K % 128" in str(ei.value)
+    tg.tg_gemm_w4_ex(None, None, None, None, None, 0, 64, 256, 0, tg.W4_FP4_E2M1, 0, None)

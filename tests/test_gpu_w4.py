@@ -143,3 +143,83 @@ def test_extreme_nibbles_and_scales(tg):
     C = tg.gemm_w4(*_dev(A, Bq, s))
     _check_tol(C.cpu().numpy(), ref, "extreme nibbles")
     _status_ok(tg)
+
+
+# ---------------------------------------------------------------- FP4 (E2M1) weights
+
+FP4_EXACT = [(1, 8, 128), (16, 128, 256), (5, 136, 384), (17, 264, 128), (64, 1024, 1024), (128, 256, 512),
+             (33, 16, 896), (48, 392, 2048)]
+
+
+@pytest.mark.parametrize("M,N,K", FP4_EXACT, ids=[f"{m}x{n}x{k}" for m, n, k in FP4_EXACT])
+def test_fp4_exact_inputs_bitwise_every_split(tg, M, N, K):
+    # integer activations, power-of-two scales, E2M1 values (multiples of 1/2 up to 6):
+    # every product and partial sum is exact in fp32, so the result is the oracle's bit for bit
+    w = workloads.W4Workload(f"fp4_exact_{M}x{N}x{K}", M, N, K, seed=M * 37 + N + K, a_dist=INT2,
+                             bias_dist=INT2, scale_kind="pow2", fmt="fp4")
+    A, Bq, s, bias = w.inputs()
+    dA, dBq, ds, dbias = _dev(A, Bq, s, bias)
+    ref = oracle.gemm_w4(A, Bq, s, bias, fmt=1).view(np.uint16)
+    kb = (K + 255) // 256
+    for split_k in sorted({0, 1, 2, kb}):
+        C = tg.gemm_w4(dA, dBq, ds, dbias, split_k=split_k, fmt=tg.W4_FP4_E2M1)
+        got = C.cpu().numpy().view(np.uint16)
+        mism = np.argwhere(got != ref)
+        assert mism.size == 0, (f"split_k={split_k}: {len(mism)} mismatches, first {tuple(mism[0])}: "
+                                f"gpu={got[tuple(mism[0])]:#06x} ref={ref[tuple(mism[0])]:#06x}")
+    _status_ok(tg)
+
+
+def test_fp4_every_code_through_an_identity_product(tg):
+    # A = [I | 0] picks rows of W: C[m, n] = W[m, n] = value(q[m, n]) * scale[0, n], so every
+    # one of the 16 codes in both nibble positions and every column is read back exactly
+    M, N, K = 64, 256, 256
+    codes = (np.arange(K)[:, None] + 3 * np.arange(N)[None, :]) % 16  # every code in every column
+    u = codes.T.astype(np.uint8)
+    Bq = torch.from_numpy(np.ascontiguousarray(u[:, 0::2] | (u[:, 1::2] << 4)))
+    s = torch.from_numpy(np.where(np.arange(N) % 2 == 0, 1.0, 0.25).astype(np.float16)[None, :].repeat(2, 0))
+    A = torch.zeros((M, K), dtype=torch.float16)
+    A[torch.arange(M), torch.arange(M)] = 1.0
+    # values compared as numbers: a sum of zeros may come out as +0 or -0 (the sign of an
+    # exact zero is not fixed by the definition, and differs between compilers of the oracle)
+    ref = oracle.gemm_w4(A, Bq, s, fmt=1).astype(np.float64)
+    W = oracle.dequant_w4(Bq, s, fmt=1).astype(np.float64)
+    assert np.array_equal(ref, W[:M])
+    C = tg.gemm_w4(*_dev(A, Bq, s), fmt=tg.W4_FP4_E2M1)
+    assert np.array_equal(C.cpu().numpy().astype(np.float64), ref)
+    _status_ok(tg)
+
+
+@pytest.mark.parametrize("M,N,K,gelu", [(16, 4096, 4096, True), (3, 1000, 1152, False), (64, 2048, 1024, True)])
+def test_fp4_random_inputs(tg, M, N, K, gelu):
+    w = workloads.W4Workload(f"fp4_rand_{M}x{N}x{K}", M, N, K, seed=M + N + K + 1,
+                             bias_dist=workloads.Dist("normal", 0.0, 0.02), gelu=gelu, fmt="fp4")
+    A, Bq, s, bias = w.inputs()
+    ref = oracle.gemm_w4(A, Bq, s, bias, gelu=gelu, fmt=1)
+    C = tg.gemm_w4(*_dev(A, Bq, s, bias), gelu=gelu, fmt=tg.W4_FP4_E2M1)
+    _check_tol(C.cpu().numpy(), ref, f"fp4 {M}x{N}x{K}")
+    _status_ok(tg)
+
+
+def test_fp4_decode_workload_every_element(tg):
+    w = workloads.DECODE_FP4
+    A, Bq, s, bias = w.inputs()
+    ref = oracle.gemm_w4(A, Bq, s, bias, fmt=1)
+    dA, dBq, ds, dbias = _dev(A, Bq, s, bias)
+    for split_k in (0, 1, 4):
+        C = tg.gemm_w4(dA, dBq, ds, dbias, split_k=split_k, fmt=tg.W4_FP4_E2M1)
+        _check_tol(C.cpu().numpy(), ref, f"fp4 decode split_k={split_k}")
+    _status_ok(tg)
+
+
+def test_unaligned_32_byte_weight_base(tg):
+    # packed weights 16- but not 32-byte aligned take the 16-byte loads
+    w = workloads.W4Workload("w4_off16", 16, 512, 1024, seed=77, a_dist=INT2, scale_kind="pow2")
+    A, Bq, s, _ = w.inputs()
+    buf = torch.zeros(Bq.numel() + 16, dtype=torch.uint8, device="cuda")
+    dBq = buf[16:16 + Bq.numel()].view(Bq.shape)
+    dBq.copy_(Bq.cuda())
+    assert dBq.data_ptr() % 32 == 16
+    C = tg.gemm_w4(A.cuda(), dBq, s.cuda())
+    assert np.array_equal(C.cpu().numpy().view(np.uint16), oracle.gemm_w4(A, Bq, s).view(np.uint16))
+    _status_ok(tg)

@@ -151,22 +151,6 @@ tg_status current_device(int* dev_out) {
     return TG_OK;
 }
 
-// Row-major [outer][inner] matrix of `elem_bytes`-byte elements, box of
-// box_inner x box_outer with the given swizzle; out-of-bounds elements read as
-// zero.
-tg_status make_map_ex(CUtensorMap* m, CUtensorMapDataType dtype, uint32_t elem_bytes, const void* base,
-                      uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
-                      CUtensorMapSwizzle swizzle) {
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * elem_bytes};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    CUresult r = encode_cached(m, dtype, 2, base, dims, strides, box, swizzle);
-    if (r != CUDA_SUCCESS)
-        return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %llu x %llu matrix", (int)r,
-                    (unsigned long long)outer, (unsigned long long)inner);
-    return TG_OK;
-}
-
 // (batch, sequence, head, dim) fp16 tensor as a 4-D map, innermost first:
 // {dim, head, sequence, batch}; box {64, 1, 128, 1} with the 128-byte swizzle
 // (one 64-column slice of 128 consecutive positions of one head).
@@ -760,12 +744,16 @@ extern "C" tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const 
 // ---------------------------------------------------------------------------
 // tg_gemm_w4: the skinny GEMM with 4-bit weights.
 
-extern "C" tg_status tg_gemm_w4(const void* A, const void* Bq, const void* scales, const void* bias, void* C,
-                                int64_t M, int64_t N, int64_t K, int epilogue, int split_k, tg_stream_t stream_) {
+extern "C" tg_status tg_gemm_w4_ex(const void* A, const void* Bq, const void* scales, const void* bias, void* C,
+                                   int64_t M, int64_t N, int64_t K, int epilogue, int weight_format, int split_k,
+                                   tg_stream_t stream_) {
     t_last_error.clear();
     const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_GELU)
         return fail(TG_ERR_INVALID_ARG, "epilogue must be TG_EPI_NONE (0) or TG_EPI_GELU (1), got %d", epilogue);
+    if (weight_format != TG_W4_INT4 && weight_format != TG_W4_FP4_E2M1)
+        return fail(TG_ERR_INVALID_ARG, "weight_format must be TG_W4_INT4 (0) or TG_W4_FP4_E2M1 (1), got %d",
+                    weight_format);
     const int64_t kMax = 0x7FFFFFFFll;
     if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax)
         return fail(TG_ERR_INVALID_ARG, "sizes must be in [0, 2^31): M=%lld N=%lld K=%lld", (long long)M,
@@ -811,7 +799,7 @@ extern "C" tg_status tg_gemm_w4(const void* A, const void* Bq, const void* scale
         a.C = static_cast<__half*>(C) + r0 * N;
         a.M = (int)rows; a.N = (int)N; a.K = (int)K; a.gelu = gelu;
         a.m_pad = (a.M + 15) / 16 * 16;
-        w4_pipeline(a.m_pad, &a.stages, &w.a_slots, &w.b_slots);
+        w4_pipeline(a.m_pad, &w.act_stages, &w.b_slots);
         a.n_tiles = (a.N + kW4BN - 1) / kW4BN;
         a.kb_total = (a.K + kW4BK - 1) / kW4BK;
         int s = split_k > 0 ? split_k : choose_splits(a.n_tiles, a.kb_total, d.sm_count, 2.0, 1.0, 1.0);
@@ -830,20 +818,21 @@ extern "C" tg_status tg_gemm_w4(const void* A, const void* Bq, const void* scale
         }
         w.Bq = static_cast<const uint8_t*>(Bq);
         w.scales = static_cast<const __half*>(scales);
+        w.fmt = weight_format;
+        w.bq_v8 = aligned(Bq, 32) ? 1 : 0;  // rows are K/2 bytes, a multiple of 64
         w.c_vec = aligned(a.C, 16) ? 1 : 0;  // N % 8 == 0 is required above
-        CUtensorMap tmBq, tmA, tmS;
-        if ((st = make_map_ex(&tmBq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Bq, K / 2, N, kW4BK / 2, kW4BN,
-                              CU_TENSOR_MAP_SWIZZLE_128B)) != TG_OK)
-            return st;
+        CUtensorMap tmA;
         if ((st = make_map(&tmA, a.A, K, a.M, 64, a.m_pad)) != TG_OK) return st;
-        if ((st = make_map_ex(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, scales, N, K / kW4Group, kW4BN,
-                              kW4BK / kW4Group, CU_TENSOR_MAP_SWIZZLE_NONE)) != TG_OK)
-            return st;
         const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
-        cudaError_t e = launch_w4(w, tmBq, tmA, tmS, grid, stream);
+        cudaError_t e = launch_w4(w, tmA, grid, stream);
         if (e != cudaSuccess) return cuda_fail(e, "4-bit kernel launch");
     }
     return TG_OK;
+}
+
+extern "C" tg_status tg_gemm_w4(const void* A, const void* Bq, const void* scales, const void* bias, void* C,
+                                int64_t M, int64_t N, int64_t K, int epilogue, int split_k, tg_stream_t stream) {
+    return tg_gemm_w4_ex(A, Bq, scales, bias, C, M, N, K, epilogue, TG_W4_INT4, split_k, stream);
 }
 
 // ---------------------------------------------------------------------------
