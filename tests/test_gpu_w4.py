@@ -213,7 +213,7 @@ def test_fp4_decode_workload_every_element(tg):
 
 
 def test_unaligned_32_byte_weight_base(tg):
-    # packed weights 16- but not 32-byte aligned take the 16-byte loads
+    # packed weights at a base that is 16- but not 32-byte aligned (the documented minimum)
     w = workloads.W4Workload("w4_off16", 16, 512, 1024, seed=77, a_dist=INT2, scale_kind="pow2")
     A, Bq, s, _ = w.inputs()
     buf = torch.zeros(Bq.numel() + 16, dtype=torch.uint8, device="cuda")

@@ -151,6 +151,35 @@ tg_status current_device(int* dev_out) {
     return TG_OK;
 }
 
+// Row-major [outer][inner] byte matrix, box of box_inner x box_outer bytes,
+// 128-byte swizzle; out-of-bounds bytes read as zero.
+tg_status make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                      uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    CUresult r = encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r != CUDA_SUCCESS)
+        return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %llu x %llu byte matrix", (int)r,
+                    (unsigned long long)outer, (unsigned long long)inner);
+    return TG_OK;
+}
+
+// Row-major [outer][inner] fp16 matrix, unswizzled box (the 4-bit GEMM's scale rows).
+tg_status make_map_scales(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                          uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    CUresult r = encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %llu x %llu scale matrix", (int)r,
+                    (unsigned long long)outer, (unsigned long long)inner);
+    return TG_OK;
+}
+
 // (batch, sequence, head, dim) fp16 tensor as a 4-D map, innermost first:
 // {dim, head, sequence, batch}; box {64, 1, 128, 1} with the 128-byte swizzle
 // (one 64-column slice of 128 consecutive positions of one head).
@@ -799,7 +828,7 @@ extern "C" tg_status tg_gemm_w4_ex(const void* A, const void* Bq, const void* sc
         a.C = static_cast<__half*>(C) + r0 * N;
         a.M = (int)rows; a.N = (int)N; a.K = (int)K; a.gelu = gelu;
         a.m_pad = (a.M + 15) / 16 * 16;
-        w4_pipeline(a.m_pad, &w.act_stages, &w.b_slots);
+        w4_pipeline(a.m_pad, &a.stages, &w.a_slots, &w.b_slots);
         a.n_tiles = (a.N + kW4BN - 1) / kW4BN;
         a.kb_total = (a.K + kW4BK - 1) / kW4BK;
         int s = split_k > 0 ? split_k : choose_splits(a.n_tiles, a.kb_total, d.sm_count, 2.0, 1.0, 1.0);
@@ -819,12 +848,13 @@ extern "C" tg_status tg_gemm_w4_ex(const void* A, const void* Bq, const void* sc
         w.Bq = static_cast<const uint8_t*>(Bq);
         w.scales = static_cast<const __half*>(scales);
         w.fmt = weight_format;
-        w.bq_v8 = aligned(Bq, 32) ? 1 : 0;  // rows are K/2 bytes, a multiple of 64
         w.c_vec = aligned(a.C, 16) ? 1 : 0;  // N % 8 == 0 is required above
-        CUtensorMap tmA;
+        CUtensorMap tmBq, tmA, tmS;
+        if ((st = make_map_u8(&tmBq, Bq, K / 2, N, kW4BK / 2, kW4BN)) != TG_OK) return st;
         if ((st = make_map(&tmA, a.A, K, a.M, 64, a.m_pad)) != TG_OK) return st;
+        if ((st = make_map_scales(&tmS, scales, N, K / kW4Group, kW4BN, kW4BK / kW4Group)) != TG_OK) return st;
         const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
-        cudaError_t e = launch_w4(w, tmA, grid, stream);
+        cudaError_t e = launch_w4(w, tmBq, tmA, tmS, grid, stream);
         if (e != cudaSuccess) return cuda_fail(e, "4-bit kernel launch");
     }
     return TG_OK;

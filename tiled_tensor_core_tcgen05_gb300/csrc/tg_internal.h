@@ -42,8 +42,10 @@ constexpr int kSkMaxSplits = 64;
 constexpr int kSkSmemBudget = 200 * 1024;  // operand ring budget per CTA
 
 // ---- weight-only 4-bit kernel geometry: one work unit is a 256-column slice
-// of N (the MMA's N) times a range of 256-wide K blocks (stages); tokens are
-// the MMA's M (128 rows from tensor memory, at most 64 real ones per launch).
+// of N (the MMA's N) times a range of 256-wide K blocks; tokens are the MMA's
+// M (64 rows, at most 64 real ones per launch). A stage holds the slice's
+// packed weights (256 rows of 128 bytes), the matching 256 columns of A and
+// the two scale rows of the block.
 constexpr int kW4BN = 256;
 constexpr int kW4BK = 256;
 constexpr int kW4Group = 128;          // rows of K sharing one scale per column
@@ -110,15 +112,14 @@ struct SplitArgs {
 };
 
 // The 4-bit kernel: the skinny fields above (A, bias, C, sizes, m_pad,
-// split bookkeeping) plus the packed weights, their scales, their format and
-// the depth of the converted-weight ring.
+// split bookkeeping, stages = raw ring depth) plus the packed weights, their
+// scales, their format and the depth of the converted-weight ring.
 struct W4Args {
-    SplitArgs s;               // s.B, s.stages and s.tmem_* unused
+    SplitArgs s;               // s.B and s.tmem_* unused
     const uint8_t* Bq;         // N rows of K/2 bytes, low nibble = even k
     const __half* scales;      // K/128 rows of N
     int fmt;                   // 0: two's-complement INT4, 1: FP4 (E2M1)
-    int bq_v8;                 // Bq 32-byte aligned: 32-byte loads of packed weights
-    int act_stages;            // shared-memory activation stages (256 k each)
+    int a_slots;               // activation slots (one 256-k stage of A each)
     int b_slots;               // converted 64-k sub-tiles in flight
     int c_vec;                 // C 16-byte aligned and N % 8 == 0: 16-byte stores
 };
@@ -155,9 +156,10 @@ cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const 
                               cudaStream_t stream);
 cudaError_t launch_splitk(const SplitArgs& a, const CUtensorMap& tmB, const CUtensorMap& tmA,
                           int grid, cudaStream_t stream);
-void w4_pipeline(int m_pad, int* act_stages, int* slots);
-int w4_smem_bytes(int m_pad, int act_stages, int slots);
-cudaError_t launch_w4(const W4Args& a, const CUtensorMap& tmA, int grid, cudaStream_t stream);
+void w4_pipeline(int m_pad, int* stages, int* act_slots, int* slots);
+int w4_smem_bytes(int m_pad, int stages, int act_slots, int slots);
+cudaError_t launch_w4(const W4Args& a, const CUtensorMap& tmBq, const CUtensorMap& tmA, const CUtensorMap& tmS,
+                      int grid, cudaStream_t stream);
 cudaError_t launch_softmax(const __half* X, __half* Y, int M, int N, bool vec, int sm_count, cudaStream_t stream);
 int attn_smem_bytes();
 cudaError_t launch_attn(const AttnArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
