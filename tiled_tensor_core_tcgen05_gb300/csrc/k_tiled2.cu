@@ -56,8 +56,11 @@ constexpr int kBarAccEmpty = kBarAccFull + 16;
 constexpr int kBarDrain = kBarAccEmpty + 16;
 constexpr int kTmemSlot = kBarDrain + 8;
 constexpr int kAbortSlot = kTmemSlot + 4;
-constexpr int kEpiStage = (kAbortSlot + 4 + 127) / 128 * 128;  // per-warp output staging
-constexpr int kSmemUsed = kEpiStage + kEpiWarps * kStageWarpBytes;
+// per-warp output staging: two TMA-store boxes (or one padded st.global chunk)
+constexpr int kEpiWarpBytes = 2 * kStoreBoxBytes;
+static_assert(kEpiWarpBytes >= kStageWarpBytes, "staging covers both store paths");
+constexpr int kEpiStage = (kAbortSlot + 4 + 1023) / 1024 * 1024;
+constexpr int kSmemUsed = kEpiStage + kEpiWarps * kEpiWarpBytes;
 constexpr int kSmemAlloc = kSmemUsed + 1024;
 
 // M=256 (pair), N=256, A K-major, B N-major; and the half-width form (N=128)
@@ -90,9 +93,12 @@ __device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks
     nb = local / gsize;
 }
 
+// kTmaStore: C is written by TMA stores from swizzled staging boxes (C 16-byte
+// aligned with N % 8 == 0), otherwise by ordinary stores of staged row segments.
+template <bool kTmaStore>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tiled_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const TiledArgs args) {
+                      const __grid_constant__ CUtensorMap tmC, const TiledArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -217,9 +223,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int half = (warp - kEpiWarp0) >> 2;
         const int row_in_tile = rank * kHalfM + quarter * 32 + lane;
-        uint8_t* stage = smem + kEpiStage + (warp - kEpiWarp0) * kStageWarpBytes;
+        uint8_t* stage = smem + kEpiStage + (warp - kEpiWarp0) * kEpiWarpBytes;
         const uint32_t leader_acc_empty0 = mapa_shared(acc_empty_bar(0), 0);
-        int it = 0;
+        int it = 0, nstore = 0;
         for (int u = cluster; u < args.num_units; u += num_clusters, ++it) {
             const Unit un = unit_of(u, args.split_from);
             int mb, nb;
@@ -250,10 +256,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(leader_acc_empty0 + 8 * b);
                 }
-                epilogue_chunk(r, stage, args.C, args.bias, row - lane, n0 + c * 32, args.M, args.N, args.gelu,
-                               args.c_store, args.bias_vec);
+                if (kTmaStore) {
+                    // this warp's two staging boxes alternate: the store issued two chunks ago
+                    // must have read its box before the box is written again
+                    if (lane == 0 && nstore >= 2) bulk_wait_group_read<1>();
+                    __syncwarp();
+                    epilogue_chunk_tma(r, smem_u32(stage) + (nstore & 1) * kStoreBoxBytes, &tmC, args.bias,
+                                       row - lane, n0 + c * 32, args.N, args.gelu, args.bias_vec);
+                    ++nstore;
+                } else {
+                    epilogue_chunk(r, stage, args.C, args.bias, row - lane, n0 + c * 32, args.M, args.N, args.gelu,
+                                   args.c_store, args.bias_vec);
+                }
             }
         }
+        if (kTmaStore && lane == 0) bulk_wait_group_all();  // every store of this warp has completed
     }
 
     tc_fence_before_sync();
@@ -269,15 +286,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 int tiled_pair_smem_bytes() { return kSmemAlloc; }
 
-cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, int max_clusters,
-                              cudaStream_t stream) {
+template <bool kTmaStore>
+static cudaError_t launch_pair_t(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                 const CUtensorMap& tmC, int max_clusters, cudaStream_t stream) {
     static int attr_gen[64] = {};
     static int active_clusters[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && attr_gen[dev] != g_generation) {
-        e = cudaFuncSetAttribute(tiled_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+        e = cudaFuncSetAttribute(tiled_pair_kernel<kTmaStore>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemAlloc);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * max_clusters);
@@ -291,7 +310,7 @@ cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const 
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, tiled_pair_kernel, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, tiled_pair_kernel<kTmaStore>, &cfg);
         if (e != cudaSuccess) return e;
         active_clusters[dev] = n > 0 ? n : 1;
         attr_gen[dev] = g_generation;
@@ -307,8 +326,14 @@ cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const 
     const int rest = a.num_tiles - full_waves * clusters;
     args.split_from = (full_waves > 0 && rest > 0 && 2 * rest <= clusters) ? full_waves * clusters : a.num_tiles;
     args.num_units = args.split_from + 2 * (a.num_tiles - args.split_from);
-    tiled_pair_kernel<<<2 * clusters, kThreads, kSmemAlloc, stream>>>(tmA, tmB, args);
+    tiled_pair_kernel<kTmaStore><<<2 * clusters, kThreads, kSmemAlloc, stream>>>(tmA, tmB, tmC, args);
     return cudaGetLastError();
+}
+
+cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                              const CUtensorMap* tmC, int max_clusters, cudaStream_t stream) {
+    if (tmC != nullptr) return launch_pair_t<true>(a, tmA, tmB, *tmC, max_clusters, stream);
+    return launch_pair_t<false>(a, tmA, tmB, tmA, max_clusters, stream);
 }
 
 }  // namespace tg

@@ -151,6 +151,20 @@ tg_status current_device(int* dev_out) {
     return TG_OK;
 }
 
+// C (M x N fp16, row-major) for the epilogue's TMA stores: 32 x 32 boxes,
+// 64-byte swizzle.
+tg_status make_map_c(CUtensorMap* m, const void* base, uint64_t N, uint64_t M) {
+    cuuint64_t dims[2] = {N, M};
+    cuuint64_t strides[1] = {N * 2};
+    cuuint32_t box[2] = {32, 32};
+    CUresult r = encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_64B);
+    if (r != CUDA_SUCCESS)
+        return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for the %llu x %llu output", (int)r,
+                    (unsigned long long)M, (unsigned long long)N);
+    return TG_OK;
+}
+
 // Row-major [outer][inner] byte matrix, box of box_inner x box_outer bytes,
 // 128-byte swizzle; out-of-bounds bytes read as zero.
 tg_status make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
@@ -399,6 +413,12 @@ tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, 
     return TG_OK;
 }
 
+// The pair kernel writes an aligned C by TMA stores (else by ordinary stores).
+#ifndef TG_PAIR_TMA_STORE
+#define TG_PAIR_TMA_STORE 1
+#endif
+constexpr bool kPairTmaStore = TG_PAIR_TMA_STORE != 0;
+
 tg_status run_tiled_pair(DeviceState& d, const __half* A, const __half* B, const __half* bias, __half* C, int M,
                          int N, int K, int gelu, cudaStream_t stream, int64_t lda = 0, int64_t ldb = 0) {
     TiledArgs a{};
@@ -414,11 +434,15 @@ tg_status run_tiled_pair(DeviceState& d, const __half* A, const __half* B, const
     a.bias_vec = (bias != nullptr && aligned(bias, 16)) ? 1 : 0;
     a.a_vec = a.b_vec = 8;
     a.wd = watchdog(d);
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmC;
     tg_status st = make_map_ld(&tmA, A, K, M, lda ? lda : K, kBK, kBM);
     if (st != TG_OK) return st;
     if ((st = make_map_ld(&tmB, B, N, K, ldb ? ldb : N, 64, kBK)) != TG_OK) return st;
-    cudaError_t e = launch_tiled_pair(a, tmA, tmB, d.sm_count / 2, stream);
+    // C aligned for TMA (16-byte base, rows of a multiple of 16 bytes): the epilogue writes it by
+    // TMA stores of 32 x 32 boxes
+    const bool tma_store = kPairTmaStore && a.c_store == 2;
+    if (tma_store && (st = make_map_c(&tmC, C, N, M)) != TG_OK) return st;
+    cudaError_t e = launch_tiled_pair(a, tmA, tmB, tma_store ? &tmC : nullptr, d.sm_count / 2, stream);
     if (e != cudaSuccess) return cuda_fail(e, "pair tiled kernel launch");
     return TG_OK;
 }

@@ -118,17 +118,11 @@ constexpr int kStageWarpBytes = 32 * kStagePitch;
 // 4-byte units (4-byte aligned, N even) or single elements.
 enum CStoreMode : int { kStore16 = 2, kStore4 = 1, kStore2 = 0 };
 
-// One warp's 32 x 32 chunk of C, rows row0..row0+31 (lane l computed row
-// row0 + l), columns col0..col0+31. Each lane holds its row's 32 accumulator
-// values (fp32 bits): add bias, apply GELU, round once to binary16, stage the
-// row in this warp's shared buffer, then write the chunk back row by row so
-// each store instruction covers whole 64-byte row segments. Rows >= M and
-// columns >= N are not written.
-__device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], uint8_t* stage, __half* __restrict__ C,
-                                               const __half* __restrict__ bias, int row0, int col0, int M, int N,
-                                               int gelu, int store_mode, int bias_vec) {
-    const int lane = threadIdx.x & 31;
-    float v[32];
+// The epilogue of one lane's 32 accumulator values (fp32 bits) of columns
+// col0..col0+31: add the bias (columns >= N get none), apply GELU.
+__device__ __forceinline__ void epilogue_values(const uint32_t (&r)[32], float (&v)[32],
+                                                const __half* __restrict__ bias, int col0, int N, int gelu,
+                                                int bias_vec) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
     const bool full = col0 + 32 <= N;
@@ -156,6 +150,21 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], uint8_t*
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
     }
+}
+
+// One warp's 32 x 32 chunk of C, rows row0..row0+31 (lane l computed row
+// row0 + l), columns col0..col0+31. Each lane holds its row's 32 accumulator
+// values (fp32 bits): add bias, apply GELU, round once to binary16, stage the
+// row in this warp's shared buffer, then write the chunk back row by row so
+// each store instruction covers whole 64-byte row segments. Rows >= M and
+// columns >= N are not written.
+__device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], uint8_t* stage, __half* __restrict__ C,
+                                               const __half* __restrict__ bias, int row0, int col0, int M, int N,
+                                               int gelu, int store_mode, int bias_vec) {
+    const int lane = threadIdx.x & 31;
+    float v[32];
+    epilogue_values(r, v, bias, col0, N, gelu, bias_vec);
+    const bool full = col0 + 32 <= N;
     // this lane's row into the staging buffer
     uint4* mine = reinterpret_cast<uint4*>(stage + lane * kStagePitch);
 #pragma unroll
@@ -206,6 +215,42 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], uint8_t*
         }
     }
     __syncwarp();  // the buffer is rewritten by this warp's next chunk
+}
+
+// Bytes of one TMA-store staging buffer: a 32 x 32 fp16 box, 64-byte rows.
+constexpr int kStoreBoxBytes = 32 * 32 * 2;
+
+// The same chunk written back by a TMA store: the lanes stage their rows in a
+// dense 32 x 64-byte box at shared address `buf` (1024-byte aligned) in the
+// 64-byte swizzle the tensor map of C uses (16-byte unit q of row rr at unit
+// q ^ ((rr >> 1) & 3), so the warp's writes fall in distinct banks), then lane
+// 0 issues one store of the box at (col0, row0) and commits it as a bulk
+// group; the store leaves out rows >= M and columns >= N. The caller lets lane
+// 0 wait (bulk_wait_group_read) before `buf` is written again.
+__device__ __forceinline__ void epilogue_chunk_tma(const uint32_t (&r)[32], uint32_t buf, const CUtensorMap* tmC,
+                                                   const __half* __restrict__ bias, int row0, int col0, int N,
+                                                   int gelu, int bias_vec) {
+    const int lane = threadIdx.x & 31;
+    float v[32];
+    epilogue_values(r, v, bias, col0, N, gelu, bias_vec);
+    const uint32_t row_base = buf + static_cast<uint32_t>(lane) * 64;
+    const uint32_t swz = static_cast<uint32_t>((lane >> 1) & 3);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 u;
+        __half2* h = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(v[q * 8 + 2 * e], v[q * 8 + 2 * e + 1]);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row_base + ((static_cast<uint32_t>(q) ^ swz) << 4)),
+                     "r"(u.x), "r"(u.y), "r"(u.z), "r"(u.w)
+                     : "memory");
+    }
+    fence_proxy_async_smem();  // the generic-proxy writes -> visible to the TMA unit
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(tmC, buf, col0, row0);
+        bulk_commit_group();
+    }
 }
 
 }  // namespace tg

@@ -152,8 +152,10 @@ cudaError_t launch_tiled_tma(const TiledArgs& a, const CUtensorMap& tmA, const C
                              int grid, cudaStream_t stream);
 cudaError_t launch_tiled_lsu(const TiledArgs& a, int grid, cudaStream_t stream);
 int tiled_pair_smem_bytes();
-cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, int max_clusters,
-                              cudaStream_t stream);
+// tmC: map of C (32 x 32 box, 64-byte swizzle) to write C by TMA stores, or
+// NULL for ordinary stores.
+cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                              const CUtensorMap* tmC, int max_clusters, cudaStream_t stream);
 cudaError_t launch_splitk(const SplitArgs& a, const CUtensorMap& tmB, const CUtensorMap& tmA,
                           int grid, cudaStream_t stream);
 void w4_pipeline(int m_pad, int* stages, int* act_slots, int* slots);
