@@ -83,6 +83,9 @@ __device__ __forceinline__ Unit unit_of(int u, int split_from) {
     return Unit{split_from + (j >> 1), (j & 1) * (kPairBN / 2), kPairBN / 2};
 }
 
+#ifndef TG_PAIR_SERPENTINE
+#define TG_PAIR_SERPENTINE 1
+#endif
 __device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks, int group_m, int& mb, int& nb) {
     const int per_group = group_m * n_blocks;
     const int g = tile / per_group;
@@ -91,6 +94,9 @@ __device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks
     const int local = tile - g * per_group;
     mb = first_m + local % gsize;
     nb = local / gsize;
+    // serpentine: odd groups walk the columns backwards, so a group starts on the B strips the
+    // previous group used last
+    if (TG_PAIR_SERPENTINE && (g & 1)) nb = n_blocks - 1 - nb;
 }
 
 // kTmaStore: C is written by TMA stores from swizzled staging boxes (C 16-byte

@@ -21,7 +21,10 @@ constexpr int kStages = 4;
 // bytes) take about kGroupBytes: measured on GB300 for 8192^3, groups of
 // 8 x 256 rows (32 MB) read 1.06 GB from HBM per launch, 16 rows 1.25 GB and
 // 32 rows 2.09 GB.
-constexpr int64_t kGroupBytes = 32ll << 20;
+#ifndef TG_GROUP_MB
+#define TG_GROUP_MB 32
+#endif
+constexpr int64_t kGroupBytes = static_cast<int64_t>(TG_GROUP_MB) << 20;
 // Epilogue warps of the tiled kernels: one per TMEM lane quarter (4), or two
 // per quarter each taking half of a tile's 32-column chunks (8). Measured on
 // GB300, 4 is as fast as 8 with erf-GELU and slightly faster without it.
