@@ -242,8 +242,13 @@ tg_status tg_gemm_w4_ex(const void* A, const void* Bq, const void* scales, const
  * Scores, the softmax and the accumulation are fp32 (the exponentials in base
  * 2 with log2(e) folded into the scale; P is rounded to binary16 for the P V
  * product); O is rounded once to binary16. Results agree with the exact
- * definition within |O - ref| <= 1e-2 + 1e-2 |ref| per element. O must not
- * overlap Q, K or V. Stream-ordered; allocates nothing.
+ * definition within |O - ref| <= 1e-2 + 1e-2 |ref| per element, and are
+ * bit-identical from run to run. O must not overlap Q, K or V.
+ * Stream-ordered. Without the causal mask, when the last round of 128-query
+ * blocks would leave at least half of the GPU idle, those blocks are computed
+ * in two key halves whose partial results are merged; their fp32 partials use
+ * the library's per-stream scratch buffer (allocated on first need, grown as
+ * needed, freed by tg_shutdown; TG_ERR_NO_MEMORY if it cannot be allocated).
  */
 tg_status tg_attention_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t S,
                            int64_t H, int64_t D, int causal, tg_stream_t stream);

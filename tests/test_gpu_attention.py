@@ -221,3 +221,29 @@ def test_rescale_at_full_length_sampled_rows(tg):
     ref = oracle.attention(Q, K, V, causal=True, rows=rows)
     _check(got.reshape(-1, w.D)[rows], ref, w.name)
     _status_ok(tg)
+
+
+# ---------------------------------------------------------------- the split last round
+#
+# Without the mask, when the grid's last round of query blocks (two per SM) is at most half
+# full, each of those blocks runs as two CTAs over the two halves of the key blocks, and the
+# second to finish merges the partial outputs, maxima and sums. These shapes make the host
+# split a known number of blocks: 8 query blocks per head, heads chosen so the blocks fill
+# one round of 2 x SMs and leave 16 (the last 16 in launch order).
+
+def _split_heads(per_head_blocks, left_over):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return (2 * sms + left_over) // per_head_blocks
+
+
+@pytest.mark.parametrize("S", [1000, 1024])
+def test_split_last_round_every_element(tg, S):
+    H = _split_heads(8, 16)
+    w = workloads.AttnWorkload(f"split_1x{S}x{H}", 1, S, H, 128, seed=980 + S, k_ramp=0.5)
+    Q, K, V = w.inputs()
+    dQ, dK, dV = Q.cuda(), K.cuda(), V.cuda()
+    got = tg.attention(dQ, dK, dV).cpu().numpy()
+    _check(got, oracle.attention(Q, K, V), w.name)
+    again = tg.attention(dQ, dK, dV).cpu().numpy()  # the merge is symmetric: same bits every time
+    assert np.array_equal(got.view(np.uint16), again.view(np.uint16))
+    _status_ok(tg)

@@ -78,7 +78,11 @@ constexpr int kOffRedMax = kBarDrain + 8;                 // [2 (key-block parit
 constexpr int kOffRedSum = kOffRedMax + 2 * 2 * 128 * 4;  // [2 halves][128 rows] floats
 constexpr int kTmemSlot = kOffRedSum + 2 * 128 * 4;
 constexpr int kAbortSlot = kTmemSlot + 4;
-constexpr int kSmemUsed = kAbortSlot + 4;
+constexpr int kMergeSlot = kAbortSlot + 4;     // split blocks: this CTA merges the two parts
+constexpr int kSmemUsed = kMergeSlot + 4;
+// a split block's part in the scratch: O (128 x 128 fp32, unnormalised), then per row the
+// running maximum (base-2 units) and the sum
+constexpr int kPartFloats = kBM * kD + 2 * kBM;
 constexpr int kSmemAlloc = kSmemUsed + 1024;
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -115,20 +119,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // from L2; within a group, every head's last query block first, then the one before, ...
     // so with the causal mask the longest CTAs start first (and the shortest fill the tail),
     // and the CTAs in flight spread over many heads rather than queueing on one head's blocks
-    const int n_bh = static_cast<int>(gridDim.x) / args.n_qt;
+    // The last n_split query blocks of that order (the last, partial round of the grid) are
+    // each split into two CTAs, one per half of the key blocks, whose partial results the
+    // second to finish merges: CTA n_plain + 2 p + part is part `part` of block n_plain + p.
+    const int n_blocks = args.n_plain + args.n_split;
+    const int split_idx = static_cast<int>(blockIdx.x) - args.n_plain;
+    const int part = split_idx >= 0 ? (split_idx & 1) : -1;
+    const int pair = split_idx >= 0 ? (split_idx >> 1) : 0;
+    const int blk = split_idx >= 0 ? args.n_plain + pair : static_cast<int>(blockIdx.x);
+    const int n_bh = n_blocks / args.n_qt;
     const long long kv_bytes = 4LL * args.S * kD;
     const int gsz = static_cast<int>(max(1LL, min(static_cast<long long>(n_bh), kL2Budget / kv_bytes)));
     const int per_group = gsz * args.n_qt;
-    const int grp = static_cast<int>(blockIdx.x) / per_group;
+    const int grp = blk / per_group;
     const int first = grp * gsz;
     const int this_gsz = min(gsz, n_bh - first);
-    const int local = static_cast<int>(blockIdx.x) - grp * per_group;
+    const int local = blk - grp * per_group;
     const int qt = args.n_qt - 1 - local / this_gsz;
     const int bh = first + local % this_gsz;
     const int h = bh % args.H;
     const int b = bh / args.H;
     const int n_kt = (args.S + kBN - 1) / kBN;
-    const int j_last = args.causal ? min(qt, n_kt - 1) : n_kt - 1;  // key blocks 0..j_last
+    // key blocks j_first..j_last (a split block's halves: [0, n_kt / 2) and [n_kt / 2, n_kt))
+    const int j_first = part == 1 ? n_kt / 2 : 0;
+    const int j_last = part == 0 ? n_kt / 2 - 1 : (args.causal ? min(qt, n_kt - 1) : n_kt - 1);
 
     const uint32_t bar_q = sbase + kBarQ, k_full = sbase + kBarKFull, k_empty = sbase + kBarKEmpty;
     const uint32_t v_full = sbase + kBarVFull, v_empty = sbase + kBarVEmpty, s_full = sbase + kBarSFull;
@@ -136,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const uint32_t o_done = sbase + kBarODone, drain_bar = sbase + kBarDrain;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortSlot);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
+    volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + kMergeSlot);
 
     if (threadIdx.x == 0) {
         mbar_init(bar_q, 1);
@@ -171,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             for (int i = 0; i < 2; ++i)
                 tma_load_4d(sbase + kOffQ + i * kBoxBytes, &tmQ, bar_q, 64 * i, h, qt * kBM, b);
             int k_issued = 0, v_issued = 0;
-            for (int j = 0; j <= j_last; ++j) {
-                const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+            for (int j = j_first; j <= j_last; ++j) {
+                const uint32_t ph = static_cast<uint32_t>(j - j_first) & 1u;
                 if (!wait_phase_sleep(k_empty, ph ^ 1, wc, kSiteProducerEmpty, 64)) break;
                 mbar_arrive_expect_tx(k_full, kTileBytes);
                 for (int i = 0; i < 2; ++i)
@@ -195,12 +210,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const uint32_t idesc_s = idesc_f16_f32(kBM, kBN, /*a_mn_major=*/false, /*b_mn_major=*/false);
             const uint32_t idesc_o = idesc_f16_f32(kBM, kD, /*a_mn_major=*/false, /*b_mn_major=*/true);
             bool ok = wait_phase(bar_q, 0, wc, kSiteMmaFull);
-            for (int j = 0; ok && j <= j_last; ++j) {
-                const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+            for (int j = j_first; ok && j <= j_last; ++j) {
+                const uint32_t ph = static_cast<uint32_t>(j - j_first) & 1u;
                 // S_j = Q K_j^T (both operands K-major, d contiguous, two 64-column boxes); it
                 // overwrites P_{j-1}, so O += P_{j-1} V_{j-1} must have completed
                 if (!wait_phase(k_full, ph, wc, kSiteMmaFull) ||
-                    (j > 0 && !wait_phase(o_done, ph ^ 1, wc, kSiteMmaAccEmpty))) {
+                    (j > j_first && !wait_phase(o_done, ph ^ 1, wc, kSiteMmaAccEmpty))) {
                     ok = false;
                     break;
                 }
@@ -227,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                                         static_cast<uint64_t>((kk * 2048) >> 4);
                     // keys 64 g .. 64 g + 63 (softmax half g) are P columns 64 g .. 64 g + 31
                     const uint32_t a_col = kColP + (kk >> 2) * 64 + (kk & 3) * 8;
-                    mma_f16_tmem_a(tmem_base + kColO, tmem_base + a_col, bd, idesc_o, (j != 0) || (kk != 0));
+                    mma_f16_tmem_a(tmem_base + kColO, tmem_base + a_col, bd, idesc_o, (j != j_first) || (kk != 0));
                 };
                 pv_step(0);
                 pv_step(1);
@@ -267,8 +282,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int limit = args.causal ? min(args.S, q_pos + 1) : args.S;  // visible keys: < limit
         float m_run = 0.0f, l_run = 0.0f;
         bool ok = true;
-        for (int j = 0; j <= j_last; ++j) {
-            const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+        for (int j = j_first; j <= j_last; ++j) {
+            const uint32_t ph = static_cast<uint32_t>(j - j_first) & 1u;
             // a wait that gave up still reads the scores (allocated columns: harmless values) and
             // reaches the barrier of the maximum exchange, where every softmax warp learns of it and
             // all stop together, so no named barrier ever waits for a thread that has left
@@ -300,16 +315,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             acc[1] = fmax3(acc[1], score(62), score(63));
             float mx = fmaxf(fmax3(acc[0], acc[1], acc[2]), acc[3]);
             // the row maximum over both halves
-            red_max[(j & 1) * 256 + g * 128 + row] = mx;
+            red_max[ph * 256 + g * 128 + row] = mx;
             if (named_barrier_or(1, kSoftmaxThreads, !ok)) {
                 ok = false;
                 break;
             }
-            mx = fmaxf(mx, red_max[(j & 1) * 256 + (g ^ 1) * 128 + row]);
+            mx = fmaxf(mx, red_max[ph * 256 + (g ^ 1) * 128 + row]);
             const float m_tile = mx * scale;
             float alpha = 1.0f;
             bool rescale = false;
-            if (j == 0) {
+            if (j == j_first) {
                 m_run = m_tile;
             } else if (m_tile > m_run + kRescaleLog2) {
                 alpha = ex2_approx(m_run - m_tile);
@@ -336,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 // this half's O columns *= alpha before the first hand-off: O holds
                 // P_{j-1} V_{j-1} (S_j was issued after it completed) and O += P_j V_j starts
                 // at the first hand-off; both halves of a row take the same decision
-                if (hc == 0 && j >= 1 && __any_sync(0xFFFFFFFFu, rescale)) {
+                if (hc == 0 && j > j_first && __any_sync(0xFFFFFFFFu, rescale)) {
 #pragma unroll 1
                     for (int c = 0; c < 2; ++c) {
                         uint32_t o[32];
@@ -356,27 +371,87 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const float sum = s2.x + s2.y;
             l_run = l_run * alpha + sum;
         }
-        // O / (sum of both halves), written as fp16 once the last O += P V has landed
+        // O / (sum of both halves), written as fp16 once the last O += P V has landed; a split
+        // block's part first publishes its unnormalised O, running maximum and sum
         if (!named_barrier_or(1, kSoftmaxThreads, !ok)) {
             red_sum[g * 128 + row] = l_run;
-            const bool done = wait_phase_sleep(o_done, static_cast<uint32_t>(j_last) & 1u, wc, kSiteEpilogueAccFull, 64);
+            const bool done = wait_phase_sleep(o_done, static_cast<uint32_t>(j_last - j_first) & 1u, wc,
+                                               kSiteEpilogueAccFull, 64);
             if (!named_barrier_or(1, kSoftmaxThreads, !done)) {
                 tc_fence_after_sync();
-                const float inv = 1.0f / (l_run + red_sum[(g ^ 1) * 128 + row]);
+                const float l_tot = __fadd_rn(l_run, red_sum[(g ^ 1) * 128 + row]);
                 __half* dst = args.O + ((static_cast<int64_t>(b) * args.S + q_pos) * args.H + h) * kD + g * 64;
+                float inv = 1.0f / l_tot, a_own = 1.0f, a_oth = 0.0f;
+                const float* other = nullptr;
+                bool store = true;
+                if (part >= 0) {
+                    float* mine = args.ws + static_cast<int64_t>(2 * pair + part) * kPartFloats;
 #pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t o[32];
-                    tmem_ld_32x32b_x32(lane_base + kColO + g * 64 + c * 32, o);
-                    tmem_ld_wait();
-                    if (q_pos < args.S) {
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t o[32];
+                        tmem_ld_32x32b_x32(lane_base + kColO + g * 64 + c * 32, o);
+                        tmem_ld_wait();
+                        float4* w4 = reinterpret_cast<float4*>(mine + row * kD + g * 64 + c * 32);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            reinterpret_cast<uint4*>(dst + c * 32)[q] = make_uint4(
-                                pack_half2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
-                                pack_half2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
-                                pack_half2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
-                                pack_half2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
+                        for (int q = 0; q < 8; ++q)
+                            __stcg(w4 + q, make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                                                       __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3])));
+                    }
+                    if (g == 0) {
+                        __stcg(mine + kBM * kD + row, m_run);
+                        __stcg(mine + kBM * kD + kBM + row, l_tot);
+                    }
+                    // the second part of the pair to get here merges both
+                    __threadfence();
+                    named_barrier_sync(1, kSoftmaxThreads);
+                    if (threadIdx.x == 64) *merge_flag = atomicAdd(args.counters + pair, 1u) == 1u ? 1 : 0;
+                    named_barrier_sync(1, kSoftmaxThreads);
+                    store = *merge_flag != 0;
+                    if (store) {
+                        __threadfence();
+                        other = args.ws + static_cast<int64_t>(2 * pair + (part ^ 1)) * kPartFloats;
+                        const float m_oth = __ldcg(other + kBM * kD + row);
+                        const float l_oth = __ldcg(other + kBM * kD + kBM + row);
+                        // symmetric in the two parts (no fused operations), so the result does not
+                        // depend on which part finished first
+                        const float m_max = fmaxf(m_run, m_oth);
+                        a_own = ex2_approx(m_run - m_max);
+                        a_oth = ex2_approx(m_oth - m_max);
+                        inv = 1.0f / __fadd_rn(__fmul_rn(l_tot, a_own), __fmul_rn(l_oth, a_oth));
+                        if (threadIdx.x == 64) atomicExch(args.counters + pair, 0u);
+                    }
+                }
+                if (store) {
+#pragma unroll 1
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t o[32];
+                        tmem_ld_32x32b_x32(lane_base + kColO + g * 64 + c * 32, o);
+                        tmem_ld_wait();
+                        float v[32];
+                        if (other != nullptr) {
+                            const float4* r4 = reinterpret_cast<const float4*>(other + row * kD + g * 64 + c * 32);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 x = __ldcg(r4 + q);
+                                const float xo[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    v[4 * q + e] = __fmul_rn(__fadd_rn(__fmul_rn(__uint_as_float(o[4 * q + e]), a_own),
+                                                                       __fmul_rn(xo[e], a_oth)),
+                                                             inv);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv;
+                        }
+                        if (q_pos < args.S) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                reinterpret_cast<uint4*>(dst + c * 32)[q] =
+                                    make_uint4(pack_half2(v[8 * q], v[8 * q + 1]), pack_half2(v[8 * q + 2], v[8 * q + 3]),
+                                               pack_half2(v[8 * q + 4], v[8 * q + 5]),
+                                               pack_half2(v[8 * q + 6], v[8 * q + 7]));
+                        }
                     }
                 }
             }
@@ -394,6 +469,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 }  // namespace
 
 int attn_smem_bytes() { return kSmemAlloc; }
+
+int attn_part_floats() { return kPartFloats; }
 
 cudaError_t launch_attn(const AttnArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                         int grid, cudaStream_t stream) {

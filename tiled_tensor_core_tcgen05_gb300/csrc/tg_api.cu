@@ -892,6 +892,12 @@ extern "C" tg_status tg_gemm_w4(const void* A, const void* Bq, const void* scale
 // ---------------------------------------------------------------------------
 // tg_attention_fwd: FlashAttention forward on (batch, sequence, head, dim).
 
+// Split the last, partial round of query blocks into key halves (non-causal).
+#ifndef TG_ATTN_SPLIT_TAIL
+#define TG_ATTN_SPLIT_TAIL 1
+#endif
+constexpr bool kAttnSplitTail = TG_ATTN_SPLIT_TAIL != 0;
+
 extern "C" tg_status tg_attention_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t S,
                                       int64_t H, int64_t D, int causal, tg_stream_t stream_) {
     t_last_error.clear();
@@ -910,23 +916,41 @@ extern "C" tg_status tg_attention_fwd(const void* Q, const void* K, const void* 
     if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) || overlaps(O, bytes, V, bytes))
         return fail(TG_ERR_INVALID_ARG, "O overlaps an input");
     const int64_t n_qt = (S + 127) / 128;
-    if (B * H * n_qt > 0x7FFFFFFFll) return fail(TG_ERR_INVALID_ARG, "too many query blocks");
+    if (B * H * n_qt > 0x3FFFFFFFll) return fail(TG_ERR_INVALID_ARG, "too many query blocks");
 
     std::lock_guard<std::mutex> lock(g_mu);
     int dev = 0;
     tg_status st = current_device(&dev);
     if (st != TG_OK) return st;
+    DeviceState& ds = g_dev[dev];
     AttnArgs a{};
     a.O = static_cast<__half*>(O);
     a.S = (int)S; a.H = (int)H; a.causal = causal;
     a.n_qt = (int)n_qt;
     a.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
-    a.wd = watchdog(g_dev[dev]);
+    a.wd = watchdog(ds);
+    // Query blocks run two per SM. Without the mask every block costs the same, so when the
+    // last round is at most half full its blocks are split into key halves (two CTAs each),
+    // which fills that round and halves its length.
+    const int64_t n_blocks = B * H * n_qt;
+    const int64_t slots = 2LL * ds.sm_count;
+    const int64_t rest = n_blocks % slots;
+    a.n_plain = static_cast<int>(n_blocks);
+    if (kAttnSplitTail && !causal && n_blocks >= slots && rest > 0 && 2 * rest <= slots && (S + 127) / 128 >= 2) {
+        Scratch* sc = nullptr;
+        st = ensure_scratch(ds, stream, static_cast<size_t>(rest) * 2 * attn_part_floats() * sizeof(float),
+                            static_cast<size_t>(rest), &sc);
+        if (st != TG_OK) return st;
+        a.n_plain = static_cast<int>(n_blocks - rest);
+        a.n_split = static_cast<int>(rest);
+        a.ws = sc->ws;
+        a.counters = sc->counters;
+    }
     CUtensorMap tmQ, tmK, tmV;
     if ((st = make_map_bshd(&tmQ, Q, B, S, H, D)) != TG_OK) return st;
     if ((st = make_map_bshd(&tmK, K, B, S, H, D)) != TG_OK) return st;
     if ((st = make_map_bshd(&tmV, V, B, S, H, D)) != TG_OK) return st;
-    cudaError_t e = launch_attn(a, tmQ, tmK, tmV, (int)(B * H * n_qt), stream);
+    cudaError_t e = launch_attn(a, tmQ, tmK, tmV, a.n_plain + 2 * a.n_split, stream);
     if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
     return TG_OK;
 }

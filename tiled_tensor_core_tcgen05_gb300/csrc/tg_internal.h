@@ -135,6 +135,10 @@ struct AttnArgs {
     int causal;
     int n_qt;            // 128-query blocks per (batch, head)
     float scale_log2;    // log2(e) / sqrt(dim): scores in base-2 exponent units
+    int n_plain;         // query blocks computed by one CTA each (the first in launch order)
+    int n_split;         // query blocks after those, each computed by two CTAs (key halves)
+    float* ws;           // n_split pairs of parts (attn_part_floats() floats each), or null
+    unsigned int* counters;  // n_split arrival counters, zero between launches
     Watchdog wd;
 };
 
@@ -167,6 +171,7 @@ cudaError_t launch_w4(const W4Args& a, const CUtensorMap& tmBq, const CUtensorMa
                       int grid, cudaStream_t stream);
 cudaError_t launch_softmax(const __half* X, __half* Y, int M, int N, bool vec, int sm_count, cudaStream_t stream);
 int attn_smem_bytes();
+int attn_part_floats();
 cudaError_t launch_attn(const AttnArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                         int grid, cudaStream_t stream);
 cudaError_t launch_bias_gelu(__half* C, const __half* bias, int64_t M, int64_t N, int gelu, bool vec8, int sm_count,
