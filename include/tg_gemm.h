@@ -280,6 +280,10 @@ tg_status tg_softmax_rows(const void* X, void* Y, int64_t M, int64_t N, tg_strea
  */
 tg_status tg_device_status(tg_stream_t stream, int* where);
 
+/* tg_device_status(stream, NULL): the same synchronising check, for callers
+ * that need only the status. */
+tg_status tg_debug_status(tg_stream_t stream);
+
 /* Watchdog limit for every bounded wait, in ns (default 2e9; 0 restores it). */
 tg_status tg_set_watchdog_ns(uint64_t ns);
 

@@ -30,7 +30,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NO_MEMOR
 EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_gemm_w4_ex",
            "tg_attention_fwd",
            "tg_softmax_rows", "tg_bias_gelu",
-           "tg_device_status",
+           "tg_device_status", "tg_debug_status",
            "tg_set_watchdog_ns",
            "tg_debug_skip_first_arrive", "tg_status_string", "tg_last_error", "tg_version",
            "tg_ring_bytes", "tg_shutdown")
@@ -51,6 +51,7 @@ _lib.tg_attention_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i
 _lib.tg_softmax_rows.argtypes = [_vp, _vp, _i64, _i64, _vp]
 _lib.tg_bias_gelu.argtypes = [_vp, _vp, _i64, _i64, _int, _vp]
 _lib.tg_device_status.argtypes = [_vp, ctypes.POINTER(_int)]
+_lib.tg_debug_status.argtypes = [_vp]
 _lib.tg_set_watchdog_ns.argtypes = [_u64]
 _lib.tg_debug_skip_first_arrive.argtypes = [_int]
 _lib.tg_status_string.argtypes = [_int]
@@ -65,7 +66,7 @@ _lib.tg_shutdown.restype = None
 for _name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_gemm_w4_ex",
               "tg_attention_fwd",
               "tg_softmax_rows", "tg_bias_gelu",
-              "tg_device_status",
+              "tg_device_status", "tg_debug_status",
               "tg_set_watchdog_ns",
               "tg_debug_skip_first_arrive", "tg_version"):
     getattr(_lib, _name).restype = _int
@@ -177,6 +178,11 @@ def tg_device_status(stream: int | None) -> tuple[int, int]:
     where = _int(0)
     st = _lib.tg_device_status(stream, ctypes.byref(where))
     return st, where.value
+
+
+def tg_debug_status(stream: int | None) -> int:
+    """Synchronises `stream` and returns (and clears) the kernels' watchdog status."""
+    return _lib.tg_debug_status(stream)
 
 
 def tg_set_watchdog_ns(ns: int) -> None:

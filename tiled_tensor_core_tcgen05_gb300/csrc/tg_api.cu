@@ -643,6 +643,8 @@ tg_status tg_device_status(tg_stream_t stream_, int* where) {
     return fail(TG_ERR_TIMEOUT, "a kernel wait expired (site %d)", v);
 }
 
+tg_status tg_debug_status(tg_stream_t stream) { return tg_device_status(stream, nullptr); }
+
 tg_status tg_bias_gelu(void* C, const void* bias, int64_t M, int64_t N, int epilogue, tg_stream_t stream_) {
     t_last_error.clear();
     const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
