@@ -62,7 +62,9 @@ typedef enum {
     TG_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not compute capability 10.3 */
     TG_ERR_CUDA = 3,               /* a CUDA runtime/driver call or a launch failed */
     TG_ERR_TIMEOUT = 4,            /* a kernel's bounded wait expired (see tg_device_status) */
-    TG_ERR_NO_MEMORY = 5           /* the library could not allocate its scratch buffer */
+    TG_ERR_NO_MEMORY = 5,          /* the library could not allocate its scratch buffer */
+    TG_ERR_BOUNDS = 6              /* a device-side bounds check failed (debug builds only,
+                                      see tg_debug_build) */
 } tg_status;
 
 /* Kernel selection for tg_gemm_ex (tg_gemm always uses TG_KERNEL_AUTO). */
@@ -272,7 +274,7 @@ tg_status tg_softmax_rows(const void* X, void* Y, int64_t M, int64_t N, tg_strea
 /*
  * Synchronises `stream`, then reports (and clears) the device-side status word
  * that kernels set when one of their bounded waits expires: TG_OK or
- * TG_ERR_TIMEOUT. `*where` (if not NULL) receives the code of the wait that
+ * TG_ERR_TIMEOUT (or, in debug builds, TG_ERR_BOUNDS for a failed bounds check). `*where` (if not NULL) receives the code of the wait that
  * expired first (0 if none). Every wait inside the kernels gives up after the
  * watchdog limit (tg_set_watchdog_ns) instead of spinning forever; the kernel
  * then drains its in-flight copies, frees its tensor memory and exits, leaving
@@ -294,6 +296,24 @@ tg_status tg_set_watchdog_ns(uint64_t ns);
  * from tg_device_status. Off by default; has no effect on other kernels.
  */
 tg_status tg_debug_skip_first_arrive(int on);
+
+/*
+ * 1 if this library was compiled with TG_DEBUG=1, else 0. Debug builds check,
+ * on the device, that every scratch-buffer, arrival-counter and TMA-store
+ * coordinate a kernel computes lies inside its buffer (and, for stores, on a
+ * 16-byte boundary and not negative); a failed check is recorded in the status
+ * word that tg_device_status reads (TG_ERR_BOUNDS) and the access is skipped,
+ * so nothing faults. In normal builds the checks are compiled away.
+ */
+int tg_debug_build(void);
+
+/*
+ * Test hook for the bounds checks of debug builds: while `floats` > 0, kernels
+ * are told that their scratch holds at most that many floats (the buffer itself
+ * is unchanged), so a check fails as soon as a kernel's partial sums reach
+ * beyond it. 0 restores the real sizes. No effect in normal builds.
+ */
+tg_status tg_debug_bounds_limit(int64_t floats);
 
 /* Static description of a status code. */
 const char* tg_status_string(int status);

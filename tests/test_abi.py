@@ -191,3 +191,12 @@ def test_w4_ex_rejects_an_unknown_format_and_shares_the_checks(tg):
         tg.tg_gemm_w4_ex(0x10000, 0x20000000, 0x30000000, None, 0x40000000, 16, 64, 192, 0, tg.W4_FP4_E2M1, 0, None)
     assert ei.value.status == tg.ERR_INVALID_ARG and "K % 128" in str(ei.value)
     tg.tg_gemm_w4_ex(None, None, None, None, None, 0, 64, 256, 0, tg.W4_FP4_E2M1, 0, None)
+
+
+def test_release_build_has_no_device_checks_and_the_hook_validates(tg):
+    assert tg.tg_debug_build() == 0
+    tg.tg_debug_bounds_limit(0)
+    with pytest.raises(tg.TgError) as ei:
+        tg.tg_debug_bounds_limit(-1)
+    assert ei.value.status == tg.ERR_INVALID_ARG
+    assert "BOUNDS" in tg.tg_status_string(tg.ERR_BOUNDS)

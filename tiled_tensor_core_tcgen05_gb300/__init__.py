@@ -24,7 +24,7 @@ EPI_NONE, EPI_GELU = 0, 1
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024  # TG_NOALLOC_SCRATCH_BYTES
 KERNEL_AUTO, KERNEL_TILED_TMA, KERNEL_TILED_LSU, KERNEL_SPLITK, KERNEL_TILED_PAIR = 0, 1, 2, 3, 4
 W4_INT4, W4_FP4_E2M1 = 0, 1
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NO_MEMORY = range(6)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NO_MEMORY, ERR_BOUNDS = range(7)
 
 # every symbol include/tg_gemm.h declares
 EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_gemm_w4_ex",
@@ -32,44 +32,54 @@ EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", 
            "tg_softmax_rows", "tg_bias_gelu",
            "tg_device_status", "tg_debug_status",
            "tg_set_watchdog_ns",
-           "tg_debug_skip_first_arrive", "tg_status_string", "tg_last_error", "tg_version",
+           "tg_debug_skip_first_arrive", "tg_debug_bounds_limit", "tg_debug_build", "tg_status_string",
+           "tg_last_error", "tg_version",
            "tg_ring_bytes", "tg_shutdown")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
                       "(or python tiled_tensor_core_tcgen05_gb300/build.py); there is no fallback path")
 
-_lib = ctypes.CDLL(LIB_PATH)
 _vp, _i64, _int, _u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64
-_lib.tg_gemm.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
-_lib.tg_gemm_ex.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp]
-_lib.tg_gemm_staged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
-_lib.tg_gemm_splitk_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
-_lib.tg_gemm_w4.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
-_lib.tg_gemm_w4_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp]
-_lib.tg_attention_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _vp]
-_lib.tg_softmax_rows.argtypes = [_vp, _vp, _i64, _i64, _vp]
-_lib.tg_bias_gelu.argtypes = [_vp, _vp, _i64, _i64, _int, _vp]
-_lib.tg_device_status.argtypes = [_vp, ctypes.POINTER(_int)]
-_lib.tg_debug_status.argtypes = [_vp]
-_lib.tg_set_watchdog_ns.argtypes = [_u64]
-_lib.tg_debug_skip_first_arrive.argtypes = [_int]
-_lib.tg_status_string.argtypes = [_int]
-_lib.tg_status_string.restype = ctypes.c_char_p
-_lib.tg_last_error.argtypes = []
-_lib.tg_last_error.restype = ctypes.c_char_p
-_lib.tg_version.argtypes = []
-_lib.tg_ring_bytes.argtypes = [_int]
-_lib.tg_ring_bytes.restype = _i64
-_lib.tg_shutdown.argtypes = []
-_lib.tg_shutdown.restype = None
-for _name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_gemm_w4_ex",
-              "tg_attention_fwd",
-              "tg_softmax_rows", "tg_bias_gelu",
-              "tg_device_status", "tg_debug_status",
-              "tg_set_watchdog_ns",
-              "tg_debug_skip_first_arrive", "tg_version"):
-    getattr(_lib, _name).restype = _int
+
+
+def bind(path: str) -> ctypes.CDLL:
+    """Load a build of the library (this package's, or its debug build
+    libtg_gemm_debug.so) with every entry point's C signature set."""
+    lib = ctypes.CDLL(path)
+    lib.tg_gemm.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
+    lib.tg_gemm_ex.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp]
+    lib.tg_gemm_staged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
+    lib.tg_gemm_splitk_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
+    lib.tg_gemm_w4.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
+    lib.tg_gemm_w4_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp]
+    lib.tg_attention_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _vp]
+    lib.tg_softmax_rows.argtypes = [_vp, _vp, _i64, _i64, _vp]
+    lib.tg_bias_gelu.argtypes = [_vp, _vp, _i64, _i64, _int, _vp]
+    lib.tg_device_status.argtypes = [_vp, ctypes.POINTER(_int)]
+    lib.tg_debug_status.argtypes = [_vp]
+    lib.tg_set_watchdog_ns.argtypes = [_u64]
+    lib.tg_debug_skip_first_arrive.argtypes = [_int]
+    lib.tg_debug_bounds_limit.argtypes = [_i64]
+    lib.tg_debug_build.argtypes = []
+    lib.tg_status_string.argtypes = [_int]
+    lib.tg_status_string.restype = ctypes.c_char_p
+    lib.tg_last_error.argtypes = []
+    lib.tg_last_error.restype = ctypes.c_char_p
+    lib.tg_version.argtypes = []
+    lib.tg_ring_bytes.argtypes = [_int]
+    lib.tg_ring_bytes.restype = _i64
+    lib.tg_shutdown.argtypes = []
+    lib.tg_shutdown.restype = None
+    for name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_gemm_w4_ex",
+                 "tg_attention_fwd", "tg_softmax_rows", "tg_bias_gelu", "tg_device_status", "tg_debug_status",
+                 "tg_set_watchdog_ns", "tg_debug_skip_first_arrive", "tg_debug_bounds_limit", "tg_debug_build",
+                 "tg_version"):
+        getattr(lib, name).restype = _int
+    return lib
+
+
+_lib = bind(LIB_PATH)
 
 
 class TgError(RuntimeError):
@@ -191,6 +201,16 @@ def tg_set_watchdog_ns(ns: int) -> None:
 
 def tg_debug_skip_first_arrive(on: bool) -> None:
     _check(_lib.tg_debug_skip_first_arrive(1 if on else 0))
+
+
+def tg_debug_bounds_limit(floats: int) -> None:
+    """Debug builds: make the device-side bounds checks treat scratch as `floats` long (0: real size)."""
+    _check(_lib.tg_debug_bounds_limit(floats))
+
+
+def tg_debug_build() -> int:
+    """1 if the loaded library was compiled with its device-side bounds checks, else 0."""
+    return _lib.tg_debug_build()
 
 
 def tg_status_string(status: int) -> str:

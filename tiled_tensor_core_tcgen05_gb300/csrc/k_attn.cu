@@ -385,26 +385,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const float* other = nullptr;
                 bool store = true;
                 if (part >= 0) {
-                    float* mine = args.ws + static_cast<int64_t>(2 * pair + part) * kPartFloats;
+                    // in debug builds a part whose scratch lies outside the buffer writes nothing and
+                    // merges nothing (the failed check is reported)
+                    const bool ws_ok = dbg_check(dbg_in(static_cast<int64_t>(2 * pair) * kPartFloats, 2 * kPartFloats,
+                                                        args.wd.ws_floats) &&
+                                                     dbg_in(pair, 1, args.wd.n_counters),
+                                                 args.wd);
+                    float* mine = args.ws + (ws_ok ? static_cast<int64_t>(2 * pair + part) * kPartFloats : 0);
 #pragma unroll 1
                     for (int c = 0; c < 2; ++c) {
                         uint32_t o[32];
                         tmem_ld_32x32b_x32(lane_base + kColO + g * 64 + c * 32, o);
                         tmem_ld_wait();
+                        if (!ws_ok) continue;
                         float4* w4 = reinterpret_cast<float4*>(mine + row * kD + g * 64 + c * 32);
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
                             __stcg(w4 + q, make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
                                                        __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3])));
                     }
-                    if (g == 0) {
+                    if (g == 0 && ws_ok) {
                         __stcg(mine + kBM * kD + row, m_run);
                         __stcg(mine + kBM * kD + kBM + row, l_tot);
                     }
                     // the second part of the pair to get here merges both
                     __threadfence();
                     named_barrier_sync(1, kSoftmaxThreads);
-                    if (threadIdx.x == 64) *merge_flag = atomicAdd(args.counters + pair, 1u) == 1u ? 1 : 0;
+                    if (threadIdx.x == 64) *merge_flag = ws_ok && atomicAdd(args.counters + pair, 1u) == 1u ? 1 : 0;
                     named_barrier_sync(1, kSoftmaxThreads);
                     store = *merge_flag != 0;
                     if (store) {

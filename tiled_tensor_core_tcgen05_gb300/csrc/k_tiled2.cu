@@ -268,7 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (lane == 0 && nstore >= 2) bulk_wait_group_read<1>();
                     __syncwarp();
                     epilogue_chunk_tma(r, smem_u32(stage) + (nstore & 1) * kStoreBoxBytes, &tmC, args.bias,
-                                       row - lane, n0 + c * 32, args.N, args.gelu, args.bias_vec);
+                                       row - lane, n0 + c * 32, args.N, args.gelu, args.bias_vec, args.wd);
                     ++nstore;
                 } else {
                     epilogue_chunk(r, stage, args.C, args.bias, row - lane, n0 + c * 32, args.M, args.N, args.gelu,

@@ -401,7 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
                     // partials as [slice][m_pad][N] fp32: this thread's 32 columns are 128 contiguous bytes
-                    float* wp = args.ws + (static_cast<int64_t>(sp) * args.m_pad + row) * args.N + col0;
+                    const int64_t off = (static_cast<int64_t>(sp) * args.m_pad + row) * args.N + col0;
+                    if (!dbg_check(dbg_in(off, min(32, args.N - col0), args.wd.ws_floats), args.wd)) continue;
+                    float* wp = args.ws + off;
                     if (col0 + 32 <= args.N) {
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
@@ -418,8 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __threadfence();
                 named_barrier_sync(1, kEpiThreads);
                 if (ept == 0) {
-                    const unsigned int prev = atomicAdd(args.counters + nt, 1u);
-                    *last_flag = (prev == static_cast<unsigned int>(args.splits - 1)) ? 1 : 0;
+                    *last_flag = 0;
+                    if (dbg_check(dbg_in(nt, 1, args.wd.n_counters), args.wd)) {
+                        const unsigned int prev = atomicAdd(args.counters + nt, 1u);
+                        *last_flag = (prev == static_cast<unsigned int>(args.splits - 1)) ? 1 : 0;
+                    }
                 }
                 named_barrier_sync(1, kEpiThreads);
                 if (*last_flag) {
@@ -447,10 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                     for (int i = 0; i < 4; ++i) {
                                         const int m = m0 + 2 * i;
-                                        p[qq][i] = (q0 + qq < args.splits && m < args.M)
-                                                       ? __ldcg(reinterpret_cast<const float4*>(
-                                                             args.ws + (q0 + qq) * slice_stride +
-                                                             static_cast<int64_t>(m) * args.N + n))
+                                        const int64_t off =
+                                            (q0 + qq) * slice_stride + static_cast<int64_t>(m) * args.N + n;
+                                        p[qq][i] = (q0 + qq < args.splits && m < args.M &&
+                                                    dbg_check(dbg_in(off, 4, args.wd.ws_floats), args.wd))
+                                                       ? __ldcg(reinterpret_cast<const float4*>(args.ws + off))
                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                                     }
 #pragma unroll

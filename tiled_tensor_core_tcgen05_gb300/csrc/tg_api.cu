@@ -23,6 +23,7 @@ using namespace tg;
 thread_local std::string t_last_error;
 std::atomic<uint64_t> g_watchdog_ns{2000000000ull};
 std::atomic<int> g_skip_first_arrive{0};
+std::atomic<int64_t> g_bounds_limit{0};  // debug builds: cap on the scratch floats the checks allow
 
 // First expired wait of any kernel since the last tg_device_status (0 = none).
 __device__ int g_status_word;
@@ -244,8 +245,19 @@ int vec_width(const void* p, int64_t ld) {
     return 1;
 }
 
+// The kernels' watchdog settings; no scratch until the caller grants some (debug_limits).
 Watchdog watchdog(const DeviceState& d) {
-    return Watchdog{d.status_ptr, g_watchdog_ns.load(), g_skip_first_arrive.load()};
+    return Watchdog{d.status_ptr, g_watchdog_ns.load(), g_skip_first_arrive.load(), 0, 0};
+}
+
+// The scratch a kernel may touch, for the bounds checks of debug builds (capped by the
+// tg_debug_bounds_limit test hook).
+void debug_limits(Watchdog& wd, size_t ws_bytes, size_t n_counters) {
+    int64_t floats = static_cast<int64_t>(ws_bytes / sizeof(float));
+    const int64_t cap = g_bounds_limit.load();
+    if (cap > 0 && cap < floats) floats = cap;
+    wd.ws_floats = floats;
+    wd.n_counters = static_cast<int64_t>(n_counters);
 }
 
 // Tile rows per rasterisation group: A strips of about kGroupBytes, at least 1,
@@ -375,6 +387,7 @@ tg_status run_splitk(DeviceState& d, const __half* A, const __half* B, const __h
         if (st != TG_OK) return st;
         a.ws = sc->ws;
         a.counters = sc->counters;
+        debug_limits(a.wd, sc->ws_bytes, sc->n_counters);
     }
     return splitk_launch(d, a, stream);
 }
@@ -640,8 +653,17 @@ tg_status tg_device_status(tg_stream_t stream_, int* where) {
         if (kv.second.counters) cudaMemset(kv.second.counters, 0, kv.second.n_counters * sizeof(unsigned int));
     cudaDeviceSynchronize();
     if (where) *where = v;
+    if (v == kSiteBounds) return fail(TG_ERR_BOUNDS, "a device-side bounds check failed (debug build)");
     return fail(TG_ERR_TIMEOUT, "a kernel wait expired (site %d)", v);
 }
+
+tg_status tg_debug_bounds_limit(int64_t floats) {
+    if (floats < 0) return fail(TG_ERR_INVALID_ARG, "the limit must be >= 0, got %lld", (long long)floats);
+    g_bounds_limit.store(floats);
+    return TG_OK;
+}
+
+int tg_debug_build(void) { return TG_DEBUG ? 1 : 0; }
 
 tg_status tg_debug_status(tg_stream_t stream) { return tg_device_status(stream, nullptr); }
 
@@ -683,6 +705,7 @@ const char* tg_status_string(int s) {
         case TG_ERR_CUDA: return "TG_ERR_CUDA: a CUDA call failed";
         case TG_ERR_TIMEOUT: return "TG_ERR_TIMEOUT: a kernel wait expired";
         case TG_ERR_NO_MEMORY: return "TG_ERR_NO_MEMORY: scratch allocation failed";
+        case TG_ERR_BOUNDS: return "TG_ERR_BOUNDS: a device-side bounds check failed";
         default: return "unknown tg_status";
     }
 }
@@ -792,6 +815,7 @@ extern "C" tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const 
         if (e != cudaSuccess) return cuda_fail(e, "clear static split-K counters");
         a.counters = reinterpret_cast<unsigned int*>(g_noalloc_ptr[dev]);
         a.ws = reinterpret_cast<float*>(g_noalloc_ptr[dev] + counter_bytes);
+        debug_limits(a.wd, TG_NOALLOC_SCRATCH_BYTES - counter_bytes, counter_bytes / sizeof(unsigned int));
     }
     return splitk_launch(d, a, stream);
 }
@@ -870,6 +894,7 @@ extern "C" tg_status tg_gemm_w4_ex(const void* A, const void* Bq, const void* sc
             if (st != TG_OK) return st;
             a.ws = sc->ws;
             a.counters = sc->counters;
+            debug_limits(a.wd, sc->ws_bytes, sc->n_counters);
         }
         w.Bq = static_cast<const uint8_t*>(Bq);
         w.scales = static_cast<const __half*>(scales);
@@ -947,6 +972,7 @@ extern "C" tg_status tg_attention_fwd(const void* Q, const void* K, const void* 
         a.n_split = static_cast<int>(rest);
         a.ws = sc->ws;
         a.counters = sc->counters;
+        debug_limits(a.wd, sc->ws_bytes, sc->n_counters);
     }
     CUtensorMap tmQ, tmK, tmV;
     if ((st = make_map_bshd(&tmQ, Q, B, S, H, D)) != TG_OK) return st;

@@ -79,6 +79,25 @@ __device__ __forceinline__ bool wait_phase_drain(uint32_t bar, uint32_t parity, 
     return true;
 }
 
+// Bounds check of debug builds: records kSiteBounds in the status word (the
+// first failure of any kind wins) and returns false, so the caller skips the
+// access; in normal builds it is compiled away and returns true.
+__device__ __forceinline__ bool dbg_check(bool ok, const Watchdog& wd) {
+#if TG_DEBUG
+    if (!ok) atomicCAS(wd.status, 0, kSiteBounds);
+    return ok;
+#else
+    (void)ok;
+    (void)wd;
+    return true;
+#endif
+}
+
+// [first, first + count) inside [0, limit)
+__device__ __forceinline__ bool dbg_in(int64_t first, int64_t count, int64_t limit) {
+    return first >= 0 && count >= 0 && first + count <= limit;
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -229,7 +248,7 @@ constexpr int kStoreBoxBytes = 32 * 32 * 2;
 // 0 wait (bulk_wait_group_read) before `buf` is written again.
 __device__ __forceinline__ void epilogue_chunk_tma(const uint32_t (&r)[32], uint32_t buf, const CUtensorMap* tmC,
                                                    const __half* __restrict__ bias, int row0, int col0, int N,
-                                                   int gelu, int bias_vec) {
+                                                   int gelu, int bias_vec, const Watchdog& wd) {
     const int lane = threadIdx.x & 31;
     float v[32];
     epilogue_values(r, v, bias, col0, N, gelu, bias_vec);
@@ -247,7 +266,8 @@ __device__ __forceinline__ void epilogue_chunk_tma(const uint32_t (&r)[32], uint
     }
     fence_proxy_async_smem();  // the generic-proxy writes -> visible to the TMA unit
     __syncwarp();
-    if (lane == 0) {
+    // a store's x must start on a 16-byte boundary and no store may start at a negative coordinate
+    if (lane == 0 && dbg_check(row0 >= 0 && col0 >= 0 && col0 % 8 == 0, wd)) {
         tma_store_2d(tmC, buf, col0, row0);
         bulk_commit_group();
     }

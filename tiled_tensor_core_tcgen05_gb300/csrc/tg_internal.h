@@ -55,12 +55,23 @@ constexpr int kW4Group = 128;          // rows of K sharing one scale per column
 constexpr int kW4MaxM = 64;            // rows of A per launch
 constexpr int kW4SmemBudget = 224 * 1024;
 
+// Debug builds (compiled with TG_DEBUG=1) check, on the device, that every
+// scratch, counter and output index a kernel computes lies inside its buffer,
+// record a failure in the status word (kSiteBounds) and skip the access; in
+// normal builds the checks compile away.
+#ifndef TG_DEBUG
+#define TG_DEBUG 0
+#endif
+
 // Watchdog plumbing handed to every kernel: where to record the first wait that
-// expired, the limit, and the test hook that withholds one producer arrival.
+// expired, the limit, and the test hook that withholds one producer arrival;
+// plus the buffer sizes the debug builds' bounds checks compare against.
 struct Watchdog {
-    int* status;          // device word; 0 = ok, else the code of the expired wait
+    int* status;          // device word; 0 = ok, else the code of the expired wait or failed check
     uint64_t limit_ns;
     int skip_first_arrive;
+    int64_t ws_floats;    // floats of scratch the kernel may touch (debug checks)
+    int64_t n_counters;   // arrival counters it may touch (debug checks)
 };
 
 // Codes recorded in the status word (which wait expired first).
@@ -72,6 +83,7 @@ enum WaitSite : int {
     kSiteDrain = 5,
     kSiteConvFull = 6,   // 4-bit kernel: a converter waiting for packed weights
     kSiteConvEmpty = 7,  // 4-bit kernel: a converter waiting for a free TMEM slot
+    kSiteBounds = 8,     // debug builds: a device-side bounds check failed
 };
 
 struct TiledArgs {

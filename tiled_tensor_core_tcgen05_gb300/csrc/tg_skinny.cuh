@@ -74,8 +74,9 @@ __device__ __forceinline__ void skinny_epilogue(const SplitArgs& args, uint32_t 
                     }
                 } else {
                     // partials as [slice][n][m_pad]: this thread's 16 rows are 64 contiguous bytes
-                    uint4* wp = reinterpret_cast<uint4*>(
-                        args.ws + (static_cast<int64_t>(sp) * args.N + n) * args.m_pad + c * 16);
+                    const int64_t off = (static_cast<int64_t>(sp) * args.N + n) * args.m_pad + c * 16;
+                    if (!dbg_check(dbg_in(off, 16, args.wd.ws_floats), args.wd)) continue;
+                    uint4* wp = reinterpret_cast<uint4*>(args.ws + off);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) wp[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
                 }
@@ -86,8 +87,11 @@ __device__ __forceinline__ void skinny_epilogue(const SplitArgs& args, uint32_t 
             __threadfence();
             named_barrier_sync(1, kSkEpiThreads);
             if (ept == 0) {
-                const unsigned int prev = atomicAdd(args.counters + nt, 1u);
-                *last_flag = (prev == static_cast<unsigned int>(args.splits - 1)) ? 1 : 0;
+                *last_flag = 0;
+                if (dbg_check(dbg_in(nt, 1, args.wd.n_counters), args.wd)) {
+                    const unsigned int prev = atomicAdd(args.counters + nt, 1u);
+                    *last_flag = (prev == static_cast<unsigned int>(args.splits - 1)) ? 1 : 0;
+                }
             }
             named_barrier_sync(1, kSkEpiThreads);
             if (*last_flag) {
@@ -104,8 +108,9 @@ __device__ __forceinline__ void skinny_epilogue(const SplitArgs& args, uint32_t 
 #pragma unroll
                         for (int i = 0; i < 16; ++i) s[i] = 0.0f;
                         for (int q = 0; q < args.splits; ++q) {
-                            const float4* wq = reinterpret_cast<const float4*>(
-                                args.ws + (static_cast<int64_t>(q) * args.N + n) * args.m_pad + m0);
+                            const int64_t off = (static_cast<int64_t>(q) * args.N + n) * args.m_pad + m0;
+                            if (!dbg_check(dbg_in(off, 16, args.wd.ws_floats), args.wd)) continue;
+                            const float4* wq = reinterpret_cast<const float4*>(args.ws + off);
 #pragma unroll
                             for (int v4 = 0; v4 < 4; ++v4) {
                                 const float4 p = __ldcg(wq + v4);
