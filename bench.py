@@ -59,6 +59,7 @@ KERNEL_SOURCES = {
     "tiled_gemm_kernel": ("k_tiled.cu",),
     "splitk_gemm_kernel": ("k_splitk.cu", "tg_skinny.cuh"),
     "w4_gemm_kernel": ("k_w4.cu",),
+    "w4r_gemm_kernel": ("k_w4r.cu",),
     "attn_fwd_kernel": ("k_attn.cu",),
     "softmax_rows": ("k_softmax.cu",),
 }

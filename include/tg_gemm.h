@@ -227,6 +227,29 @@ tg_status tg_gemm_w4_ex(const void* A, const void* Bq, const void* scales, const
                         int64_t M, int64_t N, int64_t K, int epilogue, int weight_format, int split_k,
                         tg_stream_t stream);
 
+/* Kernels of the 4-bit GEMM (tg_gemm_w4_kernel). */
+typedef enum {
+    TG_W4_KERNEL_AUTO = 0, /* TG_W4_KERNEL_REG when M <= 16, split_k is 0 or 1 and N has at
+                              least one 64-column block per SM; otherwise TG_W4_KERNEL_TMEM */
+    TG_W4_KERNEL_TMEM = 1, /* weights converted into shared memory, tcgen05 MMAs into tensor
+                              memory (64-row MMAs: M > 64 runs as row blocks); split K */
+    TG_W4_KERNEL_REG = 2   /* weights converted in registers into the operands of warp-level
+                              16-row MMAs; M <= 16; one CTA per 64 output columns over the
+                              whole K (no K slices) */
+} tg_w4_kernel;
+
+/*
+ * tg_gemm_w4_ex with the kernel chosen by the caller (`kernel`, a tg_w4_kernel
+ * value): the same product, storage, sizes, errors and tolerance. Both
+ * kernels round W to binary16 once per weight and accumulate in fp32; on
+ * integer-valued inputs with power-of-two scales their results are identical.
+ * TG_W4_KERNEL_REG with M > 16 or split_k > 1, or an unknown kernel, is
+ * TG_ERR_INVALID_ARG. tg_gemm_w4_ex is this call with TG_W4_KERNEL_AUTO.
+ */
+tg_status tg_gemm_w4_kernel(const void* A, const void* Bq, const void* scales, const void* bias, void* C,
+                            int64_t M, int64_t N, int64_t K, int epilogue, int weight_format, int kernel,
+                            int split_k, tg_stream_t stream);
+
 /*
  * Attention forward (FlashAttention), the fused attention kernel of
  * "TileLang: writing LLM GPU kernels by thinking in tiles", section 5, with

@@ -96,6 +96,16 @@ def test_w4_and_attention_with_the_checks_on(libs):
                                  w.K, 0, 1, split, None) == 0
         assert np.array_equal(C.cpu().numpy().view(np.uint16), ref), f"split_k={split}"
     assert _status(dbg) == (0, 0)
+    # the register-dequant kernel (M <= 16), ragged N and K
+    w = workloads.W4Workload("dbg_w4r", 13, 200, 1152, seed=7, a_dist=INT2, bias_dist=INT2, scale_kind="pow2")
+    A, Bq, s, bias = w.inputs()
+    ref = oracle.gemm_w4(A, Bq, s, bias).view(np.uint16)
+    dA, dBq, ds, db = A.cuda(), Bq.cuda(), s.cuda(), bias.cuda()
+    C = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
+    assert dbg.tg_gemm_w4_kernel(dA.data_ptr(), dBq.data_ptr(), ds.data_ptr(), db.data_ptr(), C.data_ptr(), w.M,
+                                 w.N, w.K, 0, 0, 2, 0, None) == 0
+    assert np.array_equal(C.cpu().numpy().view(np.uint16), ref), "register kernel"
+    assert _status(dbg) == (0, 0)
     # a shape whose last round of query blocks is split into key halves (uses the scratch)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     H = (2 * sms + 16) // 8

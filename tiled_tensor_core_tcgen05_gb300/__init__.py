@@ -24,11 +24,12 @@ EPI_NONE, EPI_GELU = 0, 1
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024  # TG_NOALLOC_SCRATCH_BYTES
 KERNEL_AUTO, KERNEL_TILED_TMA, KERNEL_TILED_LSU, KERNEL_SPLITK, KERNEL_TILED_PAIR = 0, 1, 2, 3, 4
 W4_INT4, W4_FP4_E2M1 = 0, 1
+W4_KERNEL_AUTO, W4_KERNEL_TMEM, W4_KERNEL_REG = 0, 1, 2
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NO_MEMORY, ERR_BOUNDS = range(7)
 
 # every symbol include/tg_gemm.h declares
 EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_gemm_w4_ex",
-           "tg_attention_fwd",
+           "tg_gemm_w4_kernel", "tg_attention_fwd",
            "tg_softmax_rows", "tg_bias_gelu",
            "tg_device_status", "tg_debug_status",
            "tg_set_watchdog_ns",
@@ -53,6 +54,7 @@ def bind(path: str) -> ctypes.CDLL:
     lib.tg_gemm_splitk_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
     lib.tg_gemm_w4.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
     lib.tg_gemm_w4_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp]
+    lib.tg_gemm_w4_kernel.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _int, _vp]
     lib.tg_attention_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _vp]
     lib.tg_softmax_rows.argtypes = [_vp, _vp, _i64, _i64, _vp]
     lib.tg_bias_gelu.argtypes = [_vp, _vp, _i64, _i64, _int, _vp]
@@ -72,7 +74,7 @@ def bind(path: str) -> ctypes.CDLL:
     lib.tg_shutdown.argtypes = []
     lib.tg_shutdown.restype = None
     for name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_gemm_w4_ex",
-                 "tg_attention_fwd", "tg_softmax_rows", "tg_bias_gelu", "tg_device_status", "tg_debug_status",
+                 "tg_gemm_w4_kernel", "tg_attention_fwd", "tg_softmax_rows", "tg_bias_gelu", "tg_device_status", "tg_debug_status",
                  "tg_set_watchdog_ns", "tg_debug_skip_first_arrive", "tg_debug_bounds_limit", "tg_debug_build",
                  "tg_version"):
         getattr(lib, name).restype = _int
@@ -129,6 +131,12 @@ def tg_gemm_w4(A: int, Bq: int, scales: int, bias: int | None, C: int, M: int, N
 def tg_gemm_w4_ex(A: int, Bq: int, scales: int, bias: int | None, C: int, M: int, N: int, K: int, epilogue: int,
                   weight_format: int, split_k: int, stream: int | None) -> None:
     _check(_lib.tg_gemm_w4_ex(A, Bq, scales, bias, C, M, N, K, epilogue, weight_format, split_k, stream))
+
+
+def tg_gemm_w4_kernel(A: int, Bq: int, scales: int, bias: int | None, C: int, M: int, N: int, K: int,
+                      epilogue: int, weight_format: int, kernel: int, split_k: int, stream: int | None) -> None:
+    _check(_lib.tg_gemm_w4_kernel(A, Bq, scales, bias, C, M, N, K, epilogue, weight_format, kernel, split_k,
+                                  stream))
 
 
 def tg_attention_fwd(Q: int, K: int, V: int, O: int, B: int, S: int, H: int, D: int, causal: bool,
@@ -280,11 +288,12 @@ def gemm(A, B, bias=None, gelu: bool = False, out=None, kernel: int = KERNEL_AUT
 
 
 def gemm_w4(A, Bq, scales, bias=None, gelu: bool = False, out=None, split_k: int = 0, stream=None,
-            fmt: int = W4_INT4):
+            fmt: int = W4_INT4, kernel: int = W4_KERNEL_AUTO):
     """C = epi(A @ W + bias) with 4-bit weights: A (M, K) float16, Bq (N, K/2)
     uint8 (low nibble = even k; two's complement for W4_INT4, E2M1 codes for
     W4_FP4_E2M1), scales (K/128, N) float16, W[k, n] = fp16(value(q[k, n]) *
-    scales[k // 128, n]). CUDA tensors, contiguous."""
+    scales[k // 128, n]). CUDA tensors, contiguous. `kernel`: W4_KERNEL_AUTO,
+    W4_KERNEL_TMEM or W4_KERNEL_REG (M <= 16, one K slice)."""
     import torch
     if A.dim() != 2 or Bq.dim() != 2 or scales.dim() != 2:
         raise ValueError("A, Bq and scales must be matrices")
@@ -302,11 +311,11 @@ def gemm_w4(A, Bq, scales, bias=None, gelu: bool = False, out=None, split_k: int
         out = torch.empty((M, N), dtype=torch.float16, device=A.device)
     elif tuple(out.shape) != (M, N):
         raise ValueError("out has the wrong shape")
-    tg_gemm_w4_ex(_dev_fp16(A, "A") if A.numel() else None, Bq.data_ptr() if Bq.numel() else None,
-                  _dev_fp16(scales, "scales") if scales.numel() else None,
-                  _dev_fp16(bias, "bias") if bias is not None else None,
-                  _dev_fp16(out, "out") if out.numel() else None, M, N, K, EPI_GELU if gelu else EPI_NONE, fmt,
-                  split_k, _stream_handle(stream))
+    tg_gemm_w4_kernel(_dev_fp16(A, "A") if A.numel() else None, Bq.data_ptr() if Bq.numel() else None,
+                      _dev_fp16(scales, "scales") if scales.numel() else None,
+                      _dev_fp16(bias, "bias") if bias is not None else None,
+                      _dev_fp16(out, "out") if out.numel() else None, M, N, K, EPI_GELU if gelu else EPI_NONE, fmt,
+                      kernel, split_k, _stream_handle(stream))
     return out
 
 

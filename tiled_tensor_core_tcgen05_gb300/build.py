@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libtg_gemm.so")
 # the debug build (device-side bounds checks, TG_DEBUG=1): same sources, its own objects
 OBJDIR_DEBUG = os.path.join(PKG, "_build_debug")
 LIB_DEBUG = os.path.join(PKG, "libtg_gemm_debug.so")
-SOURCES = ["tg_api.cu", "k_tiled.cu", "k_tiled2.cu", "k_splitk.cu", "k_w4.cu", "k_attn.cu", "k_softmax.cu", "k_fill.cu", "k_epilogue.cu", "k_pad.cu"]
+SOURCES = ["tg_api.cu", "k_tiled.cu", "k_tiled2.cu", "k_splitk.cu", "k_w4.cu", "k_w4r.cu", "k_attn.cu", "k_softmax.cu", "k_fill.cu", "k_epilogue.cu", "k_pad.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
           "--expt-relaxed-constexpr"]

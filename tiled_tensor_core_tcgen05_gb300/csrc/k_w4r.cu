@@ -1,0 +1,274 @@
+// Weight-only 4-bit GEMM for decode-sized M (at most 16 rows of A):
+// C = epi(A @ W + bias), W[k][n] = fp16(v(q[k][n]) * scale[k/128][n]), the
+// same product as the tensor-memory kernel (k_w4.cu), for the shape where that
+// kernel is furthest from the HBM bound.
+//
+// "TileLang: writing LLM GPU kernels by thinking in tiles" (section
+// "Quantized LLM inference") has the packed weights brought on chip, converted
+// there and fed to the tensor-core product without an fp16 copy in memory.
+// Here the converted tile does not touch shared memory either: each thread
+// decodes its own packed words into the fp16 pairs of a warp-level MMA's
+// operand registers.
+//
+// Why warp-level MMAs. A tcgen05 MMA has at least 64 rows and costs at least
+// ~93 cycles per instruction; with 16 tokens the tensor-memory kernel pads M
+// to 64 and still spends ~29 us on MMA issue for 16 x 28672 x 8192. The
+// m16n8k16 MMA has exactly 16 rows (the tokens), takes its B operand (the
+// weights) from registers, and issues one per 8 cycles per warp; the 7.5 GFLOP
+// of that shape need ~12 us of it, and no converted tile is written to or read
+// back from shared memory (the tensor-memory kernel's bound: 4 bytes of
+// shared-memory traffic per converted weight).
+//
+// Work. A CTA owns 64 consecutive output columns (two warp-columns of 32) for
+// the whole K, so no partial sums leave the CTA. K is streamed in chunks of
+// 256 through a ring of shared-memory stages filled by TMA: the chunk's
+// activations (16 rows x 256 k, one 3-D box whose lines are (row, 64-k block)
+// pairs, so the 128-byte swizzle phase differs between the k blocks the four
+// lanes of a quad read: conflict-free), the packed weights of the 64 columns
+// (64 rows x 128 bytes, 128-byte swizzle) and their two scale rows.
+// Per CTA:
+//   warps 0-3  consumers: warp (nw, ks) = (warp % 2, warp / 2) computes
+//              warp-column nw over the chunks c with c % 2 == ks; lane
+//              (g, t) = (lane / 4, lane % 4) holds weight column 8 i + g of
+//              the warp-column's four 8-column tiles i and the k range
+//              [64 t, 64 t + 64) of each chunk (two 16-byte words per tile),
+//              decodes each 8-weight word into the B registers of two MMAs,
+//              and reads the matching activation fragment from shared
+//              memory (for INT4 reordered into the decoder's (k, k+4) pairs
+//              with byte permutes; FP4 pairs are already in order);
+//   warp 4     producer: one lane issues the three TMA copies of each chunk.
+// The two partial sums of a warp-column (even and odd chunks) are added in
+// that order through shared memory; bias, GELU and one rounding to fp16 follow.
+// Barriers: full[s] (TMA bytes), empty[s] (the two warps that read stage s,
+// after a proxy fence: the next TMA write into the stage is an async-proxy
+// write after their generic-proxy reads).
+#include "tg_device.cuh"
+#include "tg_internal.h"
+
+namespace tg {
+namespace {
+
+constexpr int kRWarpCols = kW4rCols / 32;          // 2
+constexpr int kRKSplit = 2;                        // warps per warp-column, alternate chunks
+constexpr int kRConsumers = kRWarpCols * kRKSplit;
+constexpr int kRThreads = (kRConsumers + 1) * 32;
+constexpr int kRChunk = 256;                       // k per stage (two scale groups)
+constexpr int kRXBytes = 16 * kRChunk * 2;         // 8 KB of activations
+constexpr int kRWBytes = kW4rCols * kRChunk / 2;   // 8 KB of packed weights
+constexpr int kRSBytes = kW4rCols * 2 * 2;         // two scale rows
+constexpr int kRTx = kRXBytes + kRWBytes + kRSBytes;
+constexpr int kRStage = (kRTx + 1023) / 1024 * 1024;
+constexpr int kRStages = 4;
+constexpr int kRRedBytes = kRWarpCols * (kRKSplit - 1) * 32 * 16 * 4;  // 16 floats per lane
+static_assert(kRStages % kRKSplit == 0, "a stage is always read by the same warps");
+static_assert(kRChunk == 2 * kW4Group, "a chunk spans two scale groups");
+
+struct RLayout {
+    static constexpr int red = kRStages * kRStage;
+    static constexpr int bar_full = red + kRRedBytes;
+    static constexpr int bar_empty = bar_full + 8 * kRStages;
+    static constexpr int abort_slot = bar_empty + 8 * kRStages;
+    static constexpr int used = abort_slot + 16;
+    static constexpr int alloc = used + 1024;  // 1 KB alignment slack
+};
+
+__device__ __forceinline__ void mma_m16n8k16(float (&c)[4], const uint4& a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+
+template <int kFmt>
+__global__ void __launch_bounds__(kRThreads, 3)
+    w4r_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
+                    const __grid_constant__ CUtensorMap tmX, const W4rArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    auto full = [&](int s) { return sb + RLayout::bar_full + 8 * s; };
+    auto empty = [&](int s) { return sb + RLayout::bar_empty + 8 * s; };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + RLayout::abort_slot);
+    const int n0 = blockIdx.x * kW4rCols;
+    const int nch = a.n_chunks;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kRWarpCols);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmS);
+        tma_prefetch_desc(&tmX);
+    }
+    __syncthreads();
+    const WaitCtx wc{abort_flag, a.wd.status, a.wd.limit_ns};
+
+    if (warp == kRConsumers) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_stream = l2_policy_evict_first();  // weights and scales: read once
+            const uint64_t pol_keep = l2_policy_evict_last();     // activations: read by every CTA
+            int issued = 0;
+            for (int c = 0; c < nch; ++c) {
+                const int slot = c % kRStages;
+                if (!wait_phase(empty(slot), ((c / kRStages) & 1) ^ 1, wc, kSiteProducerEmpty)) break;
+                const uint32_t st = sb + slot * kRStage;
+                mbar_arrive_expect_tx(full(slot), kRTx);
+                tma_load_3d_hint(st, &tmX, full(slot), 0, c * (kRChunk / 64), 0, pol_keep);
+                tma_load_2d_hint(st + kRXBytes, &tmW, full(slot), c * (kRChunk / 2), n0, pol_stream);
+                tma_load_2d_hint(st + kRXBytes + kRWBytes, &tmS, full(slot), n0, c * (kRChunk / kW4Group), pol_stream);
+                issued = c + 1;
+            }
+            // let the copies in flight land before the CTA can exit (consumers that
+            // gave up no longer wait for them)
+            for (int c = issued - kRStages < 0 ? 0 : issued - kRStages; c < issued; ++c)
+                wait_phase_drain(full(c % kRStages), (c / kRStages) & 1, wc);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int g = lane >> 2, t = lane & 3;
+    const int nw = warp % kRWarpCols, ks = warp / kRWarpCols;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    // activation lines of this lane's rows g and g + 8 for k block t: line = row * 4 + block
+    const int l0 = g * 4 + t, l1 = (g + 8) * 4 + t;
+    for (int c = ks; c < nch; c += kRKSplit) {
+        const int slot = c % kRStages;
+        if (!__all_sync(0xFFFFFFFFu, wait_phase(full(slot), (c / kRStages) & 1, wc, kSiteConvFull))) break;
+        const uint32_t st = sb + slot * kRStage;
+        // this lane's packed words: rows 8 i + g of the warp-column, bytes [32 t, 32 t + 32)
+        // of the 128-byte row = 16-byte units 2 t and 2 t + 1 (128-byte swizzle by row % 8 = g)
+        uint4 wq[4][2];
+        __half2 sc[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = nw * 32 + 8 * i + g;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) wq[i][j] = lds_v4(st + kRXBytes + r * 128 + 16 * ((2 * t + j) ^ g));
+            // k range [64 t, 64 t + 64) lies in scale group t / 2 of the chunk
+            sc[i] = __half2half2(__ushort_as_half(lds_u16(st + kRXBytes + kRWBytes + (t >> 1) * kW4rCols * 2 + 2 * r)));
+        }
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {  // word w: k = 64 t + 8 w .. + 7 (line unit w)
+            const uint4 u0 = lds_v4(st + l0 * 128 + 16 * (w ^ (l0 & 7)));
+            const uint4 u1 = lds_v4(st + l1 * 128 + 16 * (w ^ (l1 & 7)));
+            // A fragments of the two k16 steps this word feeds: {row g, row g + 8} x {pair b0, pair b1}
+            uint4 e0, e1;
+            if (kFmt == 0) {  // pairs (k, k+4) as dequant_word delivers them
+                e0.x = __byte_perm(u0.x, u0.z, 0x5410);
+                e0.y = __byte_perm(u1.x, u1.z, 0x5410);
+                e0.z = __byte_perm(u0.x, u0.z, 0x7632);
+                e0.w = __byte_perm(u1.x, u1.z, 0x7632);
+                e1.x = __byte_perm(u0.y, u0.w, 0x5410);
+                e1.y = __byte_perm(u1.y, u1.w, 0x5410);
+                e1.z = __byte_perm(u0.y, u0.w, 0x7632);
+                e1.w = __byte_perm(u1.y, u1.w, 0x7632);
+            } else {  // natural pairs (k, k+1)
+                e0 = make_uint4(u0.x, u1.x, u0.y, u1.y);
+                e1 = make_uint4(u0.z, u1.z, u0.w, u1.w);
+            }
+            uint32_t bw[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4& q = wq[i][w >> 2];
+                const uint32_t word = (w & 3) == 0 ? q.x : (w & 3) == 1 ? q.y : (w & 3) == 2 ? q.z : q.w;
+                if (kFmt == 0)
+                    dequant_word(word, sc[i], bw[i]);
+                else
+                    dequant_word_fp4(word, sc[i], bw[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mma_m16n8k16(acc[i], e0, bw[i][0], bw[i][1]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mma_m16n8k16(acc[i], e1, bw[i][2], bw[i][3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(slot));
+    }
+
+    // ---------------------------------------------------------------- epilogue
+    // accumulator fragment of tile i: (row g, columns 2t, 2t+1) and (row g + 8, same columns)
+    float* red = reinterpret_cast<float*>(smem + RLayout::red);
+    if (ks > 0) {
+        float* dst = red + ((ks - 1) * kRWarpCols + nw) * 512;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<float4*>(dst + (i * 32 + lane) * 4) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    }
+    named_barrier_sync(1, kRConsumers * 32);
+    if (ks != 0) return;
+    for (int q = 1; q < kRKSplit; ++q) {
+        const float* src = red + ((q - 1) * kRWarpCols + nw) * 512;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 v = *reinterpret_cast<const float4*>(src + (i * 32 + lane) * 4);
+            acc[i][0] += v.x;
+            acc[i][1] += v.y;
+            acc[i][2] += v.z;
+            acc[i][3] += v.w;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int col = n0 + nw * 32 + 8 * i + 2 * t;
+        if (col >= a.N) continue;  // N % 8 == 0: a tile is wholly in or out
+        float b0 = 0.f, b1 = 0.f;
+        if (a.bias) {
+            b0 = __half2float(a.bias[col]);
+            b1 = __half2float(a.bias[col + 1]);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = g + 8 * h;
+            if (row >= a.M) continue;
+            const __half v0 = __float2half_rn(epi_value(acc[i][2 * h], b0, a.gelu));
+            const __half v1 = __float2half_rn(epi_value(acc[i][2 * h + 1], b1, a.gelu));
+            const int64_t off = static_cast<int64_t>(row) * a.N + col;
+            if (!dbg_check(dbg_in(off, 2, static_cast<int64_t>(a.M) * a.N), a.wd)) continue;
+            if (a.c_vec) {
+                *reinterpret_cast<__half2*>(a.C + off) = __halves2half2(v0, v1);
+            } else {
+                a.C[off] = v0;
+                a.C[off + 1] = v1;
+            }
+        }
+    }
+}
+
+}  // namespace
+
+int w4r_smem_bytes() { return RLayout::alloc; }
+
+template <int kFmt>
+static cudaError_t launch_w4r_t(const W4rArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmS,
+                                const CUtensorMap& tmX, int grid, cudaStream_t stream) {
+    static int attr_gen[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && attr_gen[dev] != g_generation) {
+        e = cudaFuncSetAttribute(w4r_gemm_kernel<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize, RLayout::alloc);
+        if (e != cudaSuccess) return e;
+        attr_gen[dev] = g_generation;
+    }
+    w4r_gemm_kernel<kFmt><<<grid, kRThreads, RLayout::alloc, stream>>>(tmW, tmS, tmX, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_w4r(const W4rArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmS, const CUtensorMap& tmX,
+                       int grid, cudaStream_t stream) {
+    return a.fmt == 1 ? launch_w4r_t<1>(a, tmW, tmS, tmX, grid, stream)
+                      : launch_w4r_t<0>(a, tmW, tmS, tmX, grid, stream);
+}
+
+}  // namespace tg

@@ -195,6 +195,21 @@ tg_status make_map_scales(CUtensorMap* m, const void* base, uint64_t inner, uint
     return TG_OK;
 }
 
+// M x K fp16 activations (row-major, M <= 16) as a 3-D map {64, K/64, M}: box
+// {64, 4, 16} = 16 rows x 256 k whose 128-byte lines are (row, 64-k block)
+// pairs, 128-byte swizzle; rows past M read as zero.
+tg_status make_map_x3(CUtensorMap* m, const void* base, uint64_t M, uint64_t K) {
+    cuuint64_t dims[3] = {64, K / 64, M};
+    cuuint64_t strides[2] = {128, K * 2};
+    cuuint32_t box[3] = {64, 4, 16};
+    CUresult r = encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r != CUDA_SUCCESS)
+        return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for the %llu x %llu activations", (int)r,
+                    (unsigned long long)M, (unsigned long long)K);
+    return TG_OK;
+}
+
 // (batch, sequence, head, dim) fp16 tensor as a 4-D map, innermost first:
 // {dim, head, sequence, batch}; box {64, 1, 128, 1} with the 128-byte swizzle
 // (one 64-column slice of 128 consecutive positions of one head).
@@ -823,9 +838,9 @@ extern "C" tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const 
 // ---------------------------------------------------------------------------
 // tg_gemm_w4: the skinny GEMM with 4-bit weights.
 
-extern "C" tg_status tg_gemm_w4_ex(const void* A, const void* Bq, const void* scales, const void* bias, void* C,
-                                   int64_t M, int64_t N, int64_t K, int epilogue, int weight_format, int split_k,
-                                   tg_stream_t stream_) {
+extern "C" tg_status tg_gemm_w4_kernel(const void* A, const void* Bq, const void* scales, const void* bias,
+                                       void* C, int64_t M, int64_t N, int64_t K, int epilogue, int weight_format,
+                                       int kernel, int split_k, tg_stream_t stream_) {
     t_last_error.clear();
     const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_GELU)
@@ -840,6 +855,12 @@ extern "C" tg_status tg_gemm_w4_ex(const void* A, const void* Bq, const void* sc
     if (split_k < 0 || split_k > kSkMaxSplits)
         return fail(TG_ERR_INVALID_ARG, "split_k must be 0 (automatic) or 1..%d, got %d", kSkMaxSplits, split_k);
     if (M > kSkMaxM) return fail(TG_ERR_INVALID_ARG, "tg_gemm_w4 needs M <= %d, got %lld", kSkMaxM, (long long)M);
+    if (kernel != TG_W4_KERNEL_AUTO && kernel != TG_W4_KERNEL_TMEM && kernel != TG_W4_KERNEL_REG)
+        return fail(TG_ERR_INVALID_ARG, "kernel must be TG_W4_KERNEL_AUTO, _TMEM or _REG (0..2), got %d", kernel);
+    if (kernel == TG_W4_KERNEL_REG && M > kW4rMaxM)
+        return fail(TG_ERR_INVALID_ARG, "TG_W4_KERNEL_REG needs M <= %d, got %lld", kW4rMaxM, (long long)M);
+    if (kernel == TG_W4_KERNEL_REG && split_k > 1)
+        return fail(TG_ERR_INVALID_ARG, "TG_W4_KERNEL_REG runs one K slice, got split_k=%d", split_k);
     if (K % kW4Group != 0)
         return fail(TG_ERR_INVALID_ARG, "tg_gemm_w4 needs K %% %d == 0, got K=%lld", kW4Group, (long long)K);
     if (N % 8 != 0) return fail(TG_ERR_INVALID_ARG, "tg_gemm_w4 needs N %% 8 == 0, got N=%lld", (long long)N);
@@ -865,6 +886,26 @@ extern "C" tg_status tg_gemm_w4_ex(const void* A, const void* Bq, const void* sc
         cudaError_t e = launch_fill(static_cast<const __half*>(bias), static_cast<__half*>(C), M, N, gelu,
                                     d.sm_count, stream);
         return e == cudaSuccess ? TG_OK : cuda_fail(e, "fill kernel launch");
+    }
+
+    const bool use_reg = kernel == TG_W4_KERNEL_REG ||
+                         (kernel == TG_W4_KERNEL_AUTO && M <= kW4rMaxM && split_k <= 1 &&
+                          (N + kW4rCols - 1) / kW4rCols >= d.sm_count);
+    if (use_reg) {
+        W4rArgs r{};
+        r.bias = static_cast<const __half*>(bias);
+        r.C = static_cast<__half*>(C);
+        r.M = (int)M; r.N = (int)N; r.gelu = gelu; r.fmt = weight_format;
+        r.n_chunks = (int)((K + 255) / 256);
+        r.c_vec = aligned(C, 4) ? 1 : 0;
+        r.wd = watchdog(d);
+        CUtensorMap tmW, tmS, tmX;
+        if ((st = make_map_u8(&tmW, Bq, K / 2, N, 128, kW4rCols)) != TG_OK) return st;
+        if ((st = make_map_scales(&tmS, scales, N, K / kW4Group, kW4rCols, 2)) != TG_OK) return st;
+        if ((st = make_map_x3(&tmX, A, M, K)) != TG_OK) return st;
+        const int grid = (int)((N + kW4rCols - 1) / kW4rCols);
+        cudaError_t e = launch_w4r(r, tmW, tmS, tmX, grid, stream);
+        return e == cudaSuccess ? TG_OK : cuda_fail(e, "4-bit register kernel launch");
     }
 
     // at most kW4MaxM rows of A per launch: larger M runs as row blocks (each
@@ -909,6 +950,13 @@ extern "C" tg_status tg_gemm_w4_ex(const void* A, const void* Bq, const void* sc
         if (e != cudaSuccess) return cuda_fail(e, "4-bit kernel launch");
     }
     return TG_OK;
+}
+
+extern "C" tg_status tg_gemm_w4_ex(const void* A, const void* Bq, const void* scales, const void* bias, void* C,
+                                   int64_t M, int64_t N, int64_t K, int epilogue, int weight_format, int split_k,
+                                   tg_stream_t stream) {
+    return tg_gemm_w4_kernel(A, Bq, scales, bias, C, M, N, K, epilogue, weight_format, TG_W4_KERNEL_AUTO, split_k,
+                             stream);
 }
 
 extern "C" tg_status tg_gemm_w4(const void* A, const void* Bq, const void* scales, const void* bias, void* C,

@@ -117,6 +117,57 @@ __device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred
     return r != 0;
 }
 
+// ---------------------------------------------------------------------------
+// 4-bit weight decoding, shared by the two 4-bit GEMM kernels.
+
+// INT4: one 32-bit word of packed weights (eight consecutive k of one column, byte
+// p holding k = 2p in its low and 2p + 1 in its high nibble) into four fp16
+// pairs (w[k] * scale, each product rounded once), in the order
+// (k0, k4), (k1, k5), (k2, k6), (k3, k7): the order in which masks that keep
+// one nibble of each 16-bit half deliver them. The kernels that use it pair
+// the activations the same way, so the dot product over k is unchanged.
+// A nibble masked under the exponent bits 0x64 and XORed with 8 (two's
+// complement q -> q + 8) reads 1024 + (q + 8) in the low nibble position and
+// 1024 + 16 (q + 8) in the high one; one fp16 fused multiply-add maps either
+// exactly to q, and the scale multiply is the only rounding.
+__device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, uint32_t* out) {
+    const __half2 one = __halves2half2(__ushort_as_half(0x3C00), __ushort_as_half(0x3C00));        // 1
+    const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
+    const __half2 off_lo = __halves2half2(__ushort_as_half(0xE408), __ushort_as_half(0xE408));     // -1032
+    const __half2 off_hi = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));     // -72
+    const uint32_t w8 = w >> 8;
+    uint32_t x[4] = {(w & 0x000F000Fu) ^ 0x64086408u, (w & 0x00F000F0u) ^ 0x64806480u,
+                     (w8 & 0x000F000Fu) ^ 0x64086408u, (w8 & 0x00F000F0u) ^ 0x64806480u};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        __half2 h = *reinterpret_cast<__half2*>(&x[p]);
+        h = __hmul2((p & 1) ? __hfma2(h, sixteenth, off_hi) : __hfma2(h, one, off_lo), s2);
+        out[p] = *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+// FP4 (E2M1): the same word into four fp16 pairs in natural order (k0, k1),
+// (k2, k3), (k4, k5), (k6, k7): each byte holds one pair, converted exactly by
+// the hardware's e2m1x2 -> f16x2 conversion (every E2M1 value is exact in
+// fp16); the scale multiply is the only rounding. In this order the
+// activations need no reordering.
+__device__ __forceinline__ void dequant_word_fp4(uint32_t w, __half2 s2, uint32_t* out) {
+    uint32_t h[4];
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h[p]), s2);
+        out[p] = *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
 // GELU with the exact Gaussian CDF, in fp32: 0.5 x (1 + erf(x / sqrt 2)).
 __device__ __forceinline__ float gelu_erf(float x) {
     return 0.5f * x * (1.0f + erff(x * 0.70710678118654752440f));

@@ -54,6 +54,8 @@ constexpr int kW4BK = 256;
 constexpr int kW4Group = 128;          // rows of K sharing one scale per column
 constexpr int kW4MaxM = 64;            // rows of A per launch
 constexpr int kW4SmemBudget = 224 * 1024;
+constexpr int kW4rCols = 64;           // register-dequant 4-bit kernel: output columns per CTA
+constexpr int kW4rMaxM = 16;           // and rows of A (its MMA's M)
 
 // Debug builds (compiled with TG_DEBUG=1) check, on the device, that every
 // scratch, counter and output index a kernel computes lies inside its buffer,
@@ -139,6 +141,19 @@ struct W4Args {
     int c_vec;                 // C 16-byte aligned and N % 8 == 0: 16-byte stores
 };
 
+// The register-dequant 4-bit kernel (M <= kW4rMaxM): a CTA per kW4rCols
+// output columns over the whole K.
+struct W4rArgs {
+    const __half* bias;
+    __half* C;
+    int M, N;
+    int n_chunks;              // K / 256, rounded up
+    int gelu;
+    int fmt;                   // 0: two's-complement INT4, 1: FP4 (E2M1)
+    int c_vec;                 // C 4-byte aligned: paired stores
+    Watchdog wd;
+};
+
 // Attention forward: (batch, sequence, head, dim) fp16, dim = kAttnD.
 constexpr int kAttnD = 128;
 struct AttnArgs {
@@ -181,6 +196,9 @@ void w4_pipeline(int m_pad, int* stages, int* act_slots, int* slots);
 int w4_smem_bytes(int m_pad, int stages, int act_slots, int slots);
 cudaError_t launch_w4(const W4Args& a, const CUtensorMap& tmBq, const CUtensorMap& tmA, const CUtensorMap& tmS,
                       int grid, cudaStream_t stream);
+int w4r_smem_bytes();
+cudaError_t launch_w4r(const W4rArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmS, const CUtensorMap& tmX,
+                       int grid, cudaStream_t stream);
 cudaError_t launch_softmax(const __half* X, __half* Y, int M, int N, bool vec, int sm_count, cudaStream_t stream);
 int attn_smem_bytes();
 int attn_part_floats();
