@@ -48,20 +48,25 @@
 namespace tg {
 namespace {
 
-constexpr int kRWarpCols = kW4rCols / 32;          // 2
-constexpr int kRKSplit = 2;                        // warps per warp-column, alternate chunks
+constexpr int kRTiles = 4;                         // 8-column MMA tiles per warp
+constexpr int kRWarpCols = kW4rCols / (8 * kRTiles);  // warp-columns per CTA (2)
+constexpr int kRKSplit = 2;                        // warps per warp-column, taking chunks in turn
 constexpr int kRConsumers = kRWarpCols * kRKSplit;
 constexpr int kRThreads = (kRConsumers + 1) * 32;
-constexpr int kRChunk = 256;                       // k per stage (two scale groups)
-constexpr int kRXBytes = 16 * kRChunk * 2;         // 8 KB of activations
-constexpr int kRWBytes = kW4rCols * kRChunk / 2;   // 8 KB of packed weights
-constexpr int kRSBytes = kW4rCols * 2 * 2;         // two scale rows
+constexpr int kRChunk = 256;                       // k per stage
+constexpr int kRWRow = kRChunk / 2;                // bytes of one weight row per stage (128)
+constexpr int kRXB = kRChunk / 64;                 // 64-k activation blocks per stage
+constexpr int kRWords = kRChunk / 32;              // 8-weight words per lane and tile per stage
+constexpr int kRGroups = kRChunk / kW4Group;       // scale rows per stage
+constexpr int kRXBytes = 16 * kRChunk * 2;         // activations: 16 rows
+constexpr int kRWBytes = kW4rCols * kRWRow;        // packed weights
+constexpr int kRSBytes = kW4rCols * 2 * kRGroups;  // scale rows
 constexpr int kRTx = kRXBytes + kRWBytes + kRSBytes;
 constexpr int kRStage = (kRTx + 1023) / 1024 * 1024;
 constexpr int kRStages = 4;
-constexpr int kRRedBytes = kRWarpCols * (kRKSplit - 1) * 32 * 16 * 4;  // 16 floats per lane
+constexpr int kRRedBytes = kRWarpCols * (kRKSplit - 1) * 32 * kRTiles * 4 * 4;  // 4 floats per lane and tile
 static_assert(kRStages % kRKSplit == 0, "a stage is always read by the same warps");
-static_assert(kRChunk == 2 * kW4Group, "a chunk spans two scale groups");
+static_assert(kRWRow == 128, "weight rows of one 128-byte swizzle span");
 
 struct RLayout {
     static constexpr int red = kRStages * kRStage;
@@ -120,9 +125,9 @@ __global__ void __launch_bounds__(kRThreads, 3)
                 if (!wait_phase(empty(slot), ((c / kRStages) & 1) ^ 1, wc, kSiteProducerEmpty)) break;
                 const uint32_t st = sb + slot * kRStage;
                 mbar_arrive_expect_tx(full(slot), kRTx);
-                tma_load_3d_hint(st, &tmX, full(slot), 0, c * (kRChunk / 64), 0, pol_keep);
-                tma_load_2d_hint(st + kRXBytes, &tmW, full(slot), c * (kRChunk / 2), n0, pol_stream);
-                tma_load_2d_hint(st + kRXBytes + kRWBytes, &tmS, full(slot), n0, c * (kRChunk / kW4Group), pol_stream);
+                tma_load_3d_hint(st, &tmX, full(slot), 0, c * kRXB, 0, pol_keep);
+                tma_load_2d_hint(st + kRXBytes, &tmW, full(slot), c * kRWRow, n0, pol_stream);
+                tma_load_2d_hint(st + kRXBytes + kRWBytes, &tmS, full(slot), n0, c * kRGroups, pol_stream);
                 issued = c + 1;
             }
             // let the copies in flight land before the CTA can exit (consumers that
@@ -136,31 +141,38 @@ __global__ void __launch_bounds__(kRThreads, 3)
     // ---------------------------------------------------------------- consumers
     const int g = lane >> 2, t = lane & 3;
     const int nw = warp % kRWarpCols, ks = warp / kRWarpCols;
-    float acc[4][4];
+    float acc[kRTiles][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    // activation lines of this lane's rows g and g + 8 for k block t: line = row * 4 + block
-    const int l0 = g * 4 + t, l1 = (g + 8) * 4 + t;
+    for (int i = 0; i < kRTiles; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    constexpr int kTk = kRChunk / 4;  // k per lane per stage: [kTk t, kTk t + kTk)
     for (int c = ks; c < nch; c += kRKSplit) {
         const int slot = c % kRStages;
         if (!__all_sync(0xFFFFFFFFu, wait_phase(full(slot), (c / kRStages) & 1, wc, kSiteConvFull))) break;
         const uint32_t st = sb + slot * kRStage;
-        // this lane's packed words: rows 8 i + g of the warp-column, bytes [32 t, 32 t + 32)
-        // of the 128-byte row = 16-byte units 2 t and 2 t + 1 (128-byte swizzle by row % 8 = g)
-        uint4 wq[4][2];
-        __half2 sc[4];
+        // this lane's packed words: rows 8 i + g of the warp-column, bytes [kTk t / 2, kTk t / 2 + kTk / 2)
+        // of the 128-byte row: 16-byte units 2 t + j, swizzled by row % 8 = g
+        uint4 wq[kRTiles][kRWords / 4];
+        __half2 sc[kRTiles];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = nw * 32 + 8 * i + g;
+        for (int i = 0; i < kRTiles; ++i) {
+            const int r = nw * 8 * kRTiles + 8 * i + g;
 #pragma unroll
-            for (int j = 0; j < 2; ++j) wq[i][j] = lds_v4(st + kRXBytes + r * 128 + 16 * ((2 * t + j) ^ g));
-            // k range [64 t, 64 t + 64) lies in scale group t / 2 of the chunk
-            sc[i] = __half2half2(__ushort_as_half(lds_u16(st + kRXBytes + kRWBytes + (t >> 1) * kW4rCols * 2 + 2 * r)));
+            for (int j = 0; j < kRWords / 4; ++j) {
+                wq[i][j] = lds_v4(st + kRXBytes + r * kRWRow + 16 * ((2 * t + j) ^ g));
+            }
+            // the lane's k range lies in scale group (kTk t) / 128 of the stage
+            sc[i] = __half2half2(__ushort_as_half(
+                lds_u16(st + kRXBytes + kRWBytes + (kTk * t / kW4Group) * kW4rCols * 2 + 2 * r)));
         }
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {  // word w: k = 64 t + 8 w .. + 7 (line unit w)
-            const uint4 u0 = lds_v4(st + l0 * 128 + 16 * (w ^ (l0 & 7)));
-            const uint4 u1 = lds_v4(st + l1 * 128 + 16 * (w ^ (l1 & 7)));
+        for (int w = 0; w < kRWords; ++w) {
+            // word w: k = kTk t + 8 w .. + 7; activation line (row, 64-k block), unit within the line
+            const int k = kTk * t + 8 * w;
+            const int l0 = g * kRXB + k / 64, l1 = (g + 8) * kRXB + k / 64, unit = (k % 64) / 8;
+            const uint4 u0 = lds_v4(st + l0 * 128 + 16 * (unit ^ (l0 & 7)));
+            const uint4 u1 = lds_v4(st + l1 * 128 + 16 * (unit ^ (l1 & 7)));
             // A fragments of the two k16 steps this word feeds: {row g, row g + 8} x {pair b0, pair b1}
             uint4 e0, e1;
             if (kFmt == 0) {  // pairs (k, k+4) as dequant_word delivers them
@@ -176,9 +188,9 @@ __global__ void __launch_bounds__(kRThreads, 3)
                 e0 = make_uint4(u0.x, u1.x, u0.y, u1.y);
                 e1 = make_uint4(u0.z, u1.z, u0.w, u1.w);
             }
-            uint32_t bw[4][4];
+            uint32_t bw[kRTiles][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < kRTiles; ++i) {
                 const uint4& q = wq[i][w >> 2];
                 const uint32_t word = (w & 3) == 0 ? q.x : (w & 3) == 1 ? q.y : (w & 3) == 2 ? q.z : q.w;
                 if (kFmt == 0)
@@ -187,9 +199,9 @@ __global__ void __launch_bounds__(kRThreads, 3)
                     dequant_word_fp4(word, sc[i], bw[i]);
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) mma_m16n8k16(acc[i], e0, bw[i][0], bw[i][1]);
+            for (int i = 0; i < kRTiles; ++i) mma_m16n8k16(acc[i], e0, bw[i][0], bw[i][1]);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) mma_m16n8k16(acc[i], e1, bw[i][2], bw[i][3]);
+            for (int i = 0; i < kRTiles; ++i) mma_m16n8k16(acc[i], e1, bw[i][2], bw[i][3]);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -199,18 +211,19 @@ __global__ void __launch_bounds__(kRThreads, 3)
     // ---------------------------------------------------------------- epilogue
     // accumulator fragment of tile i: (row g, columns 2t, 2t+1) and (row g + 8, same columns)
     float* red = reinterpret_cast<float*>(smem + RLayout::red);
+    constexpr int kRedWarp = 32 * kRTiles * 4;  // floats per warp
     if (ks > 0) {
-        float* dst = red + ((ks - 1) * kRWarpCols + nw) * 512;
+        float* dst = red + ((ks - 1) * kRWarpCols + nw) * kRedWarp;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < kRTiles; ++i)
             *reinterpret_cast<float4*>(dst + (i * 32 + lane) * 4) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
     }
     named_barrier_sync(1, kRConsumers * 32);
     if (ks != 0) return;
     for (int q = 1; q < kRKSplit; ++q) {
-        const float* src = red + ((q - 1) * kRWarpCols + nw) * 512;
+        const float* src = red + ((q - 1) * kRWarpCols + nw) * kRedWarp;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < kRTiles; ++i) {
             const float4 v = *reinterpret_cast<const float4*>(src + (i * 32 + lane) * 4);
             acc[i][0] += v.x;
             acc[i][1] += v.y;
@@ -219,8 +232,8 @@ __global__ void __launch_bounds__(kRThreads, 3)
         }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int col = n0 + nw * 32 + 8 * i + 2 * t;
+    for (int i = 0; i < kRTiles; ++i) {
+        const int col = n0 + nw * 8 * kRTiles + 8 * i + 2 * t;
         if (col >= a.N) continue;  // N % 8 == 0: a tile is wholly in or out
         float b0 = 0.f, b1 = 0.f;
         if (a.bias) {
@@ -248,6 +261,7 @@ __global__ void __launch_bounds__(kRThreads, 3)
 }  // namespace
 
 int w4r_smem_bytes() { return RLayout::alloc; }
+int w4r_chunk() { return kRChunk; }
 
 template <int kFmt>
 static cudaError_t launch_w4r_t(const W4rArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmS,

@@ -167,14 +167,14 @@ tg_status make_map_c(CUtensorMap* m, const void* base, uint64_t N, uint64_t M) {
 }
 
 // Row-major [outer][inner] byte matrix, box of box_inner x box_outer bytes,
-// 128-byte swizzle; out-of-bounds bytes read as zero.
+// 128-byte swizzle (or none); out-of-bounds bytes read as zero.
 tg_status make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                      uint32_t box_outer) {
+                      uint32_t box_outer, bool swizzle = true) {
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner};
     cuuint32_t box[2] = {box_inner, box_outer};
     CUresult r = encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box,
-                               CU_TENSOR_MAP_SWIZZLE_128B);
+                               swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
     if (r != CUDA_SUCCESS)
         return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %llu x %llu byte matrix", (int)r,
                     (unsigned long long)outer, (unsigned long long)inner);
@@ -196,12 +196,12 @@ tg_status make_map_scales(CUtensorMap* m, const void* base, uint64_t inner, uint
 }
 
 // M x K fp16 activations (row-major, M <= 16) as a 3-D map {64, K/64, M}: box
-// {64, 4, 16} = 16 rows x 256 k whose 128-byte lines are (row, 64-k block)
-// pairs, 128-byte swizzle; rows past M read as zero.
-tg_status make_map_x3(CUtensorMap* m, const void* base, uint64_t M, uint64_t K) {
+// {64, chunk/64, 16} = 16 rows x chunk k whose 128-byte lines are (row, 64-k
+// block) pairs, 128-byte swizzle; rows past M read as zero.
+tg_status make_map_x3(CUtensorMap* m, const void* base, uint64_t M, uint64_t K, uint32_t chunk) {
     cuuint64_t dims[3] = {64, K / 64, M};
     cuuint64_t strides[2] = {128, K * 2};
-    cuuint32_t box[3] = {64, 4, 16};
+    cuuint32_t box[3] = {64, chunk / 64, 16};
     CUresult r = encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box,
                                CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS)
@@ -896,13 +896,14 @@ extern "C" tg_status tg_gemm_w4_kernel(const void* A, const void* Bq, const void
         r.bias = static_cast<const __half*>(bias);
         r.C = static_cast<__half*>(C);
         r.M = (int)M; r.N = (int)N; r.gelu = gelu; r.fmt = weight_format;
-        r.n_chunks = (int)((K + 255) / 256);
+        const int chunk = w4r_chunk();
+        r.n_chunks = (int)((K + chunk - 1) / chunk);
         r.c_vec = aligned(C, 4) ? 1 : 0;
         r.wd = watchdog(d);
         CUtensorMap tmW, tmS, tmX;
-        if ((st = make_map_u8(&tmW, Bq, K / 2, N, 128, kW4rCols)) != TG_OK) return st;
-        if ((st = make_map_scales(&tmS, scales, N, K / kW4Group, kW4rCols, 2)) != TG_OK) return st;
-        if ((st = make_map_x3(&tmX, A, M, K)) != TG_OK) return st;
+        if ((st = make_map_u8(&tmW, Bq, K / 2, N, chunk / 2, kW4rCols, chunk / 2 == 128)) != TG_OK) return st;
+        if ((st = make_map_scales(&tmS, scales, N, K / kW4Group, kW4rCols, chunk / kW4Group)) != TG_OK) return st;
+        if ((st = make_map_x3(&tmX, A, M, K, chunk)) != TG_OK) return st;
         const int grid = (int)((N + kW4rCols - 1) / kW4rCols);
         cudaError_t e = launch_w4r(r, tmW, tmS, tmX, grid, stream);
         return e == cudaSuccess ? TG_OK : cuda_fail(e, "4-bit register kernel launch");

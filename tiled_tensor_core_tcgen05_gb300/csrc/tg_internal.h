@@ -197,6 +197,7 @@ int w4_smem_bytes(int m_pad, int stages, int act_slots, int slots);
 cudaError_t launch_w4(const W4Args& a, const CUtensorMap& tmBq, const CUtensorMap& tmA, const CUtensorMap& tmS,
                       int grid, cudaStream_t stream);
 int w4r_smem_bytes();
+int w4r_chunk();   // k per ring stage of the register-dequant kernel (128 or 256)
 cudaError_t launch_w4r(const W4rArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmS, const CUtensorMap& tmX,
                        int grid, cudaStream_t stream);
 cudaError_t launch_softmax(const __half* X, __half* Y, int M, int N, bool vec, int sm_count, cudaStream_t stream);
