@@ -200,8 +200,19 @@ def barrier(pg):
 # ------------------------------------------------------------------ GPU arm
 
 KERNELS = {"auto": 0, "tiled": 1, "lsu": 2, "splitk": 3, "pair": 4}
+# the 4-bit GEMM's kernels (tg_gemm_w4_kernel), for --kernel with a 4-bit workload
+W4_KERNELS = {"auto": 0, "w4tmem": 1, "w4reg": 2}
 # one-thread oracle timings: the whole product (None) or its first rows
 ONE_THREAD_ROWS = {"square_256": None, "ragged_1000x1030x520_bias_gelu": None, "decode_16x28672x8192": 2}
+
+
+def kernel_code(w, name: str) -> int:
+    """The --kernel choice as the code the workload's entry point takes."""
+    import workloads
+    table = W4_KERNELS if isinstance(w, workloads.W4Workload) else KERNELS
+    if name not in table:
+        raise SystemExit(f"--kernel {name} does not apply to {w.name}")
+    return table[name]
 
 
 def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sampler=None, kernel: int = 0):
@@ -239,10 +250,10 @@ def time_workload(tg, w, steps: int, warmup: int, flush_bytes: int, pg=None, sam
         dA, dB, ds = A.cuda(), Bq.cuda(), sc.cuda()
         db = bias.cuda() if bias is not None else None
         args = (dA.data_ptr(), dB.data_ptr(), ds.data_ptr(), db.data_ptr() if db is not None else None,
-                dC.data_ptr(), w.M, w.N, w.K, int(w.gelu), w.fmt_code, 0, sh)
+                dC.data_ptr(), w.M, w.N, w.K, int(w.gelu), w.fmt_code, kernel, 0, sh)
 
         def call():
-            tg.tg_gemm_w4_ex(*args)
+            tg.tg_gemm_w4_kernel(*args)
     else:
         A, B, bias = w.inputs()
         host_inputs = (A, B, bias)
@@ -634,7 +645,7 @@ def run_gpu(args):
     oracle_threads()
     sampler = ClockSampler(local) if rank == 0 else None
     res = time_workload(tg, main, args.steps, args.warmup, 0 if main.bytes() > 2 * l2 else 2 * l2 + (1 << 20),
-                        pg=pg, sampler=sampler, kernel=KERNELS[args.kernel])
+                        pg=pg, sampler=sampler, kernel=kernel_code(main, args.kernel))
     ms_per_step = res["region_ms"] / args.steps
     avg_launch = res["kernel_ms"] / args.steps
     gemm_main = isinstance(main, workloads.Workload)
@@ -776,8 +787,9 @@ def main():
     ap.add_argument("--impl", choices=["tg", "reference"], default="tg")
     ap.add_argument("--workload", default="square_8192")
     ap.add_argument("--only-main", action="store_true", help="time the headline workload only")
-    ap.add_argument("--kernel", choices=sorted(KERNELS), default="auto",
-                    help="pin the kernel of the headline workload (profiling); default: the library's choice")
+    ap.add_argument("--kernel", choices=sorted(set(KERNELS) | set(W4_KERNELS)), default="auto",
+                    help="pin the kernel of the headline workload (profiling): GEMM kernels for GEMM workloads, "
+                         "w4tmem / w4reg for 4-bit ones; default: the library's choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0, help="oracle seconds for the headline workload")
     ap.add_argument("--cpu-budget-other-s", type=float, default=2.0, help="oracle seconds for each other workload")
