@@ -83,6 +83,11 @@ __device__ __forceinline__ Unit unit_of(int u, int split_from) {
     return Unit{split_from + (j >> 1), (j & 1) * (kPairBN / 2), kPairBN / 2};
 }
 
+// K order: a CTA's odd work units walk K backwards, so a wave starts on the k-blocks the
+// previous wave read last (most likely still in L2)
+#ifndef TG_PAIR_KSERP
+#define TG_PAIR_KSERP 1
+#endif
 #ifndef TG_PAIR_SERPENTINE
 #define TG_PAIR_SERPENTINE 1
 #endif
@@ -155,16 +160,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
-            for (int u = cluster; u < args.num_units && ok; u += num_clusters) {
+            int it = 0;
+            for (int u = cluster; u < args.num_units && ok; u += num_clusters, ++it) {
                 const Unit un = unit_of(u, args.split_from);
                 int mb, nb;
                 tile_coords(un.tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
+                const bool backwards = TG_PAIR_KSERP && (it & 1);
                 const int m0 = mb * kPairBM + rank * kHalfM;
                 // this CTA's half of the unit's columns: 128 of a whole tile, 64 of a half tile
                 const int n0 = nb * kPairBN + un.col0 + rank * (un.width / 2);
                 const bool whole = un.width == kPairBN;
                 const uint32_t bytes = kStageA + (whole ? kStageB : kStageB / 2);
-                for (int kb = 0; kb < args.num_kb; ++kb) {
+                for (int i = 0; i < args.num_kb; ++i) {
+                    const int kb = backwards ? args.num_kb - 1 - i : i;
                     if (!wait_phase(empty_bar(stage), phase ^ 1, wc, kSiteProducerEmpty)) { ok = false; break; }
                     const uint32_t sA = sbase + stage * kStageBytes;
                     const uint32_t sB = sA + kStageA;
