@@ -198,3 +198,18 @@ def test_all_core_baselines_survive_a_one_thread_timing():
     b.cpu_baseline_one_thread(workloads.custom(8, 16, 16, seed=8))  # leaves the oracle at one thread
     e = b.cpu_baseline(workloads.custom(32, 64, 48, seed=9), 0.05, "TFLOP/s")
     assert e["cores"] == n
+
+
+def test_kernel_pinning_maps_to_each_entry_points_codes():
+    """--kernel takes GEMM kernel names for GEMM workloads and w4tmem / w4reg for
+    4-bit ones, and refuses a name that does not apply to the workload."""
+    b = _bench()
+    import workloads
+    gemm = workloads.BY_NAME["square_8192"]
+    w4 = workloads.DECODE_W4
+    assert b.kernel_code(gemm, "auto") == 0 and b.kernel_code(gemm, "pair") == 4
+    assert b.kernel_code(w4, "auto") == 0 and b.kernel_code(w4, "w4tmem") == 1 and b.kernel_code(w4, "w4reg") == 2
+    with pytest.raises(SystemExit):
+        b.kernel_code(gemm, "w4reg")
+    with pytest.raises(SystemExit):
+        b.kernel_code(w4, "pair")
