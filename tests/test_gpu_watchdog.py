@@ -57,3 +57,28 @@ def test_hook_off_by_default(tg):
     C = tg.gemm(A.cuda(), B.cuda(), kernel=tg.KERNEL_TILED_TMA)
     assert np.array_equal(C.cpu().numpy().view(np.uint16), oracle.gemm(A, B).view(np.uint16))
     assert tg.tg_device_status(None) == (tg.OK, 0)
+
+
+def test_withheld_stage_in_the_register_4bit_kernel_times_out_and_recovers(tg):
+    """The same hook in the register-dequant 4-bit kernel: its producer never fills the
+    first stage of each CTA, so those consumers' bounded wait expires (or, a moment later,
+    the producer's wait for that stage to be freed)."""
+    w = workloads.W4Workload("wd_w4r", 16, 1024, 2048, seed=33, a_dist=workloads.Dist("int", -2, 2),
+                             scale_kind="pow2")
+    A, Bq, s, _ = w.inputs()
+    dA, dBq, ds = A.cuda(), Bq.cuda(), s.cuda()
+    assert tg.tg_device_status(None) == (tg.OK, 0)
+    tg.tg_set_watchdog_ns(20_000_000)  # 20 ms
+    tg.tg_debug_skip_first_arrive(True)
+    try:
+        tg.gemm_w4(dA, dBq, ds, kernel=tg.W4_KERNEL_REG)
+        st, where = tg.tg_device_status(None)
+    finally:
+        tg.tg_debug_skip_first_arrive(False)
+        tg.tg_set_watchdog_ns(0)
+    assert st == tg.ERR_TIMEOUT
+    assert where in (6, 1)  # a consumer's wait for the stage, or the producer's wait to refill it
+    assert tg.tg_device_status(None) == (tg.OK, 0)
+    C = tg.gemm_w4(dA, dBq, ds, kernel=tg.W4_KERNEL_REG)
+    assert np.array_equal(C.cpu().numpy().view(np.uint16), oracle.gemm_w4(A, Bq, s).view(np.uint16))
+    assert tg.tg_device_status(None) == (tg.OK, 0)

@@ -119,21 +119,26 @@ __global__ void __launch_bounds__(kRThreads, 3)
         if (lane == 0) {
             const uint64_t pol_stream = l2_policy_evict_first();  // weights and scales: read once
             const uint64_t pol_keep = l2_policy_evict_last();     // activations: read by every CTA
+            const bool skip_first = a.wd.skip_first_arrive != 0;
             int issued = 0;
             for (int c = 0; c < nch; ++c) {
                 const int slot = c % kRStages;
                 if (!wait_phase(empty(slot), ((c / kRStages) & 1) ^ 1, wc, kSiteProducerEmpty)) break;
                 const uint32_t st = sb + slot * kRStage;
-                mbar_arrive_expect_tx(full(slot), kRTx);
-                tma_load_3d_hint(st, &tmX, full(slot), 0, c * kRXB, 0, pol_keep);
-                tma_load_2d_hint(st + kRXBytes, &tmW, full(slot), c * kRWRow, n0, pol_stream);
-                tma_load_2d_hint(st + kRXBytes + kRWBytes, &tmS, full(slot), n0, c * kRGroups, pol_stream);
+                // test hook (watchdog tests): the first stage is never filled, so its
+                // consumers' bounded wait must expire
+                if (!(skip_first && c == 0)) {
+                    mbar_arrive_expect_tx(full(slot), kRTx);
+                    tma_load_3d_hint(st, &tmX, full(slot), 0, c * kRXB, 0, pol_keep);
+                    tma_load_2d_hint(st + kRXBytes, &tmW, full(slot), c * kRWRow, n0, pol_stream);
+                    tma_load_2d_hint(st + kRXBytes + kRWBytes, &tmS, full(slot), n0, c * kRGroups, pol_stream);
+                }
                 issued = c + 1;
             }
             // let the copies in flight land before the CTA can exit (consumers that
             // gave up no longer wait for them)
             for (int c = issued - kRStages < 0 ? 0 : issued - kRStages; c < issued; ++c)
-                wait_phase_drain(full(c % kRStages), (c / kRStages) & 1, wc);
+                if (!(skip_first && c == 0)) wait_phase_drain(full(c % kRStages), (c / kRStages) & 1, wc);
         }
         return;
     }
