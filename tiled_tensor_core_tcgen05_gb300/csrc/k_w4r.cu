@@ -13,11 +13,17 @@
 // Why warp-level MMAs. A tcgen05 MMA has at least 64 rows and costs at least
 // ~93 cycles per instruction; with 16 tokens the tensor-memory kernel pads M
 // to 64 and still spends ~29 us on MMA issue for 16 x 28672 x 8192. The
-// m16n8k16 MMA has exactly 16 rows (the tokens), takes its B operand (the
-// weights) from registers, and issues one per 8 cycles per warp; the 7.5 GFLOP
-// of that shape need ~12 us of it, and no converted tile is written to or read
-// back from shared memory (the tensor-memory kernel's bound: 4 bytes of
-// shared-memory traffic per converted weight).
+// m16n8k16 MMA takes both operands from registers and issues one per 8 cycles
+// per warp; the 7.5 GFLOP of that shape need ~12 us of it, and no converted
+// tile is written to or read back from shared memory (the tensor-memory
+// kernel's bound: 4 bytes of shared-memory traffic per converted weight).
+// Operand roles: the product is computed transposed, C^T = W^T A^T. The MMA's
+// 16 rows are 16 weight columns (its A operand, decoded in registers) and its 8
+// columns are 8 tokens (its B operand), two MMAs for the 16 tokens. A B
+// fragment holds consecutive k pairs of one token, which is what one 16-byte
+// shared-memory load of that token's activations delivers, so the loaded
+// registers feed the MMA as they are; the opposite roles would interleave two
+// tokens' registers in every fragment and cost a register move per pair.
 //
 // Work. A CTA owns 64 consecutive output columns (two warp-columns of 32) for
 // the whole K, so no partial sums leave the CTA. K is streamed in chunks of
@@ -32,10 +38,12 @@
 //              (g, t) = (lane / 4, lane % 4) holds weight column 8 i + g of
 //              the warp-column's four 8-column tiles i and the k range
 //              [64 t, 64 t + 64) of each chunk (two 16-byte words per tile),
-//              decodes each 8-weight word into the B registers of two MMAs,
-//              and reads the matching activation fragment from shared
-//              memory (for INT4 reordered into the decoder's (k, k+4) pairs
-//              with byte permutes; FP4 pairs are already in order);
+//              decodes each 8-weight word into the A registers of two MMAs
+//              (tiles 2b and 2b + 1 are the MMA rows g and g + 8 of 16-column
+//              block b), and reads tokens g and g + 8 of the same k range
+//              from shared memory as the B registers (for INT4 reordered
+//              into the decoder's (k, k+4) pairs with byte permutes; FP4
+//              pairs are already in order);
 //   warp 4     producer: one lane issues the three TMA copies of each chunk.
 // The two partial sums of a warp-column (even and odd chunks) are added in
 // that order through shared memory; bias, GELU and one rounding to fp16 follow.
@@ -178,20 +186,21 @@ __global__ void __launch_bounds__(kRThreads, 3)
             const int l0 = g * kRXB + k / 64, l1 = (g + 8) * kRXB + k / 64, unit = (k % 64) / 8;
             const uint4 u0 = lds_v4(st + l0 * 128 + 16 * (unit ^ (l0 & 7)));
             const uint4 u1 = lds_v4(st + l1 * 128 + 16 * (unit ^ (l1 & 7)));
-            // A fragments of the two k16 steps this word feeds: {row g, row g + 8} x {pair b0, pair b1}
-            uint4 e0, e1;
-            if (kFmt == 0) {  // pairs (k, k+4) as dequant_word delivers them
-                e0.x = __byte_perm(u0.x, u0.z, 0x5410);
-                e0.y = __byte_perm(u1.x, u1.z, 0x5410);
-                e0.z = __byte_perm(u0.x, u0.z, 0x7632);
-                e0.w = __byte_perm(u1.x, u1.z, 0x7632);
-                e1.x = __byte_perm(u0.y, u0.w, 0x5410);
-                e1.y = __byte_perm(u1.y, u1.w, 0x5410);
-                e1.z = __byte_perm(u0.y, u0.w, 0x7632);
-                e1.w = __byte_perm(u1.y, u1.w, 0x7632);
-            } else {  // natural pairs (k, k+1)
-                e0 = make_uint4(u0.x, u1.x, u0.y, u1.y);
-                e1 = make_uint4(u0.z, u1.z, u0.w, u1.w);
+            // B fragments (token g of each 8-token half h, u0 for rows 0-7 and u1 for rows 8-15):
+            // the k pairs of the word's two k16 steps, in the order the decoder delivers the weights
+            uint32_t xb[2][4];
+            if (kFmt == 0) {  // pairs (k, k+4), (k+1, k+5), ...
+                xb[0][0] = __byte_perm(u0.x, u0.z, 0x5410);
+                xb[0][1] = __byte_perm(u0.x, u0.z, 0x7632);
+                xb[0][2] = __byte_perm(u0.y, u0.w, 0x5410);
+                xb[0][3] = __byte_perm(u0.y, u0.w, 0x7632);
+                xb[1][0] = __byte_perm(u1.x, u1.z, 0x5410);
+                xb[1][1] = __byte_perm(u1.x, u1.z, 0x7632);
+                xb[1][2] = __byte_perm(u1.y, u1.w, 0x5410);
+                xb[1][3] = __byte_perm(u1.y, u1.w, 0x7632);
+            } else {  // natural pairs (k, k+1): the loaded registers as they are
+                xb[0][0] = u0.x, xb[0][1] = u0.y, xb[0][2] = u0.z, xb[0][3] = u0.w;
+                xb[1][0] = u1.x, xb[1][1] = u1.y, xb[1][2] = u1.z, xb[1][3] = u1.w;
             }
             uint32_t bw[kRTiles][4];
 #pragma unroll
@@ -203,10 +212,16 @@ __global__ void __launch_bounds__(kRThreads, 3)
                 else
                     dequant_word_fp4(word, sc[i], bw[i]);
             }
+            // A fragments: MMA rows g and g + 8 are the weight columns of tiles 2b and 2b + 1
 #pragma unroll
-            for (int i = 0; i < kRTiles; ++i) mma_m16n8k16(acc[i], e0, bw[i][0], bw[i][1]);
+            for (int s = 0; s < 2; ++s)
 #pragma unroll
-            for (int i = 0; i < kRTiles; ++i) mma_m16n8k16(acc[i], e1, bw[i][2], bw[i][3]);
+                for (int b = 0; b < kRTiles / 2; ++b) {
+                    const uint4 af = make_uint4(bw[2 * b][2 * s], bw[2 * b + 1][2 * s], bw[2 * b][2 * s + 1],
+                                                bw[2 * b + 1][2 * s + 1]);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) mma_m16n8k16(acc[2 * b + h], af, xb[h][2 * s], xb[h][2 * s + 1]);
+                }
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -214,7 +229,8 @@ __global__ void __launch_bounds__(kRThreads, 3)
     }
 
     // ---------------------------------------------------------------- epilogue
-    // accumulator fragment of tile i: (row g, columns 2t, 2t+1) and (row g + 8, same columns)
+    // accumulator 2 b + h (16-column block b, token half h): columns 16 b + g and 16 b + 8 + g
+    // of the warp-column (MMA rows g, g + 8) x tokens 8 h + 2 t and 8 h + 2 t + 1 (MMA columns)
     float* red = reinterpret_cast<float*>(smem + RLayout::red);
     constexpr int kRedWarp = 32 * kRTiles * 4;  // floats per warp
     if (ks > 0) {
@@ -237,28 +253,22 @@ __global__ void __launch_bounds__(kRThreads, 3)
         }
     }
 #pragma unroll
-    for (int i = 0; i < kRTiles; ++i) {
-        const int col = n0 + nw * 8 * kRTiles + 8 * i + 2 * t;
-        if (col >= a.N) continue;  // N % 8 == 0: a tile is wholly in or out
-        float b0 = 0.f, b1 = 0.f;
-        if (a.bias) {
-            b0 = __half2float(a.bias[col]);
-            b1 = __half2float(a.bias[col + 1]);
-        }
+    for (int b = 0; b < kRTiles / 2; ++b) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int row = g + 8 * h;
-            if (row >= a.M) continue;
-            const __half v0 = __float2half_rn(epi_value(acc[i][2 * h], b0, a.gelu));
-            const __half v1 = __float2half_rn(epi_value(acc[i][2 * h + 1], b1, a.gelu));
-            const int64_t off = static_cast<int64_t>(row) * a.N + col;
-            if (!dbg_check(dbg_in(off, 2, static_cast<int64_t>(a.M) * a.N), a.wd)) continue;
-            if (a.c_vec) {
-                *reinterpret_cast<__half2*>(a.C + off) = __halves2half2(v0, v1);
-            } else {
-                a.C[off] = v0;
-                a.C[off + 1] = v1;
-            }
+        for (int hi = 0; hi < 2; ++hi) {  // column g or g + 8 of the 16-column block
+            const int col = n0 + nw * 8 * kRTiles + 16 * b + 8 * hi + g;
+            if (col >= a.N) continue;
+            const float bv = a.bias ? __half2float(a.bias[col]) : 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int row = 8 * h + 2 * t + e;
+                    if (row >= a.M) continue;
+                    const int64_t off = static_cast<int64_t>(row) * a.N + col;
+                    if (!dbg_check(dbg_in(off, 1, static_cast<int64_t>(a.M) * a.N), a.wd)) continue;
+                    a.C[off] = __float2half_rn(epi_value(acc[2 * b + h][2 * hi + e], bv, a.gelu));
+                }
         }
     }
 }

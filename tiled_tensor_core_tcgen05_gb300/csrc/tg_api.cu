@@ -898,7 +898,6 @@ extern "C" tg_status tg_gemm_w4_kernel(const void* A, const void* Bq, const void
         r.M = (int)M; r.N = (int)N; r.gelu = gelu; r.fmt = weight_format;
         const int chunk = w4r_chunk();
         r.n_chunks = (int)((K + chunk - 1) / chunk);
-        r.c_vec = aligned(C, 4) ? 1 : 0;
         r.wd = watchdog(d);
         CUtensorMap tmW, tmS, tmX;
         if ((st = make_map_u8(&tmW, Bq, K / 2, N, chunk / 2, kW4rCols, chunk / 2 == 128)) != TG_OK) return st;

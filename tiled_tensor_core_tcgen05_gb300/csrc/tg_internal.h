@@ -150,7 +150,6 @@ struct W4rArgs {
     int n_chunks;              // K / 256, rounded up
     int gelu;
     int fmt;                   // 0: two's-complement INT4, 1: FP4 (E2M1)
-    int c_vec;                 // C 4-byte aligned: paired stores
     Watchdog wd;
 };
 
