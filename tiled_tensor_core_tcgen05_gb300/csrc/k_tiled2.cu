@@ -15,9 +15,15 @@
 // columns of B for each K block by TMA into its own 6-stage ring; the copies
 // of BOTH CTAs complete on the even CTA's "full" barrier (the pair form of the
 // TMA copy), which the even CTA arms with the bytes of both halves. Warp 1
-// lane 0 of the even CTA issues the pair MMAs; warps 2..9 are the epilogue,
-// each CTA reading its own 128 accumulator rows from its own tensor memory
-// (two warps per quarter of the rows, each taking half of the columns).
+// lane 0 of the even CTA issues the pair MMAs; warps 2..5 are the epilogue,
+// each CTA reading its own 128 accumulator rows from its own tensor memory (one
+// warp per quarter of the rows; with eight epilogue warps, two per quarter, each
+// taking half of the columns). A warp reaches only the tensor-memory lanes of its
+// scheduler (warp % 4), so the rows of quarter 1 are read on the scheduler that
+// also runs the MMA-issuing warp; measured, bias + GELU there slowed the MMA issue
+// by ~8%. So with four epilogue warps, warp 5 only moves its chunks from tensor
+// memory into a two-slot shared-memory hand-off buffer, and a helper, warp 6
+// (scheduler 2), applies bias and GELU and stores them.
 // MMA completion is committed to both CTAs at once (multicast), freeing the
 // stage in both rings and publishing the accumulator to both epilogues; both
 // epilogues release the accumulator to the issuer with one arrive per warp.
@@ -47,7 +53,13 @@ constexpr int kBoxB = kBK * 64 * 2;
 constexpr int kAccBufs = TG_PAIR_ACC_BUFS;  // accumulators per CTA (256 fp32 columns each)
 constexpr int kTmemCols = kAccBufs * kPairBN;
 constexpr int kEpiWarp0 = 2;
-constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+// hand-off of quarter 1 (the MMA warp's scheduler) to a helper warp; four epilogue warps only
+constexpr bool kHandoff = kEpiWarps == 4;
+constexpr int kHandQuarter = 1;                    // warp 1 (MMA issue) % 4
+constexpr int kHelpWarp = kEpiWarp0 + kEpiWarps;   // warp 6: scheduler 2
+constexpr int kHandSlots = 2;
+constexpr int kHandSlotBytes = 32 * 32 * 4;        // one 32-row x 32-column fp32 chunk
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps + (kHandoff ? 1 : 0)) * 32;
 
 constexpr int kBarFull = kRingBytes;
 constexpr int kBarEmpty = kBarFull + 8 * kPairStages;
@@ -59,9 +71,15 @@ constexpr int kAbortSlot = kTmemSlot + 4;
 // per-warp output staging: two TMA-store boxes (or one padded st.global chunk)
 constexpr int kEpiWarpBytes = 2 * kStoreBoxBytes;
 static_assert(kEpiWarpBytes >= kStageWarpBytes, "staging covers both store paths");
-constexpr int kEpiStage = (kAbortSlot + 4 + 1023) / 1024 * 1024;
-constexpr int kSmemUsed = kEpiStage + kEpiWarps * kEpiWarpBytes;
+constexpr int kBarHandFull = kAbortSlot + 4;
+constexpr int kBarHandEmpty = kBarHandFull + 8 * kHandSlots;
+static_assert(kBarHandFull % 8 == 0, "mbarriers are 8-byte aligned");
+constexpr int kEpiStage = (kBarHandEmpty + 8 * kHandSlots + 1023) / 1024 * 1024;
+constexpr int kStoreWarps = kEpiWarps + (kHandoff ? 1 : 0);  // warps that stage and store C
+constexpr int kHandBuf = kEpiStage + kStoreWarps * kEpiWarpBytes;
+constexpr int kSmemUsed = kHandBuf + (kHandoff ? kHandSlots * kHandSlotBytes : 0);
 constexpr int kSmemAlloc = kSmemUsed + 1024;
+static_assert(kSmemAlloc <= 227 * 1024, "one CTA's dynamic shared memory");
 
 // M=256 (pair), N=256, A K-major, B N-major; and the half-width form (N=128)
 // used for the split tiles of the last wave.
@@ -124,6 +142,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto acc_full_bar = [&](int b) { return sbase + kBarAccFull + 8 * b; };
     auto acc_empty_bar = [&](int b) { return sbase + kBarAccEmpty + 8 * b; };
     const uint32_t drain_bar = sbase + kBarDrain;
+    auto hand_full_bar = [&](int h) { return sbase + kBarHandFull + 8 * h; };
+    auto hand_empty_bar = [&](int h) { return sbase + kBarHandEmpty + 8 * h; };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortSlot);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
 
@@ -137,6 +157,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(acc_empty_bar(b), 2 * kEpiWarps);  // one arrive per epilogue warp, both CTAs
         }
         mbar_init(drain_bar, 1);
+        for (int h = 0; h < kHandSlots; ++h) {
+            mbar_init(hand_full_bar(h), 32);   // every lane of the quarter-1 warp, after its writes
+            mbar_init(hand_empty_bar(h), 32);  // every lane of the helper, after its reads
+        }
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
@@ -232,15 +256,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             wait_phase_drain(drain_bar, 0, wc);
         }
         __syncwarp();
+    } else if (kHandoff && warp == kHelpWarp) {
+        // ------------------------------------------------------------ helper: quarter 1's math
+        // Walks the same units and chunks as the quarter-1 warp, taking each chunk from the
+        // hand-off buffer instead of tensor memory.
+        const int row_in_tile = rank * kHalfM + kHandQuarter * 32 + lane;
+        uint8_t* stage = smem + kEpiStage + kEpiWarps * kEpiWarpBytes;
+        int nstore = 0, hc = 0;
+        bool ok = true;
+        for (int u = cluster; u < args.num_units && ok; u += num_clusters) {
+            const Unit un = unit_of(u, args.split_from);
+            int mb, nb;
+            tile_coords(un.tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
+            const int row = mb * kPairBM + row_in_tile;
+            const int n0 = nb * kPairBN + un.col0;
+            const int chunks = max(0, min(un.width / 32, (args.N - n0 + 31) / 32));
+            for (int c = 0; c < chunks; ++c, ++hc) {
+                const int slot = hc % kHandSlots;
+                if (!__all_sync(0xFFFFFFFFu,
+                                wait_phase(hand_full_bar(slot), (hc / kHandSlots) & 1, wc, kSiteEpilogueAccFull))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t src = sbase + kHandBuf + slot * kHandSlotBytes + lane * 128;
+                uint32_t r[32];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 v = lds_v4(src + 16 * (q ^ (lane & 7)));
+                    r[4 * q] = v.x, r[4 * q + 1] = v.y, r[4 * q + 2] = v.z, r[4 * q + 3] = v.w;
+                }
+                mbar_arrive(hand_empty_bar(slot));
+                if (kTmaStore) {
+                    if (lane == 0 && nstore >= 2) bulk_wait_group_read<1>();
+                    __syncwarp();
+                    epilogue_chunk_tma(r, smem_u32(stage) + (nstore & 1) * kStoreBoxBytes, &tmC, args.bias,
+                                       row - lane, n0 + c * 32, args.N, args.gelu, args.bias_vec, args.wd);
+                    ++nstore;
+                } else {
+                    epilogue_chunk(r, stage, args.C, args.bias, row - lane, n0 + c * 32, args.M, args.N, args.gelu,
+                                   args.c_store, args.bias_vec);
+                }
+            }
+        }
+        if (kTmaStore && lane == 0) bulk_wait_group_all();  // every store of this warp has completed
     } else {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int quarter = warp & 3;
         const int half = (warp - kEpiWarp0) >> 2;
+        const bool hand_src = kHandoff && quarter == kHandQuarter;  // this warp's math runs on the helper
         const int row_in_tile = rank * kHalfM + quarter * 32 + lane;
         uint8_t* stage = smem + kEpiStage + (warp - kEpiWarp0) * kEpiWarpBytes;
         const uint32_t leader_acc_empty0 = mapa_shared(acc_empty_bar(0), 0);
-        int it = 0, nstore = 0;
-        for (int u = cluster; u < args.num_units; u += num_clusters, ++it) {
+        int it = 0, nstore = 0, hc = 0;
+        bool ok = true;
+        for (int u = cluster; u < args.num_units && ok; u += num_clusters, ++it) {
             const Unit un = unit_of(u, args.split_from);
             int mb, nb;
             tile_coords(un.tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
@@ -270,7 +339,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(leader_acc_empty0 + 8 * b);
                 }
-                if (kTmaStore) {
+                if (hand_src) {
+                    // the chunk goes to the helper: row `lane` of the slot, 16-byte units
+                    // rotated by lane % 8 (conflict-free for both sides' 16-byte accesses)
+                    const int slot = hc % kHandSlots;
+                    if (!__all_sync(0xFFFFFFFFu, wait_phase(hand_empty_bar(slot), ((hc / kHandSlots) & 1) ^ 1, wc,
+                                                            kSiteEpilogueAccFull))) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = sbase + kHandBuf + slot * kHandSlotBytes + lane * 128;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        sts_v4(dst + 16 * (q ^ (lane & 7)), make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]));
+                    mbar_arrive(hand_full_bar(slot));
+                    ++hc;
+                } else if (kTmaStore) {
                     // this warp's two staging boxes alternate: the store issued two chunks ago
                     // must have read its box before the box is written again
                     if (lane == 0 && nstore >= 2) bulk_wait_group_read<1>();
