@@ -484,6 +484,22 @@ bool pair_pays(const DeviceState& d, int64_t M, int64_t N) {
     return pair_tiles >= d.sm_count / 2;
 }
 
+// True when the skinny split-K kernel beats the single-CTA tiled kernel for M <= 128
+// (measured on GB300 over N = 2048..57344, K = 2048..14336, M = 1..128). The split-K
+// kernel's time per K block grows with the padded M (a step between 48 and 64 rows),
+// while the tiled kernel cannot split K. So split-K is used for M <= 16; above that
+// only when the tiled kernel's 64-column tiles would leave more than half the SMs
+// idle over a long K loop (at least 2 M blocks of 64 for M <= 48, 3 M above), or
+// when, with M <= 64, the product streams 256 MB or more of B (both kernels then sit
+// near the HBM floor, split-K slightly ahead).
+bool skinny_pays(const DeviceState& d, int64_t M, int64_t N, int64_t K) {
+    if (M <= 16) return true;
+    const int64_t tiles64 = (N + 63) / 64;  // one 128-row block: M <= 128
+    const int64_t kb = (K + 63) / 64;
+    if (2 * tiles64 < d.sm_count && kb >= (M <= 48 ? 2 : 3) * M) return true;
+    return M <= 64 && 2.0 * static_cast<double>(K) * static_cast<double>(N) >= 256.0 * 1048576.0;
+}
+
 // A GEMM whose A or B TMA cannot describe (row stride not a multiple of 16
 // bytes, or base not 16-byte aligned): each such operand is first copied into
 // the stream's aligned-stride buffer (row stride rounded up to 8 elements),
@@ -603,7 +619,8 @@ tg_status tg_gemm_ex(const void* A, const void* B, const void* bias, void* C, in
                 return run_padded(d, a, b, bi, c, (int)M, (int)N, (int)K, gelu, stream);
             k = TG_KERNEL_TILED_LSU;
         } else if (M <= kSkMaxM) {
-            k = TG_KERNEL_SPLITK;
+            // 256-row pair tiles would be mostly padding here
+            k = skinny_pays(d, M, N, K) ? TG_KERNEL_SPLITK : TG_KERNEL_TILED_TMA;
         } else {
             // CTA pairs once there is at least one wave of 256x256 tiles for them;
             // smaller problems keep more, smaller 128x256 tiles on single CTAs
