@@ -116,6 +116,9 @@ def test_splitk_explicit_splits_bitwise(tg, split_k):
 @pytest.mark.parametrize("M,N,K,gelu", [
     (200, 264, 136, True), (70, 131, 67, True), (129, 257, 520, False), (512, 512, 512, True),
     (16, 1024, 4096, True), (100, 136, 1000, True), (1, 4096, 4096, False), (128, 2048, 8192, False),
+    # both sides of the automatic skinny / tiled choice for 16 < M <= 128: few 64-column tiles
+    # with a long K loop (split-K up to M = 48 here, tiled at 64), and a short K loop (tiled)
+    (24, 2048, 4096, True), (48, 1024, 8192, False), (64, 1024, 8192, True), (96, 3072, 2048, True),
 ])
 def test_random_inputs_all_kernels(tg, M, N, K, gelu):
     w = workloads.custom(M, N, K, seed=M + N + K, bias=workloads.Dist("uniform", -0.1, 0.1), gelu=gelu)
