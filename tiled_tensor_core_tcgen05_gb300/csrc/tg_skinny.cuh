@@ -103,22 +103,46 @@ __device__ __forceinline__ void skinny_epilogue(const SplitArgs& args, uint32_t 
                     const float bias_n = args.bias != nullptr ? __half2float(args.bias[n]) : 0.0f;
                     for (int m0 = 0; m0 < args.M; m0 += 16) {
                         // this column's 16 rows m0..m0+15 of every slice: four 16-byte loads per
-                        // slice; each row sums its slices in order 0, 1, ... (deterministic)
+                        // slice; each row sums its slices in order 0, 1, ... (deterministic). The
+                        // loads of kBatch slices are issued before any of them is added, so the
+                        // reduction waits for one L2 round trip per kBatch slices, not per slice.
+                        constexpr int kBatch = 4;
                         float s[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) s[i] = 0.0f;
-                        for (int q = 0; q < args.splits; ++q) {
+                        auto add_slice = [&](const float4 (&p)[4]) {
+#pragma unroll
+                            for (int v4 = 0; v4 < 4; ++v4) {
+                                s[4 * v4] += p[v4].x;
+                                s[4 * v4 + 1] += p[v4].y;
+                                s[4 * v4 + 2] += p[v4].z;
+                                s[4 * v4 + 3] += p[v4].w;
+                            }
+                        };
+                        int q = 0;
+                        for (; q + kBatch <= args.splits; q += kBatch) {
+                            float4 p[kBatch][4];
+                            bool in[kBatch];
+#pragma unroll
+                            for (int j = 0; j < kBatch; ++j) {
+                                const int64_t off = (static_cast<int64_t>(q + j) * args.N + n) * args.m_pad + m0;
+                                in[j] = dbg_check(dbg_in(off, 16, args.wd.ws_floats), args.wd);
+                                const float4* wq = reinterpret_cast<const float4*>(args.ws + (in[j] ? off : 0));
+#pragma unroll
+                                for (int v4 = 0; v4 < 4; ++v4) p[j][v4] = __ldcg(wq + v4);
+                            }
+#pragma unroll
+                            for (int j = 0; j < kBatch; ++j)
+                                if (in[j]) add_slice(p[j]);
+                        }
+                        for (; q < args.splits; ++q) {
                             const int64_t off = (static_cast<int64_t>(q) * args.N + n) * args.m_pad + m0;
                             if (!dbg_check(dbg_in(off, 16, args.wd.ws_floats), args.wd)) continue;
                             const float4* wq = reinterpret_cast<const float4*>(args.ws + off);
+                            float4 p[4];
 #pragma unroll
-                            for (int v4 = 0; v4 < 4; ++v4) {
-                                const float4 p = __ldcg(wq + v4);
-                                s[4 * v4] += p.x;
-                                s[4 * v4 + 1] += p.y;
-                                s[4 * v4 + 2] += p.z;
-                                s[4 * v4 + 3] += p.w;
-                            }
+                            for (int v4 = 0; v4 < 4; ++v4) p[v4] = __ldcg(wq + v4);
+                            add_slice(p);
                         }
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
