@@ -319,10 +319,12 @@ tg_status tg_debug_status(tg_stream_t stream);
 tg_status tg_set_watchdog_ns(uint64_t ns);
 
 /*
- * Test hook for the watchdog: while `on` is non-zero, the TMA producer of the
- * tiled kernel skips its arrival on the first pipeline stage of every CTA, so
- * the consumers' bounded waits expire and the call ends with TG_ERR_TIMEOUT
- * from tg_device_status. Off by default; has no effect on other kernels.
+ * Test hook for the watchdog: while `on` is non-zero, the TMA producers of the
+ * tiled kernels (TG_KERNEL_TILED_TMA, TG_KERNEL_TILED_PAIR) and of the 4-bit
+ * register kernel (TG_W4_KERNEL_REG) skip the first pipeline stage of every
+ * CTA (every CTA pair for the pair kernel), so the consumers' bounded waits
+ * expire and the call ends with TG_ERR_TIMEOUT from tg_device_status. Off by
+ * default; has no effect on other kernels.
  */
 tg_status tg_debug_skip_first_arrive(int on);
 

@@ -51,6 +51,32 @@ def test_withheld_arrival_times_out_and_recovers(tg):
     assert tg.tg_device_status(None) == (tg.OK, 0)
 
 
+def test_withheld_stage_in_the_pair_kernel_times_out_and_recovers(tg):
+    """The CTA-pair kernel, with its epilogue hand-off warp: a withheld first stage
+    makes the MMA thread's wait expire; every other wait (the odd CTA's, the
+    epilogue's, the hand-off's) is bounded too, so the launch ends, and the next
+    call is exact."""
+    w = workloads.custom(512, 768, 1024, seed=34, dist=workloads.Dist("int", -2, 2), bias=workloads.Dist("int", -2, 2))
+    A, B, bias = w.inputs()
+    dA, dB, db = A.cuda(), B.cuda(), bias.cuda()
+    assert tg.tg_device_status(None) == (tg.OK, 0)
+    tg.tg_set_watchdog_ns(20_000_000)  # 20 ms
+    tg.tg_debug_skip_first_arrive(True)
+    try:
+        tg.gemm(dA, dB, db, kernel=tg.KERNEL_TILED_PAIR)
+        st, where = tg.tg_device_status(None)
+    finally:
+        tg.tg_debug_skip_first_arrive(False)
+        tg.tg_set_watchdog_ns(0)
+    assert st == tg.ERR_TIMEOUT
+    assert where in (1, 2, 4, 5), where  # producer, MMA, epilogue or drain wait
+    assert tg.tg_device_status(None) == (tg.OK, 0)
+    C = tg.gemm(dA, dB, db, kernel=tg.KERNEL_TILED_PAIR)
+    ref = oracle.gemm(A, B, bias).view(np.uint16)
+    assert np.array_equal(C.cpu().numpy().view(np.uint16), ref)
+    assert tg.tg_device_status(None) == (tg.OK, 0)
+
+
 def test_hook_off_by_default(tg):
     w = workloads.custom(128, 256, 128, seed=32, dist=workloads.Dist("int", -2, 2))
     A, B, _ = w.inputs()

@@ -198,15 +198,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < args.num_kb; ++i) {
                     const int kb = backwards ? args.num_kb - 1 - i : i;
                     if (!wait_phase(empty_bar(stage), phase ^ 1, wc, kSiteProducerEmpty)) { ok = false; break; }
-                    const uint32_t sA = sbase + stage * kStageBytes;
-                    const uint32_t sB = sA + kStageA;
-                    const uint32_t fb = leader_full0 + 8 * stage;
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * bytes);
-                    tma_load_2d_pair(sA, &tmA, fb, kb * kBK, m0);
-                    tma_load_2d_pair(sB, &tmB, fb, n0, kb * kBK);
-                    if (whole) tma_load_2d_pair(sB + kBoxB, &tmB, fb, n0 + 64, kb * kBK);
-                    issued_mask |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    // test hook (watchdog tests): the first stage of each cluster's first unit is
+                    // never armed or filled, so every bounded wait behind it must expire
+                    const bool skip = args.wd.skip_first_arrive && u == cluster && i == 0;
+                    if (!skip) {
+                        const uint32_t sA = sbase + stage * kStageBytes;
+                        const uint32_t sB = sA + kStageA;
+                        const uint32_t fb = leader_full0 + 8 * stage;
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * bytes);
+                        tma_load_2d_pair(sA, &tmA, fb, kb * kBK, m0);
+                        tma_load_2d_pair(sB, &tmB, fb, n0, kb * kBK);
+                        if (whole) tma_load_2d_pair(sB + kBoxB, &tmB, fb, n0 + 64, kb * kBK);
+                        issued_mask |= 1u << stage;
+                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    }
                     if (++stage == kPairStages) { stage = 0; phase ^= 1; }
                 }
             }
