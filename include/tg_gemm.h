@@ -240,8 +240,9 @@ typedef enum {
     TG_W4_KERNEL_TMEM = 1, /* weights converted into shared memory, tcgen05 MMAs into tensor
                               memory (64-row MMAs: M > 64 runs as row blocks); split K */
     TG_W4_KERNEL_REG = 2   /* weights converted in registers into the operands of warp-level
-                              16-row MMAs; M <= 16; one CTA per 64 output columns over the
-                              whole K (no K slices) */
+                              m16n8k16 MMAs (16 weight columns x 8 tokens each, two per 16
+                              tokens); M <= 16; one CTA per 64 output columns over the whole
+                              K (no K slices) */
 } tg_w4_kernel;
 
 /*
