@@ -100,9 +100,9 @@ typedef enum {
  * up to 8 elements (one buffer per stream, grown as needed, freed by
  * tg_shutdown; TG_ERR_NO_MEMORY if it cannot be allocated), then the TMA
  * kernels below run on the copy; M <= 16, or M <= 128 where the skinny kernel
- * measured faster (fewer than SMs / 2 columns of 64 with K >= 128 M for
- * M <= 48 or K >= 192 M above, or M <= 64 with 2 K N >= 256 MiB of B) ->
- * TG_KERNEL_SPLITK; other M <= 128 -> TG_KERNEL_TILED_TMA; at least one
+ * measured faster (fewer 64-column tiles than SMs with (K / 64) * SMs / tiles
+ * >= 1.5 M, or M <= 64 with 2 K N >= 256 MiB of B) -> TG_KERNEL_SPLITK; other
+ * M <= 128 -> TG_KERNEL_TILED_TMA; at least one
  * 256x256 tile per pair of SMs -> TG_KERNEL_TILED_PAIR; otherwise
  * TG_KERNEL_TILED_TMA.
  */

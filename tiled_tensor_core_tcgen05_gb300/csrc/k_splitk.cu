@@ -200,6 +200,71 @@ int split_stages_for(int m_pad) {
 
 int split_smem_bytes(int m_pad, int stages) { return layout_for(m_pad, stages).alloc; }
 
+namespace {
+
+// The K slices' fp32 partials [slice][n][m] summed over the whole GPU: thread = one column n
+// and 16 rows m0..m0+15, slices added in order 0, 1, ... starting from 0 (the order and the
+// arithmetic of the in-kernel last-arrival reduction, so the results are the same bits),
+// then bias, GELU and one rounding. The loads of four slices are issued before they are
+// added. A warp's stores of one row are 32 consecutive columns.
+constexpr int kRedThreads = 128;
+
+__global__ void __launch_bounds__(kRedThreads) splitk_reduce_kernel(const SplitArgs a) {
+    const int n = blockIdx.x * kRedThreads + threadIdx.x;
+    const int m0 = blockIdx.y * 16;
+    if (n >= a.N) return;
+    float s[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s[i] = 0.0f;
+    auto add_slice = [&](const float4 (&p)[4]) {
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+            s[4 * v4] += p[v4].x;
+            s[4 * v4 + 1] += p[v4].y;
+            s[4 * v4 + 2] += p[v4].z;
+            s[4 * v4 + 3] += p[v4].w;
+        }
+    };
+    constexpr int kBatch = 4;
+    int q = 0;
+    for (; q + kBatch <= a.splits; q += kBatch) {
+        float4 p[kBatch][4];
+        bool in[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int64_t off = (static_cast<int64_t>(q + j) * a.N + n) * a.m_pad + m0;
+            in[j] = dbg_check(dbg_in(off, 16, a.wd.ws_floats), a.wd);
+            const float4* wq = reinterpret_cast<const float4*>(a.ws + (in[j] ? off : 0));
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) p[j][v4] = __ldcg(wq + v4);
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+            if (in[j]) add_slice(p[j]);
+    }
+    for (; q < a.splits; ++q) {
+        const int64_t off = (static_cast<int64_t>(q) * a.N + n) * a.m_pad + m0;
+        if (!dbg_check(dbg_in(off, 16, a.wd.ws_floats), a.wd)) continue;
+        const float4* wq = reinterpret_cast<const float4*>(a.ws + off);
+        float4 p[4];
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) p[v4] = __ldcg(wq + v4);
+        add_slice(p);
+    }
+    const float bias_n = a.bias != nullptr ? __half2float(a.bias[n]) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        if (m0 + i < a.M) a.C[static_cast<int64_t>(m0 + i) * a.N + n] = __float2half_rn(epi_value(s[i], bias_n, a.gelu));
+}
+
+}  // namespace
+
+cudaError_t launch_splitk_reduce(const SplitArgs& a, cudaStream_t stream) {
+    const dim3 grid((a.N + kRedThreads - 1) / kRedThreads, (a.M + 15) / 16);
+    splitk_reduce_kernel<<<grid, kRedThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_splitk(const SplitArgs& a, const CUtensorMap& tmB, const CUtensorMap& tmA, int grid,
                           cudaStream_t stream) {
     static int attr_gen[64] = {};

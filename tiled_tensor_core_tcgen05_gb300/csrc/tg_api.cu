@@ -376,6 +376,7 @@ void splitk_args(const DeviceState& d, const __half* A, const __half* B, const _
     a.kb_per_split = (a.kb_total + s - 1) / s;
     a.splits = (a.kb_total + a.kb_per_split - 1) / a.kb_per_split;
     a.num_units = a.n_tiles * a.splits;
+    a.separate_reduce = a.splits > 1 ? 1 : 0;
     a.wd = watchdog(d);
 }
 
@@ -388,6 +389,9 @@ tg_status splitk_launch(const DeviceState& d, const SplitArgs& a, cudaStream_t s
     const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
     cudaError_t e = launch_splitk(a, tmB, tmA, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "split-K kernel launch");
+    if (a.splits > 1 && a.separate_reduce) {
+        if ((e = launch_splitk_reduce(a, stream)) != cudaSuccess) return cuda_fail(e, "split-K reduction launch");
+    }
     return TG_OK;
 }
 
@@ -485,18 +489,17 @@ bool pair_pays(const DeviceState& d, int64_t M, int64_t N) {
 }
 
 // True when the skinny split-K kernel beats the single-CTA tiled kernel for M <= 128
-// (measured on GB300 over N = 2048..57344, K = 2048..14336, M = 1..128). The split-K
-// kernel's time per K block grows with the padded M (a step between 48 and 64 rows),
-// while the tiled kernel cannot split K. So split-K is used for M <= 16; above that
-// only when the tiled kernel's 64-column tiles would leave more than half the SMs
-// idle over a long K loop (at least 2 M blocks of 64 for M <= 48, 3 M above), or
-// when, with M <= 64, the product streams 256 MB or more of B (both kernels then sit
-// near the HBM floor, split-K slightly ahead).
+// (measured on GB300 over N = 2048..28672, K = 2048..28672, M = 16..128). The tiled kernel
+// cannot split K: with fewer 64-column tiles than SMs it runs one partial wave whose time
+// grows with K/64, while split-K spreads K over every SM and costs a little more per row of
+// M. So split-K is used for M <= 16; with fewer 64-column tiles than SMs, when K/64 times
+// the SMs per tile is at least 1.5 M; otherwise only when, with M <= 64, the product
+// streams 256 MB or more of B (both kernels then sit near the HBM floor).
 bool skinny_pays(const DeviceState& d, int64_t M, int64_t N, int64_t K) {
     if (M <= 16) return true;
     const int64_t tiles64 = (N + 63) / 64;  // one 128-row block: M <= 128
     const int64_t kb = (K + 63) / 64;
-    if (2 * tiles64 < d.sm_count && kb >= (M <= 48 ? 2 : 3) * M) return true;
+    if (tiles64 < d.sm_count) return 2 * kb * d.sm_count >= 3 * M * tiles64;
     return M <= 64 && 2.0 * static_cast<double>(K) * static_cast<double>(N) >= 256.0 * 1048576.0;
 }
 

@@ -125,6 +125,9 @@ struct SplitArgs {
     int n_tiles, kb_total, kb_per_split, splits, num_units;
     float* ws;               // splits * N * m_pad fp32 partial sums, [slice][n][m] (splits > 1)
     unsigned int* counters;  // n_tiles arrival counters, zero between launches
+    int separate_reduce;     // splits > 1: 1 = units only write partials and a second kernel
+                             // (launch_splitk_reduce) sums them; 0 = the last unit of each
+                             // column slice sums them in the kernel
     Watchdog wd;
 };
 
@@ -175,6 +178,7 @@ struct AttnArgs {
 // Read and written with the front end's lock held.
 extern int g_generation;
 
+cudaError_t launch_splitk_reduce(const SplitArgs& a, cudaStream_t stream);
 int split_stage_bytes(int m_pad);
 int split_smem_bytes(int m_pad, int stages);
 int split_stages_for(int m_pad);

@@ -82,7 +82,7 @@ __device__ __forceinline__ void skinny_epilogue(const SplitArgs& args, uint32_t 
                 }
             }
         }
-        if (args.splits > 1) {
+        if (args.splits > 1 && !args.separate_reduce) {
             // publish this slice's partials, then count arrivals for column slice nt
             __threadfence();
             named_barrier_sync(1, kSkEpiThreads);
