@@ -165,18 +165,19 @@ tg_status tg_bias_gelu(void* C, const void* bias, int64_t M, int64_t N, int epil
  * array (one slice needs none, so an automatic call is never refused for
  * size), 1..64 fixes it. The caller still
  * passes A, B, bias and C (device pointers it owns). With more than one K
- * slice, the partial sums and arrival counters live in one fixed array of
+ * slice, the partial sums live in one fixed array of
  * TG_NOALLOC_SCRATCH_BYTES compiled into the library's device image: every
  * device that loads the library holds it until the process exits. A call whose
  * slices need more (4 * slices * N * Mp bytes of partials, Mp = M rounded up to
- * a multiple of 16, plus 4 bytes per 256-column slice of N, rounded up to 256)
+ * a multiple of 16, plus a reserved head of 4 bytes per 256-column slice of
+ * N, rounded up to 256)
  * returns TG_ERR_INVALID_ARG and enqueues nothing. Nothing is allocated or
  * freed by any call.
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture begins. Every call zeroes the counters on `stream` before
- * its kernel and otherwise reuses the array as the previous call left it. All
+ * any stream capture begins. Every call writes the partials before a second
+ * kernel on `stream` sums them, so nothing carries over between calls. All
  * calls share the one array, so calls whose work can overlap on the GPU (for
  * example on two streams without ordering between them) race and give wrong
  * results; order them on one stream or with events.

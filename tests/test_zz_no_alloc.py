@@ -113,13 +113,13 @@ def test_repeat_call_reuses_the_array(tg):
 def test_automatic_slices_stay_within_the_array(tg):
     # 64 x 8192 x 8192: the cost model alone picks more K slices than the array holds (each
     # slice's partials are 64 x 8192 x 4 bytes = 2 MiB, at most 3 fit in 8 MiB beside the
-    # counters), so the automatic choice is capped and the call succeeds
+    # reserved head of the array), so the automatic choice is capped and the call succeeds
     M, N, K = 64, 8192, 8192
     w = workloads.custom(M, N, K, seed=430, dist=workloads.Dist("normal", 0.0, 0.02))
     A, B, _ = w.inputs()
     dA, dB = A.cuda(), B.cuda()
     C = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
-    with pytest.raises(tg.TgError) as ei:  # four explicit slices need 8 MiB + counters
+    with pytest.raises(tg.TgError) as ei:  # four explicit slices need 8 MiB + the reserved head
         _noalloc(tg, dA, dB, None, C, M, N, K, tg.EPI_NONE, 4)
     assert ei.value.status == tg.ERR_INVALID_ARG
     _noalloc(tg, dA, dB, None, C, M, N, K, tg.EPI_NONE, 0)

@@ -11,11 +11,10 @@
 // bytes of every B row it touches. Units are spread over a persistent grid,
 // slice-major, so CTAs running side by side read neighbouring columns of the
 // same rows of B. With more than one K slice, each unit
-// writes an fp32 partial tile to a scratch buffer; the last unit of a column
-// slice to finish (an arrival counter) adds the partials in slice order
-// 0, 1, ..., applies bias and GELU and writes C, so results do not depend on
-// which CTA finishes last. The counter is reset by that last unit, so it is
-// zero again for the next launch.
+// writes an fp32 partial tile to a scratch buffer, and a second kernel
+// (splitk_reduce_kernel, below) adds the partials in slice order 0, 1, ...
+// over the whole GPU, applies bias and GELU and writes C, so results do not
+// depend on which CTA finishes first.
 //
 // The product and epilogue are those of "TileLang: writing LLM GPU kernels by
 // thinking in tiles" (sections 2-3) and "Designing high-performance GPU
@@ -35,7 +34,7 @@ constexpr int kThreads = 6 * 32;            // producer, MMA, 4 epilogue warps
 
 struct Layout {
     int stage_bytes, ring, bar_full, bar_empty, bar_acc_full, bar_acc_empty, bar_drain, tmem_slot,
-        abort_slot, flag_slot, used, alloc;
+        abort_slot, used, alloc;
 };
 
 __host__ __device__ inline Layout layout_for(int m_pad, int stages) {
@@ -49,8 +48,7 @@ __host__ __device__ inline Layout layout_for(int m_pad, int stages) {
     L.bar_drain = L.bar_acc_empty + 16;
     L.tmem_slot = L.bar_drain + 8;
     L.abort_slot = L.tmem_slot + 4;
-    L.flag_slot = L.abort_slot + 4;
-    L.used = L.flag_slot + 4;
+    L.used = L.abort_slot + 4;
     L.alloc = L.used + 1024;
     return L;
 }
@@ -72,7 +70,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto acc_empty_bar = [&](int b) { return sbase + L.bar_acc_empty + 8 * b; };
     const uint32_t drain_bar = sbase + L.bar_drain;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_slot);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L.flag_slot);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.tmem_slot);
 
     if (threadIdx.x == 0) {
@@ -86,7 +83,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
-        *last_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmA);
@@ -176,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        skinny_epilogue<kSkHalves>(args, tmem_base, acc_full_bar(0), acc_empty_bar(0), last_flag, wc, 64);
+        skinny_epilogue<kSkHalves>(args, tmem_base, acc_full_bar(0), acc_empty_bar(0), wc);
     }
 
     tc_fence_before_sync();
@@ -203,9 +199,8 @@ int split_smem_bytes(int m_pad, int stages) { return layout_for(m_pad, stages).a
 namespace {
 
 // The K slices' fp32 partials [slice][n][m] summed over the whole GPU: thread = one column n
-// and 16 rows m0..m0+15, slices added in order 0, 1, ... starting from 0 (the order and the
-// arithmetic of the in-kernel last-arrival reduction, so the results are the same bits),
-// then bias, GELU and one rounding. The loads of four slices are issued before they are
+// and 16 rows m0..m0+15, slices added in order 0, 1, ... starting from 0 (a fixed order, so
+// the results do not depend on which CTA finished first), then bias, GELU and one rounding. The loads of four slices are issued before they are
 // added. A warp's stores of one row are 32 consecutive columns.
 constexpr int kRedThreads = 128;
 

@@ -376,7 +376,6 @@ void splitk_args(const DeviceState& d, const __half* A, const __half* B, const _
     a.kb_per_split = (a.kb_total + s - 1) / s;
     a.splits = (a.kb_total + a.kb_per_split - 1) / a.kb_per_split;
     a.num_units = a.n_tiles * a.splits;
-    a.separate_reduce = a.splits > 1 ? 1 : 0;
     a.wd = watchdog(d);
 }
 
@@ -389,9 +388,8 @@ tg_status splitk_launch(const DeviceState& d, const SplitArgs& a, cudaStream_t s
     const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
     cudaError_t e = launch_splitk(a, tmB, tmA, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "split-K kernel launch");
-    if (a.splits > 1 && a.separate_reduce) {
-        if ((e = launch_splitk_reduce(a, stream)) != cudaSuccess) return cuda_fail(e, "split-K reduction launch");
-    }
+    if (a.splits > 1 && (e = launch_splitk_reduce(a, stream)) != cudaSuccess)
+        return cuda_fail(e, "split-K reduction launch");
     return TG_OK;
 }
 
@@ -401,12 +399,11 @@ tg_status run_splitk(DeviceState& d, const __half* A, const __half* B, const __h
     splitk_args(d, A, B, bias, C, M, N, K, gelu, split_k, kSkMaxSplits, a);
     if (a.splits > 1) {
         Scratch* sc = nullptr;
-        tg_status st = ensure_scratch(d, stream, static_cast<size_t>(a.splits) * N * a.m_pad * sizeof(float),
-                                      static_cast<size_t>(a.n_tiles), &sc);
+        // the partials only: the reduction kernel needs no arrival counters
+        tg_status st = ensure_scratch(d, stream, static_cast<size_t>(a.splits) * N * a.m_pad * sizeof(float), 0, &sc);
         if (st != TG_OK) return st;
         a.ws = sc->ws;
-        a.counters = sc->counters;
-        debug_limits(a.wd, sc->ws_bytes, sc->n_counters);
+        debug_limits(a.wd, sc->ws_bytes, 0);
     }
     return splitk_launch(d, a, stream);
 }
@@ -550,7 +547,8 @@ tg_status run_padded(DeviceState& d, const __half* A, const __half* B, const __h
 // tg_gemm_splitk_noalloc: the skinny split-K path with its scratch in a fixed
 // array of the library's own device image instead of library-allocated memory.
 
-// Layout: one arrival counter per 256-column slice of N (padded to 256 bytes),
+// Layout: a reserved area of 4 bytes per 256-column slice of N (padded to 256 bytes; the
+// reduction kernel needs no arrival counters, the area keeps the documented size rule),
 // then the fp32 partial sums [split][N][M rounded up to 16]. Loaded with the library's device
 // code, so every device that loads the library holds these bytes until exit.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[TG_NOALLOC_SCRATCH_BYTES];
@@ -683,7 +681,7 @@ tg_status tg_device_status(tg_stream_t stream_, int* where) {
     const int zero = 0;
     if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero)) != cudaSuccess)
         return cuda_fail(e, "clear status word");
-    // a CTA that gave up may have left split-K arrival counters non-zero
+    // a CTA of the 4-bit kernel that gave up may have left arrival counters non-zero
     for (auto& kv : g_dev[dev].scratch)
         if (kv.second.counters) cudaMemset(kv.second.counters, 0, kv.second.n_counters * sizeof(unsigned int));
     cudaDeviceSynchronize();
@@ -824,7 +822,7 @@ extern "C" tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const 
         g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
     }
 
-    // the most K slices whose partials fit in the array beside the counters (one slice needs
+    // the most K slices whose partials fit in the array beside the reserved area (one slice needs
     // no scratch, so the automatic choice always fits)
     const int m_pad = (static_cast<int>(M) + 15) / 16 * 16;
     const int n_tiles = static_cast<int>((N + kSkBN - 1) / kSkBN);
@@ -845,12 +843,10 @@ extern "C" tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const 
                         "more than the %zu-byte static scratch (use fewer slices, 0 for automatic, or tg_gemm)",
                         a.splits, (long long)M, (long long)N, counter_bytes + partial_bytes,
                         static_cast<size_t>(TG_NOALLOC_SCRATCH_BYTES));
-        // the arrival counters must start at zero; the partials are written before they are read
-        cudaError_t e = cudaMemsetAsync(g_noalloc_ptr[dev], 0, counter_bytes, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "clear static split-K counters");
-        a.counters = reinterpret_cast<unsigned int*>(g_noalloc_ptr[dev]);
+        // the partials follow the counter area, which the size limit keeps reserved (the
+        // reduction kernel that sums them uses no counters); they are written before read
         a.ws = reinterpret_cast<float*>(g_noalloc_ptr[dev] + counter_bytes);
-        debug_limits(a.wd, TG_NOALLOC_SCRATCH_BYTES - counter_bytes, counter_bytes / sizeof(unsigned int));
+        debug_limits(a.wd, TG_NOALLOC_SCRATCH_BYTES - counter_bytes, 0);
     }
     return splitk_launch(d, a, stream);
 }

@@ -123,11 +123,9 @@ struct SplitArgs {
     int tmem_cols;     // TMEM columns allocated (2 * kSkHalves * tmem_stride, >= 32)
     int stages;        // ring depth
     int n_tiles, kb_total, kb_per_split, splits, num_units;
-    float* ws;               // splits * N * m_pad fp32 partial sums, [slice][n][m] (splits > 1)
-    unsigned int* counters;  // n_tiles arrival counters, zero between launches
-    int separate_reduce;     // splits > 1: 1 = units only write partials and a second kernel
-                             // (launch_splitk_reduce) sums them; 0 = the last unit of each
-                             // column slice sums them in the kernel
+    float* ws;               // splits * N * m_pad fp32 partial sums, [slice][n][m] (splits > 1),
+                             // summed by launch_splitk_reduce
+    unsigned int* counters;  // 4-bit kernel: n_tiles arrival counters, zero between launches
     Watchdog wd;
 };
 
