@@ -73,7 +73,8 @@ typedef enum {
 /* Kernel selection for tg_gemm_ex (tg_gemm always uses TG_KERNEL_AUTO). */
 typedef enum {
     TG_KERNEL_AUTO = 0,      /* choose by shape and alignment (below) */
-    TG_KERNEL_TILED_TMA = 1, /* persistent 128x256 tiles, TMA loads, tcgen05 MMA into TMEM.
+    TG_KERNEL_TILED_TMA = 1, /* persistent 128x256 tiles, TMA loads, tcgen05 MMA into TMEM;
+                                K split over slices when the tiles leave SMs idle.
                                 Needs K % 8 == 0, N % 8 == 0, A and B 16-byte aligned. */
     TG_KERNEL_TILED_LSU = 2, /* the same tiles with operands staged by ordinary loads;
                                 any shape and alignment */
@@ -103,19 +104,43 @@ typedef enum {
  * measured faster (fewer 64-column tiles than SMs with (K / 64) * SMs / tiles
  * >= 1.5 M, or M <= 64 with 2 K N >= 256 MiB of B) -> TG_KERNEL_SPLITK; other
  * M <= 128 -> TG_KERNEL_TILED_TMA; at least one
- * 256x256 tile per pair of SMs -> TG_KERNEL_TILED_PAIR; otherwise
- * TG_KERNEL_TILED_TMA.
+ * 256x256 tile per pair of SMs, or with K >= 8192 at least 0.3 of one ->
+ * TG_KERNEL_TILED_PAIR; otherwise
+ * TG_KERNEL_TILED_TMA. TG_KERNEL_TILED_TMA (and TG_KERNEL_TILED_LSU) split K
+ * when their tiles leave SMs idle and a cost model of the slices, their
+ * partial sums and the reduction predicts a gain (see tg_gemm_ex).
  */
 tg_status tg_gemm(const void* A, const void* B, const void* bias, void* C,
                   int64_t M, int64_t N, int64_t K, int epilogue, tg_stream_t stream);
 
 /*
- * tg_gemm with an explicit kernel (a tg_kernel value) and, for
- * TG_KERNEL_SPLITK, an explicit number of K slices `split_k` (0 = automatic,
- * otherwise 1..64 and at most ceil(K / 64)). A kernel whose requirements the
- * arguments do not meet is TG_ERR_INVALID_ARG. Results of all kernels agree
- * within the accumulation-order tolerance stated above; on inputs whose
- * products and partial sums are exact in fp32 they are bit-identical.
+ * The choice tg_gemm makes for these operands, without running anything:
+ * *kernel receives the tg_kernel value it runs, *split_k the number of K slices
+ * that kernel takes (1 = K is not split; always 1 for TG_KERNEL_TILED_PAIR),
+ * and *aligned_copy (may be NULL) 1 when A or B is first copied to an aligned
+ * row stride. A and B are only tested for 16-byte alignment, never read; the
+ * answer is for the current device. For K == 0 tg_gemm runs only its
+ * epilogue pass, and for M or N == 0 nothing, whatever is reported.
+ * TG_ERR_INVALID_ARG for sizes outside [0, 2^31) or a NULL kernel / split_k.
+ */
+tg_status tg_gemm_plan(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                       int* kernel, int* split_k, int* aligned_copy);
+
+/*
+ * tg_gemm with an explicit kernel (a tg_kernel value) and an explicit number
+ * of K slices `split_k` (0 = automatic, otherwise 1..64; more slices than
+ * ceil(K / 64) K blocks are reduced to one per K block). split_k applies to
+ * TG_KERNEL_SPLITK and to the single-CTA tiled kernels (TG_KERNEL_TILED_TMA,
+ * TG_KERNEL_TILED_LSU); with TG_KERNEL_TILED_PAIR it is TG_ERR_INVALID_ARG, and
+ * with TG_KERNEL_AUTO it is used only when the choice is TG_KERNEL_SPLITK.
+ * The tiled kernels' automatic count splits only problems whose 128 x 256
+ * tiles number fewer than the SMs: each slice's fp32 partial tile goes to the
+ * stream's scratch (splits * N * M rounded up to 16, fp32; allocated as for
+ * TG_KERNEL_SPLITK) and a second kernel on `stream` sums the slices in order
+ * before the epilogue (a tiled kernel's split needs M <= 1048560). A kernel
+ * whose requirements the arguments do not meet is TG_ERR_INVALID_ARG. Results of all kernels agree within the
+ * accumulation-order tolerance stated above; on inputs whose products and
+ * partial sums are exact in fp32 they are bit-identical.
  */
 tg_status tg_gemm_ex(const void* A, const void* B, const void* bias, void* C,
                      int64_t M, int64_t N, int64_t K, int epilogue, int kernel, int split_k,

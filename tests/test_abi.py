@@ -86,7 +86,7 @@ def test_footprint_worked_example(tg):
     (dict(kernel=1, A=0x10002), "TG_KERNEL_TILED_TMA"),
     (dict(kernel=3, M=129), "TG_KERNEL_SPLITK"),
     (dict(kernel=3, N=20), "TG_KERNEL_SPLITK"),
-    (dict(kernel=1, split_k=2), "split_k applies"),
+    (dict(kernel=4, split_k=2), "split_k does not apply"),
 ])
 def test_invalid_arguments_rejected_on_host(tg, args, msg):
     base = dict(A=0x10000, B=0x20000000, bias=None, C=0x40000000, M=64, N=64, K=64, epilogue=0,
@@ -200,3 +200,11 @@ def test_release_build_has_no_device_checks_and_the_hook_validates(tg):
         tg.tg_debug_bounds_limit(-1)
     assert ei.value.status == tg.ERR_INVALID_ARG
     assert "BOUNDS" in tg.tg_status_string(tg.ERR_BOUNDS)
+
+
+def test_gemm_plan_argument_checks(tg):
+    with pytest.raises(tg.TgError) as ei:
+        tg.tg_gemm_plan(None, None, -1, 8, 8)
+    assert ei.value.status == tg.ERR_INVALID_ARG
+    lib = tg.library()
+    assert lib.tg_gemm_plan(None, None, 8, 8, 8, None, None, None) == tg.ERR_INVALID_ARG

@@ -28,7 +28,7 @@ W4_KERNEL_AUTO, W4_KERNEL_TMEM, W4_KERNEL_REG = 0, 1, 2
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NO_MEMORY, ERR_BOUNDS = range(7)
 
 # every symbol include/tg_gemm.h declares
-EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_gemm_w4_ex",
+EXPORTS = ("tg_gemm", "tg_gemm_ex", "tg_gemm_plan", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_gemm_w4_ex",
            "tg_gemm_w4_kernel", "tg_attention_fwd",
            "tg_softmax_rows", "tg_bias_gelu",
            "tg_device_status", "tg_debug_status",
@@ -50,6 +50,8 @@ def bind(path: str) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     lib.tg_gemm.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
     lib.tg_gemm_ex.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp]
+    lib.tg_gemm_plan.argtypes = [_vp, _vp, _i64, _i64, _i64, ctypes.POINTER(_int), ctypes.POINTER(_int),
+                                 ctypes.POINTER(_int)]
     lib.tg_gemm_staged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
     lib.tg_gemm_splitk_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
     lib.tg_gemm_w4.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
@@ -73,7 +75,7 @@ def bind(path: str) -> ctypes.CDLL:
     lib.tg_ring_bytes.restype = _i64
     lib.tg_shutdown.argtypes = []
     lib.tg_shutdown.restype = None
-    for name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_gemm_w4_ex",
+    for name in ("tg_gemm", "tg_gemm_ex", "tg_gemm_plan", "tg_gemm_staged", "tg_gemm_splitk_noalloc", "tg_gemm_w4", "tg_gemm_w4_ex",
                  "tg_gemm_w4_kernel", "tg_attention_fwd", "tg_softmax_rows", "tg_bias_gelu", "tg_device_status", "tg_debug_status",
                  "tg_set_watchdog_ns", "tg_debug_skip_first_arrive", "tg_debug_bounds_limit", "tg_debug_build",
                  "tg_version"):
@@ -109,6 +111,13 @@ def tg_gemm(A: int, B: int, bias: int | None, C: int, M: int, N: int, K: int, ep
 def tg_gemm_ex(A: int, B: int, bias: int | None, C: int, M: int, N: int, K: int, epilogue: int,
                kernel: int, split_k: int, stream: int | None) -> None:
     _check(_lib.tg_gemm_ex(A, B, bias, C, M, N, K, epilogue, kernel, split_k, stream))
+
+
+def tg_gemm_plan(A: int | None, B: int | None, M: int, N: int, K: int) -> tuple[int, int, int]:
+    """(kernel, K slices, aligned copy 0/1) that tg_gemm would take for these operands."""
+    k, s, c = _int(), _int(), _int()
+    _check(_lib.tg_gemm_plan(A, B, M, N, K, ctypes.byref(k), ctypes.byref(s), ctypes.byref(c)))
+    return k.value, s.value, c.value
 
 
 def tg_gemm_staged(hA, hB, hbias, hC, dA, dB, dbias, dC, M, N, K, epilogue, stream) -> None:

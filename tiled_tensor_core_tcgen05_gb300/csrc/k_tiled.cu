@@ -20,7 +20,11 @@
 //     BN-column accumulators so the epilogue of one tile overlaps the
 //     mainloop of the next;
 //   * the epilogue reads TMEM with tcgen05.ld, adds bias, applies GELU in fp32,
-//     rounds once to binary16 and stores with masking for ragged M/N.
+//     rounds once to binary16 and stores with masking for ragged M/N;
+//   * when the tiles alone cannot fill the SMs (few rows, long K), K is split:
+//     a work unit is one K slice of one tile, the unit writes its fp32 tile to
+//     scratch, and the reduction kernel of the skinny path sums the slices in
+//     order and applies the epilogue.
 #include "tg_device.cuh"
 #include "tg_internal.h"
 
@@ -66,6 +70,20 @@ struct Roles {
     static constexpr int kEpiWarp0 = kProducerWarps + 1;
     static constexpr int kThreads = (kProducerWarps + 1 + kEpiWarps) * 32;
 };
+
+// Work unit u: K slice u / num_tiles of tile u % num_tiles (the tiles' first slices first, so
+// the CTAs of one wave share the K range of the strips they read), K blocks [kb0, kb1).
+struct Unit {
+    int tile, slice, kb0, kb1;
+};
+__device__ __forceinline__ Unit unit_of(const TiledArgs& a, int u) {
+    Unit w;
+    w.slice = u / a.num_tiles;
+    w.tile = u - w.slice * a.num_tiles;
+    w.kb0 = w.slice * a.kb_per_split;
+    w.kb1 = min(a.num_kb, w.kb0 + a.kb_per_split);
+    return w;
+}
 
 __device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks, int group_m,
                                             int& mb, int& nb) {
@@ -195,13 +213,14 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                 int stage = 0;
                 uint32_t phase = 0;
                 uint32_t issued_mask = 0, issued_parity = 0;
-                for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x) {
+                for (int u = blockIdx.x; u < args.num_units; u += gridDim.x) {
+                    const Unit w = unit_of(args, u);
                     int mb, nb;
-                    tile_coords(tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
+                    tile_coords(w.tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
                     bool ok = true;
-                    for (int kb = 0; kb < args.num_kb; ++kb) {
+                    for (int kb = w.kb0; kb < w.kb1; ++kb) {
                         if (!wait_phase(empty_bar(stage), phase ^ 1, wc, kSiteProducerEmpty)) { ok = false; break; }
-                        const bool skip = args.wd.skip_first_arrive && tile == (int)blockIdx.x && kb == 0;
+                        const bool skip = args.wd.skip_first_arrive && u == (int)blockIdx.x && kb == w.kb0;
                         if (!skip) {
                             const uint32_t sA = sbase + stage * kStageBytes;
                             const uint32_t sB = sA + kStageA;
@@ -225,11 +244,12 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             const int ptid = threadIdx.x;  // 0..127
             int stage = 0;
             uint32_t phase = 0;
-            for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x) {
+            for (int u = blockIdx.x; u < args.num_units; u += gridDim.x) {
+                const Unit w = unit_of(args, u);
                 int mb, nb;
-                tile_coords(tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
+                tile_coords(w.tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
                 bool ok = true;
-                for (int kb = 0; kb < args.num_kb; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_phase(empty_bar(stage), phase ^ 1, wc, kSiteProducerEmpty)) { ok = false; break; }
                     uint8_t* sA = smem + stage * kStageBytes;
                     uint8_t* sB = sA + kStageA;
@@ -255,13 +275,14 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x, ++it) {
+            for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x, ++it) {
+                const Unit w = unit_of(args, u);
                 const int b = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!wait_phase(acc_empty_bar(b), acc_phase ^ 1, wc, kSiteMmaAccEmpty)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * kBN_;
-                for (int kb = 0; kb < args.num_kb; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_phase(full_bar(stage), phase, wc, kSiteMmaFull)) { ok = false; break; }
                     tc_fence_after_sync();
                     // stages filled by cp.async / ordinary stores (generic proxy) are read
@@ -274,7 +295,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k)
                         mma_f16(d_tmem, a_desc + (uint64_t)((k * 32) >> 4), b_desc + (uint64_t)((k * 2048) >> 4),
-                                G::kIdesc, (kb | k) != 0);
+                                G::kIdesc, kb != w.kb0 || k != 0);
                     mma_commit(empty_bar(stage));  // frees the stage once these MMAs finish
                     if (++stage == kStagesN) { stage = 0; phase ^= 1; }
                 }
@@ -293,9 +314,10 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
         const int row_in_tile = quarter * 32 + lane;
         uint8_t* stage = smem + G::kEpiStage + (warp - R::kEpiWarp0) * kStageWarpBytes;
         int it = 0;
-        for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++it) {
+        for (int u = blockIdx.x; u < args.num_units; u += gridDim.x, ++it) {
+            const Unit w = unit_of(args, u);
             int mb, nb;
-            tile_coords(tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
+            tile_coords(w.tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
             const int b = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
             if (!wait_phase(acc_full_bar(b), acc_phase, wc, kSiteEpilogueAccFull)) break;
@@ -320,8 +342,23 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                     tc_fence_before_sync();
                     mbar_arrive(acc_empty_bar(b));  // this warp is done with TMEM buffer b
                 }
-                epilogue_chunk(r, stage, args.C, args.bias, row - lane, n0 + c * 32, args.M, args.N, args.gelu,
-                               args.c_store, args.bias_vec);
+                if (args.splits == 1) {
+                    epilogue_chunk(r, stage, args.C, args.bias, row - lane, n0 + c * 32, args.M, args.N, args.gelu,
+                                   args.c_store, args.bias_vec);
+                } else if (row < args.m_pad) {
+                    // fp32 partials [slice][n][m_pad]: the warp's lanes are 32 consecutive rows,
+                    // so each column's values are one 128-byte store
+                    const int nc = n0 + c * 32;
+                    const int cols = min(32, args.N - nc);
+                    const int64_t off = (static_cast<int64_t>(w.slice) * args.N + nc) * args.m_pad + row;
+                    if (dbg_check(dbg_in(off, static_cast<int64_t>(cols - 1) * args.m_pad + 1, args.wd.ws_floats),
+                                  args.wd)) {
+                        float* dst = args.ws + off;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < cols) dst[static_cast<int64_t>(j) * args.m_pad] = __uint_as_float(r[j]);
+                    }
+                }
             }
         }
     }

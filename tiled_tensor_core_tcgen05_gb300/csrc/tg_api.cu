@@ -408,26 +408,85 @@ tg_status run_splitk(DeviceState& d, const __half* A, const __half* B, const __h
     return splitk_launch(d, a, stream);
 }
 
+// Tile width of the single-CTA kernel without a K split: narrower tiles (128, then 64
+// columns) while 256-wide ones would leave more than half of the SMs idle: small and
+// ragged problems are latency-bound, more CTAs finish sooner.
+int tiled_bn(const DeviceState& d, int64_t m_blocks, int64_t N) {
+    int bn = kBN;
+    while (bn > 64 && m_blocks * ((N + bn - 1) / bn) < d.sm_count / 2) bn /= 2;
+    return bn;
+}
+
+// K slices for the single-CTA kernel (1 = no split), from a time model fitted to GB300
+// measurements (N, K in 2048..28672, M in 64..1024; it picks the fastest measured count, or
+// one within 6%, on all but one shape). Time is counted in K blocks of one 128 x 256 tile
+// (~0.38 us): a 128- or 64-column tile's K block costs 0.72 or 0.70 of one (their loads,
+// not their MMAs, bound them), a launch never beats reading A and B once from HBM (~2.4 MB
+// per unit), and a split adds ~20 for the partial-sum epilogue and the reduction launch
+// plus ~1.14 per MB of fp32 partials written and read back. Only problems whose 256-wide
+// tiles number fewer than the SMs are split.
+int tiled_splits(const DeviceState& d, int64_t M, int64_t N, int64_t K) {
+    const int64_t m_blocks = (M + kBM - 1) / kBM;
+    const int64_t kb = (K + kBK - 1) / kBK;
+    const int64_t tiles256 = m_blocks * ((N + kBN - 1) / kBN);
+    if (tiles256 >= d.sm_count) return 1;
+    const int bn = tiled_bn(d, m_blocks, N);
+    const double rel = bn == 256 ? 1.0 : bn == 128 ? 0.72 : 0.70;
+    const int64_t tiles = m_blocks * ((N + bn - 1) / bn);
+    const double hbm = (static_cast<double>(M) * K + static_cast<double>(K) * N) * 2.0 / 1e6 / 2.37;
+    double best = static_cast<double>((tiles + d.sm_count - 1) / d.sm_count) * kb * rel;
+    if (best < hbm) best = hbm;
+    int best_s = 1;
+    const double m_pad = static_cast<double>((M + 15) / 16 * 16);
+    for (int s = 2; s <= kSkMaxSplits && s <= kb; ++s) {
+        const int64_t kbps = (kb + s - 1) / s;
+        if ((kb + kbps - 1) / kbps != s) continue;
+        const int64_t waves = (tiles256 * s + d.sm_count - 1) / d.sm_count;
+        double t = static_cast<double>(waves) * kbps;
+        if (t < hbm) t = hbm;
+        t += 20.0 + 1.14 * s * m_pad * static_cast<double>(N) * 4.0 / 1e6;
+        if (t < best) {
+            best = t;
+            best_s = s;
+        }
+    }
+    return best_s;
+}
+
 tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, const __half* bias, __half* C, int M,
-                    int N, int K, int gelu, cudaStream_t stream, int64_t lda = 0, int64_t ldb = 0) {
+                    int N, int K, int gelu, cudaStream_t stream, int64_t lda = 0, int64_t ldb = 0, int split_k = 0) {
     TiledArgs a{};
     a.A = A; a.B = B; a.bias = bias; a.C = C;
     a.M = M; a.N = N; a.K = K; a.gelu = gelu;
     a.m_blocks = (M + kBM - 1) / kBM;
-    // narrower tiles (128, then 64 columns) while 256-wide ones would leave more than half
-    // of the SMs idle: small and ragged problems are latency-bound, more CTAs finish sooner
-    a.bn = kBN;
-    while (a.bn > 64 && static_cast<int64_t>(a.m_blocks) * ((N + a.bn - 1) / a.bn) < d.sm_count / 2) a.bn /= 2;
+    a.num_kb = (K + kBK - 1) / kBK;
+    int s = split_k > 0 ? split_k : tiled_splits(d, M, N, K);
+    if (s > a.num_kb) s = a.num_kb;
+    a.kb_per_split = (a.num_kb + s - 1) / s;
+    a.splits = (a.num_kb + a.kb_per_split - 1) / a.kb_per_split;
+    // a split problem keeps the full-width tiles (their MMAs are the most efficient); the
+    // slices fill the SMs
+    a.bn = a.splits > 1 ? kBN : tiled_bn(d, a.m_blocks, N);
     a.n_blocks = (N + a.bn - 1) / a.bn;
     a.num_tiles = a.m_blocks * a.n_blocks;
-    a.num_kb = (K + kBK - 1) / kBK;
+    a.num_units = a.num_tiles * a.splits;
+    a.m_pad = (M + 15) / 16 * 16;
     a.group_m = group_rows(kBM, K, a.m_blocks);
     a.c_store = (N % 8 == 0 && aligned(C, 16)) ? 2 : ((N % 2 == 0 && aligned(C, 4)) ? 1 : 0);
     a.bias_vec = (bias != nullptr && aligned(bias, 16)) ? 1 : 0;
     a.a_vec = vec_width(A, K);
     a.b_vec = vec_width(B, N);
     a.wd = watchdog(d);
-    const int grid = a.num_tiles < d.sm_count ? a.num_tiles : d.sm_count;
+    if (a.splits > 1) {
+        if ((static_cast<int64_t>(M) + 15) / 16 > 65535)
+            return fail(TG_ERR_INVALID_ARG, "a K split of the tiled kernels supports M <= 1048560, got %d", M);
+        Scratch* sc = nullptr;
+        tg_status st = ensure_scratch(d, stream, static_cast<size_t>(a.splits) * N * a.m_pad * sizeof(float), 0, &sc);
+        if (st != TG_OK) return st;
+        a.ws = sc->ws;
+        debug_limits(a.wd, sc->ws_bytes, 0);
+    }
+    const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
     cudaError_t e;
     if (tma) {
         CUtensorMap tmA, tmB;
@@ -439,6 +498,17 @@ tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, 
         e = launch_tiled_lsu(a, grid, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "tiled kernel launch");
+    if (a.splits > 1) {
+        // the skinny path's reduction: slices summed in order, then bias, GELU, one rounding
+        SplitArgs r{};
+        r.bias = bias; r.C = C;
+        r.M = M; r.N = N; r.K = K; r.gelu = gelu;
+        r.m_pad = a.m_pad;
+        r.splits = a.splits;
+        r.ws = a.ws;
+        r.wd = a.wd;
+        if ((e = launch_splitk_reduce(r, stream)) != cudaSuccess) return cuda_fail(e, "split-K reduction launch");
+    }
     return TG_OK;
 }
 
@@ -479,10 +549,14 @@ tg_status run_tiled_pair(DeviceState& d, const __half* A, const __half* B, const
 // Unaligned operands: products of at least this many flops take the aligned-copy path.
 constexpr double kCopyPathFlops = 4294967296.0;  // 2^32
 
-// True when the CTA-pair kernel has at least one wave of 256x256 tiles.
-bool pair_pays(const DeviceState& d, int64_t M, int64_t N) {
+// True when the CTA-pair kernel beats the single-CTA kernel (with its K split): with at least
+// one wave of 256x256 tiles, or, for K >= 8192, at least 0.3 of a wave (measured on GB300:
+// 8192 x 8192 at M = 512, 64 pair tiles, 49 vs 55 us; 4096 x 14336 at M = 768, 48 tiles,
+// 76 vs 85 us; with K = 4096 the single-CTA kernel stays ahead at 48-64 tiles).
+bool pair_pays(const DeviceState& d, int64_t M, int64_t N, int64_t K) {
     const int64_t pair_tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kBN - 1) / kBN);
-    return pair_tiles >= d.sm_count / 2;
+    if (pair_tiles >= d.sm_count / 2) return true;
+    return K >= 8192 && 10 * pair_tiles >= 3 * static_cast<int64_t>(d.sm_count);
 }
 
 // True when the skinny split-K kernel beats the single-CTA tiled kernel for M <= 128
@@ -539,8 +613,52 @@ tg_status run_padded(DeviceState& d, const __half* A, const __half* B, const __h
             return cuda_fail(e, "copy of B to an aligned stride");
         b = pb;
     }
-    if (pair_pays(d, M, N)) return run_tiled_pair(d, a, b, bias, C, M, N, K, gelu, stream, lda, ldb);
+    if (pair_pays(d, M, N, K)) return run_tiled_pair(d, a, b, bias, C, M, N, K, gelu, stream, lda, ldb);
     return run_tiled(d, true, a, b, bias, C, M, N, K, gelu, stream, lda, ldb);
+}
+
+// The automatic choice of tg_gemm: the kernel, whether operands are first copied to aligned
+// strides, and the K slices (1 = none) the chosen kernel's own model takes.
+struct Plan {
+    int kernel;
+    bool copy;
+    int splits;
+};
+
+Plan plan_auto(const DeviceState& d, int64_t M, int64_t N, int64_t K, bool tma_ok) {
+    Plan p{TG_KERNEL_TILED_TMA, false, 1};
+    if (!tma_ok) {
+        // large problems: an aligned copy of the operand plus the TMA kernels beats staging it
+        // by 4- or 2-byte loads (4096 x 4094 x 4096: 3.6x); small ones are latency-bound and the
+        // copy's launch costs more than it saves (1000 x 1030 x 520: 19.3 vs 17.3 us); skinny M
+        // keeps the loads (a copy would double the weight traffic that bounds it)
+        if (M > kSkMaxM && 2.0 * M * N * K >= kCopyPathFlops) {
+            p.copy = true;
+            p.kernel = pair_pays(d, M, N, K) ? TG_KERNEL_TILED_PAIR : TG_KERNEL_TILED_TMA;
+        } else {
+            p.kernel = TG_KERNEL_TILED_LSU;
+        }
+    } else if (M <= kSkMaxM) {
+        // 256-row pair tiles would be mostly padding here
+        p.kernel = skinny_pays(d, M, N, K) ? TG_KERNEL_SPLITK : TG_KERNEL_TILED_TMA;
+    } else {
+        // CTA pairs once there are enough 256x256 tiles for them (pair_pays); smaller problems
+        // keep more, smaller tiles on single CTAs, with K split when they leave SMs idle
+        p.kernel = pair_pays(d, M, N, K) ? TG_KERNEL_TILED_PAIR : TG_KERNEL_TILED_TMA;
+    }
+    if (K > 0 && p.kernel == TG_KERNEL_SPLITK) {
+        SplitArgs a;
+        splitk_args(d, nullptr, nullptr, nullptr, nullptr, static_cast<int>(M), static_cast<int>(N),
+                    static_cast<int>(K), 0, 0, kSkMaxSplits, a);
+        p.splits = a.splits;
+    } else if (K > 0 && p.kernel != TG_KERNEL_TILED_PAIR) {
+        const int kb = static_cast<int>((K + kBK - 1) / kBK);
+        int s = tiled_splits(d, M, N, K);
+        if (s > kb) s = kb;
+        const int kbps = (kb + s - 1) / s;
+        p.splits = (kb + kbps - 1) / kbps;
+    }
+    return p;
 }
 
 // ---------------------------------------------------------------------------
@@ -590,8 +708,8 @@ tg_status tg_gemm_ex(const void* A, const void* B, const void* bias, void* C, in
     if (kernel == TG_KERNEL_SPLITK && (!tma_ok || M > kSkMaxM))
         return fail(TG_ERR_INVALID_ARG, "TG_KERNEL_SPLITK needs M <= %d, K %% 8 == 0, N %% 8 == 0 and 16-byte aligned A, B",
                     kSkMaxM);
-    if (split_k > 0 && kernel != TG_KERNEL_SPLITK && kernel != TG_KERNEL_AUTO)
-        return fail(TG_ERR_INVALID_ARG, "split_k applies to TG_KERNEL_SPLITK only");
+    if (split_k > 0 && kernel == TG_KERNEL_TILED_PAIR)
+        return fail(TG_ERR_INVALID_ARG, "split_k does not apply to TG_KERNEL_TILED_PAIR");
 
     std::lock_guard<std::mutex> lock(g_mu);
     int dev = 0;
@@ -610,33 +728,40 @@ tg_status tg_gemm_ex(const void* A, const void* B, const void* bias, void* C, in
     }
     int k = kernel;
     if (k == TG_KERNEL_AUTO) {
-        if (!tma_ok) {
-            // large problems: an aligned copy of the operand plus the TMA kernels beats
-            // staging it by 4- or 2-byte loads (4096 x 4094 x 4096: 3.6x); small ones are
-            // latency-bound and the copy's launch costs more than it saves (1000 x 1030 x 520:
-            // 19.3 vs 17.3 us); skinny M keeps the loads (a copy would double the weight
-            // traffic that bounds it)
-            if (M > kSkMaxM && 2.0 * M * N * K >= kCopyPathFlops)
-                return run_padded(d, a, b, bi, c, (int)M, (int)N, (int)K, gelu, stream);
-            k = TG_KERNEL_TILED_LSU;
-        } else if (M <= kSkMaxM) {
-            // 256-row pair tiles would be mostly padding here
-            k = skinny_pays(d, M, N, K) ? TG_KERNEL_SPLITK : TG_KERNEL_TILED_TMA;
-        } else {
-            // CTA pairs once there is at least one wave of 256x256 tiles for them;
-            // smaller problems keep more, smaller 128x256 tiles on single CTAs
-            k = pair_pays(d, M, N) ? TG_KERNEL_TILED_PAIR : TG_KERNEL_TILED_TMA;
-        }
+        const Plan p = plan_auto(d, M, N, K, tma_ok);
+        if (p.copy) return run_padded(d, a, b, bi, c, (int)M, (int)N, (int)K, gelu, stream);
+        k = p.kernel;
     }
     if (k == TG_KERNEL_SPLITK)
         return run_splitk(d, a, b, bi, c, (int)M, (int)N, (int)K, gelu, split_k, stream);
     if (k == TG_KERNEL_TILED_PAIR) return run_tiled_pair(d, a, b, bi, c, (int)M, (int)N, (int)K, gelu, stream);
-    return run_tiled(d, k == TG_KERNEL_TILED_TMA, a, b, bi, c, (int)M, (int)N, (int)K, gelu, stream);
+    return run_tiled(d, k == TG_KERNEL_TILED_TMA, a, b, bi, c, (int)M, (int)N, (int)K, gelu, stream, 0, 0,
+                     kernel == TG_KERNEL_AUTO ? 0 : split_k);
 }
 
 tg_status tg_gemm(const void* A, const void* B, const void* bias, void* C, int64_t M, int64_t N, int64_t K,
                   int epilogue, tg_stream_t stream) {
     return tg_gemm_ex(A, B, bias, C, M, N, K, epilogue, TG_KERNEL_AUTO, 0, stream);
+}
+
+tg_status tg_gemm_plan(const void* A, const void* B, int64_t M, int64_t N, int64_t K, int* kernel, int* split_k,
+                       int* aligned_copy) {
+    t_last_error.clear();
+    const int64_t kMax = 0x7FFFFFFFll;
+    if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax)
+        return fail(TG_ERR_INVALID_ARG, "sizes must be in [0, 2^31): M=%lld N=%lld K=%lld", (long long)M,
+                    (long long)N, (long long)K);
+    if (kernel == nullptr || split_k == nullptr) return fail(TG_ERR_INVALID_ARG, "kernel or split_k is NULL");
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    tg_status st = current_device(&dev);
+    if (st != TG_OK) return st;
+    const bool tma_ok = K % 8 == 0 && N % 8 == 0 && aligned(A, 16) && aligned(B, 16);
+    const Plan p = plan_auto(g_dev[dev], M, N, K, tma_ok);
+    *kernel = p.kernel;
+    *split_k = p.splits;
+    if (aligned_copy) *aligned_copy = p.copy ? 1 : 0;
+    return TG_OK;
 }
 
 tg_status tg_gemm_staged(const void* hA, const void* hB, const void* hbias, void* hC, void* dA, void* dB, void* dbias,

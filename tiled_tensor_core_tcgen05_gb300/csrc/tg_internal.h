@@ -101,12 +101,19 @@ struct TiledArgs {
     int bias_vec;  // bias 16-byte aligned: 16-byte loads
     int a_vec;     // ordinary-load staging width for A in elements: 8, 2 or 1
     int b_vec;     // same for B
-    // CTA-pair kernel only: tiles [split_from, num_tiles) of the last, partial
-    // wave run as two half-width units each; num_units = split_from +
-    // 2 * (num_tiles - split_from). Set by the launcher.
+    // CTA-pair kernel: tiles [split_from, num_tiles) of the last, partial wave
+    // run as two half-width units each; num_units = split_from +
+    // 2 * (num_tiles - split_from), set by its launcher. Single-CTA kernel:
+    // num_units = num_tiles * splits.
     int split_from, num_units;
     int bn;        // single-CTA kernel: tile width (256, or 128 / 64 when 256-wide tiles would
                    // leave most SMs idle)
+    // Single-CTA kernel, K split over `splits` slices of kb_per_split K blocks (1 = no split,
+    // num_units = num_tiles then): unit u is slice u / num_tiles of tile u % num_tiles, and
+    // with splits > 1 each unit writes fp32 partials [slice][n][m_pad] to ws, summed by
+    // launch_splitk_reduce.
+    int splits, kb_per_split, m_pad;
+    float* ws;
     Watchdog wd;
 };
 
