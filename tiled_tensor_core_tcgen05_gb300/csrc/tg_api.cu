@@ -418,8 +418,8 @@ int tiled_bn(const DeviceState& d, int64_t m_blocks, int64_t N) {
 }
 
 // K slices for the single-CTA kernel (1 = no split), from a time model fitted to GB300
-// measurements (N, K in 2048..28672, M in 64..1024; it picks the fastest measured count, or
-// one within 6%, on all but one shape). Time is counted in K blocks of one 128 x 256 tile
+// measurements (N, K in 2048..28672, M in 64..1024; wherever the tiled kernel runs, its pick
+// is within 3% of the fastest measured count). Time is counted in K blocks of one 128 x 256 tile
 // (~0.38 us): a 128- or 64-column tile's K block costs 0.72 or 0.70 of one (their loads,
 // not their MMAs, bound them), a launch never beats reading A and B once from HBM (~2.4 MB
 // per unit), and a split adds ~20 for the partial-sum epilogue and the reduction launch
