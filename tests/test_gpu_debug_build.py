@@ -3,15 +3,15 @@ that record a failure in the status word instead of trapping, so no GPU is
 faulted.
 
 With the checks live, small shapes that cross every tile boundary go through
-each kernel family (CTA pair with TMA stores, single CTA, ordinary loads,
-skinny split-K at several slice counts, the 4-bit GEMM with split K, the
-attention forward with a split last round) and must match the fp64 oracle bit
-for bit on exact-arithmetic inputs, twice in a row, with no check failing. Then
-the test hook that shrinks the scratch size the checks allow makes a split-K
-call's partial sums reach past it: the call must end with TG_ERR_BOUNDS (the
-skipped accesses fault nothing), and the next call, with the real size, must be
-exact again. The normal build compiles the checks away: the same hook has no
-effect there."""
+each kernel family (CTA pair with TMA stores, single CTA, ordinary loads, both
+single-CTA variants with K split, skinny split-K at several slice counts, the
+4-bit GEMM with split K, the attention forward with a split last round) and
+must match the fp64 oracle bit for bit on exact-arithmetic inputs, twice in a
+row, with no check failing. Then the test hook that shrinks the scratch size
+the checks allow makes a split call's partial sums reach past it: the call
+must end with TG_ERR_BOUNDS (the skipped accesses fault nothing), and the next
+call, with the real size, must be exact again. The normal build compiles the
+checks away: the same hook has no effect there."""
 import ctypes
 import os
 
@@ -73,6 +73,8 @@ def test_every_kernel_exact_with_the_checks_on(libs, M, N, K):
     ref = oracle.gemm(A, B, bias).view(np.uint16)
     dA, dB, db = A.cuda(), B.cuda(), bias.cuda()
     runs = [("pair", 0), ("tiled", 0), ("lsu", 0)]
+    if K >= 128:  # the single-CTA kernels with K split over slices
+        runs += [("tiled", 2), ("lsu", 3)]
     if M <= 128:
         runs += [("splitk", s) for s in (0, 1, 3, max(1, min(16, (K + 63) // 64)))]
     for name, split in runs:
@@ -141,6 +143,27 @@ def test_a_failed_check_is_reported_not_faulted(libs):
     assert _status(dbg) == (0, 0)  # cleared, and the next call is exact again
     C = _gemm(dbg, dA, dB, None, M, N, K, KERNELS["splitk"], 4)
     assert np.array_equal(C.cpu().numpy().view(np.uint16), ref)
+    assert _status(dbg) == (0, 0)
+
+
+def test_a_failed_check_in_a_tiled_split_is_reported_not_faulted(libs):
+    tg, dbg = libs
+    M, N, K = 256, 512, 1024
+    w = workloads.custom(M, N, K, seed=79, dist=INT1)
+    A, B, _ = w.inputs()
+    dA, dB = A.cuda(), B.cuda()
+    assert _status(dbg) == (0, 0)
+    # three K slices of 256 x 512 fp32 partials; allow the checks only 4096 floats of them
+    assert dbg.tg_debug_bounds_limit(4096) == 0
+    try:
+        _gemm(dbg, dA, dB, None, M, N, K, KERNELS["tiled"], 3)
+        st, where = _status(dbg)
+    finally:
+        dbg.tg_debug_bounds_limit(0)
+    assert st == tg.ERR_BOUNDS and where == 8
+    assert _status(dbg) == (0, 0)
+    C = _gemm(dbg, dA, dB, None, M, N, K, KERNELS["tiled"], 3)
+    assert np.array_equal(C.cpu().numpy().view(np.uint16), oracle.gemm(A, B).view(np.uint16))
     assert _status(dbg) == (0, 0)
 
 

@@ -51,6 +51,30 @@ def test_withheld_arrival_times_out_and_recovers(tg):
     assert tg.tg_device_status(None) == (tg.OK, 0)
 
 
+def test_withheld_arrival_in_a_split_launch_times_out_and_recovers(tg):
+    """The tiled kernel with K split over slices: the first unit of every CTA never gets its
+    first stage, so that launch times out; the reduction that follows sums whatever the
+    partials hold (the result is void, the status says so), and the next call is exact."""
+    w = workloads.custom(256, 1024, 2048, seed=35, dist=workloads.Dist("int", -2, 2))
+    A, B, _ = w.inputs()
+    dA, dB = A.cuda(), B.cuda()
+    assert tg.tg_device_status(None) == (tg.OK, 0)
+    tg.tg_set_watchdog_ns(20_000_000)
+    tg.tg_debug_skip_first_arrive(True)
+    try:
+        tg.gemm(dA, dB, kernel=tg.KERNEL_TILED_TMA, split_k=4)
+        st, where = tg.tg_device_status(None)
+    finally:
+        tg.tg_debug_skip_first_arrive(False)
+        tg.tg_set_watchdog_ns(0)
+    assert st == tg.ERR_TIMEOUT
+    assert where == 2
+    assert tg.tg_device_status(None) == (tg.OK, 0)
+    C = tg.gemm(dA, dB, kernel=tg.KERNEL_TILED_TMA, split_k=4)
+    assert np.array_equal(C.cpu().numpy().view(np.uint16), oracle.gemm(A, B).view(np.uint16))
+    assert tg.tg_device_status(None) == (tg.OK, 0)
+
+
 def test_withheld_stage_in_the_pair_kernel_times_out_and_recovers(tg):
     """The CTA-pair kernel, with its epilogue hand-off warp: a withheld first stage
     makes the MMA thread's wait expire; every other wait (the odd CTA's, the
