@@ -153,16 +153,17 @@ def test_a_failed_check_in_a_tiled_split_is_reported_not_faulted(libs):
     A, B, _ = w.inputs()
     dA, dB = A.cuda(), B.cuda()
     assert _status(dbg) == (0, 0)
-    # three K slices of 256 x 512 fp32 partials; allow the checks only 4096 floats of them
+    # three K slices of 256 x 512 fp32 partials in scratch (the ordinary-load variant; the TMA
+    # variant sums up to 8 slices on chip); allow the checks only 4096 floats of them
     assert dbg.tg_debug_bounds_limit(4096) == 0
     try:
-        _gemm(dbg, dA, dB, None, M, N, K, KERNELS["tiled"], 3)
+        _gemm(dbg, dA, dB, None, M, N, K, KERNELS["lsu"], 3)
         st, where = _status(dbg)
     finally:
         dbg.tg_debug_bounds_limit(0)
     assert st == tg.ERR_BOUNDS and where == 8
     assert _status(dbg) == (0, 0)
-    C = _gemm(dbg, dA, dB, None, M, N, K, KERNELS["tiled"], 3)
+    C = _gemm(dbg, dA, dB, None, M, N, K, KERNELS["lsu"], 3)
     assert np.array_equal(C.cpu().numpy().view(np.uint16), oracle.gemm(A, B).view(np.uint16))
     assert _status(dbg) == (0, 0)
 

@@ -22,9 +22,13 @@
 //   * the epilogue reads TMEM with tcgen05.ld, adds bias, applies GELU in fp32,
 //     rounds once to binary16 and stores with masking for ragged M/N;
 //   * when the tiles alone cannot fill the SMs (few rows, long K), K is split:
-//     a work unit is one K slice of one tile, the unit writes its fp32 tile to
-//     scratch, and the reduction kernel of the skinny path sums the slices in
-//     order and applies the epilogue.
+//     a work unit is one K slice of one tile. Up to 8 slices run as one
+//     thread-block cluster (one CTA per slice, one unit each): every CTA stages
+//     its fp32 tile in its own shared memory, and after a cluster barrier each
+//     sums its share of the tile's rows over all slices (distributed shared
+//     memory, slices in order) and applies the epilogue. Otherwise each unit
+//     writes its fp32 tile to scratch and the reduction kernel of the skinny
+//     path sums the slices in order and applies the epilogue.
 #include "tg_device.cuh"
 #include "tg_internal.h"
 
@@ -72,14 +76,21 @@ struct Roles {
 };
 
 // Work unit u: K slice u / num_tiles of tile u % num_tiles (the tiles' first slices first, so
-// the CTAs of one wave share the K range of the strips they read), K blocks [kb0, kb1).
+// the CTAs of one wave share the K range of the strips they read), K blocks [kb0, kb1). In a
+// cluster launch the CTAs of one cluster are the slices of one tile: slice u % splits.
 struct Unit {
     int tile, slice, kb0, kb1;
 };
+template <bool kCl>
 __device__ __forceinline__ Unit unit_of(const TiledArgs& a, int u) {
     Unit w;
-    w.slice = u / a.num_tiles;
-    w.tile = u - w.slice * a.num_tiles;
+    if (kCl) {
+        w.tile = u / a.splits;
+        w.slice = u - w.tile * a.splits;
+    } else {
+        w.slice = u / a.num_tiles;
+        w.tile = u - w.slice * a.num_tiles;
+    }
     w.kb0 = w.slice * a.kb_per_split;
     w.kb1 = min(a.num_kb, w.kb0 + a.kb_per_split);
     return w;
@@ -156,10 +167,17 @@ __device__ __forceinline__ void stage_B(uint8_t* sB, const __half* __restrict__ 
     }
 }
 
-template <bool kTma, int BN>
+// Cluster split: each CTA's fp32 tile, staged in its ring after its last MMA (row pitch
+// padded by 16 bytes).
+constexpr int kClPitch = kBN + 4;  // floats
+constexpr int kClStageBytes = kBM * kClPitch * 4;
+
+template <bool kTma, int BN, bool kCl>
 __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
     tiled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const TiledArgs args) {
+    static_assert(!kCl || (kTma && BN == kBN && kClStageBytes <= Geom<BN>::kRingBytes),
+                  "cluster split: TMA loads, 256-column tiles, the fp32 tile fits in the ring");
     using R = Roles<kTma>;
     using G = Geom<BN>;
     constexpr int kStageA = G::kStageA, kStageBytes = G::kStageBytes, kStagesN = G::kStagesN;
@@ -214,7 +232,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                 uint32_t phase = 0;
                 uint32_t issued_mask = 0, issued_parity = 0;
                 for (int u = blockIdx.x; u < args.num_units; u += gridDim.x) {
-                    const Unit w = unit_of(args, u);
+                    const Unit w = unit_of<kCl>(args, u);
                     int mb, nb;
                     tile_coords(w.tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
                     bool ok = true;
@@ -245,7 +263,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             for (int u = blockIdx.x; u < args.num_units; u += gridDim.x) {
-                const Unit w = unit_of(args, u);
+                const Unit w = unit_of<kCl>(args, u);
                 int mb, nb;
                 tile_coords(w.tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
                 bool ok = true;
@@ -276,7 +294,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x, ++it) {
-                const Unit w = unit_of(args, u);
+                const Unit w = unit_of<kCl>(args, u);
                 const int b = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!wait_phase(acc_empty_bar(b), acc_phase ^ 1, wc, kSiteMmaAccEmpty)) break;
@@ -315,7 +333,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
         uint8_t* stage = smem + G::kEpiStage + (warp - R::kEpiWarp0) * kStageWarpBytes;
         int it = 0;
         for (int u = blockIdx.x; u < args.num_units; u += gridDim.x, ++it) {
-            const Unit w = unit_of(args, u);
+            const Unit w = unit_of<kCl>(args, u);
             int mb, nb;
             tile_coords(w.tile, args.m_blocks, args.n_blocks, args.group_m, mb, nb);
             const int b = it & 1;
@@ -345,6 +363,12 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                 if (args.splits == 1) {
                     epilogue_chunk(r, stage, args.C, args.bias, row - lane, n0 + c * 32, args.M, args.N, args.gelu,
                                    args.c_store, args.bias_vec);
+                } else if (kCl) {
+                    // the ring is idle once the accumulator is complete: stage this slice's tile
+                    const uint32_t dst = sbase + static_cast<uint32_t>((row_in_tile * kClPitch + c * 32) * 4);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        sts_v4(dst + 16 * q, make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]));
                 } else if (row < args.m_pad) {
                     // fp32 partials [slice][n][m_pad]: the warp's lanes are 32 consecutive rows,
                     // so each column's values are one 128-byte store
@@ -365,13 +389,68 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (kCl) {
+        // every CTA of the cluster has staged its slice (each runs exactly one unit, and every
+        // thread reaches both cluster barriers, whether or not a wait gave up)
+        cluster_sync();
+        const int s = args.splits;
+        int tmb, tnb;
+        const Unit w = unit_of<kCl>(args, blockIdx.x);
+        tile_coords(w.tile, args.m_blocks, args.n_blocks, args.group_m, tmb, tnb);
+        // this CTA's share of the tile's rows, summed over the slices in order 0, 1, ...
+        const int rows_per = (kBM + s - 1) / s;
+        const int r_begin = w.slice * rows_per;
+        const int r_end = min(kBM, r_begin + rows_per);
+        const int m_tile = tmb * kBM, n_tile = tnb * kBN;
+        constexpr int kWarps = R::kThreads / 32;
+        for (int rr = r_begin + warp; rr < r_end; rr += kWarps) {
+            const int m = m_tile + rr;
+            if (m >= args.M) break;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int col = h * (kBN / 2) + lane * 4;
+                const int n = n_tile + col;
+                if (n >= args.N) continue;  // N % 8 == 0: four columns are all in or all out
+                const uint32_t off = sbase + static_cast<uint32_t>((rr * kClPitch + col) * 4);
+                float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                for (int q = 0; q < s; ++q) {
+                    const float4 p = ld_cluster_f4(mapa_shared(off, q));
+                    acc.x += p.x;
+                    acc.y += p.y;
+                    acc.z += p.z;
+                    acc.w += p.w;
+                }
+                float b[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                if (args.bias != nullptr)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) b[j] = __half2float(args.bias[n + j]);
+                const __half2 lo = __halves2half2(__float2half_rn(epi_value(acc.x, b[0], args.gelu)),
+                                                  __float2half_rn(epi_value(acc.y, b[1], args.gelu)));
+                const __half2 hi = __halves2half2(__float2half_rn(epi_value(acc.z, b[2], args.gelu)),
+                                                  __float2half_rn(epi_value(acc.w, b[3], args.gelu)));
+                __half* dst = args.C + static_cast<int64_t>(m) * args.N + n;
+                if (args.c_store == 2) {
+                    uint2 v;
+                    v.x = *reinterpret_cast<const uint32_t*>(&lo);
+                    v.y = *reinterpret_cast<const uint32_t*>(&hi);
+                    *reinterpret_cast<uint2*>(dst) = v;
+                } else {
+                    dst[0] = __low2half(lo);
+                    dst[1] = __high2half(lo);
+                    dst[2] = __low2half(hi);
+                    dst[3] = __high2half(hi);
+                }
+            }
+        }
+        cluster_sync();  // no CTA leaves while another may still read its shared memory
+    }
     if (warp == R::kMmaWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, G::kTmemCols);
     }
 }
 
-template <bool kTma, int BN>
+template <bool kTma, int BN, bool kCl = false>
 cudaError_t launch(const TiledArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB, int grid,
                    cudaStream_t stream) {
     using R = Roles<kTma>;
@@ -381,13 +460,32 @@ cudaError_t launch(const TiledArgs& a, const CUtensorMap* tmA, const CUtensorMap
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && attr_gen[dev] != g_generation) {
-        e = cudaFuncSetAttribute(tiled_gemm_kernel<kTma, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        e = cudaFuncSetAttribute(tiled_gemm_kernel<kTma, BN, kCl>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
         attr_gen[dev] = g_generation;
     }
     CUtensorMap dummy{};
-    tiled_gemm_kernel<kTma, BN><<<grid, R::kThreads, kSmem, stream>>>(tmA ? *tmA : dummy, tmB ? *tmB : dummy, a);
-    return cudaGetLastError();
+    if constexpr (kCl) {
+        // one cluster of `splits` CTAs per tile, one unit per CTA
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(a.num_units);
+        cfg.blockDim = dim3(R::kThreads);
+        cfg.dynamicSmemBytes = kSmem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = a.splits;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        (void)grid;
+        return cudaLaunchKernelEx(&cfg, tiled_gemm_kernel<kTma, BN, kCl>, tmA ? *tmA : dummy, tmB ? *tmB : dummy, a);
+    } else {
+        tiled_gemm_kernel<kTma, BN, kCl><<<grid, R::kThreads, kSmem, stream>>>(tmA ? *tmA : dummy, tmB ? *tmB : dummy,
+                                                                              a);
+        return cudaGetLastError();
+    }
 }
 
 template <bool kTma>
@@ -406,6 +504,47 @@ int tiled_threads(bool tma) { return tma ? Roles<true>::kThreads : Roles<false>:
 cudaError_t launch_tiled_tma(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                              cudaStream_t stream) {
     return launch_bn<true>(a, &tmA, &tmB, grid, stream);
+}
+
+int tiled_cluster_capacity(int splits) {
+    if (splits < 2 || splits > kTiledClusterMax) return 0;
+    static int gen[64] = {};
+    static int cap[64][kTiledClusterMax + 1] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 0;
+    if (gen[dev] != g_generation) {
+        using R = Roles<true>;
+        constexpr int kSmem = Geom<kBN>::kSmemAlloc;
+        auto kern = tiled_gemm_kernel<true, kBN, true>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess) return 0;
+        for (int c = 2; c <= kTiledClusterMax; ++c) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(c * 64);
+            cfg.blockDim = dim3(R::kThreads);
+            cfg.dynamicSmemBytes = kSmem;
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = c;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+            cap[dev][c] = n;
+        }
+        gen[dev] = g_generation;
+    }
+    return cap[dev][splits];
+}
+
+cudaError_t launch_tiled_cluster(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                 cudaStream_t stream) {
+    if (a.bn != kBN || a.splits < 2 || a.splits > kTiledClusterMax) return cudaErrorInvalidValue;
+    return launch<true, kBN, true>(a, &tmA, &tmB, a.num_units, stream);
 }
 
 cudaError_t launch_tiled_lsu(const TiledArgs& a, int grid, cudaStream_t stream) {

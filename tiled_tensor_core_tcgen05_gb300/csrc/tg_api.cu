@@ -2,6 +2,7 @@
 // scratch, the device watchdog word, and launches. The operation and its
 // conventions are documented in include/tg_gemm.h.
 #include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -417,34 +418,48 @@ int tiled_bn(const DeviceState& d, int64_t m_blocks, int64_t N) {
     return bn;
 }
 
+#ifndef TG_TILED_CLUSTER_SPLIT
+#define TG_TILED_CLUSTER_SPLIT 1
+#endif
+
+// True when a K split of `splits` slices runs as clusters that sum the slices on chip: TMA
+// loads, at most kTiledClusterMax slices, and every tile's cluster resident at once.
+bool tiled_on_chip(bool tma, int64_t tiles256, int splits) {
+    return TG_TILED_CLUSTER_SPLIT && tma && splits > 1 && splits <= kTiledClusterMax &&
+           tiles256 <= tiled_cluster_capacity(splits);
+}
+
 // K slices for the single-CTA kernel (1 = no split), from a time model fitted to GB300
 // measurements (N, K in 2048..28672, M in 64..1024; wherever the tiled kernel runs, its pick
-// is within 3% of the fastest measured count). Time is counted in K blocks of one 128 x 256 tile
-// (~0.38 us): a 128- or 64-column tile's K block costs 0.72 or 0.70 of one (their loads,
-// not their MMAs, bound them), a launch never beats reading A and B once from HBM (~2.4 MB
-// per unit), and a split adds ~20 for the partial-sum epilogue and the reduction launch
-// plus ~1.14 per MB of fp32 partials written and read back. Only problems whose 256-wide
-// tiles number fewer than the SMs are split.
-int tiled_splits(const DeviceState& d, int64_t M, int64_t N, int64_t K) {
+// is within 1% of the fastest measured choice). Times in us: a K block costs 0.36 (a 128 x
+// 256 tile) or 0.26 (128 or 64 columns: loads, not MMAs, bound those tiles) per wave; reading
+// A and B once from HBM at ~7.4 TB/s is the other term, and the two combine as a 2.5-norm (the
+// larger dominates, the smaller still counts). A split adds 5.5 when the slices of each tile
+// run as one cluster and are summed on chip, or 7.4 plus 0.44 per MB of fp32 partials when
+// they go through scratch and the reduction kernel. Only problems whose 256-wide tiles number
+// fewer than the SMs are split.
+int tiled_splits(const DeviceState& d, int64_t M, int64_t N, int64_t K, bool tma) {
     const int64_t m_blocks = (M + kBM - 1) / kBM;
     const int64_t kb = (K + kBK - 1) / kBK;
     const int64_t tiles256 = m_blocks * ((N + kBN - 1) / kBN);
     if (tiles256 >= d.sm_count) return 1;
+    const double hbm = (static_cast<double>(M) * K + static_cast<double>(K) * N) * 2.0 / 1e6 / 7.4;
+    auto time = [&](double compute) { return std::pow(std::pow(compute, 2.5) + std::pow(hbm, 2.5), 0.4); };
     const int bn = tiled_bn(d, m_blocks, N);
-    const double rel = bn == 256 ? 1.0 : bn == 128 ? 0.72 : 0.70;
     const int64_t tiles = m_blocks * ((N + bn - 1) / bn);
-    const double hbm = (static_cast<double>(M) * K + static_cast<double>(K) * N) * 2.0 / 1e6 / 2.37;
-    double best = static_cast<double>((tiles + d.sm_count - 1) / d.sm_count) * kb * rel;
-    if (best < hbm) best = hbm;
+    double best = time(static_cast<double>((tiles + d.sm_count - 1) / d.sm_count) * kb * (bn == 256 ? 0.36 : 0.26));
     int best_s = 1;
     const double m_pad = static_cast<double>((M + 15) / 16 * 16);
     for (int s = 2; s <= kSkMaxSplits && s <= kb; ++s) {
         const int64_t kbps = (kb + s - 1) / s;
         if ((kb + kbps - 1) / kbps != s) continue;
-        const int64_t waves = (tiles256 * s + d.sm_count - 1) / d.sm_count;
-        double t = static_cast<double>(waves) * kbps;
-        if (t < hbm) t = hbm;
-        t += 20.0 + 1.14 * s * m_pad * static_cast<double>(N) * 4.0 / 1e6;
+        double t;
+        if (tiled_on_chip(tma, tiles256, s)) {
+            t = time(static_cast<double>(kbps) * 0.36) + 5.5;
+        } else {
+            const int64_t waves = (tiles256 * s + d.sm_count - 1) / d.sm_count;
+            t = time(static_cast<double>(waves) * kbps * 0.36) + 7.4 + 0.44 * s * m_pad * static_cast<double>(N) * 4.0 / 1e6;
+        }
         if (t < best) {
             best = t;
             best_s = s;
@@ -460,7 +475,7 @@ tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, 
     a.M = M; a.N = N; a.K = K; a.gelu = gelu;
     a.m_blocks = (M + kBM - 1) / kBM;
     a.num_kb = (K + kBK - 1) / kBK;
-    int s = split_k > 0 ? split_k : tiled_splits(d, M, N, K);
+    int s = split_k > 0 ? split_k : tiled_splits(d, M, N, K, tma);
     if (s > a.num_kb) s = a.num_kb;
     a.kb_per_split = (a.num_kb + s - 1) / s;
     a.splits = (a.num_kb + a.kb_per_split - 1) / a.kb_per_split;
@@ -477,7 +492,10 @@ tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, 
     a.a_vec = vec_width(A, K);
     a.b_vec = vec_width(B, N);
     a.wd = watchdog(d);
-    if (a.splits > 1) {
+    // slices summed on chip by clusters when they fit (tiled_on_chip); otherwise through scratch
+    // and the reduction kernel
+    const bool on_chip = tiled_on_chip(tma, static_cast<int64_t>(a.m_blocks) * ((N + kBN - 1) / kBN), a.splits);
+    if (a.splits > 1 && !on_chip) {
         if ((static_cast<int64_t>(M) + 15) / 16 > 65535)
             return fail(TG_ERR_INVALID_ARG, "a K split of the tiled kernels supports M <= 1048560, got %d", M);
         Scratch* sc = nullptr;
@@ -493,12 +511,12 @@ tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, 
         tg_status st = make_map_ld(&tmA, A, K, M, lda ? lda : K, kBK, kBM);
         if (st != TG_OK) return st;
         if ((st = make_map_ld(&tmB, B, N, K, ldb ? ldb : N, 64, kBK)) != TG_OK) return st;
-        e = launch_tiled_tma(a, tmA, tmB, grid, stream);
+        e = on_chip ? launch_tiled_cluster(a, tmA, tmB, stream) : launch_tiled_tma(a, tmA, tmB, grid, stream);
     } else {
         e = launch_tiled_lsu(a, grid, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "tiled kernel launch");
-    if (a.splits > 1) {
+    if (a.splits > 1 && !on_chip) {
         // the skinny path's reduction: slices summed in order, then bias, GELU, one rounding
         SplitArgs r{};
         r.bias = bias; r.C = C;
@@ -560,18 +578,23 @@ bool pair_pays(const DeviceState& d, int64_t M, int64_t N, int64_t K) {
 }
 
 // True when the skinny split-K kernel beats the single-CTA tiled kernel for M <= 128
-// (measured on GB300 over N = 2048..28672, K = 2048..28672, M = 16..128). The tiled kernel
-// cannot split K: with fewer 64-column tiles than SMs it runs one partial wave whose time
-// grows with K/64, while split-K spreads K over every SM and costs a little more per row of
-// M. So split-K is used for M <= 16; with fewer 64-column tiles than SMs, when K/64 times
-// the SMs per tile is at least 1.5 M; otherwise only when, with M <= 64, the product
-// streams 256 MB or more of B (both kernels then sit near the HBM floor).
+// (measured on GB300 over N = 2048..28672, K = 2048..28672, M = 16..128). Skinny for M <= 16.
+// Above that, where the tiled kernel can split K on chip (its 256-column tiles fit the
+// two-CTA clusters at once), it ties or wins except for the skinniest products streaming a
+// large B through a split: skinny only for M <= 32 with at least 64 MiB of B when the tiled
+// kernel would split K (4096 x 14336 at M = 32: 29.1 vs 30.9 us). Where it cannot, the earlier
+// rule against the unsplit tiled kernel stands: with fewer 64-column tiles than SMs,
+// skinny when K/64 times the SMs per tile is at least 1.5 M; otherwise only when, with
+// M <= 64, the product streams 256 MiB or more of B (both kernels then sit near the HBM floor).
 bool skinny_pays(const DeviceState& d, int64_t M, int64_t N, int64_t K) {
     if (M <= 16) return true;
+    const double b_bytes = 2.0 * static_cast<double>(K) * static_cast<double>(N);
+    if (tiled_on_chip(true, (N + kBN - 1) / kBN, 2))
+        return M <= 32 && b_bytes >= 64.0 * 1048576.0 && tiled_splits(d, M, N, K, true) > 1;
     const int64_t tiles64 = (N + 63) / 64;  // one 128-row block: M <= 128
     const int64_t kb = (K + 63) / 64;
     if (tiles64 < d.sm_count) return 2 * kb * d.sm_count >= 3 * M * tiles64;
-    return M <= 64 && 2.0 * static_cast<double>(K) * static_cast<double>(N) >= 256.0 * 1048576.0;
+    return M <= 64 && b_bytes >= 256.0 * 1048576.0;
 }
 
 // A GEMM whose A or B TMA cannot describe (row stride not a multiple of 16
@@ -653,7 +676,7 @@ Plan plan_auto(const DeviceState& d, int64_t M, int64_t N, int64_t K, bool tma_o
         p.splits = a.splits;
     } else if (K > 0 && p.kernel != TG_KERNEL_TILED_PAIR) {
         const int kb = static_cast<int>((K + kBK - 1) / kBK);
-        int s = tiled_splits(d, M, N, K);
+        int s = tiled_splits(d, M, N, K, p.kernel == TG_KERNEL_TILED_TMA);
         if (s > kb) s = kb;
         const int kbps = (kb + s - 1) / s;
         p.splits = (kb + kbps - 1) / kbps;

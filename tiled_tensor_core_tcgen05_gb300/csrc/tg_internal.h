@@ -192,6 +192,15 @@ int tiled_threads(bool tma);
 
 cudaError_t launch_tiled_tma(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
                              int grid, cudaStream_t stream);
+// The single-CTA kernel with K split over 2..kTiledClusterMax slices as thread-block clusters
+// (one CTA per slice of each 256-column tile, num_units = num_tiles * splits CTAs): the slices
+// are summed in distributed shared memory, no scratch, no second kernel.
+constexpr int kTiledClusterMax = 8;
+// Clusters of `splits` CTAs of that kernel that fit on the current device at once (0 when
+// splits is out of range or the query fails).
+int tiled_cluster_capacity(int splits);
+cudaError_t launch_tiled_cluster(const TiledArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                 cudaStream_t stream);
 cudaError_t launch_tiled_lsu(const TiledArgs& a, int grid, cudaStream_t stream);
 int tiled_pair_smem_bytes();
 // tmC: map of C (32 x 32 box, 64-byte swizzle) to write C by TMA stores, or

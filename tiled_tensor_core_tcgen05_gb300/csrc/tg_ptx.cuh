@@ -40,6 +40,16 @@ __device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
+// 16-byte load from the shared memory of any CTA of the cluster (a mapa address).
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint16_t lds_u16(uint32_t addr) {
     uint16_t v;
     asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
