@@ -1,12 +1,14 @@
 """GPU parity of the single-CTA tiled kernel with K split over slices.
 
 When a problem's 128 x 256 tiles leave SMs idle (few rows, long K), a work unit
-of the tiled kernel is one K slice of one tile; each unit writes its fp32 tile
-to scratch and a second kernel sums the slices in order, then applies bias,
-GELU and one rounding (the epilogue of "Designing high-performance GPU kernels
-with TileLang ...", section 3, applied once to the full sum). The product is
-still the tile program of "TileLang: writing LLM GPU kernels by thinking in
-tiles", section 3: only the K loop is divided.
+of the tiled kernel is one K slice of one tile. With TMA loads and up to 8
+slices, the slices of a tile run as one thread-block cluster and are summed in
+distributed shared memory; otherwise each unit writes its fp32 tile to scratch
+and a second kernel sums the slices. Either way the slices are added in order,
+then bias, GELU and one rounding follow (the epilogue of "Designing
+high-performance GPU kernels with TileLang ...", section 3, applied once to the
+full sum). The product is still the tile program of "TileLang: writing LLM GPU
+kernels by thinking in tiles", section 3: only the K loop is divided.
 
 Integer inputs keep every partial sum exact in fp32, so every split count must
 reproduce the oracle bit for bit; float inputs are held to the parity
@@ -136,3 +138,21 @@ def test_pair_kernel_refuses_a_split(tg):
     with pytest.raises(tg.TgError) as ei:
         tg.gemm(A, B, kernel=tg.KERNEL_TILED_PAIR, split_k=2)
     assert ei.value.status == tg.ERR_INVALID_ARG
+
+
+def test_on_chip_and_scratch_reductions_agree_bit_for_bit(tg):
+    # The TMA variant sums up to 8 slices inside a cluster (distributed shared memory); the
+    # ordinary-load variant sums them in scratch with the reduction kernel. Both add the
+    # slices in order 0, 1, ... to the same fp32 partials, so on float inputs their outputs
+    # must be the same bits, and both within the oracle's tolerance.
+    M, N, K = 200, 1032, 4104
+    w = workloads.custom(M, N, K, seed=7400, bias=workloads.Dist("uniform", -0.1, 0.1), gelu=True)
+    A, B, bias = w.inputs()
+    dA, dB, dbias = A.cuda(), B.cuda(), bias.cuda()
+    ref = oracle.gemm(A, B, bias, gelu=True)
+    for split_k in (2, 3, 7):
+        on_chip = tg.gemm(dA, dB, dbias, gelu=True, kernel=tg.KERNEL_TILED_TMA, split_k=split_k)
+        scratch = tg.gemm(dA, dB, dbias, gelu=True, kernel=tg.KERNEL_TILED_LSU, split_k=split_k)
+        assert torch.equal(on_chip.view(torch.int16), scratch.view(torch.int16)), f"split_k={split_k}"
+        _check_tol(on_chip.cpu().float().numpy(), ref, f"split_k={split_k}")
+    _status_ok(tg)
