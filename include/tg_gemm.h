@@ -101,14 +101,18 @@ typedef enum {
  * up to 8 elements (one buffer per stream, grown as needed, freed by
  * tg_shutdown; TG_ERR_NO_MEMORY if it cannot be allocated), then the TMA
  * kernels below run on the copy; M <= 16, or M <= 128 where the skinny kernel
- * measured faster (fewer 64-column tiles than SMs with (K / 64) * SMs / tiles
- * >= 1.5 M, or M <= 64 with 2 K N >= 256 MiB of B) -> TG_KERNEL_SPLITK; other
- * M <= 128 -> TG_KERNEL_TILED_TMA; at least one
- * 256x256 tile per pair of SMs, or with K >= 8192 at least 0.3 of one ->
- * TG_KERNEL_TILED_PAIR; otherwise
- * TG_KERNEL_TILED_TMA. TG_KERNEL_TILED_TMA (and TG_KERNEL_TILED_LSU) split K
- * when their tiles leave SMs idle and a cost model of the slices, their
- * partial sums and the reduction predicts a gain (see tg_gemm_ex).
+ * measured faster -> TG_KERNEL_SPLITK; other M <= 128 -> TG_KERNEL_TILED_TMA.
+ * "Measured faster" means one of two cases:
+ *   - where the tiled kernel can sum a K split on chip (N at most one
+ *     256-column tile per two-CTA cluster the device holds at once): M <= 32,
+ *     2 K N >= 64 MiB of B, and the tiled kernel would split K;
+ *   - elsewhere: fewer 64-column tiles than SMs with
+ *     (K / 64) * SMs / tiles >= 1.5 M, or M <= 64 with 2 K N >= 256 MiB of B.
+ * M > 128: at least one 256x256 tile per pair of SMs, or with K >= 8192 at
+ * least 0.3 of one -> TG_KERNEL_TILED_PAIR; otherwise TG_KERNEL_TILED_TMA.
+ * TG_KERNEL_TILED_TMA (and TG_KERNEL_TILED_LSU) split K when their tiles leave
+ * SMs idle and a cost model of the slices and their summation predicts a gain
+ * (see tg_gemm_ex).
  */
 tg_status tg_gemm(const void* A, const void* B, const void* bias, void* C,
                   int64_t M, int64_t N, int64_t K, int epilogue, tg_stream_t stream);
@@ -134,12 +138,17 @@ tg_status tg_gemm_plan(const void* A, const void* B, int64_t M, int64_t N, int64
  * TG_KERNEL_TILED_LSU); with TG_KERNEL_TILED_PAIR it is TG_ERR_INVALID_ARG, and
  * with TG_KERNEL_AUTO it is used only when the choice is TG_KERNEL_SPLITK.
  * The tiled kernels' automatic count splits only problems whose 128 x 256
- * tiles number fewer than the SMs: each slice's fp32 partial tile goes to the
- * stream's scratch (splits * N * M rounded up to 16, fp32; allocated as for
- * TG_KERNEL_SPLITK) and a second kernel on `stream` sums the slices in order
- * before the epilogue (a tiled kernel's split needs M <= 1048560). A kernel
- * whose requirements the arguments do not meet is TG_ERR_INVALID_ARG. Results of all kernels agree within the
- * accumulation-order tolerance stated above; on inputs whose products and
+ * tiles number fewer than the SMs. With TG_KERNEL_TILED_TMA and 2..8 slices
+ * whose clusters (one per tile, one CTA per slice) all fit on the device at
+ * once, the slices are summed on chip through distributed shared memory.
+ * Otherwise each slice's fp32 partial tile goes to the stream's scratch
+ * (splits * N * M rounded up to 16, fp32; allocated as for TG_KERNEL_SPLITK)
+ * and a second kernel on `stream` sums the slices (this form needs
+ * M <= 1048560). Both add the slices in order, so they give the same bits,
+ * and the epilogue follows the full sum. A kernel whose requirements the
+ * arguments do not meet is TG_ERR_INVALID_ARG. Results of all kernels agree
+ * within the accumulation-order tolerance stated above; on inputs whose
+ * products and
  * partial sums are exact in fp32 they are bit-identical.
  */
 tg_status tg_gemm_ex(const void* A, const void* B, const void* bias, void* C,
