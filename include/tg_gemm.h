@@ -148,8 +148,7 @@ tg_status tg_gemm_plan(const void* A, const void* B, int64_t M, int64_t N, int64
  * and the epilogue follows the full sum. A kernel whose requirements the
  * arguments do not meet is TG_ERR_INVALID_ARG. Results of all kernels agree
  * within the accumulation-order tolerance stated above; on inputs whose
- * products and
- * partial sums are exact in fp32 they are bit-identical.
+ * products and partial sums are exact in fp32 they are bit-identical.
  */
 tg_status tg_gemm_ex(const void* A, const void* B, const void* bias, void* C,
                      int64_t M, int64_t N, int64_t K, int epilogue, int kernel, int split_k,
