@@ -144,8 +144,10 @@ tg_status tg_gemm_plan(const void* A, const void* B, int64_t M, int64_t N, int64
  * Otherwise each slice's fp32 partial tile goes to the stream's scratch
  * (splits * N * M rounded up to 16, fp32; allocated as for TG_KERNEL_SPLITK)
  * and a second kernel on `stream` sums the slices (this form needs
- * M <= 1048560). Both add the slices in order, so they give the same bits,
- * and the epilogue follows the full sum. A kernel whose requirements the
+ * M <= 1048560). TG_KERNEL_SPLITK sums its slices the same two ways (on chip
+ * for 2..8 slices whose clusters, one per 256-column unit, all fit at once).
+ * Both ways add the slices in order, so they give the same bits, and the
+ * epilogue follows the full sum. A kernel whose requirements the
  * arguments do not meet is TG_ERR_INVALID_ARG. Results of all kernels agree
  * within the accumulation-order tolerance stated above; on inputs whose
  * products and partial sums are exact in fp32 they are bit-identical.
@@ -197,23 +199,25 @@ tg_status tg_bias_gelu(void* C, const void* bias, int64_t M, int64_t N, int epil
  * the number of K slices automatically, never more than fit in the fixed
  * array (one slice needs none, so an automatic call is never refused for
  * size), 1..64 fixes it. The caller still
- * passes A, B, bias and C (device pointers it owns). With more than one K
- * slice, the partial sums live in one fixed array of
- * TG_NOALLOC_SCRATCH_BYTES compiled into the library's device image: every
- * device that loads the library holds it until the process exits. A call whose
- * slices need more (4 * slices * N * Mp bytes of partials, Mp = M rounded up to
- * a multiple of 16, plus a reserved head of 4 bytes per 256-column slice of
- * N, rounded up to 256)
+ * passes A, B, bias and C (device pointers it owns). With 2..8 K slices whose
+ * clusters (one per 256-column unit, one CTA per slice) all fit on the device
+ * at once, the slices are summed on chip and no scratch is used, as in
+ * tg_gemm_ex. Otherwise, with more than one slice, the partial sums live in
+ * one fixed array of TG_NOALLOC_SCRATCH_BYTES compiled into the library's
+ * device image: every device that loads the library holds it until the
+ * process exits. A call whose partials go through the array and need more
+ * (4 * slices * N * Mp bytes, Mp = M rounded up to a multiple of 16, plus a
+ * reserved head of 4 bytes per 256-column slice of N, rounded up to 256)
  * returns TG_ERR_INVALID_ARG and enqueues nothing. Nothing is allocated or
  * freed by any call.
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture begins. Every call writes the partials before a second
- * kernel on `stream` sums them, so nothing carries over between calls. All
- * calls share the one array, so calls whose work can overlap on the GPU (for
- * example on two streams without ordering between them) race and give wrong
- * results; order them on one stream or with events.
+ * any stream capture begins. Every call that uses the array writes the
+ * partials before a second kernel on `stream` sums them, so nothing carries
+ * over between calls. All calls share the one array, so calls whose work can
+ * overlap on the GPU (for example on two streams without ordering between
+ * them) race and give wrong results; order them on one stream or with events.
  */
 tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const void* bias, void* C,
                                  int64_t M, int64_t N, int64_t K, int epilogue, int split_k,

@@ -132,16 +132,17 @@ def test_a_failed_check_is_reported_not_faulted(libs):
     ref = oracle.gemm(A, B).view(np.uint16)
     dA, dB = A.cuda(), B.cuda()
     assert _status(dbg) == (0, 0)
-    # four K slices write 4 x 16 x 2048 floats of partials; allow the checks only 1024 of them
+    # sixteen K slices (more than a cluster sums on chip) write 16 x 16 x 2048 floats of
+    # partials to scratch; allow the checks only 1024 of them
     assert dbg.tg_debug_bounds_limit(1024) == 0
     try:
-        _gemm(dbg, dA, dB, None, M, N, K, KERNELS["splitk"], 4)
+        _gemm(dbg, dA, dB, None, M, N, K, KERNELS["splitk"], 16)
         st, where = _status(dbg)
     finally:
         dbg.tg_debug_bounds_limit(0)
     assert st == tg.ERR_BOUNDS and where == 8
     assert _status(dbg) == (0, 0)  # cleared, and the next call is exact again
-    C = _gemm(dbg, dA, dB, None, M, N, K, KERNELS["splitk"], 4)
+    C = _gemm(dbg, dA, dB, None, M, N, K, KERNELS["splitk"], 16)
     assert np.array_equal(C.cpu().numpy().view(np.uint16), ref)
     assert _status(dbg) == (0, 0)
 

@@ -24,6 +24,10 @@
 #include "tg_internal.h"
 #include "tg_skinny.cuh"
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 namespace tg {
 namespace {
 
@@ -53,6 +57,10 @@ __host__ __device__ inline Layout layout_for(int m_pad, int stages) {
     return L;
 }
 
+// kCl: the K slices of one unit run as one thread-block cluster (one unit per CTA) and are
+// summed across the cluster's shared memory after the product; otherwise partials go to
+// scratch for splitk_reduce_kernel.
+template <bool kCl>
 __global__ void __launch_bounds__(kThreads, 1)
     splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
                        const SplitArgs args) {
@@ -108,8 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x) {
-                const int sp = u / args.n_tiles;
-                const int nt = u - sp * args.n_tiles;
+                const int sp = kCl ? u % args.splits : u / args.n_tiles;
+                const int nt = kCl ? u / args.splits : u - sp * args.n_tiles;
                 const int kb0 = sp * args.kb_per_split;
                 const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -139,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x, ++it) {
-                const int sp = u / args.n_tiles;
+                const int sp = kCl ? u % args.splits : u / args.n_tiles;
                 const int kb0 = sp * args.kb_per_split;
                 const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
                 const int b = it & 1;
@@ -172,11 +180,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        skinny_epilogue<kSkHalves>(args, tmem_base, acc_full_bar(0), acc_empty_bar(0), wc);
+        skinny_epilogue<kSkHalves, kCl>(args, tmem_base, acc_full_bar(0), acc_empty_bar(0), wc, sbase);
     }
 
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (kCl) {
+        // every CTA of the cluster has staged its slice (one unit each; every thread reaches both
+        // cluster barriers, whether or not a wait gave up). The unit's m_pad x 256 outputs, as
+        // 4-column groups, are shared out over the cluster's CTAs; each group's slices are added
+        // in order 0, 1, ... (the order of the reduction kernel, so the same bits).
+        cluster_sync();
+        const int s = args.splits;
+        const int sp = blockIdx.x % s;
+        const int n_unit = (blockIdx.x / s) * kSkBN;
+        const int groups = args.M * (kSkBN / 4);
+        const int per = (groups + s - 1) / s;
+        const int g1 = min(groups, (sp + 1) * per);
+        for (int g = sp * per + static_cast<int>(threadIdx.x); g < g1; g += kThreads) {
+            const int m = g / (kSkBN / 4);
+            const int col = (g - m * (kSkBN / 4)) * 4;
+            const int n = n_unit + col;
+            if (n >= args.N) continue;  // N % 8 == 0: four columns are all in or all out
+            const uint32_t off = sbase + static_cast<uint32_t>((m * kSkClPitch + col) * 4);
+            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            for (int q = 0; q < s; ++q) {
+                const float4 p = ld_cluster_f4(mapa_shared(off, q));
+                acc.x += p.x;
+                acc.y += p.y;
+                acc.z += p.z;
+                acc.w += p.w;
+            }
+            const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+            __half* dst = args.C + static_cast<int64_t>(m) * args.N + n;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                dst[j] = __float2half_rn(epi_value(v[j], args.bias != nullptr ? __half2float(args.bias[n + j]) : 0.0f,
+                                                   args.gelu));
+        }
+        cluster_sync();  // no CTA leaves while another may still read its shared memory
+    }
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, args.tmem_cols);
@@ -195,6 +238,10 @@ int split_stages_for(int m_pad) {
 }
 
 int split_smem_bytes(int m_pad, int stages) { return layout_for(m_pad, stages).alloc; }
+
+bool split_on_chip_fits(int m_pad, int stages) {
+    return layout_for(m_pad, stages).ring >= m_pad * kSkClPitch * 4;
+}
 
 namespace {
 
@@ -267,13 +314,80 @@ cudaError_t launch_splitk(const SplitArgs& a, const CUtensorMap& tmB, const CUte
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && attr_gen[dev] != g_generation) {
-        e = cudaFuncSetAttribute(splitk_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e != cudaSuccess) return e;
+        for (auto kern : {splitk_gemm_kernel<false>, splitk_gemm_kernel<true>})
+            if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)) != cudaSuccess)
+                return e;
         attr_gen[dev] = g_generation;
     }
     const int smem = split_smem_bytes(a.m_pad, a.stages);
-    splitk_gemm_kernel<<<grid, kThreads, smem, stream>>>(tmB, tmA, a);
+    splitk_gemm_kernel<false><<<grid, kThreads, smem, stream>>>(tmB, tmA, a);
     return cudaGetLastError();
+}
+
+int split_cluster_capacity(int splits, int m_pad, int stages) {
+    if (splits < 2 || splits > kTiledClusterMax) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const int smem = split_smem_bytes(m_pad, stages);
+    // cached by (device, generation, cluster size, shared memory)
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int>, int> cache;
+    const auto key = std::make_tuple(dev, g_generation, splits, smem);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaFuncSetAttribute(splitk_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
+        cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(splits * 64);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = splits;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, splitk_gemm_kernel<true>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+    } else {
+        cudaGetLastError();
+    }
+    cache[key] = n;
+    return n;
+}
+
+cudaError_t launch_splitk_cluster(const SplitArgs& a, const CUtensorMap& tmB, const CUtensorMap& tmA,
+                                  cudaStream_t stream) {
+    if (a.splits < 2 || a.splits > kTiledClusterMax || !split_on_chip_fits(a.m_pad, a.stages))
+        return cudaErrorInvalidValue;
+    static int attr_gen[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && attr_gen[dev] != g_generation) {
+        if ((e = cudaFuncSetAttribute(splitk_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      227 * 1024)) != cudaSuccess)
+            return e;
+        attr_gen[dev] = g_generation;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.num_units);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = split_smem_bytes(a.m_pad, a.stages);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = a.splits;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_gemm_kernel<true>, tmB, tmA, a);
 }
 
 }  // namespace tg

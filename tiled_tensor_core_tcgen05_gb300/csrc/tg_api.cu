@@ -380,12 +380,28 @@ void splitk_args(const DeviceState& d, const __half* A, const __half* B, const _
     a.wd = watchdog(d);
 }
 
-// Tensor maps and launch of the skinny kernel, its scratch already in `a`.
+#ifndef TG_SPLIT_CLUSTER
+#define TG_SPLIT_CLUSTER 1
+#endif
+
+// True when the skinny kernel's K slices run as clusters summed on chip: 2..kTiledClusterMax
+// slices, the staged fp32 tile fits the ring, and every unit's cluster is resident at once.
+bool split_on_chip(const SplitArgs& a) {
+    return TG_SPLIT_CLUSTER && a.splits > 1 && a.splits <= kTiledClusterMax && split_on_chip_fits(a.m_pad, a.stages) &&
+           a.n_tiles <= split_cluster_capacity(a.splits, a.m_pad, a.stages);
+}
+
+// Tensor maps and launch of the skinny kernel, its scratch (when the slices are not summed
+// on chip) already in `a`.
 tg_status splitk_launch(const DeviceState& d, const SplitArgs& a, cudaStream_t stream) {
     CUtensorMap tmB, tmA;
     tg_status st = make_map(&tmB, a.B, a.N, a.K, 64, kSkBK);
     if (st != TG_OK) return st;
     if ((st = make_map(&tmA, a.A, a.K, a.M, kSkBK, a.m_pad)) != TG_OK) return st;
+    if (split_on_chip(a)) {
+        const cudaError_t e = launch_splitk_cluster(a, tmB, tmA, stream);
+        return e == cudaSuccess ? TG_OK : cuda_fail(e, "split-K cluster kernel launch");
+    }
     const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
     cudaError_t e = launch_splitk(a, tmB, tmA, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "split-K kernel launch");
@@ -398,7 +414,7 @@ tg_status run_splitk(DeviceState& d, const __half* A, const __half* B, const __h
                      int K, int gelu, int split_k, cudaStream_t stream) {
     SplitArgs a;
     splitk_args(d, A, B, bias, C, M, N, K, gelu, split_k, kSkMaxSplits, a);
-    if (a.splits > 1) {
+    if (a.splits > 1 && !split_on_chip(a)) {
         Scratch* sc = nullptr;
         // the partials only: the reduction kernel needs no arrival counters
         tg_status st = ensure_scratch(d, stream, static_cast<size_t>(a.splits) * N * a.m_pad * sizeof(float), 0, &sc);
@@ -983,7 +999,7 @@ extern "C" tg_status tg_gemm_splitk_noalloc(const void* A, const void* B, const 
     splitk_args(d, static_cast<const __half*>(A), static_cast<const __half*>(B), static_cast<const __half*>(bias),
                 static_cast<__half*>(C), static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), gelu, split_k,
                 fit < 1 ? 1 : fit, a);
-    if (a.splits > 1) {
+    if (a.splits > 1 && !split_on_chip(a)) {
         const size_t partial_bytes = static_cast<size_t>(a.splits) * per_split;
         if (counter_bytes + partial_bytes > static_cast<size_t>(TG_NOALLOC_SCRATCH_BYTES))
             return fail(TG_ERR_INVALID_ARG,

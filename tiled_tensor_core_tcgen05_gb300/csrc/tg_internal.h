@@ -209,6 +209,14 @@ cudaError_t launch_tiled_pair(const TiledArgs& a, const CUtensorMap& tmA, const 
                               const CUtensorMap* tmC, int max_clusters, cudaStream_t stream);
 cudaError_t launch_splitk(const SplitArgs& a, const CUtensorMap& tmB, const CUtensorMap& tmA,
                           int grid, cudaStream_t stream);
+// The skinny kernel with its 2..kTiledClusterMax K slices of each unit as one thread-block
+// cluster (num_units = n_tiles * splits CTAs, one unit each), summed across the cluster's
+// shared memory: no scratch, no second kernel. split_on_chip_fits: the ring holds the staged
+// fp32 tile. split_cluster_capacity: such clusters resident at once (0 if unknown).
+cudaError_t launch_splitk_cluster(const SplitArgs& a, const CUtensorMap& tmB, const CUtensorMap& tmA,
+                                  cudaStream_t stream);
+bool split_on_chip_fits(int m_pad, int stages);
+int split_cluster_capacity(int splits, int m_pad, int stages);
 void w4_pipeline(int m_pad, int* stages, int* act_slots, int* slots);
 int w4_smem_bytes(int m_pad, int stages, int act_slots, int slots);
 cudaError_t launch_w4(const W4Args& a, const CUtensorMap& tmBq, const CUtensorMap& tmA, const CUtensorMap& tmS,

@@ -40,6 +40,10 @@ __device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // 16-byte load from the shared memory of any CTA of the cluster (a mapa address).
 __device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
     float4 v;

@@ -5,7 +5,8 @@
 // C; with several, each unit stores its partial tile to scratch laid out
 // [slice][n][m_pad], and a second kernel (launch_splitk_reduce) adds the
 // partials over the whole GPU in slice order 0, 1, ..., applies the epilogue
-// and writes C. (Reducing in the last CTA of each column slice to arrive left
+// and writes C; or, in the cluster form, each CTA stages its tile in shared
+// memory for an in-kernel sum across the cluster. (Reducing in the last CTA of each column slice to arrive left
 // one CTA per 256 columns summing every slice alone: at 64 rows and eight
 // slices that serial tail took longer than the product.)
 //
@@ -27,9 +28,14 @@ constexpr int kSkEpiThreads = 128;
 // TMEM column b * kHalves * tmem_stride; half h at + h * tmem_stride.
 // acc_full0 / acc_empty0: the first of two consecutive mbarriers each (8 bytes
 // apart); acc_empty counts kSkEpiThreads arrivals. Named barrier 1 is used.
-template <int kHalves>
+// Cluster form (kCl): the CTAs of a cluster are the K slices of one unit, one unit per CTA;
+// each stages its fp32 tile transposed back to C's orientation, [m][256 columns] with a row
+// pitch of kSkClPitch floats, at stage_base (its idle operand ring), for the in-kernel sum.
+constexpr int kSkClPitch = 256 + 4;
+
+template <int kHalves, bool kCl = false>
 __device__ __forceinline__ void skinny_epilogue(const SplitArgs& args, uint32_t tmem_base, uint32_t acc_full0,
-                                                uint32_t acc_empty0, const WaitCtx& wc) {
+                                                uint32_t acc_empty0, const WaitCtx& wc, uint32_t stage_base = 0) {
     constexpr int kUnitCols = 128 * kHalves;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -37,8 +43,8 @@ __device__ __forceinline__ void skinny_epilogue(const SplitArgs& args, uint32_t 
     const int chunks = args.m_pad / 16;
     int it = 0;
     for (int u = blockIdx.x; u < args.num_units; u += gridDim.x, ++it) {
-        const int sp = u / args.n_tiles;
-        const int nt = u - sp * args.n_tiles;
+        const int sp = kCl ? u % args.splits : u / args.n_tiles;
+        const int nt = kCl ? u / args.splits : u - sp * args.n_tiles;
         const int b = it & 1;
         const bool ok = wait_phase(acc_full0 + 8 * b, (it >> 1) & 1, wc, kSiteEpilogueAccFull);
         // all 128 epilogue threads stop together, so the named barriers below
@@ -60,6 +66,14 @@ __device__ __forceinline__ void skinny_epilogue(const SplitArgs& args, uint32_t 
                 if (h == kHalves - 1 && c == chunks - 1) {
                     tc_fence_before_sync();
                     mbar_arrive(acc_empty0 + 8 * b);  // every accumulator of buffer b is read
+                }
+                if (kCl && args.splits > 1) {
+                    // every lane stages its column (rows beyond M are zeros and are not stored)
+                    const int nl = h * 128 + quarter * 32 + lane;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        st_shared_u32(stage_base + static_cast<uint32_t>(((c * 16 + i) * kSkClPitch + nl) * 4), r[i]);
+                    continue;
                 }
                 if (!n_ok) continue;
                 if (args.splits == 1) {
