@@ -297,8 +297,11 @@ int group_rows(int tile_rows, int K, int m_blocks) {
 // of the SMs; the 4-bit kernel is limited per SM (decoding and staging the
 // weights), so every SM counts and its K block (256 x 256 packed, 32 KB) is
 // charged less fixed overhead.
-int choose_splits(int n_tiles, int kb_total, int sm_count, double unit_overhead = 6.0,
-                  double reduce_per_split = 2.0, double hbm_fraction = 0.7) {
+// extra(s): a further cost of s slices (the skinny path charges a split summed through scratch
+// for the reduction kernel's launch, ~6 us or 11 K blocks, which a split summed on chip avoids).
+template <typename Extra>
+int choose_splits(int n_tiles, int kb_total, int sm_count, double unit_overhead, double reduce_per_split,
+                  double hbm_fraction, Extra extra) {
     const double kUnitOverhead = unit_overhead;
     const double kReducePerSplit = reduce_per_split;
     const double kHbmFraction = hbm_fraction;  // share of SMs whose streams saturate HBM
@@ -314,13 +317,19 @@ int choose_splits(int n_tiles, int kb_total, int sm_count, double unit_overhead 
         const long waves = (units + sm_count - 1) / sm_count;
         double t = static_cast<double>(waves) * (kbps + kUnitOverhead);
         if (t < hbm_floor) t = hbm_floor;
-        const double cost = t + kReducePerSplit * (s - 1);
+        const double cost = t + kReducePerSplit * (s - 1) + extra(s);
         if (cost < best) {
             best = cost;
             best_s = s;
         }
     }
     return best_s;
+}
+
+int choose_splits(int n_tiles, int kb_total, int sm_count, double unit_overhead = 6.0,
+                  double reduce_per_split = 2.0, double hbm_fraction = 0.7) {
+    return choose_splits(n_tiles, kb_total, sm_count, unit_overhead, reduce_per_split, hbm_fraction,
+                         [](int) { return 0.0; });
 }
 
 tg_status ensure_scratch(DeviceState& d, cudaStream_t stream, size_t ws_bytes, size_t n_counters, Scratch** out) {
@@ -353,6 +362,10 @@ tg_status ensure_scratch(DeviceState& d, cudaStream_t stream, size_t ws_bytes, s
 }
 
 // The skinny kernel's arguments for one call, all but its scratch pointers.
+#ifndef TG_SPLIT_CLUSTER
+#define TG_SPLIT_CLUSTER 1
+#endif
+
 // split_k > 0 fixes the number of K slices; 0 takes the cost model's choice,
 // capped at max_splits (at least 1).
 void splitk_args(const DeviceState& d, const __half* A, const __half* B, const __half* bias, __half* C, int M, int N,
@@ -369,7 +382,12 @@ void splitk_args(const DeviceState& d, const __half* A, const __half* B, const _
     a.kb_total = (K + kSkBK - 1) / kSkBK;
     int s = split_k;
     if (s <= 0) {
-        s = choose_splits(a.n_tiles, a.kb_total, d.sm_count);
+        const int m_pad = a.m_pad, stages = a.stages, n_tiles = a.n_tiles;
+        s = choose_splits(a.n_tiles, a.kb_total, d.sm_count, 6.0, 2.0, 0.7, [&](int c) {
+            const bool on_chip = TG_SPLIT_CLUSTER && c <= kTiledClusterMax && split_on_chip_fits(m_pad, stages) &&
+                                 n_tiles <= split_cluster_capacity(c, m_pad, stages);
+            return c > 1 && !on_chip ? 11.0 : 0.0;
+        });
         if (s > max_splits) s = max_splits;
     }
     if (s > a.kb_total) s = a.kb_total;
@@ -379,10 +397,6 @@ void splitk_args(const DeviceState& d, const __half* A, const __half* B, const _
     a.num_units = a.n_tiles * a.splits;
     a.wd = watchdog(d);
 }
-
-#ifndef TG_SPLIT_CLUSTER
-#define TG_SPLIT_CLUSTER 1
-#endif
 
 // True when the skinny kernel's K slices run as clusters summed on chip: 2..kTiledClusterMax
 // slices, the staged fp32 tile fits the ring, and every unit's cluster is resident at once.
@@ -594,23 +608,20 @@ bool pair_pays(const DeviceState& d, int64_t M, int64_t N, int64_t K) {
 }
 
 // True when the skinny split-K kernel beats the single-CTA tiled kernel for M <= 128
-// (measured on GB300 over N = 2048..28672, K = 2048..28672, M = 16..128). Skinny for M <= 16.
-// Above that, where the tiled kernel can split K on chip (its 256-column tiles fit the
-// two-CTA clusters at once), it ties or wins except for the skinniest products streaming a
-// large B through a split: skinny only for M <= 32 with at least 64 MiB of B when the tiled
-// kernel would split K (4096 x 14336 at M = 32: 29.1 vs 30.9 us). Where it cannot, the earlier
-// rule against the unsplit tiled kernel stands: with fewer 64-column tiles than SMs,
-// skinny when K/64 times the SMs per tile is at least 1.5 M; otherwise only when, with
-// M <= 64, the product streams 256 MiB or more of B (both kernels then sit near the HBM floor).
+// (measured on GB300 over N = 2048..28672, K = 2048..28672, M = 16..128, both kernels summing
+// their K slices on chip where they can). With K >= 2048, skinny up to 64 rows and tiled above
+// (the tiled kernel wins by up to 9% at 48-64 rows on 14336 x 4096 and 4096 x 8192, skinny by
+// up to 16% elsewhere at those sizes; at 96 rows and up the tiled kernel is within 5%). For
+// shorter K, outside that sweep, the earlier rule against the unsplit tiled kernel: with
+// fewer 64-column tiles than SMs, skinny when K/64 times the SMs per tile is at least 1.5 M;
+// otherwise only when, with M <= 64, the product streams 256 MiB or more of B.
 bool skinny_pays(const DeviceState& d, int64_t M, int64_t N, int64_t K) {
     if (M <= 16) return true;
-    const double b_bytes = 2.0 * static_cast<double>(K) * static_cast<double>(N);
-    if (tiled_on_chip(true, (N + kBN - 1) / kBN, 2))
-        return M <= 32 && b_bytes >= 64.0 * 1048576.0 && tiled_splits(d, M, N, K, true) > 1;
+    if (K >= 2048) return M <= 64;
     const int64_t tiles64 = (N + 63) / 64;  // one 128-row block: M <= 128
     const int64_t kb = (K + 63) / 64;
     if (tiles64 < d.sm_count) return 2 * kb * d.sm_count >= 3 * M * tiles64;
-    return M <= 64 && b_bytes >= 256.0 * 1048576.0;
+    return M <= 64 && 2.0 * static_cast<double>(K) * static_cast<double>(N) >= 256.0 * 1048576.0;
 }
 
 // A GEMM whose A or B TMA cannot describe (row stride not a multiple of 16
