@@ -102,12 +102,9 @@ typedef enum {
  * tg_shutdown; TG_ERR_NO_MEMORY if it cannot be allocated), then the TMA
  * kernels below run on the copy; M <= 16, or M <= 128 where the skinny kernel
  * measured faster -> TG_KERNEL_SPLITK; other M <= 128 -> TG_KERNEL_TILED_TMA.
- * "Measured faster" means one of two cases:
- *   - where the tiled kernel can sum a K split on chip (N at most one
- *     256-column tile per two-CTA cluster the device holds at once): M <= 32,
- *     2 K N >= 64 MiB of B, and the tiled kernel would split K;
- *   - elsewhere: fewer 64-column tiles than SMs with
- *     (K / 64) * SMs / tiles >= 1.5 M, or M <= 64 with 2 K N >= 256 MiB of B.
+ * "Measured faster" means M <= 64 when K >= 2048; for shorter K, fewer
+ * 64-column tiles than SMs with (K / 64) * SMs / tiles >= 1.5 M, or M <= 64
+ * with 2 K N >= 256 MiB of B.
  * M > 128: at least one 256x256 tile per pair of SMs, or with K >= 8192 at
  * least 0.3 of one -> TG_KERNEL_TILED_PAIR; otherwise TG_KERNEL_TILED_TMA.
  * TG_KERNEL_TILED_TMA (and TG_KERNEL_TILED_LSU) split K when their tiles leave
