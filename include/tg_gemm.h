@@ -105,11 +105,16 @@ typedef enum {
  * "Measured faster" means M <= 64 when K >= 2048; for shorter K, fewer
  * 64-column tiles than SMs with (K / 64) * SMs / tiles >= 1.5 M, or M <= 64
  * with 2 K N >= 256 MiB of B.
- * M > 128: at least one 256x256 tile per pair of SMs, or with K >= 8192 at
- * least 0.3 of one -> TG_KERNEL_TILED_PAIR; otherwise TG_KERNEL_TILED_TMA.
+ * M > 128: when the 128 x 256 tiles fill at least a wave of SMs, the kernel
+ * whose waves (with the last wave's cost: pairs' half-width units, or the
+ * single-CTA kernel's split tail) measure shorter; otherwise at least one
+ * 256x256 tile per pair of SMs, or with K >= 8192 at least 0.3 of one ->
+ * TG_KERNEL_TILED_PAIR; else TG_KERNEL_TILED_TMA.
  * TG_KERNEL_TILED_TMA (and TG_KERNEL_TILED_LSU) split K when their tiles leave
  * SMs idle and a cost model of the slices and their summation predicts a gain
- * (see tg_gemm_ex).
+ * (see tg_gemm_ex). When TG_KERNEL_TILED_TMA's tiles fill whole waves plus a
+ * short last one, with split_k 0 the last wave's tiles may run K-split in a
+ * second launch (clusters summing on chip) after the whole waves.
  */
 tg_status tg_gemm(const void* A, const void* B, const void* bias, void* C,
                   int64_t M, int64_t N, int64_t K, int epilogue, tg_stream_t stream);
@@ -117,7 +122,9 @@ tg_status tg_gemm(const void* A, const void* B, const void* bias, void* C,
 /*
  * The choice tg_gemm makes for these operands, without running anything:
  * *kernel receives the tg_kernel value it runs, *split_k the number of K slices
- * that kernel takes (1 = K is not split; always 1 for TG_KERNEL_TILED_PAIR),
+ * that kernel takes (1 = K is not split; always 1 for TG_KERNEL_TILED_PAIR; for
+ * TG_KERNEL_TILED_TMA with whole waves of tiles and a split last wave, that
+ * wave's slices),
  * and *aligned_copy (may be NULL) 1 when A or B is first copied to an aligned
  * row stride. A and B are only tested for 16-byte alignment, never read; the
  * answer is for the current device. For K == 0 tg_gemm runs only its

@@ -156,3 +156,24 @@ def test_on_chip_and_scratch_reductions_agree_bit_for_bit(tg):
         assert torch.equal(on_chip.view(torch.int16), scratch.view(torch.int16)), f"split_k={split_k}"
         _check_tol(on_chip.cpu().float().numpy(), ref, f"split_k={split_k}")
     _status_ok(tg)
+
+
+def test_whole_waves_then_a_split_last_wave(tg):
+    # 1280 x 4096 with K = 8192: 160 tiles of 128 x 256, a wave on 152 SMs plus 8. The whole
+    # wave runs unsplit, then the last 8 tiles (column block 15, rows 256..1279 in the grouped
+    # order) run K-split as clusters summed on chip. Exact integer inputs: sampled whole rows,
+    # inside and outside the split tiles, must match the oracle bit for bit.
+    M, N, K = 1280, 4096, 8192
+    w = workloads.custom(M, N, K, seed=7500, dist=workloads.Dist("int", -1, 1), bias=INT2)
+    A, B, bias = w.inputs()
+    dA, dB, dbias = A.cuda(), B.cuda(), bias.cuda()
+    kernel, splits, _ = tg.tg_gemm_plan(dA.data_ptr(), dB.data_ptr(), M, N, K)
+    if kernel != tg.KERNEL_TILED_TMA or splits < 2:
+        pytest.skip(f"no split last wave chosen on this device (kernel {kernel}, {splits} slices)")
+    for k in (tg.KERNEL_AUTO, tg.KERNEL_TILED_TMA):
+        C = tg.gemm(dA, dB, dbias, gelu=True, kernel=k).cpu().numpy().view(np.uint16)
+        for r0 in (0, 130, 256, 700, 1279):
+            ref = oracle.gemm(A, B, bias, gelu=True, rows=(r0, 1)).view(np.uint16)
+            mism = np.argwhere(C[r0:r0 + 1] != ref)
+            assert mism.size == 0, f"kernel {k} row {r0}: {len(mism)} mismatches, first {tuple(mism[0])}"
+    _status_ok(tg)

@@ -85,8 +85,9 @@ template <bool kCl>
 __device__ __forceinline__ Unit unit_of(const TiledArgs& a, int u) {
     Unit w;
     if (kCl) {
-        w.tile = u / a.splits;
-        w.slice = u - w.tile * a.splits;
+        const int t = u / a.splits;
+        w.slice = u - t * a.splits;
+        w.tile = a.tile0 + t;
     } else {
         w.slice = u / a.num_tiles;
         w.tile = u - w.slice * a.num_tiles;

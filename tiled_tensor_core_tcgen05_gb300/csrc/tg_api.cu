@@ -498,6 +498,30 @@ int tiled_splits(const DeviceState& d, int64_t M, int64_t N, int64_t K, bool tma
     return best_s;
 }
 
+// A tail split for the single-CTA kernel with TMA loads: when its 128 x 256 tiles fill whole
+// waves plus a short last one, the whole waves run as usual and the last wave's tiles run K
+// split over `s` slices as clusters summed on chip (one more launch), instead of a wave of a
+// few tiles with most SMs idle. Returns s (0: no tail split). Same time model as tiled_splits:
+// the tail costs a wave of K / s blocks plus the cluster launch (5.5 us) against a whole wave.
+int tiled_tail_split(const DeviceState& d, int64_t M, int64_t N, int64_t K) {
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+    const int64_t rest = tiles % d.sm_count;
+    if (tiles < d.sm_count || rest == 0) return 0;
+    const int64_t kb = (K + kBK - 1) / kBK;
+    const double whole = static_cast<double>(kb) * 0.36;
+    double best = whole;
+    int best_s = 0;
+    for (int s = 2; s <= kTiledClusterMax && s <= kb; ++s) {
+        if (rest > tiled_cluster_capacity(s)) continue;
+        const double t = static_cast<double>((kb + s - 1) / s) * 0.36 + 5.5;
+        if (t < best) {
+            best = t;
+            best_s = s;
+        }
+    }
+    return best_s;
+}
+
 tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, const __half* bias, __half* C, int M,
                     int N, int K, int gelu, cudaStream_t stream, int64_t lda = 0, int64_t ldb = 0, int split_k = 0) {
     TiledArgs a{};
@@ -536,12 +560,28 @@ tg_status run_tiled(DeviceState& d, bool tma, const __half* A, const __half* B, 
     }
     const int grid = a.num_units < d.sm_count ? a.num_units : d.sm_count;
     cudaError_t e;
+    // whole waves, then the short last wave's tiles split over K (automatic choice only)
+    const int tail_s = (tma && split_k == 0 && a.splits == 1 && a.bn == kBN) ? tiled_tail_split(d, M, N, K) : 0;
     if (tma) {
         CUtensorMap tmA, tmB;
         tg_status st = make_map_ld(&tmA, A, K, M, lda ? lda : K, kBK, kBM);
         if (st != TG_OK) return st;
         if ((st = make_map_ld(&tmB, B, N, K, ldb ? ldb : N, 64, kBK)) != TG_OK) return st;
-        e = on_chip ? launch_tiled_cluster(a, tmA, tmB, stream) : launch_tiled_tma(a, tmA, tmB, grid, stream);
+        if (tail_s > 1) {
+            const int whole = a.num_tiles - a.num_tiles % d.sm_count;
+            TiledArgs w = a;
+            w.num_units = whole;  // tiles [0, whole), one slice each
+            if ((e = launch_tiled_tma(w, tmA, tmB, d.sm_count, stream)) != cudaSuccess)
+                return cuda_fail(e, "tiled kernel launch");
+            TiledArgs t = a;
+            t.tile0 = whole;
+            t.kb_per_split = (a.num_kb + tail_s - 1) / tail_s;
+            t.splits = (a.num_kb + t.kb_per_split - 1) / t.kb_per_split;
+            t.num_units = (a.num_tiles - whole) * t.splits;
+            e = launch_tiled_cluster(t, tmA, tmB, stream);
+        } else {
+            e = on_chip ? launch_tiled_cluster(a, tmA, tmB, stream) : launch_tiled_tma(a, tmA, tmB, grid, stream);
+        }
     } else {
         e = launch_tiled_lsu(a, grid, stream);
     }
@@ -597,12 +637,34 @@ tg_status run_tiled_pair(DeviceState& d, const __half* A, const __half* B, const
 // Unaligned operands: products of at least this many flops take the aligned-copy path.
 constexpr double kCopyPathFlops = 4294967296.0;  // 2^32
 
-// True when the CTA-pair kernel beats the single-CTA kernel (with its K split): with at least
-// one wave of 256x256 tiles, or, for K >= 8192, at least 0.3 of a wave (measured on GB300:
+// True when the CTA-pair kernel beats the single-CTA kernel (with its K split). When the
+// single-CTA kernel's tiles fill a wave, by their waves (below); otherwise with at least one
+// wave of 256x256 tiles, or, for K >= 8192, at least 0.3 of a wave (measured on GB300:
 // 8192 x 8192 at M = 512, 64 pair tiles, 49 vs 55 us; 4096 x 14336 at M = 768, 48 tiles,
 // 76 vs 85 us; with K = 4096 the single-CTA kernel stays ahead at 48-64 tiles).
 bool pair_pays(const DeviceState& d, int64_t M, int64_t N, int64_t K) {
     const int64_t pair_tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kBN - 1) / kBN);
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+    if (tiles >= d.sm_count) {
+        // both kernels fill at least a wave: compare their waves, the last one weighted by what
+        // it costs (pair: a last wave that fits as half-width units costs 0.63 of one; single
+        // CTA: a last wave split over K costs 1/s of one plus its launch), a pair wave counting
+        // 0.9 of a single-CTA wave (measured per-SM throughput). 14336 x 4096 at M = 640: single
+        // CTAs with a split tail 57.5 us against pairs 68.9; 8192 x 8192 at M = 640: 73.9 vs 87.8.
+        const int64_t clusters = d.sm_count / 2;
+        const int64_t kb = (K + kBK - 1) / kBK;
+        const int64_t prest = pair_tiles % clusters;
+        const double pair = static_cast<double>(pair_tiles / clusters) + (prest == 0 ? 0.0 : 2 * prest <= clusters ? 0.63 : 1.0);
+        const int64_t trest = tiles % d.sm_count;
+        double tail = trest == 0 ? 0.0 : 1.0;
+        if (trest > 0)
+            for (int s = 2; s <= kTiledClusterMax && s <= kb; ++s)
+                if (trest <= tiled_cluster_capacity(s)) {
+                    const double t = static_cast<double>((kb + s - 1) / s) / kb + 5.5 / (0.36 * kb);
+                    if (t < tail) tail = t;
+                }
+        return 0.9 * pair < static_cast<double>(tiles / d.sm_count) + tail;
+    }
     if (pair_tiles >= d.sm_count / 2) return true;
     return K >= 8192 && 10 * pair_tiles >= 3 * static_cast<int64_t>(d.sm_count);
 }
@@ -707,6 +769,10 @@ Plan plan_auto(const DeviceState& d, int64_t M, int64_t N, int64_t K, bool tma_o
         if (s > kb) s = kb;
         const int kbps = (kb + s - 1) / s;
         p.splits = (kb + kbps - 1) / kbps;
+        if (p.splits == 1 && p.kernel == TG_KERNEL_TILED_TMA) {
+            const int t = tiled_tail_split(d, M, N, K);  // whole waves, then a split last wave
+            if (t > 1) p.splits = (kb + (kb + t - 1) / t - 1) / ((kb + t - 1) / t);
+        }
     }
     return p;
 }

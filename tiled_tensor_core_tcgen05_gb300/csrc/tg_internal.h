@@ -113,6 +113,7 @@ struct TiledArgs {
     // with splits > 1 each unit writes fp32 partials [slice][n][m_pad] to ws, summed by
     // launch_splitk_reduce.
     int splits, kb_per_split, m_pad;
+    int tile0;     // cluster split: the launch's first tile (a split tail after whole-tile waves)
     float* ws;
     Watchdog wd;
 };
