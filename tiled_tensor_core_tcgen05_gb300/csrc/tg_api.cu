@@ -501,19 +501,19 @@ int tiled_splits(const DeviceState& d, int64_t M, int64_t N, int64_t K, bool tma
 // A tail split for the single-CTA kernel with TMA loads: when its 128 x 256 tiles fill whole
 // waves plus a short last one, the whole waves run as usual and the last wave's tiles run K
 // split over `s` slices as clusters summed on chip (one more launch), instead of a wave of a
-// few tiles with most SMs idle. Returns s (0: no tail split). Same time model as tiled_splits:
-// the tail costs a wave of K / s blocks plus the cluster launch (5.5 us) against a whole wave.
+// few tiles with most SMs idle. Returns s (0: no tail split). The tail costs a launch of K / s
+// blocks (0.36 us each) plus 11.5 us against a whole wave of K blocks at 0.41 us each (GB300).
 int tiled_tail_split(const DeviceState& d, int64_t M, int64_t N, int64_t K) {
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
     const int64_t rest = tiles % d.sm_count;
     if (tiles < d.sm_count || rest == 0) return 0;
     const int64_t kb = (K + kBK - 1) / kBK;
-    const double whole = static_cast<double>(kb) * 0.36;
+    const double whole = static_cast<double>(kb) * 0.41;
     double best = whole;
     int best_s = 0;
     for (int s = 2; s <= kTiledClusterMax && s <= kb; ++s) {
         if (rest > tiled_cluster_capacity(s)) continue;
-        const double t = static_cast<double>((kb + s - 1) / s) * 0.36 + 5.5;
+        const double t = static_cast<double>((kb + s - 1) / s) * 0.36 + 11.5;
         if (t < best) {
             best = t;
             best_s = s;
@@ -638,33 +638,40 @@ tg_status run_tiled_pair(DeviceState& d, const __half* A, const __half* B, const
 constexpr double kCopyPathFlops = 4294967296.0;  // 2^32
 
 // True when the CTA-pair kernel beats the single-CTA kernel (with its K split). When the
-// single-CTA kernel's tiles fill a wave, by their waves (below); otherwise with at least one
-// wave of 256x256 tiles, or, for K >= 8192, at least 0.3 of a wave (measured on GB300:
+// single-CTA kernel's tiles fill a wave and the pairs' fewer than eight, by a time model of
+// their waves (below); with more, always; otherwise with at least one wave of 256x256
+// tiles, or, for K >= 8192, at least 0.3 of a wave (measured on GB300:
 // 8192 x 8192 at M = 512, 64 pair tiles, 49 vs 55 us; 4096 x 14336 at M = 768, 48 tiles,
 // 76 vs 85 us; with K = 4096 the single-CTA kernel stays ahead at 48-64 tiles).
 bool pair_pays(const DeviceState& d, int64_t M, int64_t N, int64_t K) {
     const int64_t pair_tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kBN - 1) / kBN);
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-    if (tiles >= d.sm_count) {
-        // both kernels fill at least a wave: compare their waves, the last one weighted by what
-        // it costs (pair: a last wave that fits as half-width units costs 0.63 of one; single
-        // CTA: a last wave split over K costs 1/s of one plus its launch), a pair wave counting
-        // 0.9 of a single-CTA wave (measured per-SM throughput). 14336 x 4096 at M = 640: single
-        // CTAs with a split tail 57.5 us against pairs 68.9; 8192 x 8192 at M = 640: 73.9 vs 87.8.
-        const int64_t clusters = d.sm_count / 2;
-        const int64_t kb = (K + kBK - 1) / kBK;
+    const int64_t clusters = d.sm_count / 2;
+    if (tiles >= d.sm_count && pair_tiles < 8 * clusters) {
+        // both kernels fill at least a wave, and the last wave still weighs: compare their
+        // times (us). A wave of K blocks costs 0.41 per block for single-CTA tiles, 0.97 of
+        // that for pairs. The pairs' last wave costs 0.63 of one when it fits as half-width
+        // units. The single-CTA kernel's last wave may instead run K-split on chip: a second
+        // launch of K / s blocks at 0.36 plus 11.5. 14336 x 4096 at M = 640: single CTAs
+        // 57.5 us against pairs 68.9; 8192 x 8192 at M = 640 (split tail): 73.9 vs 87.8;
+        // 14336 x 4096 at M = 384: pairs 48.9 vs 52.7; 28672 x 8192 at M = 640: single CTAs 233
+        // vs 258. From eight waves of pairs on (square 8192, the FFN shapes) the pairs stay.
+        const double kb = static_cast<double>((K + kBK - 1) / kBK);
         const int64_t prest = pair_tiles % clusters;
-        const double pair = static_cast<double>(pair_tiles / clusters) + (prest == 0 ? 0.0 : 2 * prest <= clusters ? 0.63 : 1.0);
+        const double pair = 0.97 * 0.41 * kb *
+                            (static_cast<double>(pair_tiles / clusters) +
+                             (prest == 0 ? 0.0 : 2 * prest <= clusters ? 0.63 : 1.0));
         const int64_t trest = tiles % d.sm_count;
-        double tail = trest == 0 ? 0.0 : 1.0;
+        double tail = trest == 0 ? 0.0 : 0.41 * kb;
         if (trest > 0)
             for (int s = 2; s <= kTiledClusterMax && s <= kb; ++s)
                 if (trest <= tiled_cluster_capacity(s)) {
-                    const double t = static_cast<double>((kb + s - 1) / s) / kb + 5.5 / (0.36 * kb);
+                    const double t = std::ceil(kb / s) * 0.36 + 11.5;
                     if (t < tail) tail = t;
                 }
-        return 0.9 * pair < static_cast<double>(tiles / d.sm_count) + tail;
+        return pair < static_cast<double>(tiles / d.sm_count) * 0.41 * kb + tail;
     }
+    if (tiles >= d.sm_count) return true;
     if (pair_tiles >= d.sm_count / 2) return true;
     return K >= 8192 && 10 * pair_tiles >= 3 * static_cast<int64_t>(d.sm_count);
 }
