@@ -105,11 +105,13 @@ typedef enum {
  * "Measured faster" means M <= 64 when K >= 2048; for shorter K, fewer
  * 64-column tiles than SMs with (K / 64) * SMs / tiles >= 1.5 M, or M <= 64
  * with 2 K N >= 256 MiB of B.
- * M > 128: when the 128 x 256 tiles fill at least a wave of SMs, the kernel
- * whose waves (with the last wave's cost: pairs' half-width units, or the
- * single-CTA kernel's split tail) measure shorter; otherwise at least one
- * 256x256 tile per pair of SMs, or with K >= 8192 at least 0.3 of one ->
- * TG_KERNEL_TILED_PAIR; else TG_KERNEL_TILED_TMA.
+ * M > 128: when the 128 x 256 tiles fill at least a wave of SMs and the
+ * 256x256 pair tiles fewer than eight waves of SM pairs, the kernel a time
+ * model of their waves (with the last wave's cost: pairs' half-width units,
+ * or the single-CTA kernel's split tail) predicts faster; with more pair
+ * tiles TG_KERNEL_TILED_PAIR; below a wave, at least one 256x256 tile per
+ * pair of SMs, or with K >= 8192 at least 0.3 of one -> TG_KERNEL_TILED_PAIR;
+ * else TG_KERNEL_TILED_TMA.
  * TG_KERNEL_TILED_TMA (and TG_KERNEL_TILED_LSU) split K when their tiles leave
  * SMs idle and a cost model of the slices and their summation predicts a gain
  * (see tg_gemm_ex). When TG_KERNEL_TILED_TMA's tiles fill whole waves plus a
